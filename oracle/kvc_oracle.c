@@ -1,0 +1,486 @@
+/*
+ * kvc_oracle.c -- plain CPU oracle for the decoding-time KV-cache eviction step.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg load this file's library. The product path never
+ * calls it and shares no code, header or table with it.
+ *
+ * What it computes, and where each step comes from. "BeaconKV page" is the
+ * article "长推理把显存吃爆了？BeaconKV：用几个「信标查询」预判模型会回头看什么"
+ * (a write-up of the ICML 2026 BeaconKV paper); "ReasonAlloc page" is the note
+ * "arXiv ReasonAlloc: hierarchical decoding-time KV cache" (budget source only).
+ *
+ *   fps        BeaconKV page, section "Continual FPS：有界内存的在线最远点采样":
+ *              farthest-point sampling greedily picks m mutually most dissimilar
+ *              points; the buffer is filled to B_Q^max = 32 and compressed to
+ *              B_Q^min = 16. The page's formula is missing from the text; the
+ *              classic greedy k-centre rule is used: start at the oldest entry,
+ *              then repeatedly add the candidate whose distance to the chosen set
+ *              is largest (cosine distance 1 - cos on the pre-RoPE queries;
+ *              exact ties go to the lower index). Survivors keep time order.
+ *   rope       BeaconKV page, section "打分时的 RoPE 对齐": beacons are rotated to
+ *              the current step t, recent queries keep their own positions.
+ *              Rotate-half pairing (i, i + D/2), frequency theta^(-2i/D).
+ *              Rotated beacons are rounded to the cache's storage type before
+ *              the dot products (the kernels multiply storage-type operands).
+ *   score      BeaconKV page, same section: score_j = max over observation
+ *              queries r of softmax_r(q_r . k_j / sqrt(D)) over all cached keys;
+ *              the max also runs over the query heads sharing KV head h.
+ *   select     BeaconKV page, same section, last paragraph: prefix tokens and the
+ *              most recent tokens are always kept; the rest of the budget goes
+ *              to the top scores (ties: lower index). Section "实验": on reaching
+ *              B_KV^max, evict 1/8 so the cache drops to 7/8 B_KV^max. ReasonAlloc
+ *              page, "Core Mechanism": a per-head budget B_{L_i,H_j} caps each
+ *              head instead.
+ *   compact    The kept tokens' K and V rows, in original order, at the head's
+ *              front (out-of-place gather here); slots past the kept count keep
+ *              their old contents.
+ *
+ * Arithmetic is fp64 throughout; stored values are rounded once, at the end,
+ * to the storage type (bf16 round-to-nearest-even, or fp32).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define DT_BF16 0
+#define DT_F32 1
+
+/* ------------------------------------------------------------------------- */
+/* Storage conversions, from the formats' definitions.                        */
+/* ------------------------------------------------------------------------- */
+
+/* bf16 is the top half of an IEEE-754 binary32: widening is exact. */
+static double bf16_bits_to_f64(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* Nearest bf16 to x (ties to even mantissa), computed from the value, not from
+ * bit tricks: bf16 has 8 exponent bits like binary32 and 7 stored mantissa
+ * bits, so its spacing at |x| in [2^E, 2^(E+1)) is 2^(E-7), with E floored at
+ * -126 (subnormals). Values at or beyond the overflow midpoint become inf. */
+uint16_t oracle_f64_to_bf16(double x) {
+  uint16_t sign = signbit(x) ? 0x8000u : 0u;
+  if (isnan(x)) return (uint16_t)(0x7fc0u | sign);
+  double a = fabs(x);
+  if (a == 0.0) return sign;
+  if (isinf(a)) return (uint16_t)(0x7f80u | sign);
+  int e;
+  frexp(a, &e); /* a = f * 2^e, f in [0.5, 1) -> a in [2^(e-1), 2^e) */
+  int E = e - 1;
+  if (E < -126) E = -126;
+  double q = ldexp(1.0, E - 7);
+  double n = a / q;           /* exact: scaling by a power of two */
+  double r = floor(n);
+  double frac = n - r;
+  if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+  double v = r * q;           /* exact bf16 value (or 2^128 on overflow) */
+  if (v >= ldexp(1.0, 128)) return (uint16_t)(0x7f80u | sign);
+  float vf = (float)v;        /* exact: v has at most 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &vf, 4);
+  return (uint16_t)((u >> 16) | sign);
+}
+
+static double load_elem(const void* base, int dtype, int64_t i) {
+  if (dtype == DT_BF16) return bf16_bits_to_f64(((const uint16_t*)base)[i]);
+  return (double)((const float*)base)[i];
+}
+
+/* Round to the storage type and back (the value the kernels will multiply). */
+static double round_to_storage(double x, int dtype) {
+  if (dtype == DT_BF16) return bf16_bits_to_f64(oracle_f64_to_bf16(x));
+  return (double)(float)x;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Farthest-point sampling (BeaconKV page, "Continual FPS").                   */
+/* ------------------------------------------------------------------------- */
+
+/* Cosine distance between rows i and j of a row-normalised matrix; a zero row
+ * was left as zeros, which puts it at distance 1 from everything. */
+static double cos_dist(const double* xh, int D, int i, int j) {
+  double s = 0.0;
+  for (int d = 0; d < D; ++d) s += xh[(int64_t)i * D + d] * xh[(int64_t)j * D + d];
+  return 1.0 - s;
+}
+
+static void normalise_rows(const double* x, int n, int D, double* xh) {
+  for (int i = 0; i < n; ++i) {
+    double nn = 0.0;
+    for (int d = 0; d < D; ++d) nn += x[(int64_t)i * D + d] * x[(int64_t)i * D + d];
+    double inv = nn > 0.0 ? 1.0 / sqrt(nn) : 0.0;
+    for (int d = 0; d < D; ++d) xh[(int64_t)i * D + d] = x[(int64_t)i * D + d] * inv;
+  }
+}
+
+static int cmp_int(const void* a, const void* b) {
+  int x = *(const int*)a, y = *(const int*)b;
+  return (x > y) - (x < y);
+}
+
+/* Greedy FPS of m out of n rows of x[n][D] (fp64). Writes the picks in the
+ * order they were chosen to order_out (may be NULL) and, sorted ascending, to
+ * picks. gap_out (may be NULL) receives, per step k >= 1, the margin between
+ * the chosen candidate's distance and the best other candidate's distance
+ * (+inf when it was the only one left). Returns 0, or -1 on bad sizes. */
+int oracle_fps_f64(const double* x, int n, int D, int m, int* picks, int* order_out, double* gap_out) {
+  if (n < 1 || m < 1 || m > n || D < 1) return -1;
+  double* xh = (double*)malloc(sizeof(double) * (size_t)n * D);
+  double* mind = (double*)malloc(sizeof(double) * (size_t)n);
+  char* chosen = (char*)calloc((size_t)n, 1);
+  int* order = (int*)malloc(sizeof(int) * (size_t)m);
+  normalise_rows(x, n, D, xh);
+  order[0] = 0; /* start at the oldest buffered query */
+  chosen[0] = 1;
+  for (int i = 0; i < n; ++i) mind[i] = cos_dist(xh, D, i, 0);
+  if (gap_out) gap_out[0] = INFINITY;
+  for (int k = 1; k < m; ++k) {
+    int best = -1;
+    double bv = -INFINITY, second = -INFINITY;
+    for (int i = 0; i < n; ++i) {
+      if (chosen[i]) continue;
+      if (mind[i] > bv) { second = bv; bv = mind[i]; best = i; }
+      else if (mind[i] > second) second = mind[i];
+    }
+    order[k] = best;
+    chosen[best] = 1;
+    if (gap_out) gap_out[k] = bv - second;
+    for (int i = 0; i < n; ++i) {
+      double dd = cos_dist(xh, D, i, best);
+      if (dd < mind[i]) mind[i] = dd;
+    }
+  }
+  for (int k = 0; k < m; ++k) picks[k] = order[k];
+  if (order_out) memcpy(order_out, order, sizeof(int) * (size_t)m);
+  qsort(picks, (size_t)m, sizeof(int), cmp_int);
+  free(xh); free(mind); free(chosen); free(order);
+  return 0;
+}
+
+/* Is the ascending set `picks` (size m) a greedy FPS result of x, allowing a
+ * different choice wherever the chosen candidate's distance is within tol of
+ * the best one? Replays the greedy rule restricted to the set. Returns 0 if
+ * valid, else 1 + the step at which no member of the set was within tol, or
+ * -1 on bad input. */
+int oracle_fps_check_f64(const double* x, int n, int D, const int* picks, int m, double tol) {
+  if (n < 1 || m < 1 || m > n) return -1;
+  for (int k = 0; k < m; ++k) {
+    if (picks[k] < 0 || picks[k] >= n) return -1;
+    if (k && picks[k] <= picks[k - 1]) return -1;
+  }
+  if (picks[0] != 0) return 1;
+  double* xh = (double*)malloc(sizeof(double) * (size_t)n * D);
+  double* mind = (double*)malloc(sizeof(double) * (size_t)n);
+  char* chosen = (char*)calloc((size_t)n, 1);
+  char* inset = (char*)calloc((size_t)n, 1);
+  normalise_rows(x, n, D, xh);
+  for (int k = 0; k < m; ++k) inset[picks[k]] = 1;
+  chosen[0] = 1;
+  for (int i = 0; i < n; ++i) mind[i] = cos_dist(xh, D, i, 0);
+  int bad = 0;
+  for (int k = 1; k < m && !bad; ++k) {
+    double gbest = -INFINITY, sbest = -INFINITY;
+    int s = -1;
+    for (int i = 0; i < n; ++i) {
+      if (chosen[i]) continue;
+      if (mind[i] > gbest) gbest = mind[i];
+      if (inset[i] && mind[i] > sbest) { sbest = mind[i]; s = i; }
+    }
+    if (s < 0 || sbest < gbest - tol) { bad = k + 1; break; }
+    chosen[s] = 1;
+    for (int i = 0; i < n; ++i) {
+      double dd = cos_dist(xh, D, i, s);
+      if (dd < mind[i]) mind[i] = dd;
+    }
+  }
+  free(xh); free(mind); free(chosen); free(inset);
+  return bad;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Rotary position encoding (BeaconKV page, "打分时的 RoPE 对齐").               */
+/* ------------------------------------------------------------------------- */
+
+void oracle_rope_f64(const double* x, int D, long long pos, double theta, double* y) {
+  int h = D / 2;
+  for (int i = 0; i < h; ++i) {
+    double inv_freq = pow(theta, -2.0 * (double)i / (double)D);
+    double ang = (double)pos * inv_freq;
+    double c = cos(ang), s = sin(ang);
+    double a = x[i], b = x[i + h];
+    y[i] = a * c - b * s;
+    y[i + h] = b * c + a * s;
+  }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Scores (BeaconKV page, "打分时的 RoPE 对齐", the max aggregation).            */
+/* ------------------------------------------------------------------------- */
+
+/* q[M][D] observation rows, k[N][D] keys (fp64). out[j] = max_r softmax_r(j)
+ * where softmax_r is over all N keys of s_rj = q_r . k_j / sqrt(D). Also
+ * returns each row's log-sum-exp in lse (may be NULL). */
+void oracle_score_f64(const double* q, int M, const double* k, int N, int D, double* out, double* lse) {
+  double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+  double scale = 1.0 / sqrt((double)D);
+  for (int j = 0; j < N; ++j) out[j] = 0.0;
+  for (int r = 0; r < M; ++r) {
+    double mx = -INFINITY;
+    for (int j = 0; j < N; ++j) {
+      double acc = 0.0;
+      for (int d = 0; d < D; ++d) acc += q[(int64_t)r * D + d] * k[(int64_t)j * D + d];
+      s[j] = acc * scale;
+      if (s[j] > mx) mx = s[j];
+    }
+    double sum = 0.0;
+    for (int j = 0; j < N; ++j) sum += exp(s[j] - mx);
+    double l = mx + log(sum);
+    if (lse) lse[r] = l;
+    for (int j = 0; j < N; ++j) {
+      double p = exp(s[j] - l);
+      if (p > out[j]) out[j] = p;
+    }
+  }
+  free(s);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Selection (BeaconKV page, end of "打分时的 RoPE 对齐"; section "实验").       */
+/* ------------------------------------------------------------------------- */
+
+static const float* g_sort_scores; /* only used inside one qsort call per thread */
+#ifdef _OPENMP
+#pragma omp threadprivate(g_sort_scores)
+#endif
+
+static int cmp_score_desc(const void* a, const void* b) {
+  int i = *(const int*)a, j = *(const int*)b;
+  float si = g_sort_scores[i], sj = g_sort_scores[j];
+  if (si > sj) return -1;
+  if (si < sj) return 1;
+  return (i > j) - (i < j);
+}
+
+/* Keep [0,P) and [N-R,N), plus the (budget-P-R) highest-scoring middle keys
+ * (ties: lower index). kept[] receives the kept indices in ascending order.
+ * budget >= N keeps everything. Returns the kept count, or -1 if
+ * budget < P + R (the always-kept windows would not fit). */
+int oracle_select(const float* score, int N, int P, int R, int budget, int32_t* kept) {
+  if (budget >= N) {
+    for (int j = 0; j < N; ++j) kept[j] = j;
+    return N;
+  }
+  if (P < 0 || R < 0 || budget < P + R) return -1;
+  int mid_lo = P, mid_hi = N - R; /* middle is [P, N-R); P+R <= budget < N so it is non-empty */
+  int nmid = mid_hi - mid_lo;
+  int kmid = budget - P - R;
+  int* idx = (int*)malloc(sizeof(int) * (size_t)(nmid > 0 ? nmid : 1));
+  char* keep = (char*)calloc((size_t)N, 1);
+  for (int i = 0; i < nmid; ++i) idx[i] = mid_lo + i;
+  g_sort_scores = score;
+  qsort(idx, (size_t)nmid, sizeof(int), cmp_score_desc);
+  for (int i = 0; i < kmid; ++i) keep[idx[i]] = 1;
+  for (int j = 0; j < P; ++j) keep[j] = 1;
+  for (int j = mid_hi; j < N; ++j) keep[j] = 1;
+  int c = 0;
+  for (int j = 0; j < N; ++j)
+    if (keep[j]) kept[c++] = j;
+  free(idx);
+  free(keep);
+  return c;
+}
+
+/* ------------------------------------------------------------------------- */
+/* The whole step over every (layer, batch, KV head).                          */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+  int32_t dtype; /* 0 = bf16 (uint16 bit patterns), 1 = f32 */
+  int32_t L, B, Hq, Hkv, D, N;
+  int32_t n_r, n_b, qmax;
+  int32_t prefix, recent, budget_all;
+  int64_t t;
+  double theta;
+  const void* K;            /* [L,B,Hkv,N,D] */
+  const void* V;            /* [L,B,Hkv,N,D] */
+  const void* q_recent;     /* [L,B,Hq,n_r,D], post-RoPE at their own positions */
+  const void* qbuf;         /* [L,B,Hq,qmax,D], pre-RoPE, oldest first */
+  const int32_t* count;     /* [L,B,Hq] */
+  const int32_t* budget;    /* [L,B,Hkv] or NULL -> budget_all */
+  const int32_t* forced_picks; /* [L,B,Hq,n_b] beacon rows to use instead of FPS, or NULL */
+} oracle_problem;
+
+typedef struct {
+  float* scores;        /* [L,B,Hkv,N] or NULL */
+  int32_t* kept_idx;    /* [L,B,Hkv,N] or NULL (entries past kept_len are -1) */
+  int32_t* kept_len;    /* [L,B,Hkv] or NULL */
+  void* K_out;          /* [L,B,Hkv,N,D] or NULL: a copy of K, compacted */
+  void* V_out;          /* [L,B,Hkv,N,D] or NULL */
+  int32_t* beacon_picks;/* [L,B,Hq,n_b] or NULL: buffer rows used as beacons (-1 = none) */
+  int32_t* error;       /* [L,B,Hkv] or NULL: 0, or -1 when the head's budget was out of range */
+} oracle_outputs;
+
+/* Beacon rows of one query head: the buffer's first `count` rows if there are
+ * at most n_b of them, else an FPS of n_b out of those rows (non-destructive).
+ * Returns how many rows were picked. */
+static int beacon_rows(const oracle_problem* p, int64_t qh, int* rows) {
+  int cnt = p->count[qh];
+  if (cnt < 0) cnt = 0;
+  if (cnt > p->qmax) cnt = p->qmax;
+  if (p->forced_picks) {
+    int c = 0;
+    for (int k = 0; k < p->n_b; ++k) {
+      int r = p->forced_picks[qh * p->n_b + k];
+      if (r >= 0) rows[c++] = r;
+    }
+    return c;
+  }
+  if (cnt <= p->n_b) {
+    for (int k = 0; k < cnt; ++k) rows[k] = k;
+    return cnt;
+  }
+  int D = p->D;
+  double* x = (double*)malloc(sizeof(double) * (size_t)cnt * D);
+  const int64_t base = qh * (int64_t)p->qmax * D;
+  for (int i = 0; i < cnt; ++i)
+    for (int d = 0; d < D; ++d) x[(int64_t)i * D + d] = load_elem(p->qbuf, p->dtype, base + (int64_t)i * D + d);
+  oracle_fps_f64(x, cnt, D, p->n_b, rows, NULL, NULL);
+  free(x);
+  return p->n_b;
+}
+
+static void store_elem(void* base, int dtype, int64_t i, const void* src_base, int64_t si) {
+  if (dtype == DT_BF16) ((uint16_t*)base)[i] = ((const uint16_t*)src_base)[si];
+  else ((float*)base)[i] = ((const float*)src_base)[si];
+}
+
+static void evict_head(const oracle_problem* p, const oracle_outputs* o, int64_t head) {
+  const int D = p->D, N = p->N, G = p->Hq / p->Hkv;
+  const int l = (int)(head / ((int64_t)p->B * p->Hkv));
+  const int b = (int)((head / p->Hkv) % p->B);
+  const int h = (int)(head % p->Hkv);
+  const int maxrows = G * (p->n_r + p->n_b);
+  double* q = (double*)malloc(sizeof(double) * (size_t)(maxrows > 0 ? maxrows : 1) * D);
+  double* k = (double*)malloc(sizeof(double) * (size_t)N * D);
+  double* sc = (double*)malloc(sizeof(double) * (size_t)N);
+  float* scf = (float*)malloc(sizeof(float) * (size_t)N);
+  int32_t* kept = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+  int* rows = (int*)malloc(sizeof(int) * (size_t)(p->qmax > 0 ? p->qmax : 1));
+  double* tmp = (double*)malloc(sizeof(double) * (size_t)D);
+
+  /* observation rows: for each query head of the group, its recent queries as
+   * stored, then its beacons rotated to step t and rounded to storage type */
+  int M = 0;
+  for (int g = 0; g < G; ++g) {
+    const int hq = h * G + g;
+    const int64_t qh = ((int64_t)l * p->B + b) * p->Hq + hq;
+    for (int r = 0; r < p->n_r; ++r, ++M)
+      for (int d = 0; d < D; ++d)
+        q[(int64_t)M * D + d] = load_elem(p->q_recent, p->dtype, (qh * p->n_r + r) * D + d);
+    int nb = beacon_rows(p, qh, rows);
+    if (o->beacon_picks)
+      for (int kk = 0; kk < p->n_b; ++kk) o->beacon_picks[qh * p->n_b + kk] = kk < nb ? rows[kk] : -1;
+    for (int kk = 0; kk < nb; ++kk, ++M) {
+      for (int d = 0; d < D; ++d) tmp[d] = load_elem(p->qbuf, p->dtype, (qh * p->qmax + rows[kk]) * D + d);
+      oracle_rope_f64(tmp, D, (long long)p->t, p->theta, &q[(int64_t)M * D]);
+      for (int d = 0; d < D; ++d) q[(int64_t)M * D + d] = round_to_storage(q[(int64_t)M * D + d], p->dtype);
+    }
+  }
+  const int64_t kbase = head * (int64_t)N * D;
+  for (int64_t i = 0; i < (int64_t)N * D; ++i) k[i] = load_elem(p->K, p->dtype, kbase + i);
+  oracle_score_f64(q, M, k, N, D, sc, NULL);
+  for (int j = 0; j < N; ++j) scf[j] = (float)sc[j];
+  if (o->scores) memcpy(&o->scores[head * N], scf, sizeof(float) * (size_t)N);
+
+  int budget = p->budget ? p->budget[head] : p->budget_all;
+  int len = oracle_select(scf, N, p->prefix, p->recent, budget, kept);
+  if (o->error) o->error[head] = len < 0 ? -1 : 0;
+  if (len < 0) { /* out-of-range budget: the head is left whole */
+    for (int j = 0; j < N; ++j) kept[j] = j;
+    len = N;
+  }
+  if (o->kept_len) o->kept_len[head] = len;
+  if (o->kept_idx)
+    for (int j = 0; j < N; ++j) o->kept_idx[head * N + j] = j < len ? kept[j] : -1;
+  /* compaction: out-of-place gather into the output copies */
+  if (o->K_out)
+    for (int j = 0; j < len; ++j)
+      for (int d = 0; d < D; ++d) store_elem(o->K_out, p->dtype, kbase + (int64_t)j * D + d, p->K, kbase + (int64_t)kept[j] * D + d);
+  if (o->V_out)
+    for (int j = 0; j < len; ++j)
+      for (int d = 0; d < D; ++d) store_elem(o->V_out, p->dtype, kbase + (int64_t)j * D + d, p->V, kbase + (int64_t)kept[j] * D + d);
+  free(q); free(k); free(sc); free(scf); free(kept); free(rows); free(tmp);
+}
+
+/* The eviction step for every (l, b, h_kv). K_out / V_out must already hold a
+ * copy of K / V (slots past the kept count are left as they are). heads /
+ * nheads (optional) restrict the work to the listed flat head ids
+ * (l*B + b)*Hkv + h. Returns 0, or -1 on bad sizes. */
+int oracle_evict(const oracle_problem* p, const oracle_outputs* o, const int64_t* heads, int64_t nheads) {
+  if (!p || !o || p->L < 1 || p->B < 1 || p->Hkv < 1 || p->Hq < p->Hkv || p->Hq % p->Hkv) return -1;
+  if (p->D < 2 || p->D % 2 || p->N < 1 || p->n_r < 0 || p->n_b < 0 || p->qmax < 0) return -1;
+  const int64_t total = (int64_t)p->L * p->B * p->Hkv;
+  const int64_t n = heads ? nheads : total;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t head = heads ? heads[i] : i;
+    if (head >= 0 && head < total) evict_head(p, o, head);
+  }
+  return 0;
+}
+
+/* Continual-FPS compression of every query head whose buffer is full: the
+ * qmax buffered pre-RoPE queries are cut to qmax/2 by FPS, the survivors move
+ * to the buffer's front in time order and count becomes qmax/2. Heads with
+ * count < qmax are left alone. picks [L*B*Hq, qmax/2] (may be NULL) receives
+ * the surviving rows' old indices (-1 for heads left alone). Returns the
+ * number of compressed heads, or -1 on bad sizes. */
+int oracle_fps_update(int32_t dtype, int32_t nheads_q, int32_t D, void* qbuf, int32_t qmax, int32_t* count,
+                      int32_t* picks) {
+  if (nheads_q < 0 || D < 1 || qmax < 2 || qmax % 2) return -1;
+  const int m = qmax / 2;
+  int done = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : done)
+  for (int64_t qh = 0; qh < nheads_q; ++qh) {
+    if (count[qh] != qmax) {
+      if (picks)
+        for (int k = 0; k < m; ++k) picks[qh * m + k] = -1;
+      continue;
+    }
+    double* x = (double*)malloc(sizeof(double) * (size_t)qmax * D);
+    int* sel = (int*)malloc(sizeof(int) * (size_t)m);
+    const int64_t base = qh * (int64_t)qmax * D;
+    for (int i = 0; i < qmax; ++i)
+      for (int d = 0; d < D; ++d) x[(int64_t)i * D + d] = load_elem(qbuf, dtype, base + (int64_t)i * D + d);
+    oracle_fps_f64(x, qmax, D, m, sel, NULL, NULL);
+    /* sel is ascending and sel[k] >= k, so a forward copy never overwrites a
+     * row that is still to be read */
+    for (int k = 0; k < m; ++k)
+      for (int d = 0; d < D; ++d) store_elem(qbuf, dtype, base + (int64_t)k * D + d, qbuf, base + (int64_t)sel[k] * D + d);
+    count[qh] = m;
+    if (picks)
+      for (int k = 0; k < m; ++k) picks[qh * m + k] = sel[k];
+    free(x);
+    free(sel);
+    done += 1;
+  }
+  return done;
+}
+
+int oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
+}
