@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark of the eviction step (one kvc_evict over the whole cache) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+Prints ONE JSON line. A step is one pass of the whole hot path (beacons, scores, selection,
+in-place compaction) over every (layer, sequence, KV head) of the workload. Inputs are
+resident in HBM; between timed steps the cache is restored from a pristine copy and L2 is
+flushed (both untimed); each step is bracketed by CUDA events on the launch stream.
+
+value = cached tokens per second = B * N / step time (a token spans all layers and heads),
+summed over ranks. For N > 1 (torchrun) every rank runs an independent replica on its own
+GPU: the step has no cross-GPU exchange, so there is no collective on the data path.
+``--impl reference`` times the CPU oracle (the reference arm) on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "eviction-step cached tokens/sec and achieved HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "cached tokens/s"
+DEFAULT_CONFIG = "qwen3-4b"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# environment helpers
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region (read-only)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(1.0)
+        except OSError:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            except ValueError:
+                continue
+            rows.append((ts, parts))
+        lo, hi = (self.t0 or 0) - 1.0, (self.t1 or 1e18) + 1.0
+        inwin = [p for ts, p in rows if lo <= ts <= hi] or [p for _, p in rows]
+        sm = [float(p[2]) for p in inwin if p[2].replace(".", "").isdigit()]
+        smax = [float(p[3]) for p in inwin if p[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inwin for i in range(4) if p[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inwin)}
+
+
+def src_hash() -> str:
+    """Hash of the CUDA sources; ncu traffic figures are only reported for the build they came from."""
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "decoding_kv_cache_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str, kernel: str):
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(config, {}).get(kernel)
+    if not e or e.get("src_hash") != src_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def workload_desc(inp):
+    keep = "per-head budgets" if inp.budget is not None else f"{inp.budget_all}"
+    return (f"{inp.name} eviction step: L{inp.L} B{inp.B} Hq{inp.Hq} Hkv{inp.Hkv} D{inp.D} {inp.dtype} "
+            f"N{inp.N}->{keep}, obs {inp.n_r} recent + {inp.n_b} beacons (buffer {inp.qmax})")
+
+
+def algorithmic_bytes(inp, kept_idx, kept_len):
+    """K read once for scoring + K and V read and written for every kept token that moves."""
+    import torch
+    es = 2 if inp.dtype == "bf16" else 4
+    row = inp.D * es
+    k_read = inp.heads * inp.N * row
+    n = kept_idx.shape[-1]
+    ar = torch.arange(n, device=kept_idx.device, dtype=torch.int32)
+    valid = ar < kept_len[..., None]
+    moved = int(((kept_idx != ar) & valid).sum().item())
+    return k_read, moved * 4 * row, moved
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    from decoding_kv_cache_gb300 import build as kbuild
+    from decoding_kv_cache_gb300 import kvc
+    from decoding_kv_cache_gb300.inputs import make_inputs
+
+    if not kbuild.up_to_date():
+        kbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    inp = make_inputs(args.config, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    K0, V0 = inp.K.clone(), inp.V.clone()
+    cache = kvc.Cache(inp.K, inp.V, inp.Hq)
+    shape = (inp.L, inp.B, inp.Hkv)
+    kept_len = torch.zeros(shape, dtype=torch.int32, device=dev)
+    kept_idx = torch.zeros(shape + (inp.N,), dtype=torch.int32, device=dev)
+    scores = torch.zeros(shape + (inp.N,), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(kvc.kvc_evict_workspace_size(cache, inp.n_r, inp.n_b), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > 129 MB of L2
+
+    def reset():
+        inp.K.copy_(K0)
+        inp.V.copy_(V0)
+        flush.zero_()
+
+    def evict():
+        kvc.kvc_evict(cache, inp.q_recent, inp.qbuf, inp.count, inp.n_b, inp.t, inp.theta, inp.prefix, inp.recent,
+                      kept_len, budget=inp.budget, budget_all=inp.budget_all, kept_idx=kept_idx, scores=None,
+                      status=status, workspace=ws)
+
+    for _ in range(args.warmup):
+        reset()
+        evict()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {status.item()} after warm-up")
+    k_read, moved_bytes, moved = algorithmic_bytes(inp, kept_idx, kept_len)
+    alg = k_read + moved_bytes
+
+    # ---- headline: K timed steps of kvc_evict ------------------------------------------
+    clocks = ClockSampler(local_rank)
+    if rank == 0:
+        clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    for i in range(args.steps):
+        reset()
+        ev[i][0].record(stream)
+        evict()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    barrier(world)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    clk = clocks.stop() if rank == 0 else None
+    ms_per_step = total_ms / args.steps
+    tokens = inp.B * inp.N
+    value = world * tokens * args.steps / (total_ms / 1e3)
+
+    # ---- phase split (same work through the three entry points) to find the dominant kernel
+    phase_ms = {"kvc_score": 0.0, "kvc_select": 0.0, "kvc_compact": 0.0}
+    nph = max(3, min(args.steps, 50))
+    sc_ws = torch.empty(kvc.kvc_score_workspace_size(cache, inp.n_r, inp.n_b), dtype=torch.uint8, device=dev)
+    evs = []
+    for i in range(nph):
+        reset()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        kvc.kvc_score(cache, inp.q_recent, inp.qbuf, inp.count, inp.n_b, inp.t, inp.theta, scores, workspace=sc_ws)
+        e[1].record(stream)
+        kvc.kvc_select(scores, inp.prefix, inp.recent, kept_idx, kept_len, budget=inp.budget,
+                       budget_all=inp.budget_all)
+        e[2].record(stream)
+        kvc.kvc_compact(cache, kept_idx, kept_len, status=status)
+        e[3].record(stream)
+        evs.append(e)
+    torch.cuda.synchronize()
+    for e in evs:
+        phase_ms["kvc_score"] += e[0].elapsed_time(e[1]) / nph
+        phase_ms["kvc_select"] += e[1].elapsed_time(e[2]) / nph
+        phase_ms["kvc_compact"] += e[2].elapsed_time(e[3]) / nph
+    phase_bytes = {"kvc_score": k_read, "kvc_select": 0, "kvc_compact": moved_bytes}
+    dom = max(phase_ms, key=phase_ms.get)
+
+    # ---- end to end: host buffers in, step, result out ------------------------------------
+    pin = lambda t: t.cpu().pin_memory()
+    hK, hV, hqr, hqb, hc = pin(K0), pin(V0), pin(inp.q_recent), pin(inp.qbuf), pin(inp.count)
+    hkl, hki = torch.empty_like(kept_len, device="cpu").pin_memory(), torch.empty_like(kept_idx, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hK, hV, hqr, hqb, hc))
+    d2h = hkl.numel() * 4 + hki.numel() * 4
+    n_e2e = max(3, min(args.steps, 20))
+    ee = []
+    for i in range(n_e2e):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        inp.K.copy_(hK, non_blocking=True)
+        inp.V.copy_(hV, non_blocking=True)
+        inp.q_recent.copy_(hqr, non_blocking=True)
+        inp.qbuf.copy_(hqb, non_blocking=True)
+        inp.count.copy_(hc, non_blocking=True)
+        evict()
+        hkl.copy_(kept_len, non_blocking=True)
+        hki.copy_(kept_idx, non_blocking=True)
+        b.record(stream)
+        ee.append((a, b))
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ee) / n_e2e, world)
+
+    pk, pk_kind = peaks()
+    hbm = float(pk["hbm_gbs"])
+    dom_ms = phase_ms[dom]
+    achieved = phase_bytes[dom] / (dom_ms / 1e3) / 1e9 if phase_bytes[dom] else 0.0
+    step_gbs = alg / (ms_per_step / 1e3) / 1e9
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": inp.dtype, "data": "synthetic",
+        "config": {"workload": workload_desc(inp), "l2": "flushed between steps (512 MB write), cache restored "
+                   "from a pristine copy between steps; both untimed", "parallelism": f"replicas x{world}",
+                   "timing": "CUDA events around each kvc_evict on the launch stream"},
+        "head_tokens_per_s": world * inp.heads * inp.N * args.steps / (total_ms / 1e3),
+        "achieved_gbs": step_gbs, "step_roofline_frac": step_gbs / hbm,
+        "algorithmic_bytes_per_step": {"k_read": k_read, "kv_moved": moved_bytes, "moved_tokens": moved},
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_source": pk_kind,
+                     "traffic": recorded_traffic(args.config, dom)},
+        "phases_ms": phase_ms,
+        "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * kvc.kvc_evict_launch_count(cache, inp.n_r, inp.n_b),
+        "clocks": clk,
+    }
+    return res, inp
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(config: str, budget_s: float = 12.0):
+    """Time the oracle, as it stands, on a bounded sample of the workload's heads.
+    Returns (tokens/s scaled to the full step, cores, sample description, seconds)."""
+    from decoding_kv_cache_gb300.inputs import make_inputs
+    from oracle import oracle as O
+    from decoding_kv_cache_gb300.inputs import CONFIGS
+    spec = CONFIGS[config]
+    cores = O.set_threads(os.cpu_count() or 1)
+    heads_full = spec["L"] * spec["B"] * spec["Hkv"]
+    # one layer of one sequence first, to size the sample
+    probe = make_inputs(config, L=1, B=1)
+    t0 = time.perf_counter()
+    O.evict(probe)
+    dt = time.perf_counter() - t0
+    per_head = dt / probe.heads
+    want_heads = max(probe.heads, min(heads_full, int(budget_s / max(per_head, 1e-9))))
+    L = max(1, min(spec["L"], want_heads // (spec["B"] * spec["Hkv"])))
+    B = spec["B"] if L > 1 else max(1, min(spec["B"], want_heads // spec["Hkv"]))
+    samp = make_inputs(config, L=L, B=B)
+    t0 = time.perf_counter()
+    O.evict(samp)
+    dt = time.perf_counter() - t0
+    full_s = dt * heads_full / samp.heads
+    tok = spec["B"] * spec["N"] / full_s
+    desc = (f"oracle on {samp.heads} of {heads_full} heads (L={L}, B={B}) of {config}, {dt:.2f} s wall on "
+            f"{cores} threads, scaled linearly to the full step")
+    return tok, cores, desc, dt
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    vals, descs = [], []
+    if args.warmup > 0:
+        oracle_sample(args.config, budget_s=2.0)
+    for _ in range(args.steps):
+        tok, cores, desc, _ = oracle_sample(args.config, budget_s=min(12.0, 120.0 / max(args.steps, 1)))
+        vals.append(tok)
+        descs.append(desc)
+    value = statistics.mean(vals)
+    from decoding_kv_cache_gb300.inputs import CONFIGS
+    spec = CONFIGS[args.config]
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": spec["B"] * spec["N"] / value * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.config}, "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores,
+                                                                 "kind": "oracle", "sample": descs[-1]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            dist.init_process_group("nccl")
+    if args.impl == "reference":
+        out = reference_arm(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    res, _ = gpu_arm(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            tok, cores, desc, _ = oracle_sample(args.config)
+            res["cpu_baseline"] = {"value": tok, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

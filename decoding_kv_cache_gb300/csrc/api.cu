@@ -1,0 +1,215 @@
+// api.cu -- the extern "C" entry points of libkvc: argument checks, workspace layout, launches.
+//
+// Every check happens on the host before the first launch of a call, so a rejected call
+// has touched nothing. Conditions that only the device can see are OR-ed into the
+// caller's status word by the kernels (see kvc.h).
+#include <math.h>
+#include <string.h>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dtype_dim(int dtype, int D) {
+  if (dtype != KVC_BF16 && dtype != KVC_F32) return KVC_ERR_UNSUPPORTED_DTYPE;
+  if (D != 64 && D != 128) return KVC_ERR_UNSUPPORTED_HEAD_DIM;
+  return KVC_OK;
+}
+
+// Validates the cache description and copies its layer pointers.
+int check_cache(const kvc_cache* c, CacheGeom* g, LayerPtrs* K, LayerPtrs* V) {
+  if (!c || !c->K || !c->V) return KVC_ERR_INVALID_ARG;
+  int rc = check_dtype_dim(c->dtype, c->D);
+  if (rc) return rc;
+  if (c->L < 1 || c->L > KVC_MAX_LAYERS || c->B < 1 || c->Hq < 1 || c->Hkv < 1 || c->N < 1 || c->pad_ != 0)
+    return KVC_ERR_INVALID_ARG;
+  if (c->Hq % c->Hkv) return KVC_ERR_NOT_DIVISIBLE;
+  if (c->ncap < c->N) return KVC_ERR_INVALID_ARG;
+  const long long heads = (long long)c->L * c->B * c->Hkv;
+  if (heads > 65535 || (long long)c->N > (1LL << 30) || (long long)c->B * c->Hq * c->L > (1LL << 30))
+    return KVC_ERR_TOO_LARGE;
+  for (int l = 0; l < c->L; ++l) {
+    if (!c->K[l] || !c->V[l]) return KVC_ERR_INVALID_ARG;
+    if (!aligned16(c->K[l]) || !aligned16(c->V[l])) return KVC_ERR_ALIGNMENT;
+    K->p[l] = c->K[l];
+    V->p[l] = c->V[l];
+  }
+  for (int l = c->L; l < KVC_MAX_LAYERS; ++l) K->p[l] = V->p[l] = nullptr;
+  *g = CacheGeom{c->L, c->B, c->Hq, c->Hkv, c->D, c->N, (long long)c->ncap};
+  return KVC_OK;
+}
+
+int check_queries(const kvc_cache* c, const void* q_recent, int n_r, const void* qbuf, const int32_t* count,
+                  int qmax, int n_b, double theta) {
+  if (n_r < 0 || n_r > 64 || qmax < 0 || qmax > kMaxQmax || n_b < 0 || n_b > qmax || n_r + n_b < 1)
+    return KVC_ERR_INVALID_ARG;
+  if (n_r > 0 && !q_recent) return KVC_ERR_INVALID_ARG;
+  if (qmax > 0 && (!qbuf || !count)) return KVC_ERR_INVALID_ARG;
+  if (!(theta > 1.0) || !isfinite(theta)) return KVC_ERR_INVALID_ARG;
+  const int G = c->Hq / c->Hkv;
+  if ((long long)G * (n_r + n_b) > kMaxRows) return KVC_ERR_TOO_LARGE;
+  if ((q_recent && !aligned16(q_recent)) || (qbuf && !aligned16(qbuf))) return KVC_ERR_ALIGNMENT;
+  return KVC_OK;
+}
+
+void fill_score_args(ScoreArgs* a, const CacheGeom& g, int dtype, const LayerPtrs& K, const void* q_recent, int n_r,
+                     const void* qbuf, const int32_t* count, int qmax, int n_b, int64_t t, double theta,
+                     float* scores, int32_t* beacon_picks, int32_t* status) {
+  a->g = g;
+  a->dtype = dtype;
+  a->K = K;
+  a->q_recent = q_recent;
+  a->n_r = n_r;
+  a->qbuf = qbuf;
+  a->count = count;
+  a->qmax = qmax;
+  a->n_b = n_b;
+  a->t = (long long)t;
+  a->theta = theta;
+  a->scores = scores;
+  a->beacon_picks = beacon_picks;
+  a->status = status;
+  a->M = (g.Hq / g.Hkv) * (n_r + n_b);
+  a->M_pad = (a->M + 15) / 16 * 16;
+  a->nchunk = (g.N + kChunk - 1) / kChunk;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+}  // namespace kvc
+
+using namespace kvc;
+
+extern "C" {
+
+int kvc_abi_version(void) { return KVC_ABI_VERSION; }
+
+int kvc_evict_launch_count(const kvc_cache* c, int32_t n_r, int32_t n_b) {
+  (void)c;
+  (void)n_r;
+  (void)n_b;
+  return 7;  // rope table, observation rows, pass 1, combine, pass 2, select, compact
+}
+
+const char* kvc_strerror(int code) {
+  switch (code) {
+    case KVC_OK: return "ok";
+    case KVC_ERR_INVALID_ARG: return "invalid argument";
+    case KVC_ERR_UNSUPPORTED_DTYPE: return "unsupported storage type";
+    case KVC_ERR_UNSUPPORTED_HEAD_DIM: return "unsupported head dimension (64 or 128)";
+    case KVC_ERR_BUDGET_RANGE: return "budget smaller than prefix + recent";
+    case KVC_ERR_NOT_DIVISIBLE: return "query heads not a multiple of KV heads, or odd buffer size";
+    case KVC_ERR_LAUNCH: return "CUDA launch failed";
+    case KVC_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVC_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+    case KVC_ERR_TOO_LARGE: return "size too large";
+    default: return "unknown error";
+  }
+}
+
+int kvc_fps_update(int32_t dtype, int32_t L, int32_t B, int32_t Hq, int32_t D, void* qbuf, int32_t qmax,
+                   int32_t* count, int32_t* picks, int32_t* status, void* stream) {
+  int rc = check_dtype_dim(dtype, D);
+  if (rc) return rc;
+  if (L < 1 || B < 1 || Hq < 1 || !qbuf || !count || qmax < 2 || qmax > kMaxQmax) return KVC_ERR_INVALID_ARG;
+  if (qmax % 2) return KVC_ERR_NOT_DIVISIBLE;
+  const long long nq = (long long)L * B * Hq;
+  if (nq > (1LL << 30)) return KVC_ERR_TOO_LARGE;
+  if (!aligned16(qbuf)) return KVC_ERR_ALIGNMENT;
+  return launch_fps_update(dtype, (int)nq, D, qbuf, qmax, count, picks, status, static_cast<cudaStream_t>(stream));
+}
+
+size_t kvc_score_workspace_size(const kvc_cache* c, int32_t n_r, int32_t n_b) {
+  CacheGeom g;
+  LayerPtrs K, V;
+  if (!c || n_r < 0 || n_b < 0) return 0;
+  kvc_cache probe = *c;
+  if (check_cache(&probe, &g, &K, &V)) return 0;
+  return score_ws_bytes(g, c->dtype, n_r, n_b, nullptr, nullptr);
+}
+
+int kvc_score(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf, const int32_t* count,
+              int32_t qmax, int32_t n_b, int64_t t, double rope_theta, float* scores, int32_t* beacon_picks,
+              void* workspace, size_t ws_bytes, void* stream) {
+  CacheGeom g;
+  LayerPtrs K, V;
+  int rc = check_cache(c, &g, &K, &V);
+  if (rc) return rc;
+  rc = check_queries(c, q_recent, n_r, qbuf, count, qmax, n_b, rope_theta);
+  if (rc) return rc;
+  if (!scores) return KVC_ERR_INVALID_ARG;
+  const size_t need = score_ws_bytes(g, c->dtype, n_r, n_b, nullptr, nullptr);
+  if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return KVC_ERR_WORKSPACE;
+  ScoreWs ws;
+  score_ws_bytes(g, c->dtype, n_r, n_b, &ws, workspace);
+  ScoreArgs a;
+  fill_score_args(&a, g, c->dtype, K, q_recent, n_r, qbuf, count, qmax, n_b, t, rope_theta, scores, beacon_picks,
+                  nullptr);
+  return launch_score(a, ws, static_cast<cudaStream_t>(stream));
+}
+
+int kvc_select(const float* scores, int32_t L, int32_t B, int32_t Hkv, int32_t N, int32_t prefix, int32_t recent,
+               const int32_t* budget, int32_t budget_all, int32_t* kept_idx, int32_t* kept_len, int32_t* status,
+               void* stream) {
+  if (!scores || !kept_idx || !kept_len || L < 1 || B < 1 || Hkv < 1 || N < 1 || prefix < 0 || recent < 0)
+    return KVC_ERR_INVALID_ARG;
+  const long long heads = (long long)L * B * Hkv;
+  if (heads > (1LL << 31) - 1 || (long long)N > (1LL << 30)) return KVC_ERR_TOO_LARGE;
+  if (!budget && budget_all < prefix + recent && budget_all < N) return KVC_ERR_BUDGET_RANGE;
+  return launch_select(scores, (int)heads, N, prefix, recent, budget, budget_all, kept_idx, kept_len, status,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int kvc_compact(const kvc_cache* c, const int32_t* kept_idx, const int32_t* kept_len, int32_t* status,
+                void* stream) {
+  CacheGeom g;
+  LayerPtrs K, V;
+  int rc = check_cache(c, &g, &K, &V);
+  if (rc) return rc;
+  if (!kept_idx || !kept_len) return KVC_ERR_INVALID_ARG;
+  return launch_compact(g, c->dtype, K, V, kept_idx, kept_len, status, true, static_cast<cudaStream_t>(stream));
+}
+
+size_t kvc_evict_workspace_size(const kvc_cache* c, int32_t n_r, int32_t n_b) {
+  const size_t sw = kvc_score_workspace_size(c, n_r, n_b);
+  if (!sw) return 0;
+  const size_t per = (size_t)c->L * c->B * c->Hkv * (size_t)c->N * 4;
+  return sw + 2 * align256(per);  // scores and kept indices, used when the caller passes NULL
+}
+
+int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf, const int32_t* count,
+              int32_t qmax, int32_t n_b, int64_t t, double rope_theta, int32_t prefix, int32_t recent,
+              const int32_t* budget, int32_t budget_all, int32_t* kept_idx, int32_t* kept_len, float* scores,
+              int32_t* status, void* workspace, size_t ws_bytes, void* stream) {
+  CacheGeom g;
+  LayerPtrs K, V;
+  int rc = check_cache(c, &g, &K, &V);
+  if (rc) return rc;
+  rc = check_queries(c, q_recent, n_r, qbuf, count, qmax, n_b, rope_theta);
+  if (rc) return rc;
+  if (!kept_len || prefix < 0 || recent < 0) return KVC_ERR_INVALID_ARG;
+  if (!budget && budget_all < prefix + recent && budget_all < c->N) return KVC_ERR_BUDGET_RANGE;
+  const size_t sw = score_ws_bytes(g, c->dtype, n_r, n_b, nullptr, nullptr);
+  const size_t per = align256((size_t)g.L * g.B * g.Hkv * (size_t)g.N * 4);
+  if (!workspace || ws_bytes < sw + 2 * per || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return KVC_ERR_WORKSPACE;
+  char* wb = static_cast<char*>(workspace);
+  ScoreWs ws;
+  score_ws_bytes(g, c->dtype, n_r, n_b, &ws, wb);
+  float* sc = scores ? scores : reinterpret_cast<float*>(wb + sw);
+  int32_t* ki = kept_idx ? kept_idx : reinterpret_cast<int32_t*>(wb + sw + per);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ScoreArgs a;
+  fill_score_args(&a, g, c->dtype, K, q_recent, n_r, qbuf, count, qmax, n_b, t, rope_theta, sc, nullptr, status);
+  rc = launch_score(a, ws, s);
+  if (rc) return rc;
+  rc = launch_select(sc, g.L * g.B * g.Hkv, g.N, prefix, recent, budget, budget_all, ki, kept_len, status, s);
+  if (rc) return rc;
+  return launch_compact(g, c->dtype, K, V, ki, kept_len, status, false, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// fps.cu -- kvc_fps_update: continual farthest-point compression of the beacon buffers.
+//
+// BeaconKV write-up, "Continual FPS：有界内存的在线最远点采样": each head's bounded buffer of
+// pre-RoPE queries is filled to B_Q^max and then cut back to B_Q^min by FPS, so the beacon
+// set keeps evolving while memory stays bounded. One warp per query head.
+#include "fps_warp.cuh"
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+template <typename T>
+__global__ void fps_update_kernel(T* __restrict__ qbuf, int nheads, int D, int qmax, int32_t* __restrict__ count,
+                                  int32_t* __restrict__ picks_out, int32_t* status) {
+  extern __shared__ float smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int per = qmax * (D + 1) + qmax;  // normalised rows + pick list (as ints)
+  float* xs = smem + warp * per;
+  int* pk = reinterpret_cast<int*>(xs + qmax * (D + 1));
+  const int qh = blockIdx.x * wpb + warp;
+  if (qh >= nheads) return;  // the whole warp leaves together
+  const int m = qmax / 2;
+  const int c = count[qh];
+  T* x = qbuf + (size_t)qh * qmax * D;
+  if (c != qmax) {
+    if (lane == 0 && (c < 0 || c > qmax)) status_or(status, KVC_STATUS_COUNT_RANGE);
+    if (picks_out)
+      for (int k = lane; k < m; k += kWarp) picks_out[(size_t)qh * m + k] = -1;
+    return;
+  }
+  fps_warp(x, qmax, D, m, xs, pk);
+  // Survivors to the front in time order. pk is ascending with pk[k] >= k, so row k is only
+  // ever the source of an earlier-or-equal k: a forward copy never clobbers a pending source.
+  for (int k = 0; k < m; ++k) {
+    const int src = pk[k];
+    if (src != k)
+      for (int d = lane; d < D; d += kWarp) x[(size_t)k * D + d] = x[(size_t)src * D + d];
+  }
+  __syncwarp();
+  if (lane == 0) count[qh] = m;
+  if (picks_out)
+    for (int k = lane; k < m; k += kWarp) picks_out[(size_t)qh * m + k] = pk[k];
+}
+
+int launch_fps_update(int dtype, int nheads_q, int D, void* qbuf, int qmax, int32_t* count, int32_t* picks,
+                      int32_t* status, cudaStream_t s) {
+  if (nheads_q == 0) return KVC_OK;
+  const size_t per_warp = sizeof(float) * (size_t)(qmax * (D + 1) + qmax);
+  int wpb = (int)((200u * 1024u) / per_warp);
+  wpb = wpb < 1 ? 1 : (wpb > 4 ? 4 : wpb);
+  const size_t smem = per_warp * wpb;
+  const int grid = (nheads_q + wpb - 1) / wpb;
+  if (dtype == KVC_BF16) {
+    auto k = fps_update_kernel<__nv_bfloat16>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return KVC_ERR_LAUNCH;
+    k<<<grid, 32 * wpb, smem, s>>>(static_cast<__nv_bfloat16*>(qbuf), nheads_q, D, qmax, count, picks, status);
+  } else {
+    auto k = fps_update_kernel<float>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return KVC_ERR_LAUNCH;
+    k<<<grid, 32 * wpb, smem, s>>>(static_cast<float*>(qbuf), nheads_q, D, qmax, count, picks, status);
+  }
+  return launch_ok();
+}
+
+}  // namespace kvc

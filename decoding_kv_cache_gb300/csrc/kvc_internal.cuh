@@ -1,0 +1,89 @@
+// kvc_internal.cuh -- device helpers and launch parameters shared by libkvc's kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvc.h"
+
+namespace kvc {
+
+constexpr int kWarp = 32;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kChunk = 128;     // keys per scoring CTA
+constexpr int kMaxRows = 256;   // observation rows per KV head (G * (n_r + n_b), padded to 16)
+constexpr int kMaxQmax = 64;    // FPS buffer capacity
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---- storage access -------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// ---- warp reductions --------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void status_or(int32_t* status, unsigned bits) {
+  if (status) atomicOr(reinterpret_cast<unsigned*>(status), bits);
+}
+
+// ---- per-layer pointer tables passed by value -------------------------------
+struct LayerPtrs {
+  void* p[KVC_MAX_LAYERS];
+};
+
+// Geometry of one cache, as the kernels see it.
+struct CacheGeom {
+  int L, B, Hq, Hkv, D, N;
+  long long ncap;
+};
+
+// ---- launchers (host) ---------------------------------------------------------
+// Each returns KVC_OK or KVC_ERR_LAUNCH; arguments are already validated.
+int launch_fps_update(int dtype, int nheads_q, int D, void* qbuf, int qmax, int32_t* count, int32_t* picks,
+                      int32_t* status, cudaStream_t s);
+
+struct ScoreWs {            // carved out of the caller's workspace
+  float2* rope;             // [D/2] (cos, sin) at step t
+  void* obs;                // [heads][M_pad][D] storage type
+  uint8_t* valid;           // [heads][M_pad]
+  float2* part;             // [heads][nchunk][M_pad] (running max, sum) in base 2
+  float* lse2;              // [heads][M_pad] log2-sum-exp2, +inf for unused rows
+};
+
+struct ScoreArgs {
+  CacheGeom g;
+  int dtype;
+  LayerPtrs K;
+  const void* q_recent;
+  int n_r;
+  const void* qbuf;
+  const int32_t* count;
+  int qmax, n_b;
+  long long t;
+  double theta;
+  float* scores;
+  int32_t* beacon_picks;
+  int32_t* status;
+  int M, M_pad, nchunk;
+};
+
+size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, ScoreWs* carve, void* base);
+int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s);
+
+int launch_select(const float* scores, int heads, int N, int P, int R, const int32_t* budget, int budget_all,
+                  int32_t* kept_idx, int32_t* kept_len, int32_t* status, cudaStream_t s);
+
+int launch_compact(const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V, const int32_t* kept_idx,
+                   const int32_t* kept_len, int32_t* status, bool validate, cudaStream_t s);
+
+inline int launch_ok() { return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_LAUNCH; }
+
+}  // namespace kvc

@@ -1,0 +1,213 @@
+/*
+ * kvc.h -- C ABI of libkvc: the decoding-time KV-cache eviction step on one GPU.
+ *
+ * The step follows the BeaconKV write-up "长推理把显存吃爆了？BeaconKV：用几个
+ * 「信标查询」预判模型会回头看什么" (sections "观察 query 集 = 最近查询 + 信标查询",
+ * "Continual FPS：有界内存的在线最远点采样", "打分时的 RoPE 对齐" and "实验"),
+ * with per-head budgets as in the ReasonAlloc note ("Core Mechanism": a budget
+ * B_{L_i,H_j} per head fed to any eviction policy).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named in a "device" comment are CUDA device pointers (or
+ *   managed memory); everything else is host memory read during the call only.
+ *   The caller owns every buffer; the library allocates nothing, keeps no
+ *   global state and never synchronises the stream.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream). Every kernel is launched on it, in call order.
+ * - Return value: KVC_OK (0) or a negative KVC_ERR_* code. Every argument is
+ *   checked on the host BEFORE the first launch, so a call that returns an
+ *   argument error has launched nothing and changed nothing.
+ * - Conditions only the GPU can see (a per-head budget below prefix+recent,
+ *   a query-buffer count out of range, a malformed kept-index list) are
+ *   reported by OR-ing KVC_STATUS_* bits into `*status`, a caller-owned int32
+ *   in device memory (may be NULL to ignore them). The affected head is left
+ *   exactly as it was; the others proceed.
+ * - Layout: dense, no paging. One layer of the cache is [B, Hkv, ncap, D]
+ *   contiguous in the storage type; head (b, h) of layer l starts at element
+ *   ((b*Hkv + h) * ncap) * D of K[l] / V[l], and its first N tokens are valid.
+ *   Query head hq belongs to KV head hq / (Hq/Hkv) (contiguous groups).
+ *   Per-head arrays ("[L,B,Hkv]") are flat in (l, b, h) order.
+ * - Supported: storage KVC_BF16 with D in {64, 128}, KVC_F32 with D in
+ *   {64, 128}; Hq % Hkv == 0; L <= KVC_MAX_LAYERS.
+ */
+#ifndef KVC_H_
+#define KVC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVC_ABI_VERSION 1
+#define KVC_MAX_LAYERS 128
+
+#if defined(__GNUC__)
+#define KVC_API __attribute__((visibility("default")))
+#else
+#define KVC_API
+#endif
+
+typedef enum { KVC_BF16 = 0, KVC_F32 = 1 } kvc_dtype;
+
+enum {
+  KVC_OK = 0,
+  KVC_ERR_INVALID_ARG = -1,          /* null pointer, non-positive size, inconsistent sizes */
+  KVC_ERR_UNSUPPORTED_DTYPE = -2,
+  KVC_ERR_UNSUPPORTED_HEAD_DIM = -3, /* D not in {64, 128} */
+  KVC_ERR_BUDGET_RANGE = -4,         /* uniform budget < prefix + recent */
+  KVC_ERR_NOT_DIVISIBLE = -5,        /* Hq % Hkv != 0, or an odd FPS buffer size */
+  KVC_ERR_LAUNCH = -6,               /* a CUDA launch or attribute call failed */
+  KVC_ERR_WORKSPACE = -7,            /* workspace missing or smaller than *_workspace_size() */
+  KVC_ERR_ALIGNMENT = -8,            /* a device pointer is not 16-byte aligned */
+  KVC_ERR_TOO_LARGE = -9             /* a size exceeds what the kernels index with 32 bits */
+};
+
+/* Bits OR-ed into the optional device status word. */
+#define KVC_STATUS_BUDGET_RANGE 0x1u /* a per-head budget < prefix + recent: head kept whole */
+#define KVC_STATUS_COUNT_RANGE 0x2u  /* a query-buffer count < 0 or > qmax: head left alone */
+#define KVC_STATUS_BAD_INDEX 0x4u    /* kvc_compact: kept list not strictly increasing in [k, N) */
+
+/* One KV cache: every layer's K and V. */
+typedef struct {
+  int32_t dtype;   /* kvc_dtype of K and V */
+  int32_t L;       /* layers */
+  int32_t B;       /* sequences */
+  int32_t Hq;      /* query heads per layer */
+  int32_t Hkv;     /* KV heads per layer */
+  int32_t D;       /* head dimension */
+  int32_t N;       /* tokens currently cached in every head (== B_max at the trigger) */
+  int32_t pad_;    /* must be 0 */
+  int64_t ncap;    /* token capacity of every head, >= N (the head stride is ncap*D elements) */
+  void* const* K;  /* host array of L device pointers, 16-byte aligned, one per layer */
+  void* const* V;  /* host array of L device pointers, 16-byte aligned, one per layer */
+} kvc_cache;
+
+/*
+ * kvc_fps_update -- continual farthest-point compression of the beacon buffer.
+ * BeaconKV write-up, "Continual FPS：有界内存的在线最远点采样": every attention
+ * head keeps a bounded buffer of pre-RoPE queries; when it reaches B_Q^max it is
+ * cut back to B_Q^min by farthest-point sampling.
+ *
+ * For every query head whose count equals qmax: normalise the qmax buffered
+ * queries, start from the oldest (row 0), repeatedly add the candidate whose
+ * cosine distance 1 - cos to the chosen set is largest (ties to the lower row)
+ * until qmax/2 are chosen, move the chosen rows to the buffer's front in their
+ * original (time) order and set count to qmax/2. Heads with count < qmax are
+ * untouched; count > qmax or < 0 sets KVC_STATUS_COUNT_RANGE and leaves the head.
+ *
+ *   dtype        kvc_dtype of qbuf
+ *   L, B, Hq, D  sizes; qbuf is [L,B,Hq,qmax,D] (device, in/out), count is
+ *                [L,B,Hq] int32 (device, in/out)
+ *   qmax         buffer capacity, even, 2..64
+ *   picks        [L,B,Hq,qmax/2] int32 (device, out, may be NULL): the old row
+ *                index of each survivor, ascending; -1 rows for heads left alone
+ *   status       device int32 or NULL
+ */
+KVC_API int kvc_fps_update(int32_t dtype, int32_t L, int32_t B, int32_t Hq, int32_t D, void* qbuf, int32_t qmax,
+                   int32_t* count, int32_t* picks, int32_t* status, void* stream);
+
+/*
+ * kvc_score -- importance of every cached key from the observation queries.
+ * BeaconKV write-up, "观察 query 集 = 最近查询 + 信标查询" and "打分时的 RoPE 对齐":
+ * the observation set is the recent queries at their own positions plus beacon
+ * queries rotated to the current step t; a key's importance is the max over the
+ * observation set of its attention weight, so one beacon that cares is enough.
+ *
+ * Per KV head (l, b, h), the observation rows are, for each of its G = Hq/Hkv
+ * query heads: the n_r recent queries as given (post-RoPE), then its beacons.
+ * The beacons are the buffer's first count rows when count <= n_b, else the
+ * farthest-point choice of n_b of them (as kvc_fps_update, buffer unchanged),
+ * each rotated to position t (rotate-half pairs (i, i+D/2), angle
+ * t * theta^(-2i/D), cos/sin in fp64) and rounded to the storage type. Then
+ *     scores[j] = max over rows r of exp(s_rj - lse_r),  s_rj = q_r . k_j / sqrt(D),
+ *     lse_r = log sum_{j<N} exp(s_rj),
+ * over all N cached keys, in fp32 with fp32 accumulation.
+ *
+ *   c            the cache (K read only; V unused)
+ *   q_recent     [L,B,Hq,n_r,D] storage type (device), n_r in 0..64
+ *   qbuf, count  as kvc_fps_update (device, read only); qmax in 0..64
+ *   n_b          beacons per query head, 0..qmax; n_r + n_b >= 1
+ *   t, rope_theta  current step and rotary base (theta > 1)
+ *   scores       [L,B,Hkv,N] fp32 (device, out)
+ *   beacon_picks [L,B,Hq,n_b] int32 (device, out, may be NULL): buffer rows used
+ *                as beacons, ascending, -1 padded
+ *   workspace    device scratch of at least kvc_score_workspace_size() bytes,
+ *                256-byte aligned; contents on entry do not matter
+ */
+KVC_API size_t kvc_score_workspace_size(const kvc_cache* c, int32_t n_r, int32_t n_b);
+KVC_API int kvc_score(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf, const int32_t* count,
+              int32_t qmax, int32_t n_b, int64_t t, double rope_theta, float* scores, int32_t* beacon_picks,
+              void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * kvc_select -- which tokens each head keeps.
+ * BeaconKV write-up, end of "打分时的 RoPE 对齐": prefix tokens and the most
+ * recent tokens are always kept and the rest of the budget is filled by top
+ * score; "实验": on reaching B_KV^max the cache drops to 7/8 B_KV^max. ReasonAlloc
+ * note, "Core Mechanism": the budget may differ per head.
+ *
+ * Per head with budget b (the head's total kept count): if b >= N keep all;
+ * else keep [0, prefix), [N-recent, N) and the b - prefix - recent highest
+ * scores of [prefix, N-recent), equal scores going to the lower index.
+ * kept_idx receives the kept token indices in ascending order.
+ *
+ *   scores       [L,B,Hkv,N] fp32 (device); compared as IEEE bit patterns (>= 0)
+ *   budget       [L,B,Hkv] int32 (device) or NULL to use budget_all for all heads;
+ *                an entry < prefix + recent sets KVC_STATUS_BUDGET_RANGE and
+ *                keeps that head whole
+ *   kept_idx     [L,B,Hkv,N] int32 (device, out); entries past kept_len are not written
+ *   kept_len     [L,B,Hkv] int32 (device, out)
+ */
+KVC_API int kvc_select(const float* scores, int32_t L, int32_t B, int32_t Hkv, int32_t N, int32_t prefix, int32_t recent,
+               const int32_t* budget, int32_t budget_all, int32_t* kept_idx, int32_t* kept_len, int32_t* status,
+               void* stream);
+
+/*
+ * kvc_compact -- move the kept tokens' K and V rows to the head's front, in
+ * their original order, in place. The kept tokens of the BeaconKV write-up's
+ * policy stay; evicted slots are reused. Rows past kept_len keep their old bytes.
+ *
+ *   kept_idx, kept_len   as produced by kvc_select (device). Each head's list is
+ *                checked first (strictly increasing, kept_idx[k] in [k, N),
+ *                kept_len <= N); a bad list sets KVC_STATUS_BAD_INDEX and that
+ *                head is not touched.
+ * The caller then treats head h's length as kept_len[h].
+ */
+KVC_API int kvc_compact(const kvc_cache* c, const int32_t* kept_idx, const int32_t* kept_len, int32_t* status,
+                void* stream);
+
+/*
+ * kvc_evict -- the whole eviction step: beacons, scores, selection and
+ * compaction for every (l, b, h) of the cache, on one stream. Equivalent to
+ * kvc_score, kvc_select and kvc_compact in sequence (same arguments); the
+ * intermediate arrays live in the workspace unless the caller asks for them.
+ *
+ *   scores       [L,B,Hkv,N] fp32 (device, out) or NULL
+ *   kept_idx     [L,B,Hkv,N] int32 (device, out) or NULL
+ *   kept_len     [L,B,Hkv] int32 (device, out), required
+ *   workspace    at least kvc_evict_workspace_size() bytes, 256-byte aligned
+ */
+KVC_API size_t kvc_evict_workspace_size(const kvc_cache* c, int32_t n_r, int32_t n_b);
+KVC_API int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf, const int32_t* count,
+              int32_t qmax, int32_t n_b, int64_t t, double rope_theta, int32_t prefix, int32_t recent,
+              const int32_t* budget, int32_t budget_all, int32_t* kept_idx, int32_t* kept_len, float* scores,
+              int32_t* status, void* workspace, size_t ws_bytes, void* stream);
+
+/* Number of kernels one kvc_evict call with these arguments launches (host only;
+ * for accounting, e.g. counting launches inside a timed region). */
+KVC_API int kvc_evict_launch_count(const kvc_cache* c, int32_t n_r, int32_t n_b);
+
+/* Human-readable text for a KVC_ERR_* code (static storage). */
+KVC_API const char* kvc_strerror(int code);
+
+/* KVC_ABI_VERSION of the loaded library. */
+KVC_API int kvc_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H_ */

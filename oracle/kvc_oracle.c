@@ -22,7 +22,9 @@
  *              the current step t, recent queries keep their own positions.
  *              Rotate-half pairing (i, i + D/2), frequency theta^(-2i/D).
  *              Rotated beacons are rounded to the cache's storage type before
- *              the dot products (the kernels multiply storage-type operands).
+ *              the dot products (the kernels multiply storage-type operands);
+ *              that rounding is a quantisation decision, so the rotation that
+ *              feeds it is done in binary32 like the kernels (oracle_rope_f32).
  *   score      BeaconKV page, same section: score_j = max over observation
  *              queries r of softmax_r(q_r . k_j / sqrt(D)) over all cached keys;
  *              the max also runs over the query heads sharing KV head h.
@@ -36,8 +38,9 @@
  *              front (out-of-place gather here); slots past the kept count keep
  *              their old contents.
  *
- * Arithmetic is fp64 throughout; stored values are rounded once, at the end,
- * to the storage type (bf16 round-to-nearest-even, or fp32).
+ * Arithmetic is fp64 throughout except the beacon rotation above; stored
+ * values are rounded once, at the end, to the storage type (bf16
+ * round-to-nearest-even, or fp32).
  */
 #include <math.h>
 #include <stdint.h>
@@ -221,6 +224,24 @@ void oracle_rope_f64(const double* x, int D, long long pos, double theta, double
   }
 }
 
+/* The beacon rotation that feeds a rounding to the storage type. Rounding a
+ * rotated beacon to bf16 is a quantisation decision, so it is taken in the
+ * kernels' precision: cos/sin of the fp64 angle rounded once to binary32, then
+ * each product and the difference/sum rounded to binary32 (no fused
+ * multiply-add; the file is compiled with -ffp-contract=off). */
+void oracle_rope_f32(const float* x, int D, long long pos, double theta, float* y) {
+  int h = D / 2;
+  for (int i = 0; i < h; ++i) {
+    double inv_freq = pow(theta, -2.0 * (double)i / (double)D);
+    double ang = (double)pos * inv_freq;
+    float c = (float)cos(ang), s = (float)sin(ang);
+    float a = x[i], b = x[i + h];
+    float ac = a * c, bs = b * s, bc = b * c, as = a * s;
+    y[i] = ac - bs;
+    y[i + h] = bc + as;
+  }
+}
+
 /* ------------------------------------------------------------------------- */
 /* Scores (BeaconKV page, "打分时的 RoPE 对齐", the max aggregation).            */
 /* ------------------------------------------------------------------------- */
@@ -374,7 +395,8 @@ static void evict_head(const oracle_problem* p, const oracle_outputs* o, int64_t
   float* scf = (float*)malloc(sizeof(float) * (size_t)N);
   int32_t* kept = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
   int* rows = (int*)malloc(sizeof(int) * (size_t)(p->qmax > 0 ? p->qmax : 1));
-  double* tmp = (double*)malloc(sizeof(double) * (size_t)D);
+  float* tmp = (float*)malloc(sizeof(float) * (size_t)D);
+  float* rot = (float*)malloc(sizeof(float) * (size_t)D);
 
   /* observation rows: for each query head of the group, its recent queries as
    * stored, then its beacons rotated to step t and rounded to storage type */
@@ -389,9 +411,9 @@ static void evict_head(const oracle_problem* p, const oracle_outputs* o, int64_t
     if (o->beacon_picks)
       for (int kk = 0; kk < p->n_b; ++kk) o->beacon_picks[qh * p->n_b + kk] = kk < nb ? rows[kk] : -1;
     for (int kk = 0; kk < nb; ++kk, ++M) {
-      for (int d = 0; d < D; ++d) tmp[d] = load_elem(p->qbuf, p->dtype, (qh * p->qmax + rows[kk]) * D + d);
-      oracle_rope_f64(tmp, D, (long long)p->t, p->theta, &q[(int64_t)M * D]);
-      for (int d = 0; d < D; ++d) q[(int64_t)M * D + d] = round_to_storage(q[(int64_t)M * D + d], p->dtype);
+      for (int d = 0; d < D; ++d) tmp[d] = (float)load_elem(p->qbuf, p->dtype, (qh * p->qmax + rows[kk]) * D + d);
+      oracle_rope_f32(tmp, D, (long long)p->t, p->theta, rot);
+      for (int d = 0; d < D; ++d) q[(int64_t)M * D + d] = round_to_storage((double)rot[d], p->dtype);
     }
   }
   const int64_t kbase = head * (int64_t)N * D;
@@ -417,7 +439,7 @@ static void evict_head(const oracle_problem* p, const oracle_outputs* o, int64_t
   if (o->V_out)
     for (int j = 0; j < len; ++j)
       for (int d = 0; d < D; ++d) store_elem(o->V_out, p->dtype, kbase + (int64_t)j * D + d, p->V, kbase + (int64_t)kept[j] * D + d);
-  free(q); free(k); free(sc); free(scf); free(kept); free(rows); free(tmp);
+  free(q); free(k); free(sc); free(scf); free(kept); free(rows); free(tmp); free(rot);
 }
 
 /* The eviction step for every (l, b, h_kv). K_out / V_out must already hold a

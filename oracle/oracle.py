@@ -26,7 +26,8 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc (portable flags: it must build on x86 and Arm alike)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
+        subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-o", tmp,
+                        _SRC, "-lm"],
                        check=True)
         os.replace(tmp, _LIB)
     return _LIB
@@ -60,6 +61,8 @@ def lib():
         L.oracle_fps_check_f64.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_double]
         L.oracle_rope_f64.restype = None
         L.oracle_rope_f64.argtypes = [C.c_void_p, C.c_int, C.c_longlong, C.c_double, C.c_void_p]
+        L.oracle_rope_f32.restype = None
+        L.oracle_rope_f32.argtypes = [C.c_void_p, C.c_int, C.c_longlong, C.c_double, C.c_void_p]
         L.oracle_score_f64.restype = None
         L.oracle_score_f64.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         L.oracle_select.restype = C.c_int
@@ -126,6 +129,17 @@ def rope(x, pos: int, theta: float) -> np.ndarray:
     flat_out = out.reshape(-1, x.shape[-1])
     for i in range(flat_in.shape[0]):
         lib().oracle_rope_f64(_ptr(flat_in[i]), x.shape[-1], int(pos), float(theta), _ptr(flat_out[i]))
+    return out
+
+
+def rope_f32(x, pos: int, theta: float) -> np.ndarray:
+    """The binary32 beacon rotation (the one whose result is rounded to the storage type)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    flat_in = x.reshape(-1, x.shape[-1])
+    flat_out = out.reshape(-1, x.shape[-1])
+    for i in range(flat_in.shape[0]):
+        lib().oracle_rope_f32(_ptr(flat_in[i]), x.shape[-1], int(pos), float(theta), _ptr(flat_out[i]))
     return out
 
 

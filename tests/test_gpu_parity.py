@@ -1,0 +1,181 @@
+"""Parity of the CUDA path (called through the C ABI) with the CPU oracle, element by element.
+
+Sizes are small enough for the oracle to finish in seconds yet span several key chunks
+with a ragged tail; the full-size workloads are checked on sampled heads in
+test_gpu_fullsize.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+from decoding_kv_cache_gb300.inputs import make_inputs
+from oracle import oracle as O
+from parity_util import (assert_scores_close, check_beacon_picks, check_compaction, check_kept, run_evict,
+                         run_score, storage_to_f64)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+CASES = [
+    ("tiny", {}),
+    ("tiny", dict(N=1000, D=128)),
+    ("qwen3-4b", dict(L=2, N=1000)),
+    ("qwen3-4b", dict(L=1, N=129, D=64)),
+    ("llama8b-planted", dict(L=1, B=2, N=700)),
+    ("qwen7b-reasonalloc", dict(L=2, B=2, N=1500)),
+    ("qwen3-14b-long", dict(L=1, B=1, N=2100)),
+]
+
+
+def _ids(c):
+    return f"{c[0]}-" + "-".join(f"{k}{v}" for k, v in c[1].items())
+
+
+@pytest.mark.parametrize("name,over", CASES, ids=[_ids(c) for c in CASES])
+def test_evict_matches_oracle(name, over):
+    inp = make_inputs(name, **over)
+    gpu = run_evict(inp, DEV)
+    _, gpu_picks = run_score(inp, DEV)
+    ora = O.evict(inp)
+    if check_beacon_picks(inp, gpu_picks, ora["beacon_picks"]):
+        ora = O.evict(inp, forced_picks=gpu_picks)  # a valid near-tie alternative: score with the GPU's beacons
+    assert gpu["status"] == 0
+    assert_scores_close(gpu["scores"], ora["scores"], name)
+    check_kept(inp, gpu, ora, gpu["scores"])
+    check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
+
+
+@pytest.mark.parametrize("count", [0, 1, 10, 16, 17, 31, 32])
+def test_beacon_count_rules(count):
+    """count <= n_b uses the buffer as is; more runs FPS down to n_b (non-destructively)."""
+    inp = make_inputs("qwen3-4b", L=1, N=300, count=count)
+    scores, picks = run_score(inp, DEV)
+    ora = O.evict(inp)
+    if check_beacon_picks(inp, picks, ora["beacon_picks"]):
+        ora = O.evict(inp, forced_picks=picks)
+    assert_scores_close(scores, ora["scores"], f"count={count}")
+
+
+def test_recent_only_observation():
+    """n_b = 0: scores come from the recent queries alone (the RPC-style observation set)."""
+    inp = make_inputs("qwen3-4b", L=1, N=500, n_b=0)
+    gpu = run_evict(inp, DEV)
+    ora = O.evict(inp)
+    assert_scores_close(gpu["scores"], ora["scores"], "n_b=0")
+    check_kept(inp, gpu, ora, gpu["scores"])
+
+
+def test_beacons_only_observation():
+    inp = make_inputs("qwen3-4b", L=1, N=500, n_r=0)
+    gpu = run_evict(inp, DEV)
+    _, picks = run_score(inp, DEV)
+    ora = O.evict(inp)
+    if check_beacon_picks(inp, picks, ora["beacon_picks"]):
+        ora = O.evict(inp, forced_picks=picks)
+    assert_scores_close(gpu["scores"], ora["scores"], "n_r=0")
+
+
+@pytest.mark.parametrize("keep", [20, 21, 299, 300, 301])
+def test_budget_edges(keep):
+    """budget == prefix + recent keeps no middle key; budget >= N keeps everything."""
+    inp = make_inputs("qwen3-4b", L=1, N=300, keep=keep)
+    gpu = run_evict(inp, DEV)
+    ora = O.evict(inp)
+    assert_scores_close(gpu["scores"], ora["scores"], f"keep={keep}")
+    check_kept(inp, gpu, ora, gpu["scores"])
+    check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
+
+
+def test_per_head_budget_out_of_range_is_flagged_and_left_whole():
+    inp = make_inputs("qwen7b-reasonalloc", L=2, B=1, N=400)
+    b = inp.budgets().clone()
+    b[0, 0, 1] = 5     # < prefix + recent
+    b[1, 0, 3] = 400   # == N
+    inp.budget = b
+    gpu = run_evict(inp, DEV)
+    ora = O.evict(inp)
+    assert gpu["status"] & 0x1
+    assert gpu["kept_len"][0, 0, 1] == 400 and gpu["kept_len"][1, 0, 3] == 400
+    check_kept(inp, gpu, ora, gpu["scores"])
+    check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
+
+
+def test_tiny_cache_shorter_than_windows():
+    inp = make_inputs("qwen3-4b", L=1, N=12, keep=10)  # prefix + recent (20) > N: everything is kept
+    gpu = run_evict(inp, DEV)
+    assert (gpu["kept_len"] == 12).all()
+
+
+@pytest.mark.parametrize("dtype,D,qmax", [("f32", 64, 32), ("bf16", 128, 32), ("bf16", 128, 64), ("bf16", 64, 16)])
+def test_fps_update_matches_oracle(dtype, D, qmax):
+    from decoding_kv_cache_gb300 import kvc
+    g = torch.Generator().manual_seed(D + qmax)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    nq = 96
+    qb = torch.randn((nq, qmax, D), generator=g).to(dt)
+    cnt = torch.full((nq,), qmax, dtype=torch.int32)
+    cnt[5] = qmax // 2   # not full: untouched
+    cnt[7] = qmax + 3    # out of range: flagged, untouched
+    bits = qb.view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else qb.numpy()
+    ob, oc, op = O.fps_update(bits, cnt.numpy(), qmax, dtype)
+    qd, cd = qb.to(DEV), cnt.to(DEV)
+    picks = torch.full((nq, qmax // 2), -7, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvc.kvc_fps_update(qd, cd, picks=picks, status=status)
+    torch.cuda.synchronize()
+    gp = picks.cpu().numpy()
+    assert int(status.item()) & 0x2
+    assert np.array_equal(cd.cpu().numpy(), oc)
+    out = qd.cpu()
+    for h in range(nq):
+        if oc[h] != qmax // 2 or cnt[h] != qmax:
+            assert (gp[h] == -1).all() and torch.equal(out[h], qb[h])
+            continue
+        if not np.array_equal(gp[h], op[h]):
+            assert O.fps_check(storage_to_f64(qb[h]), gp[h], 1e-5) == 0
+        assert torch.equal(out[h, :qmax // 2], qb[h, torch.from_numpy(gp[h].astype(np.int64))])
+        assert torch.equal(out[h, qmax // 2:], qb[h, qmax // 2:])
+
+
+def test_select_matches_oracle_on_the_same_scores():
+    """Selection is exact given the scores: the GPU and the oracle agree bit for bit, including
+    many exact ties (quantised scores) and the empty middle."""
+    from decoding_kv_cache_gb300 import kvc
+    g = torch.Generator().manual_seed(5)
+    L, B, Hkv, N, P, R = 3, 2, 4, 3000, 4, 16
+    sc = (torch.randint(0, 50, (L, B, Hkv, N), generator=g).float() / 64.0)
+    sc[0] = torch.rand((B, Hkv, N), generator=g)
+    bud = torch.randint(P + R, N + 50, (L, B, Hkv), generator=g, dtype=torch.int32)
+    bud[1, 0, 0] = P + R
+    kept_idx = torch.full((L, B, Hkv, N), -7, dtype=torch.int32, device=DEV)
+    kept_len = torch.zeros((L, B, Hkv), dtype=torch.int32, device=DEV)
+    kvc.kvc_select(sc.to(DEV), P, R, kept_idx, kept_len, budget=bud.to(DEV))
+    torch.cuda.synchronize()
+    ki, kl = kept_idx.cpu().numpy(), kept_len.cpu().numpy()
+    for l in range(L):
+        for b in range(B):
+            for h in range(Hkv):
+                ref = O.select(sc[l, b, h].numpy(), P, R, int(bud[l, b, h]))
+                assert kl[l, b, h] == len(ref)
+                assert np.array_equal(ki[l, b, h, :len(ref)], ref)
+
+
+def test_compact_rejects_malformed_lists():
+    from decoding_kv_cache_gb300 import kvc
+    inp = make_inputs("qwen3-4b", L=1, N=256)
+    g = inp.to(DEV)
+    cache = kvc.Cache(g.K, g.V, g.Hq)
+    ki = torch.arange(256, dtype=torch.int32).repeat(1, 1, 8, 1).contiguous()
+    kl = torch.full((1, 1, 8), 200, dtype=torch.int32)
+    ki[0, 0, 0, 10] = 9       # not increasing
+    ki[0, 0, 1, 5:] += 60     # runs past N
+    kl[0, 0, 2] = 300         # longer than N
+    ki[0, 0, 3, :200] = torch.arange(56, 256)  # a valid shift
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvc.kvc_compact(cache, ki.to(DEV), kl.to(DEV), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0x4
+    K = g.K.cpu()
+    for h in (0, 1, 2):
+        assert torch.equal(K[0, 0, h], inp.K[0, 0, h])
+    assert torch.equal(K[0, 0, 3, :200], inp.K[0, 0, 3, 56:256])

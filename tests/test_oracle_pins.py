@@ -293,6 +293,27 @@ def _np_rotate(x, pos, theta):
     return np.concatenate([z.real, z.imag], axis=-1)
 
 
+def _np_rotate_f32(x, pos, theta):
+    """The same rotation in binary32 numpy arithmetic: fp64 angle, cos/sin rounded to f32, then
+    separately rounded f32 products and sums (numpy never fuses them)."""
+    D = x.shape[-1]
+    h = D // 2
+    ang = pos * theta ** (-2.0 * np.arange(h) / D)
+    c, s = np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+    a, b = x[..., :h].astype(np.float32), x[..., h:].astype(np.float32)
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def test_rope_f32_matches_f64_rotation_to_single_precision():
+    rng = np.random.default_rng(21)
+    for D, pos, theta in ((2, 3, 1e4), (64, 255, 1e4), (128, 32767, 1e6), (128, 4095, 5e5)):
+        x = rng.standard_normal((6, D)).astype(np.float32)
+        r32 = O.rope_f32(x, pos, theta)
+        r64 = O.rope(x.astype(np.float64), pos, theta)
+        assert np.allclose(r32, r64, rtol=0, atol=4e-6 * np.abs(x).max())
+        assert np.array_equal(r32, _np_rotate_f32(x, pos, theta))
+
+
 def _to_f64(t):
     return t.double().numpy()
 
@@ -311,11 +332,11 @@ def _restated_scores(inp, picks):
                     rows.append(_to_f64(inp.q_recent[l, b, hq]))
                     sel = [r for r in picks[l, b, hq] if r >= 0]
                     if sel:
-                        rot = _np_rotate(_to_f64(inp.qbuf[l, b, hq, sel]), inp.t, inp.theta)
-                        if inp.dtype == "bf16":  # direct f64 -> bf16 rounding (pinned above); torch goes via f32
-                            rows.append(O.bf16_bits_to_f64(O.f64_to_bf16_bits(rot)))
+                        rot = _np_rotate_f32(inp.qbuf[l, b, hq, sel].float().numpy(), inp.t, inp.theta)
+                        if inp.dtype == "bf16":  # f32 -> bf16 rounding with torch (round to nearest even)
+                            rows.append(torch.from_numpy(rot).to(torch.bfloat16).double().numpy())
                         else:
-                            rows.append(rot.astype(np.float32).astype(np.float64))
+                            rows.append(rot.astype(np.float64))
                 Q = torch.from_numpy(np.concatenate(rows))
                 Kh = inp.K[l, b, h].double()
                 out[l, b, h] = torch.softmax(Q @ Kh.T / math.sqrt(D), -1).amax(0).numpy()
