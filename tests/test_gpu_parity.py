@@ -101,9 +101,16 @@ def test_per_head_budget_out_of_range_is_flagged_and_left_whole():
 
 
 def test_tiny_cache_shorter_than_windows():
-    inp = make_inputs("qwen3-4b", L=1, N=12, keep=10)  # prefix + recent (20) > N: everything is kept
+    """N = 12 < prefix + recent = 20: a budget >= N keeps everything, a smaller one cannot hold
+    the always-kept windows and is rejected before any launch (as the oracle rejects it)."""
+    from decoding_kv_cache_gb300 import kvc
+    inp = make_inputs("qwen3-4b", L=1, N=12, keep=12)
     gpu = run_evict(inp, DEV)
     assert (gpu["kept_len"] == 12).all()
+    assert O.evict(make_inputs("qwen3-4b", L=1, N=12, keep=10))["error"].min() == -1
+    with pytest.raises(kvc.KvcError) as e:
+        run_evict(make_inputs("qwen3-4b", L=1, N=12, keep=10), DEV)
+    assert e.value.code == -4
 
 
 @pytest.mark.parametrize("dtype,D,qmax", [("f32", 64, 32), ("bf16", 128, 32), ("bf16", 128, 64), ("bf16", 64, 16)])
