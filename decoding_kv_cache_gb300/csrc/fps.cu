@@ -28,13 +28,14 @@ __global__ void fps_update_kernel(T* __restrict__ qbuf, int nheads, int D, int q
       for (int k = lane; k < m; k += kWarp) picks_out[(size_t)qh * m + k] = -1;
     return;
   }
-  fps_warp(x, qmax, D, m, xs, pk);
-  // Survivors to the front in time order. pk is ascending with pk[k] >= k, so row k is only
-  // ever the source of an earlier-or-equal k: a forward copy never clobbers a pending source.
+  stage_rows(x, qmax, D, xs);
+  fps_staged(xs, qmax, D, m, pk);
+  // Survivors to the front in time order, written back from the staged copy (the fp32 copy
+  // holds every storage value exactly, so the bytes are unchanged).
   for (int k = 0; k < m; ++k) {
     const int src = pk[k];
     if (src != k)
-      for (int d = lane; d < D; d += kWarp) x[(size_t)k * D + d] = x[(size_t)src * D + d];
+      for (int d = lane; d < D; d += kWarp) x[(size_t)k * D + d] = from_f32<T>(xs[src * (D + 1) + d]);
   }
   __syncwarp();
   if (lane == 0) count[qh] = m;

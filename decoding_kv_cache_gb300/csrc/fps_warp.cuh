@@ -4,49 +4,71 @@
 // m mutually most dissimilar points of the buffer. Here: cosine distance 1 - cos on the
 // (pre-RoPE) rows, start from the oldest row (index 0), each step adds the candidate with
 // the largest distance to the chosen set, ties to the lower row. Distances are fp32.
+// A query head's buffer is staged once into shared memory; everything after reads it there.
 #pragma once
 
 #include "kvc_internal.cuh"
 
 namespace kvc {
 
-// Rows of x (global, storage type T, row length D, n <= 64 rows) are normalised into the
-// warp's shared scratch xs[n][D+1] (the +1 keeps lane-per-row reads conflict-free). Lane l
-// owns candidates l and l+32. On return picks[0..m) (warp-shared) holds the chosen rows in
-// ascending order. All 32 lanes must call it.
+// Stage rows [0, n) of x (global, storage type T, row length D) into the warp's shared
+// scratch xs[n][D+1] as fp32 with coalesced 16-byte loads (the +1 keeps lane-per-row reads
+// conflict-free). Requires D % 8 == 0 and a 16-byte aligned x.
 template <typename T>
-__device__ void fps_warp(const T* __restrict__ x, int n, int D, int m, float* xs, int* picks) {
+__device__ __forceinline__ void stage_rows(const T* __restrict__ x, int n, int D, float* xs) {
   const int lane = threadIdx.x & 31;
-  const int ld = D + 1;
-  for (int i = 0; i < n; ++i) {
-    float ss = 0.f;
-    for (int d = lane; d < D; d += kWarp) {
-      const float v = to_f32(x[(size_t)i * D + d]);
-      xs[i * ld + d] = v;
-      ss = fmaf(v, v, ss);
-    }
-    ss = warp_sum(ss);
-    const float inv = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;  // a zero row stays zero: distance 1 to all
-    for (int d = lane; d < D; d += kWarp) xs[i * ld + d] *= inv;
+  constexpr int per = 16 / sizeof(T);
+  const int vpr = D / per;
+  const uint4* src = reinterpret_cast<const uint4*>(x);
+  for (int e = lane; e < n * vpr; e += kWarp) {
+    const uint4 v = src[e];
+    const int r = e / vpr, c0 = (e % vpr) * per;
+    const T* t = reinterpret_cast<const T*>(&v);
+#pragma unroll
+    for (int q = 0; q < per; ++q) xs[r * (D + 1) + c0 + q] = to_f32(t[q]);
   }
   __syncwarp();
+}
 
-  auto dist = [&](int i, int j) {
+// Greedy FPS over the n <= 64 rows already staged in xs[n][D+1] (fp32, unnormalised):
+// m picks, written ascending to picks[0..m) (warp-shared). Lane l owns candidates l and
+// l+32; cosine distances use per-row inverse norms (a zero row has inverse norm 0, which
+// puts it at distance 1 from everything). All 32 lanes must call it.
+__device__ __forceinline__ void fps_staged(const float* xs, int n, int D, int m, int* picks) {
+  const int lane = threadIdx.x & 31;
+  const int ld = D + 1;
+  float inv[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int i = lane + kWarp * c;
+    float ss = 0.f;
+    if (i < n)
+      for (int d = 0; d < D; ++d) ss = fmaf(xs[i * ld + d], xs[i * ld + d], ss);
+    inv[c] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+  }
+  // inverse norm of the row just chosen, fetched from its owning lane
+  auto inv_of = [&](int j) {
+    const float a = __shfl_sync(kFull, inv[0], j & 31);
+    const float b = __shfl_sync(kFull, inv[1], j & 31);
+    return j < kWarp ? a : b;
+  };
+  auto dist = [&](int c, int i, int j, float invj) {
     float s = 0.f;
     const float* a = xs + i * ld;
     const float* b = xs + j * ld;
     for (int d = 0; d < D; ++d) s = fmaf(a[d], b[d], s);
-    return 1.f - s;
+    return 1.f - s * inv[c] * invj;
   };
 
   float md[2];
   bool live[2], chosen[2];
+  const float inv0 = inv_of(0);
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     const int i = lane + kWarp * c;
     live[c] = i < n;
     chosen[c] = (i == 0);
-    const float d0 = live[c] ? dist(i, 0) : -INFINITY;
+    const float d0 = live[c] ? dist(c, i, 0, inv0) : -INFINITY;
     md[c] = d0 == d0 ? d0 : -INFINITY;  // a NaN row can still be picked last, never out of range
   }
   for (int k = 1; k < m; ++k) {
@@ -69,11 +91,12 @@ __device__ void fps_warp(const T* __restrict__ x, int n, int D, int m, float* xs
         bi = oi;
       }
     }
+    const float invj = inv_of(bi);
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int i = lane + kWarp * c;
       if (i == bi) chosen[c] = true;
-      if (live[c] && !chosen[c]) md[c] = fminf(md[c], dist(i, bi));
+      if (live[c] && !chosen[c]) md[c] = fminf(md[c], dist(c, i, bi, invj));
     }
   }
   // ascending output: position = number of chosen rows below this one

@@ -89,9 +89,13 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
     const int hq = h * G + g;
     const size_t qh = ((size_t)l * B + b) * Hq + hq;
     T* orow = obs + (size_t)g * per_q * D;
-    // recent queries: already rotated to their own positions, used as stored
-    const T* qr = qrec + qh * a.n_r * D;
-    for (int e = lane; e < a.n_r * D; e += kWarp) orow[e] = qr[e];
+    // recent queries: already rotated to their own positions, copied as stored (16-byte vectors)
+    {
+      const uint4* qr = reinterpret_cast<const uint4*>(qrec + qh * a.n_r * D);
+      uint4* od = reinterpret_cast<uint4*>(orow);
+      const int nv = a.n_r * D * (int)sizeof(T) / 16;
+      for (int e = lane; e < nv; e += kWarp) od[e] = qr[e];
+    }
     for (int r = lane; r < a.n_r; r += kWarp) valid[g * per_q + r] = 1;
     // beacons: the buffer itself when it holds at most n_b rows, else FPS down to n_b
     int c = a.qmax > 0 ? a.count[qh] : 0;
@@ -99,23 +103,23 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
       if (lane == 0) status_or(a.status, KVC_STATUS_COUNT_RANGE);
       c = c < 0 ? 0 : a.qmax;
     }
+    stage_rows(qbuf + qh * a.qmax * D, c, D, xs);
     int nb;
-    const T* xb = qbuf + qh * a.qmax * D;
     if (c <= a.n_b) {
       nb = c;
       for (int k = lane; k < nb; k += kWarp) pk[k] = k;
       __syncwarp();
     } else {
       nb = a.n_b;
-      fps_warp(xb, c, D, nb, xs, pk);
+      fps_staged(xs, c, D, nb, pk);
     }
     for (int k = 0; k < a.n_b; ++k) {
       T* dst = orow + (size_t)(a.n_r + k) * D;
       if (k < nb) {
-        const T* src = xb + (size_t)pk[k] * D;
+        const float* src = xs + pk[k] * (D + 1);
         for (int i = lane; i < hd; i += kWarp) {
           const float2 cs = ws.rope[i];
-          const float x0 = to_f32(src[i]), x1 = to_f32(src[i + hd]);
+          const float x0 = src[i], x1 = src[i + hd];
           // each product and the sum rounded separately (no fused multiply-add), so the
           // rounding to the storage type below is a reproducible decision
           dst[i] = from_f32<T>(__fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y)));
