@@ -73,7 +73,8 @@ void fill_score_args(ScoreArgs* a, const CacheGeom& g, int dtype, const LayerPtr
   a->beacon_picks = beacon_picks;
   a->status = status;
   a->M = (g.Hq / g.Hkv) * (n_r + n_b);
-  a->M_pad = (a->M + 15) / 16 * 16;
+  a->M_pad = obs_rows(a->M, dtype);
+  a->M_n = (a->M + 15) / 16 * 16;
   a->nchunk = (g.N + kChunk - 1) / kChunk;
 }
 

@@ -72,8 +72,10 @@ struct ScoreArgs {
   float* scores;
   int32_t* beacon_picks;
   int32_t* status;
-  int M, M_pad, nchunk;
+  int M, M_pad, M_n, nchunk;  // rows, rows stored per head, rows rounded to 16, key chunks
 };
+
+int obs_rows(int M, int dtype);
 
 size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, ScoreWs* carve, void* base);
 int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s);

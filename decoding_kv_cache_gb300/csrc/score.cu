@@ -16,45 +16,13 @@
 //   pass2        per (key chunk, head): recompute S^T = K Q^T, max over rows of
 //                s*log2(e)/sqrt(D) - lse2, exp2 -> score                        (chunks x heads)
 // Softmax is kept in base 2 throughout: exp(s/sqrt(D) - lse) = exp2(s*c2 - lse2).
+#include <cudaTypedefs.h>
+
 #include "fps_warp.cuh"
 #include "kvc_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace kvc {
-
-// ---------------------------------------------------------------------------
-// small PTX helpers (legacy warp-level tensor path: ldmatrix + mma.sync)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(a));
-}
-
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem));
-}
-__device__ __forceinline__ void cp_async_commit_wait_all() {
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
-}
-
-__device__ __forceinline__ float quad_max(float v) {
-  v = fmaxf(v, __shfl_xor_sync(kFull, v, 1));
-  return fmaxf(v, __shfl_xor_sync(kFull, v, 2));
-}
-__device__ __forceinline__ float quad_sum(float v) {
-  v += __shfl_xor_sync(kFull, v, 1);
-  return v + __shfl_xor_sync(kFull, v, 2);
-}
 
 // ---------------------------------------------------------------------------
 // rotary table and observation rows
@@ -140,22 +108,15 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
 }
 
 // ---------------------------------------------------------------------------
-// bf16 passes (mma.sync m16n8k16, fp32 accumulate)
+// bf16 passes on the 5th-generation tensor cores (tcgen05.mma, accumulators in TMEM)
+//
+// Shared memory holds the observation tile Q [D/64][M_pad rows][128 B] and one key chunk
+// K [D/64][128 rows][128 B], both written by TMA in the 128-byte-swizzled K-major layout the
+// UMMA descriptors read. Pass 1 computes S = Q K^T (TMEM lane = observation row, column =
+// key), so each epilogue thread owns one row and folds its chunk max and exp2-sum in
+// registers. Pass 2 computes S^T = K Q^T (lane = key, column = row), so each thread owns one
+// key and takes the max over rows in registers.
 // ---------------------------------------------------------------------------
-template <int D>
-__device__ __forceinline__ void load_rows_bf16(__nv_bfloat16* sm, const __nv_bfloat16* g, int rows, int valid_rows) {
-  constexpr int VPR = D / 8;
-  constexpr int LDS = D + 8;
-  for (int e = threadIdx.x; e < rows * VPR; e += blockDim.x) {
-    const int r = e / VPR, c = e % VPR;
-    __nv_bfloat16* dst = sm + r * LDS + c * 8;
-    if (r < valid_rows)
-      cp_async16(dst, g + (size_t)r * D + c * 8);
-    else
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
 struct HeadLoc {
   int l, bh;
 };
@@ -163,122 +124,168 @@ __device__ __forceinline__ HeadLoc head_loc(const CacheGeom& g, int head) {
   return HeadLoc{head / (g.B * g.Hkv), head % (g.B * g.Hkv)};
 }
 
+struct TcMaps {
+  CUtensorMap k[KVC_MAX_LAYERS];  // per layer: dims {D, ncap, B*Hkv}, box {64, 128, 1}
+  CUtensorMap q;                  // observation rows: dims {D, heads*M_pad}, box {64, 128}
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~(uintptr_t)1023);
+}
+
+// Load the observation tile and key chunk with TMA, wait, and (thread 0) issue the MMAs.
+// Returns the shared flag telling every thread whether the accumulator will arrive.
 template <int D>
-__global__ void __launch_bounds__(128) pass1_bf16_kernel(ScoreArgs a, ScoreWs ws, float c2) {
-  extern __shared__ __align__(16) unsigned char smraw[];
-  constexpr int LDS = D + 8;
-  __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smraw);
-  __nv_bfloat16* Ks = Qs + a.M_pad * LDS;
-  const int chunk = blockIdx.x, head = blockIdx.y;
-  const HeadLoc hl = head_loc(a.g, head);
-  const __nv_bfloat16* Kh = static_cast<const __nv_bfloat16*>(a.K.p[hl.l]) + (size_t)hl.bh * a.g.ncap * D;
-  const int j0 = chunk * kChunk;
-  const int nvalid = min(kChunk, a.g.N - j0);
-  load_rows_bf16<D>(Qs, static_cast<const __nv_bfloat16*>(ws.obs) + (size_t)head * a.M_pad * D, a.M_pad, a.M_pad);
-  load_rows_bf16<D>(Ks, Kh + (size_t)j0 * D, kChunk, nvalid);
-  cp_async_commit_wait_all();
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int mt = warp; mt < a.M_pad / 16; mt += 4) {
-    uint32_t af[D / 16][4];
+__device__ __forceinline__ bool tc_load_and_mma(const TcMaps& maps, const ScoreArgs& a, int head, const HeadLoc& hl,
+                                                int j0, uint8_t* Qs, uint8_t* Ks, uint64_t* bars, uint32_t tmem,
+                                                int pass, int* s_ok) {
+  constexpr int HALVES = D / 64;
+  const int MT = a.M_pad >> 7;
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    tc::mbar_expect_tx(&bars[0], (uint32_t)((a.M_pad + kChunk) * D * 2));
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) ldsm_x4(af[ks], Qs + (mt * 16 + (lane & 15)) * LDS + ks * 16 + (lane >> 4) * 8);
-    float acc[kChunk / 8][4];
-#pragma unroll
-    for (int nt = 0; nt < kChunk / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-#pragma unroll
-    for (int np = 0; np < kChunk / 16; ++np) {
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t bf[4];
-        ldsm_x4(bf, Ks + (np * 16 + ((lane >> 4) << 3) + (lane & 7)) * LDS + ks * 16 + ((lane >> 3) & 1) * 8);
-        mma_bf16_16816(acc[2 * np], af[ks], bf[0], bf[1]);
-        mma_bf16_16816(acc[2 * np + 1], af[ks], bf[2], bf[3]);
-      }
+    for (int h = 0; h < HALVES; ++h) {
+      for (int mt = 0; mt < MT; ++mt)
+        tc::tma_load_2d(Qs + h * a.M_pad * 128 + mt * 16384, &maps.q, &bars[0], h * 64, head * a.M_pad + mt * 128);
+      tc::tma_load_3d(Ks + h * 16384, &maps.k[hl.l], &bars[0], h * 64, j0, hl.bh);
     }
-    float m0 = -INFINITY, m1 = -INFINITY;
+    if (!tc::mbar_wait(&bars[0], 0)) {
+      ok = 0;
+      status_or(a.status, KVC_STATUS_TIMEOUT);
+      tc::mbar_wait(&bars[0], 0);  // give the copies in flight one more bounded chance to land
+    } else {
+      tc::fence_after_sync();
+      const uint32_t qb = tc::smem_u32(Qs), kb = tc::smem_u32(Ks);
+      if (pass == 1) {  // S[row][key]: A = Q M-tile, B = K chunk
+        const uint32_t idesc = tc::idesc_bf16(128, kChunk);
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int nt = 0; nt < kChunk / 8; ++nt)
+          for (int ks = 0; ks < D / 16; ++ks)
+            tc::umma_bf16(tmem + mt * kChunk,
+                          tc::desc_k_sw128(qb + (ks >> 2) * a.M_pad * 128 + mt * 16384 + (ks & 3) * 32),
+                          tc::desc_k_sw128(kb + (ks >> 2) * 16384 + (ks & 3) * 32), idesc, ks > 0);
+      } else {  // S^T[key][row]: A = K chunk, B = Q (N = M_n rows)
+        const uint32_t idesc = tc::idesc_bf16(128, a.M_n);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const bool ok = nt * 8 + 2 * (lane & 3) + e < nvalid;
-        acc[nt][e] = ok ? acc[nt][e] * c2 : -INFINITY;
-        acc[nt][2 + e] = ok ? acc[nt][2 + e] * c2 : -INFINITY;
-        m0 = fmaxf(m0, acc[nt][e]);
-        m1 = fmaxf(m1, acc[nt][2 + e]);
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc::umma_bf16(tmem, tc::desc_k_sw128(kb + (ks >> 2) * 16384 + (ks & 3) * 32),
+                        tc::desc_k_sw128(qb + (ks >> 2) * a.M_pad * 128 + (ks & 3) * 32), idesc, ks > 0);
       }
-    m0 = quad_max(m0);
-    m1 = quad_max(m1);
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < kChunk / 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        s0 += exp2f(acc[nt][e] - m0);
-        s1 += exp2f(acc[nt][2 + e] - m1);
-      }
-    s0 = quad_sum(s0);
-    s1 = quad_sum(s1);
-    if ((lane & 3) == 0) {
-      float2* part = ws.part + ((size_t)head * a.nchunk + chunk) * a.M_pad;
-      const int r0 = mt * 16 + (lane >> 2);
-      part[r0] = make_float2(m0, s0);
-      part[r0 + 8] = make_float2(m1, s1);
+      tc::umma_commit(&bars[1]);
     }
+    *s_ok = ok;
   }
+  __syncthreads();
+  bool ok = *s_ok != 0;
+  if (ok && !tc::mbar_wait(&bars[1], 0)) {
+    status_or(a.status, KVC_STATUS_TIMEOUT);
+    ok = false;
+  }
+  tc::fence_after_sync();
+  return ok;
 }
 
 template <int D>
-__global__ void __launch_bounds__(128) pass2_bf16_kernel(ScoreArgs a, ScoreWs ws, float c2) {
-  extern __shared__ __align__(16) unsigned char smraw[];
-  constexpr int LDS = D + 8;
-  __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smraw);
-  __nv_bfloat16* Ks = Qs + a.M_pad * LDS;
-  float* L2s = reinterpret_cast<float*>(Ks + kChunk * LDS);
+__global__ void __launch_bounds__(256) pass1_tc_kernel(const __grid_constant__ TcMaps maps, ScoreArgs a, ScoreWs ws,
+                                                       float c2) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* Qs = align1024(smraw);
+  uint8_t* Ks = Qs + (size_t)a.M_pad * D * 2;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(Ks + kChunk * D * 2);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 2);
+  int* s_ok = reinterpret_cast<int*>(slot + 1);
   const int chunk = blockIdx.x, head = blockIdx.y;
   const HeadLoc hl = head_loc(a.g, head);
-  const __nv_bfloat16* Kh = static_cast<const __nv_bfloat16*>(a.K.p[hl.l]) + (size_t)hl.bh * a.g.ncap * D;
   const int j0 = chunk * kChunk;
   const int nvalid = min(kChunk, a.g.N - j0);
-  load_rows_bf16<D>(Qs, static_cast<const __nv_bfloat16*>(ws.obs) + (size_t)head * a.M_pad * D, a.M_pad, a.M_pad);
-  load_rows_bf16<D>(Ks, Kh + (size_t)j0 * D, kChunk, nvalid);
-  for (int r = threadIdx.x; r < a.M_pad; r += blockDim.x) L2s[r] = ws.lse2[(size_t)head * a.M_pad + r];
-  cp_async_commit_wait_all();
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* out = a.scores + (size_t)head * a.g.N + j0;
-  for (int kt = warp; kt < kChunk / 16; kt += 4) {
-    if (kt * 16 >= nvalid) break;
-    uint32_t af[D / 16][4];
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) ldsm_x4(af[ks], Ks + (kt * 16 + (lane & 15)) * LDS + ks * 16 + (lane >> 4) * 8);
-    float b0 = -INFINITY, b1 = -INFINITY;
-    for (int np = 0; np < a.M_pad / 16; ++np) {
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t bf[4];
-        ldsm_x4(bf, Qs + (np * 16 + ((lane >> 4) << 3) + (lane & 7)) * LDS + ks * 16 + ((lane >> 3) & 1) * 8);
-        mma_bf16_16816(acc[0], af[ks], bf[0], bf[1]);
-        mma_bf16_16816(acc[1], af[ks], bf[2], bf[3]);
-      }
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float lb = L2s[np * 16 + t * 8 + 2 * (lane & 3) + e];
-          b0 = fmaxf(b0, acc[t][e] * c2 - lb);
-          b1 = fmaxf(b1, acc[t][2 + e] * c2 - lb);
-        }
-    }
-    b0 = quad_max(b0);
-    b1 = quad_max(b1);
-    if ((lane & 3) == 0) {
-      const int j = kt * 16 + (lane >> 2);
-      if (j < nvalid) out[j] = exp2f(b0);
-      if (j + 8 < nvalid) out[j + 8] = exp2f(b1);
-    }
+  const uint32_t ncols = (uint32_t)(a.M_pad >> 7) * kChunk;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[1], 1);
+    tc::mbar_fence_init();
   }
+  if (warp == 0) tc::tmem_alloc(slot, ncols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *slot;
+  if (tc_load_and_mma<D>(maps, a, head, hl, j0, Qs, Ks, bars, tmem, 1, s_ok)) {
+    const int mt = warp >> 2, q = warp & 3;
+    const int r = mt * 128 + q * 32 + lane;
+    float m = -INFINITY, s = 0.f;
+#pragma unroll 1
+    for (int cs = 0; cs < kChunk / 32; ++cs) {
+      float v[32];
+      tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * kChunk + cs * 32), v);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        v[i] = (cs * 32 + i < nvalid) ? v[i] * c2 : -INFINITY;
+        mx = fmaxf(mx, v[i]);
+      }
+      if (mx > -INFINITY) {
+        const float mn = fmaxf(m, mx);
+        s *= exp2f(m - mn);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s += exp2f(v[i] - mn);
+        m = mn;
+      }
+    }
+    ws.part[((size_t)head * a.nchunk + chunk) * a.M_pad + r] = make_float2(m, s);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, ncols);
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) pass2_tc_kernel(const __grid_constant__ TcMaps maps, ScoreArgs a, ScoreWs ws,
+                                                       float c2) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* Qs = align1024(smraw);
+  uint8_t* Ks = Qs + (size_t)a.M_pad * D * 2;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(Ks + kChunk * D * 2);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 2);
+  int* s_ok = reinterpret_cast<int*>(slot + 1);
+  float* L2s = reinterpret_cast<float*>(slot + 4);
+  const int chunk = blockIdx.x, head = blockIdx.y;
+  const HeadLoc hl = head_loc(a.g, head);
+  const int j0 = chunk * kChunk;
+  const int nvalid = min(kChunk, a.g.N - j0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ncols = a.M_n <= 128 ? 128u : 256u;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[1], 1);
+    tc::mbar_fence_init();
+  }
+  for (int r = threadIdx.x; r < a.M_pad; r += blockDim.x) L2s[r] = ws.lse2[(size_t)head * a.M_pad + r];
+  if (warp == 0) tc::tmem_alloc(slot, ncols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *slot;
+  if (tc_load_and_mma<D>(maps, a, head, hl, j0, Qs, Ks, bars, tmem, 2, s_ok)) {
+    const int key = warp * 32 + lane;
+    float best = -INFINITY;
+    const int nslice = (a.M_n + 31) >> 5;
+#pragma unroll 1
+    for (int cs = 0; cs < nslice; ++cs) {
+      float v[32];
+      tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cs * 32), v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int r = cs * 32 + i;
+        if (r < a.M_n) best = fmaxf(best, v[i] * c2 - L2s[r]);
+      }
+    }
+    if (key < nvalid) a.scores[(size_t)head * a.g.N + j0 + key] = exp2f(best);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, ncols);
 }
 
 // ---------------------------------------------------------------------------
@@ -368,12 +375,53 @@ __global__ void combine_kernel(ScoreArgs a, ScoreWs ws) {
 // ---------------------------------------------------------------------------
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+int obs_rows(int M, int dtype) {
+  if (dtype == KVC_BF16) return M <= 128 ? 128 : 256;  // whole 128-row MMA tiles
+  return (M + 15) / 16 * 16;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;  // resolved once from the driver
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+static bool encode_maps(TcMaps* m, const ScoreArgs& a, const ScoreWs& ws) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const int D = a.g.D;
+  const cuuint32_t es[3] = {1, 1, 1};
+  for (int l = 0; l < a.g.L; ++l) {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.g.ncap, (cuuint64_t)a.g.B * a.g.Hkv};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.g.ncap * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kChunk, 1};
+    if (enc(&m->k[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.K.p[l], dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  const int heads = a.g.L * a.g.B * a.g.Hkv;
+  const cuuint64_t qdims[2] = {(cuuint64_t)D, (cuuint64_t)heads * a.M_pad};
+  const cuuint64_t qstrides[1] = {(cuuint64_t)D * 2};
+  const cuuint32_t qbox[2] = {64, 128};
+  return enc(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws.obs, qdims, qstrides, qbox, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, ScoreWs* carve, void* base) {
   const size_t es = dtype == KVC_BF16 ? 2 : 4;
   const size_t heads = (size_t)g.L * g.B * g.Hkv;
   const int G = g.Hq / g.Hkv;
   const int M = G * (n_r + n_b);
-  const size_t M_pad = (size_t)((M + 15) / 16) * 16;
+  const size_t M_pad = (size_t)obs_rows(M, dtype);
   const size_t nchunk = (size_t)(g.N + kChunk - 1) / kChunk;
   size_t off = 0;
   const size_t o_rope = off;  off += align256(sizeof(float2) * (size_t)(g.D / 2));
@@ -421,22 +469,34 @@ int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s) {
 
   const dim3 grid(a.nchunk, heads);
   if (a.dtype == KVC_BF16) {
-    const size_t sm1 = (size_t)(a.M_pad + kChunk) * (D + 8) * 2;
-    const size_t sm2 = sm1 + (size_t)a.M_pad * 4;
+    TcMaps maps;  // host staging for the kernel parameter (copied at launch)
+    if (!encode_maps(&maps, a, ws)) return KVC_ERR_LAUNCH;
+    const int MT = a.M_pad >> 7;
+    const size_t tail = 64 + (size_t)a.M_pad * 4;  // barriers, TMEM slot, flag, lse2 copy
+    size_t sm = 1024 + (size_t)(a.M_pad + kChunk) * D * 2 + tail;
+    // Never let more CTAs share an SM than its 512 TMEM columns can serve at once: ask for
+    // enough shared memory that one more CTA would not fit.
+    int dev = 0, smem_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+      return KVC_ERR_LAUNCH;
+    const int cols = (a.M_pad > 128 || a.M_n > 128) ? 256 : 128;
+    const size_t floor_sm = (size_t)smem_sm / (size_t)(512 / cols + 1) + 1024;
+    if (sm < floor_sm) sm = floor_sm;
     if (D == 128) {
-      if (!set_smem(pass1_bf16_kernel<128>, sm1) || !set_smem(pass2_bf16_kernel<128>, sm2)) return KVC_ERR_LAUNCH;
-      pass1_bf16_kernel<128><<<grid, 128, sm1, s>>>(a, ws, c2);
+      if (!set_smem(pass1_tc_kernel<128>, sm) || !set_smem(pass2_tc_kernel<128>, sm)) return KVC_ERR_LAUNCH;
+      pass1_tc_kernel<128><<<grid, 128 * MT, sm, s>>>(maps, a, ws, c2);
       if (launch_ok()) return KVC_ERR_LAUNCH;
       combine_kernel<<<heads, (a.M_pad + 31) / 32 * 32, 0, s>>>(a, ws);
       if (launch_ok()) return KVC_ERR_LAUNCH;
-      pass2_bf16_kernel<128><<<grid, 128, sm2, s>>>(a, ws, c2);
+      pass2_tc_kernel<128><<<grid, 128, sm, s>>>(maps, a, ws, c2);
     } else {
-      if (!set_smem(pass1_bf16_kernel<64>, sm1) || !set_smem(pass2_bf16_kernel<64>, sm2)) return KVC_ERR_LAUNCH;
-      pass1_bf16_kernel<64><<<grid, 128, sm1, s>>>(a, ws, c2);
+      if (!set_smem(pass1_tc_kernel<64>, sm) || !set_smem(pass2_tc_kernel<64>, sm)) return KVC_ERR_LAUNCH;
+      pass1_tc_kernel<64><<<grid, 128 * MT, sm, s>>>(maps, a, ws, c2);
       if (launch_ok()) return KVC_ERR_LAUNCH;
       combine_kernel<<<heads, (a.M_pad + 31) / 32 * 32, 0, s>>>(a, ws);
       if (launch_ok()) return KVC_ERR_LAUNCH;
-      pass2_bf16_kernel<64><<<grid, 128, sm2, s>>>(a, ws, c2);
+      pass2_tc_kernel<64><<<grid, 128, sm, s>>>(maps, a, ws, c2);
     }
   } else {
     const size_t sm1 = sizeof(float) * ((size_t)a.M_pad * (D + 1) + (size_t)kChunk * D);

@@ -69,6 +69,7 @@ enum {
 #define KVC_STATUS_BUDGET_RANGE 0x1u /* a per-head budget < prefix + recent: head kept whole */
 #define KVC_STATUS_COUNT_RANGE 0x2u  /* a query-buffer count < 0 or > qmax: head left alone */
 #define KVC_STATUS_BAD_INDEX 0x4u    /* kvc_compact: kept list not strictly increasing in [k, N) */
+#define KVC_STATUS_TIMEOUT 0x8u      /* a bounded device-side wait gave up; that work was skipped */
 
 /* One KV cache: every layer's K and V. */
 typedef struct {
