@@ -75,6 +75,13 @@ void fill_score_args(ScoreArgs* a, const CacheGeom& g, int dtype, const LayerPtr
   a->M = (g.Hq / g.Hkv) * (n_r + n_b);
   a->M_pad = obs_rows(a->M, dtype);
   a->M_n = (a->M + 15) / 16 * 16;
+  // Rotary angles of the current step in fp64 (BeaconKV write-up, "打分时的 RoPE 对齐":
+  // beacons are turned to position t): pair (i, i + D/2) turns by t * theta^(-2i/D).
+  for (int i = 0; i < g.D / 2; ++i) {
+    const double ang = (double)t * pow(theta, -2.0 * (double)i / (double)g.D);
+    a->rope[i] = make_float2((float)cos(ang), (float)sin(ang));
+  }
+  for (int i = g.D / 2; i < 64; ++i) a->rope[i] = make_float2(0.f, 0.f);
   a->nchunk = (g.N + kChunk - 1) / kChunk;
 }
 
@@ -93,7 +100,7 @@ int kvc_evict_launch_count(const kvc_cache* c, int32_t n_r, int32_t n_b) {
   (void)c;
   (void)n_r;
   (void)n_b;
-  return 7;  // rope table, observation rows, pass 1, combine, pass 2, select, compact
+  return 6;  // observation rows, pass 1, combine, pass 2, select, compact
 }
 
 const char* kvc_strerror(int code) {

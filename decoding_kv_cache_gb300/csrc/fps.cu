@@ -8,8 +8,8 @@
 
 namespace kvc {
 
-template <typename T>
-__global__ void fps_update_kernel(T* __restrict__ qbuf, int nheads, int D, int qmax, int32_t* __restrict__ count,
+template <typename T, int D>
+__global__ void fps_update_kernel(T* __restrict__ qbuf, int nheads, int qmax, int32_t* __restrict__ count,
                                   int32_t* __restrict__ picks_out, int32_t* status) {
   extern __shared__ float smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -28,8 +28,8 @@ __global__ void fps_update_kernel(T* __restrict__ qbuf, int nheads, int D, int q
       for (int k = lane; k < m; k += kWarp) picks_out[(size_t)qh * m + k] = -1;
     return;
   }
-  stage_rows(x, qmax, D, xs);
-  fps_staged(xs, qmax, D, m, pk);
+  stage_rows<T, D>(x, qmax, xs);
+  fps_staged<D>(xs, qmax, m, pk);
   // Survivors to the front in time order, written back from the staged copy (the fp32 copy
   // holds every storage value exactly, so the bytes are unchanged).
   for (int k = 0; k < m; ++k) {
@@ -51,17 +51,20 @@ int launch_fps_update(int dtype, int nheads_q, int D, void* qbuf, int qmax, int3
   wpb = wpb < 1 ? 1 : (wpb > 4 ? 4 : wpb);
   const size_t smem = per_warp * wpb;
   const int grid = (nheads_q + wpb - 1) / wpb;
-  if (dtype == KVC_BF16) {
-    auto k = fps_update_kernel<__nv_bfloat16>;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  auto go = [&](auto kernel, auto* typed) -> int {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return KVC_ERR_LAUNCH;
-    k<<<grid, 32 * wpb, smem, s>>>(static_cast<__nv_bfloat16*>(qbuf), nheads_q, D, qmax, count, picks, status);
-  } else {
-    auto k = fps_update_kernel<float>;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return KVC_ERR_LAUNCH;
-    k<<<grid, 32 * wpb, smem, s>>>(static_cast<float*>(qbuf), nheads_q, D, qmax, count, picks, status);
-  }
+    kernel<<<grid, 32 * wpb, smem, s>>>(typed, nheads_q, qmax, count, picks, status);
+    return KVC_OK;
+  };
+  int rc;
+  if (dtype == KVC_BF16)
+    rc = D == 128 ? go(fps_update_kernel<__nv_bfloat16, 128>, static_cast<__nv_bfloat16*>(qbuf))
+                  : go(fps_update_kernel<__nv_bfloat16, 64>, static_cast<__nv_bfloat16*>(qbuf));
+  else
+    rc = D == 128 ? go(fps_update_kernel<float, 128>, static_cast<float*>(qbuf))
+                  : go(fps_update_kernel<float, 64>, static_cast<float*>(qbuf));
+  if (rc) return rc;
   return launch_ok();
 }
 

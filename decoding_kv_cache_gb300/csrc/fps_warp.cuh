@@ -14,11 +14,11 @@ namespace kvc {
 // Stage rows [0, n) of x (global, storage type T, row length D) into the warp's shared
 // scratch xs[n][D+1] as fp32 with coalesced 16-byte loads (the +1 keeps lane-per-row reads
 // conflict-free). Requires D % 8 == 0 and a 16-byte aligned x.
-template <typename T>
-__device__ __forceinline__ void stage_rows(const T* __restrict__ x, int n, int D, float* xs) {
+template <typename T, int D>
+__device__ __forceinline__ void stage_rows(const T* __restrict__ x, int n, float* xs) {
   const int lane = threadIdx.x & 31;
   constexpr int per = 16 / sizeof(T);
-  const int vpr = D / per;
+  constexpr int vpr = D / per;
   const uint4* src = reinterpret_cast<const uint4*>(x);
   for (int e = lane; e < n * vpr; e += kWarp) {
     const uint4 v = src[e];
@@ -30,20 +30,35 @@ __device__ __forceinline__ void stage_rows(const T* __restrict__ x, int n, int D
   __syncwarp();
 }
 
+// Dot product of two staged rows with four independent accumulators (the loads are
+// independent, so the FMA chain is the latency that matters).
+template <int D>
+__device__ __forceinline__ float dot_rows(const float* a, const float* b) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int d = 0; d < D; d += 4) {
+    s0 = fmaf(a[d], b[d], s0);
+    s1 = fmaf(a[d + 1], b[d + 1], s1);
+    s2 = fmaf(a[d + 2], b[d + 2], s2);
+    s3 = fmaf(a[d + 3], b[d + 3], s3);
+  }
+  return (s0 + s1) + (s2 + s3);
+}
+
 // Greedy FPS over the n <= 64 rows already staged in xs[n][D+1] (fp32, unnormalised):
 // m picks, written ascending to picks[0..m) (warp-shared). Lane l owns candidates l and
 // l+32; cosine distances use per-row inverse norms (a zero row has inverse norm 0, which
 // puts it at distance 1 from everything). All 32 lanes must call it.
-__device__ __forceinline__ void fps_staged(const float* xs, int n, int D, int m, int* picks) {
+template <int D>
+__device__ __forceinline__ void fps_staged(const float* xs, int n, int m, int* picks) {
   const int lane = threadIdx.x & 31;
-  const int ld = D + 1;
+  constexpr int ld = D + 1;
   float inv[2];
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     const int i = lane + kWarp * c;
     float ss = 0.f;
-    if (i < n)
-      for (int d = 0; d < D; ++d) ss = fmaf(xs[i * ld + d], xs[i * ld + d], ss);
+    if (i < n) ss = dot_rows<D>(xs + i * ld, xs + i * ld);
     inv[c] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
   }
   // inverse norm of the row just chosen, fetched from its owning lane
@@ -53,11 +68,7 @@ __device__ __forceinline__ void fps_staged(const float* xs, int n, int D, int m,
     return j < kWarp ? a : b;
   };
   auto dist = [&](int c, int i, int j, float invj) {
-    float s = 0.f;
-    const float* a = xs + i * ld;
-    const float* b = xs + j * ld;
-    for (int d = 0; d < D; ++d) s = fmaf(a[d], b[d], s);
-    return 1.f - s * inv[c] * invj;
+    return 1.f - dot_rows<D>(xs + i * ld, xs + j * ld) * inv[c] * invj;
   };
 
   float md[2];

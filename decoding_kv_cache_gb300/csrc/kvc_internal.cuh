@@ -51,7 +51,6 @@ int launch_fps_update(int dtype, int nheads_q, int D, void* qbuf, int qmax, int3
                       int32_t* status, cudaStream_t s);
 
 struct ScoreWs {            // carved out of the caller's workspace
-  float2* rope;             // [D/2] (cos, sin) at step t
   void* obs;                // [heads][M_pad][D] storage type
   uint8_t* valid;           // [heads][M_pad]
   float2* part;             // [heads][nchunk][M_pad] (running max, sum) in base 2
@@ -73,6 +72,7 @@ struct ScoreArgs {
   int32_t* beacon_picks;
   int32_t* status;
   int M, M_pad, M_n, nchunk;  // rows, rows stored per head, rows rounded to 16, key chunks
+  float2 rope[64];            // (cos, sin) of t * theta^(-2i/D), i < D/2, from fp64
 };
 
 int obs_rows(int M, int dtype);

@@ -7,7 +7,7 @@
 // one M x D tile, so the max over the GQA group is the max over that tile's rows.
 //
 // Launch sequence (all on the caller's stream):
-//   rope_table   cos/sin of t * theta^(-2i/D) in fp64, rounded to fp32        (1 CTA)
+//   (host)       cos/sin of t * theta^(-2i/D) in fp64, rounded to fp32, passed as a parameter
 //   build_obs    per KV head: copy recent rows, pick beacons (FPS when the buffer
 //                holds more than n_b), rotate them to t, round to storage type  (heads CTAs)
 //   pass1        per (key chunk, head): S = Q K^T, per-row chunk max and sum of
@@ -27,20 +27,10 @@ namespace kvc {
 // ---------------------------------------------------------------------------
 // rotary table and observation rows
 // ---------------------------------------------------------------------------
-__global__ void rope_table_kernel(float2* rope, int D, long long t, double theta) {
-  const int i = threadIdx.x;
-  if (i >= D / 2) return;
-  const double inv_freq = pow(theta, -2.0 * (double)i / (double)D);
-  const double ang = (double)t * inv_freq;
-  double sn, cs;
-  sincos(ang, &sn, &cs);
-  rope[i] = make_float2((float)cs, (float)sn);
-}
-
-template <typename T>
+template <typename T, int D>
 __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
   extern __shared__ float smem[];
-  const int D = a.g.D, Hkv = a.g.Hkv, B = a.g.B, Hq = a.g.Hq;
+  const int Hkv = a.g.Hkv, B = a.g.B, Hq = a.g.Hq;
   const int head = blockIdx.x;
   const int l = head / (B * Hkv), b = (head / Hkv) % B, h = head % Hkv;
   const int G = Hq / Hkv, per_q = a.n_r + a.n_b, hd = D / 2;
@@ -71,7 +61,7 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
       if (lane == 0) status_or(a.status, KVC_STATUS_COUNT_RANGE);
       c = c < 0 ? 0 : a.qmax;
     }
-    stage_rows(qbuf + qh * a.qmax * D, c, D, xs);
+    stage_rows<T, D>(qbuf + qh * a.qmax * D, c, xs);
     int nb;
     if (c <= a.n_b) {
       nb = c;
@@ -79,14 +69,14 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
       __syncwarp();
     } else {
       nb = a.n_b;
-      fps_staged(xs, c, D, nb, pk);
+      fps_staged<D>(xs, c, nb, pk);
     }
     for (int k = 0; k < a.n_b; ++k) {
       T* dst = orow + (size_t)(a.n_r + k) * D;
       if (k < nb) {
         const float* src = xs + pk[k] * (D + 1);
         for (int i = lane; i < hd; i += kWarp) {
-          const float2 cs = ws.rope[i];
+          const float2 cs = a.rope[i];
           const float x0 = src[i], x1 = src[i + hd];
           // each product and the sum rounded separately (no fused multiply-add), so the
           // rounding to the storage type below is a reproducible decision
@@ -424,14 +414,12 @@ size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, ScoreWs* 
   const size_t M_pad = (size_t)obs_rows(M, dtype);
   const size_t nchunk = (size_t)(g.N + kChunk - 1) / kChunk;
   size_t off = 0;
-  const size_t o_rope = off;  off += align256(sizeof(float2) * (size_t)(g.D / 2));
   const size_t o_obs = off;   off += align256(heads * M_pad * g.D * es);
   const size_t o_valid = off; off += align256(heads * M_pad);
   const size_t o_part = off;  off += align256(heads * nchunk * M_pad * sizeof(float2));
   const size_t o_lse = off;   off += align256(heads * M_pad * sizeof(float));
   if (carve) {
     char* b = static_cast<char*>(base);
-    carve->rope = reinterpret_cast<float2*>(b + o_rope);
     carve->obs = b + o_obs;
     carve->valid = reinterpret_cast<uint8_t*>(b + o_valid);
     carve->part = reinterpret_cast<float2*>(b + o_part);
@@ -449,21 +437,24 @@ int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s) {
   const int heads = a.g.L * a.g.B * a.g.Hkv;
   const int D = a.g.D;
   const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
-  rope_table_kernel<<<1, (D / 2 + 31) / 32 * 32, 0, s>>>(ws.rope, D, a.t, a.theta);
-  if (launch_ok()) return KVC_ERR_LAUNCH;
-
   // observation rows: one warp per query head of the group
   const int G = a.g.Hq / a.g.Hkv;
   const size_t per_warp = sizeof(float) * (size_t)(a.qmax * (D + 1) + a.qmax);
   int nw = G < 8 ? G : 8;
   while (nw > 1 && per_warp * nw > 200u * 1024u) --nw;
   const size_t obs_smem = per_warp * nw;
-  if (a.dtype == KVC_BF16) {
-    if (!set_smem(build_obs_kernel<__nv_bfloat16>, obs_smem)) return KVC_ERR_LAUNCH;
-    build_obs_kernel<__nv_bfloat16><<<heads, 32 * nw, obs_smem, s>>>(a, ws, nw);
-  } else {
-    if (!set_smem(build_obs_kernel<float>, obs_smem)) return KVC_ERR_LAUNCH;
-    build_obs_kernel<float><<<heads, 32 * nw, obs_smem, s>>>(a, ws, nw);
+  {
+    bool ok;
+    if (a.dtype == KVC_BF16) {
+      auto k = D == 128 ? build_obs_kernel<__nv_bfloat16, 128> : build_obs_kernel<__nv_bfloat16, 64>;
+      ok = set_smem(k, obs_smem);
+      if (ok) k<<<heads, 32 * nw, obs_smem, s>>>(a, ws, nw);
+    } else {
+      auto k = D == 128 ? build_obs_kernel<float, 128> : build_obs_kernel<float, 64>;
+      ok = set_smem(k, obs_smem);
+      if (ok) k<<<heads, 32 * nw, obs_smem, s>>>(a, ws, nw);
+    }
+    if (!ok) return KVC_ERR_LAUNCH;
   }
   if (launch_ok()) return KVC_ERR_LAUNCH;
 
