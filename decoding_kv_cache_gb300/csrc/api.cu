@@ -97,10 +97,10 @@ extern "C" {
 int kvc_abi_version(void) { return KVC_ABI_VERSION; }
 
 int kvc_evict_launch_count(const kvc_cache* c, int32_t n_r, int32_t n_b) {
-  (void)c;
   (void)n_r;
   (void)n_b;
-  return 6;  // observation rows, pass 1, combine, pass 2, select, compact
+  if (c && c->dtype == KVC_BF16) return 4;  // observation rows, fused scoring, select, compact
+  return 6;                                  // observation rows, pass 1, combine, pass 2, select, compact
 }
 
 const char* kvc_strerror(int code) {

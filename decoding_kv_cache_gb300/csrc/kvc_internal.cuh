@@ -14,6 +14,7 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kChunk = 128;     // keys per scoring CTA
 constexpr int kMaxRows = 256;   // observation rows per KV head (G * (n_r + n_b), padded to 16)
 constexpr int kMaxQmax = 64;    // FPS buffer capacity
+constexpr int kMaxSMs = 256;    // bound on the SM count used to size the fused kernel's exchange
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---- storage access -------------------------------------------------------
@@ -53,7 +54,7 @@ int launch_fps_update(int dtype, int nheads_q, int D, void* qbuf, int qmax, int3
 struct ScoreWs {            // carved out of the caller's workspace
   void* obs;                // [heads][M_pad][D] storage type
   uint8_t* valid;           // [heads][M_pad]
-  float2* part;             // [heads][nchunk][M_pad] (running max, sum) in base 2
+  float2* part;             // fp32: [heads][nchunk][M_pad] partial (max, sum) in base 2; bf16: fused exchange
   float* lse2;              // [heads][M_pad] log2-sum-exp2, +inf for unused rows
 };
 
@@ -79,6 +80,8 @@ int obs_rows(int M, int dtype);
 
 size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, ScoreWs* carve, void* base);
 int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s);
+size_t fused_xch_bytes(int M_pad);
+int launch_score_fused(const ScoreArgs& a, const ScoreWs& ws, void* xch_base, cudaStream_t s);
 
 int launch_select(const float* scores, int heads, int N, int P, int R, const int32_t* budget, int budget_all,
                   int32_t* kept_idx, int32_t* kept_len, int32_t* status, cudaStream_t s);

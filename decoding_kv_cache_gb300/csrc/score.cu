@@ -10,17 +10,15 @@
 //   (host)       cos/sin of t * theta^(-2i/D) in fp64, rounded to fp32, passed as a parameter
 //   build_obs    per KV head: copy recent rows, pick beacons (FPS when the buffer
 //                holds more than n_b), rotate them to t, round to storage type  (heads CTAs)
-//   pass1        per (key chunk, head): S = Q K^T, per-row chunk max and sum of
-//                exp2, i.e. a partial log-sum-exp                             (chunks x heads)
-//   combine      per head: merge the partials into lse2 per row
-//   pass2        per (key chunk, head): recompute S^T = K Q^T, max over rows of
-//                s*log2(e)/sqrt(D) - lse2, exp2 -> score                        (chunks x heads)
+//   bf16 caches: score_fused (score_fused.cu), both passes on the tensor cores in one
+//                persistent kernel
+//   fp32 caches: pass1 / combine / pass2 below on CUDA cores:
+//     pass1      per (key chunk, head): per-row chunk max and sum of exp2
+//     combine    per head: merge the partials into lse2 per row
+//     pass2      per (key chunk, head): max over rows of s*log2(e)/sqrt(D) - lse2, exp2
 // Softmax is kept in base 2 throughout: exp(s/sqrt(D) - lse) = exp2(s*c2 - lse2).
-#include <cudaTypedefs.h>
-
 #include "fps_warp.cuh"
 #include "kvc_internal.cuh"
-#include "tc_ptx.cuh"
 
 namespace kvc {
 
@@ -29,17 +27,17 @@ namespace kvc {
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
-  extern __shared__ float smem[];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   const int Hkv = a.g.Hkv, B = a.g.B, Hq = a.g.Hq;
   const int head = blockIdx.x;
   const int l = head / (B * Hkv), b = (head / Hkv) % B, h = head % Hkv;
   const int G = Hq / Hkv, per_q = a.n_r + a.n_b, hd = D / 2;
+  constexpr int LD = Staging<T, D>::LD;
   T* obs = static_cast<T*>(ws.obs) + (size_t)head * a.M_pad * D;
   uint8_t* valid = ws.valid + (size_t)head * a.M_pad;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int per = a.qmax * (D + 1) + a.qmax;
-  float* xs = smem + warp * per;
-  int* pk = reinterpret_cast<int*>(xs + a.qmax * (D + 1));
+  const int npad = (a.qmax + 15) & ~15;
+  void* scratch = smem_raw + warp * ((fps_scratch_bytes<T, D>(npad) + 15) & ~(size_t)15);
   const T* qrec = static_cast<const T*>(a.q_recent);
   const T* qbuf = static_cast<const T*>(a.qbuf);
 
@@ -61,23 +59,16 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
       if (lane == 0) status_or(a.status, KVC_STATUS_COUNT_RANGE);
       c = c < 0 ? 0 : a.qmax;
     }
-    stage_rows<T, D>(qbuf + qh * a.qmax * D, c, xs);
-    int nb;
-    if (c <= a.n_b) {
-      nb = c;
-      for (int k = lane; k < nb; k += kWarp) pk[k] = k;
-      __syncwarp();
-    } else {
-      nb = a.n_b;
-      fps_staged<D>(xs, c, nb, pk);
-    }
+    int* pk;
+    const T* xs = fps_buffer<T, D>(qbuf + qh * a.qmax * D, c, a.n_b, npad, scratch, &pk);
+    const int nb = c < a.n_b ? c : a.n_b;
     for (int k = 0; k < a.n_b; ++k) {
       T* dst = orow + (size_t)(a.n_r + k) * D;
       if (k < nb) {
-        const float* src = xs + pk[k] * (D + 1);
+        const T* src = xs + pk[k] * LD;
         for (int i = lane; i < hd; i += kWarp) {
           const float2 cs = a.rope[i];
-          const float x0 = src[i], x1 = src[i + hd];
+          const float x0 = to_f32(src[i]), x1 = to_f32(src[i + hd]);
           // each product and the sum rounded separately (no fused multiply-add), so the
           // rounding to the storage type below is a reproducible decision
           dst[i] = from_f32<T>(__fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y)));
@@ -92,190 +83,16 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
       for (int k = lane; k < a.n_b; k += kWarp) a.beacon_picks[qh * a.n_b + k] = k < nb ? pk[k] : -1;
     __syncwarp();
   }
-  // padding rows up to a multiple of 16
+  // padding rows up to the stored row count
   for (int e = threadIdx.x; e < (a.M_pad - a.M) * D; e += blockDim.x) obs[(size_t)a.M * D + e] = from_f32<T>(0.f);
   for (int r = a.M + threadIdx.x; r < a.M_pad; r += blockDim.x) valid[r] = 0;
 }
 
-// ---------------------------------------------------------------------------
-// bf16 passes on the 5th-generation tensor cores (tcgen05.mma, accumulators in TMEM)
-//
-// Shared memory holds the observation tile Q [D/64][M_pad rows][128 B] and one key chunk
-// K [D/64][128 rows][128 B], both written by TMA in the 128-byte-swizzled K-major layout the
-// UMMA descriptors read. Pass 1 computes S = Q K^T (TMEM lane = observation row, column =
-// key), so each epilogue thread owns one row and folds its chunk max and exp2-sum in
-// registers. Pass 2 computes S^T = K Q^T (lane = key, column = row), so each thread owns one
-// key and takes the max over rows in registers.
-// ---------------------------------------------------------------------------
 struct HeadLoc {
   int l, bh;
 };
 __device__ __forceinline__ HeadLoc head_loc(const CacheGeom& g, int head) {
   return HeadLoc{head / (g.B * g.Hkv), head % (g.B * g.Hkv)};
-}
-
-struct TcMaps {
-  CUtensorMap k[KVC_MAX_LAYERS];  // per layer: dims {D, ncap, B*Hkv}, box {64, 128, 1}
-  CUtensorMap q;                  // observation rows: dims {D, heads*M_pad}, box {64, 128}
-};
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~(uintptr_t)1023);
-}
-
-// Load the observation tile and key chunk with TMA, wait, and (thread 0) issue the MMAs.
-// Returns the shared flag telling every thread whether the accumulator will arrive.
-template <int D>
-__device__ __forceinline__ bool tc_load_and_mma(const TcMaps& maps, const ScoreArgs& a, int head, const HeadLoc& hl,
-                                                int j0, uint8_t* Qs, uint8_t* Ks, uint64_t* bars, uint32_t tmem,
-                                                int pass, int* s_ok) {
-  constexpr int HALVES = D / 64;
-  const int MT = a.M_pad >> 7;
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    tc::mbar_expect_tx(&bars[0], (uint32_t)((a.M_pad + kChunk) * D * 2));
-#pragma unroll
-    for (int h = 0; h < HALVES; ++h) {
-      for (int mt = 0; mt < MT; ++mt)
-        tc::tma_load_2d(Qs + h * a.M_pad * 128 + mt * 16384, &maps.q, &bars[0], h * 64, head * a.M_pad + mt * 128);
-      tc::tma_load_3d(Ks + h * 16384, &maps.k[hl.l], &bars[0], h * 64, j0, hl.bh);
-    }
-    if (!tc::mbar_wait(&bars[0], 0)) {
-      ok = 0;
-      status_or(a.status, KVC_STATUS_TIMEOUT);
-      tc::mbar_wait(&bars[0], 0);  // give the copies in flight one more bounded chance to land
-    } else {
-      tc::fence_after_sync();
-      const uint32_t qb = tc::smem_u32(Qs), kb = tc::smem_u32(Ks);
-      if (pass == 1) {  // S[row][key]: A = Q M-tile, B = K chunk
-        const uint32_t idesc = tc::idesc_bf16(128, kChunk);
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            tc::umma_bf16(tmem + mt * kChunk,
-                          tc::desc_k_sw128(qb + (ks >> 2) * a.M_pad * 128 + mt * 16384 + (ks & 3) * 32),
-                          tc::desc_k_sw128(kb + (ks >> 2) * 16384 + (ks & 3) * 32), idesc, ks > 0);
-      } else {  // S^T[key][row]: A = K chunk, B = Q (N = M_n rows)
-        const uint32_t idesc = tc::idesc_bf16(128, a.M_n);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          tc::umma_bf16(tmem, tc::desc_k_sw128(kb + (ks >> 2) * 16384 + (ks & 3) * 32),
-                        tc::desc_k_sw128(qb + (ks >> 2) * a.M_pad * 128 + (ks & 3) * 32), idesc, ks > 0);
-      }
-      tc::umma_commit(&bars[1]);
-    }
-    *s_ok = ok;
-  }
-  __syncthreads();
-  bool ok = *s_ok != 0;
-  if (ok && !tc::mbar_wait(&bars[1], 0)) {
-    status_or(a.status, KVC_STATUS_TIMEOUT);
-    ok = false;
-  }
-  tc::fence_after_sync();
-  return ok;
-}
-
-template <int D>
-__global__ void __launch_bounds__(256) pass1_tc_kernel(const __grid_constant__ TcMaps maps, ScoreArgs a, ScoreWs ws,
-                                                       float c2) {
-  extern __shared__ uint8_t smraw[];
-  uint8_t* Qs = align1024(smraw);
-  uint8_t* Ks = Qs + (size_t)a.M_pad * D * 2;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(Ks + kChunk * D * 2);
-  uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 2);
-  int* s_ok = reinterpret_cast<int*>(slot + 1);
-  const int chunk = blockIdx.x, head = blockIdx.y;
-  const HeadLoc hl = head_loc(a.g, head);
-  const int j0 = chunk * kChunk;
-  const int nvalid = min(kChunk, a.g.N - j0);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t ncols = (uint32_t)(a.M_pad >> 7) * kChunk;
-  if (threadIdx.x == 0) {
-    tc::mbar_init(&bars[0], 1);
-    tc::mbar_init(&bars[1], 1);
-    tc::mbar_fence_init();
-  }
-  if (warp == 0) tc::tmem_alloc(slot, ncols);
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *slot;
-  if (tc_load_and_mma<D>(maps, a, head, hl, j0, Qs, Ks, bars, tmem, 1, s_ok)) {
-    const int mt = warp >> 2, q = warp & 3;
-    const int r = mt * 128 + q * 32 + lane;
-    float m = -INFINITY, s = 0.f;
-#pragma unroll 1
-    for (int cs = 0; cs < kChunk / 32; ++cs) {
-      float v[32];
-      tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * kChunk + cs * 32), v);
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        v[i] = (cs * 32 + i < nvalid) ? v[i] * c2 : -INFINITY;
-        mx = fmaxf(mx, v[i]);
-      }
-      if (mx > -INFINITY) {
-        const float mn = fmaxf(m, mx);
-        s *= exp2f(m - mn);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s += exp2f(v[i] - mn);
-        m = mn;
-      }
-    }
-    ws.part[((size_t)head * a.nchunk + chunk) * a.M_pad + r] = make_float2(m, s);
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, ncols);
-}
-
-template <int D>
-__global__ void __launch_bounds__(128) pass2_tc_kernel(const __grid_constant__ TcMaps maps, ScoreArgs a, ScoreWs ws,
-                                                       float c2) {
-  extern __shared__ uint8_t smraw[];
-  uint8_t* Qs = align1024(smraw);
-  uint8_t* Ks = Qs + (size_t)a.M_pad * D * 2;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(Ks + kChunk * D * 2);
-  uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 2);
-  int* s_ok = reinterpret_cast<int*>(slot + 1);
-  float* L2s = reinterpret_cast<float*>(slot + 4);
-  const int chunk = blockIdx.x, head = blockIdx.y;
-  const HeadLoc hl = head_loc(a.g, head);
-  const int j0 = chunk * kChunk;
-  const int nvalid = min(kChunk, a.g.N - j0);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t ncols = a.M_n <= 128 ? 128u : 256u;
-  if (threadIdx.x == 0) {
-    tc::mbar_init(&bars[0], 1);
-    tc::mbar_init(&bars[1], 1);
-    tc::mbar_fence_init();
-  }
-  for (int r = threadIdx.x; r < a.M_pad; r += blockDim.x) L2s[r] = ws.lse2[(size_t)head * a.M_pad + r];
-  if (warp == 0) tc::tmem_alloc(slot, ncols);
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *slot;
-  if (tc_load_and_mma<D>(maps, a, head, hl, j0, Qs, Ks, bars, tmem, 2, s_ok)) {
-    const int key = warp * 32 + lane;
-    float best = -INFINITY;
-    const int nslice = (a.M_n + 31) >> 5;
-#pragma unroll 1
-    for (int cs = 0; cs < nslice; ++cs) {
-      float v[32];
-      tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cs * 32), v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int r = cs * 32 + i;
-        if (r < a.M_n) best = fmaxf(best, v[i] * c2 - L2s[r]);
-      }
-    }
-    if (key < nvalid) a.scores[(size_t)head * a.g.N + j0 + key] = exp2f(best);
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, ncols);
 }
 
 // ---------------------------------------------------------------------------
@@ -370,42 +187,6 @@ int obs_rows(int M, int dtype) {
   return (M + 15) / 16 * 16;
 }
 
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;  // resolved once from the driver
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-static bool encode_maps(TcMaps* m, const ScoreArgs& a, const ScoreWs& ws) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  const int D = a.g.D;
-  const cuuint32_t es[3] = {1, 1, 1};
-  for (int l = 0; l < a.g.L; ++l) {
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.g.ncap, (cuuint64_t)a.g.B * a.g.Hkv};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.g.ncap * D * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kChunk, 1};
-    if (enc(&m->k[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.K.p[l], dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return false;
-  }
-  const int heads = a.g.L * a.g.B * a.g.Hkv;
-  const cuuint64_t qdims[2] = {(cuuint64_t)D, (cuuint64_t)heads * a.M_pad};
-  const cuuint64_t qstrides[1] = {(cuuint64_t)D * 2};
-  const cuuint32_t qbox[2] = {64, 128};
-  return enc(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws.obs, qdims, qstrides, qbox, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, ScoreWs* carve, void* base) {
   const size_t es = dtype == KVC_BF16 ? 2 : 4;
   const size_t heads = (size_t)g.L * g.B * g.Hkv;
@@ -416,7 +197,9 @@ size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, ScoreWs* 
   size_t off = 0;
   const size_t o_obs = off;   off += align256(heads * M_pad * g.D * es);
   const size_t o_valid = off; off += align256(heads * M_pad);
-  const size_t o_part = off;  off += align256(heads * nchunk * M_pad * sizeof(float2));
+  // fp32 caches keep per-chunk partials; bf16 caches exchange per-range partials in the fused kernel
+  const size_t part_bytes = dtype == KVC_BF16 ? fused_xch_bytes((int)M_pad) : heads * nchunk * M_pad * sizeof(float2);
+  const size_t o_part = off;  off += align256(part_bytes);
   const size_t o_lse = off;   off += align256(heads * M_pad * sizeof(float));
   if (carve) {
     char* b = static_cast<char*>(base);
@@ -439,7 +222,11 @@ int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s) {
   const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
   // observation rows: one warp per query head of the group
   const int G = a.g.Hq / a.g.Hkv;
-  const size_t per_warp = sizeof(float) * (size_t)(a.qmax * (D + 1) + a.qmax);
+  const int npad = (a.qmax + 15) & ~15;
+  const size_t raw = a.dtype == KVC_BF16
+                         ? (D == 128 ? fps_scratch_bytes<__nv_bfloat16, 128>(npad) : fps_scratch_bytes<__nv_bfloat16, 64>(npad))
+                         : (D == 128 ? fps_scratch_bytes<float, 128>(npad) : fps_scratch_bytes<float, 64>(npad));
+  const size_t per_warp = (raw + 15) & ~(size_t)15;
   int nw = G < 8 ? G : 8;
   while (nw > 1 && per_warp * nw > 200u * 1024u) --nw;
   const size_t obs_smem = per_warp * nw;
@@ -460,35 +247,7 @@ int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s) {
 
   const dim3 grid(a.nchunk, heads);
   if (a.dtype == KVC_BF16) {
-    TcMaps maps;  // host staging for the kernel parameter (copied at launch)
-    if (!encode_maps(&maps, a, ws)) return KVC_ERR_LAUNCH;
-    const int MT = a.M_pad >> 7;
-    const size_t tail = 64 + (size_t)a.M_pad * 4;  // barriers, TMEM slot, flag, lse2 copy
-    size_t sm = 1024 + (size_t)(a.M_pad + kChunk) * D * 2 + tail;
-    // Never let more CTAs share an SM than its 512 TMEM columns can serve at once: ask for
-    // enough shared memory that one more CTA would not fit.
-    int dev = 0, smem_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
-      return KVC_ERR_LAUNCH;
-    const int cols = (a.M_pad > 128 || a.M_n > 128) ? 256 : 128;
-    const size_t floor_sm = (size_t)smem_sm / (size_t)(512 / cols + 1) + 1024;
-    if (sm < floor_sm) sm = floor_sm;
-    if (D == 128) {
-      if (!set_smem(pass1_tc_kernel<128>, sm) || !set_smem(pass2_tc_kernel<128>, sm)) return KVC_ERR_LAUNCH;
-      pass1_tc_kernel<128><<<grid, 128 * MT, sm, s>>>(maps, a, ws, c2);
-      if (launch_ok()) return KVC_ERR_LAUNCH;
-      combine_kernel<<<heads, (a.M_pad + 31) / 32 * 32, 0, s>>>(a, ws);
-      if (launch_ok()) return KVC_ERR_LAUNCH;
-      pass2_tc_kernel<128><<<grid, 128, sm, s>>>(maps, a, ws, c2);
-    } else {
-      if (!set_smem(pass1_tc_kernel<64>, sm) || !set_smem(pass2_tc_kernel<64>, sm)) return KVC_ERR_LAUNCH;
-      pass1_tc_kernel<64><<<grid, 128 * MT, sm, s>>>(maps, a, ws, c2);
-      if (launch_ok()) return KVC_ERR_LAUNCH;
-      combine_kernel<<<heads, (a.M_pad + 31) / 32 * 32, 0, s>>>(a, ws);
-      if (launch_ok()) return KVC_ERR_LAUNCH;
-      pass2_tc_kernel<64><<<grid, 128, sm, s>>>(maps, a, ws, c2);
-    }
+    return launch_score_fused(a, ws, ws.part, s);
   } else {
     const size_t sm1 = sizeof(float) * ((size_t)a.M_pad * (D + 1) + (size_t)kChunk * D);
     const size_t sm2 = sizeof(float) * ((size_t)a.M_pad * D + (size_t)kChunk * (D + 1) + a.M_pad);

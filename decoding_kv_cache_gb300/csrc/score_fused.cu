@@ -1,0 +1,467 @@
+// score_fused.cu -- the bf16 scoring passes as one persistent, warp-specialised kernel.
+//
+// What it computes is kvc_score's definition (BeaconKV write-up, "打分时的 RoPE 对齐": a key's
+// importance is the max over the observation rows of its softmax weight over all cached keys).
+// The softmax needs each row's log-sum-exp over ALL keys before any score can be formed, so
+// the keys are visited twice: pass 1 folds (max, sum of exp2) per row, pass 2 recomputes the
+// logits and takes the max over rows of exp2(s*c2 - lse2).
+//
+// Work split. A head's keys are cut into G_s contiguous ranges of whole 128-key chunks, one
+// per CTA of a "group"; the grid is (#groups x G_s) CTAs, one per SM, launched cooperatively so
+// every CTA is resident. Group g handles heads g, g + #groups, ... in rounds. In a round a CTA
+// runs pass 1 over its range, publishes its per-row partials, waits (bounded) for the rest of
+// its group, merges the partials into lse2, and runs pass 2 over the same range. Pass 2's TMA
+// reads find the range in L2: it was read moments before and at most one range per SM
+// (~256 KB) is live at a time.
+//
+// Roles inside a CTA (all derive the same chunk sequence from blockIdx, so no queue is needed):
+//   warp 0      TMA producer: the round's observation tile Q into one of two Q buffers, then
+//               each key chunk of pass 1 and again of pass 2 into a ring of K stages.
+//   warp 1      tcgen05.mma issuer (one thread) with two 256-column TMEM accumulators: pass 1
+//               S = Q K^T (lane = row), pass 2 S^T = K Q^T (lane = key).
+//   warps 2-9   epilogue: pass 1 keeps each row's running (max, sum) in registers (two warps
+//               per TMEM lane quarter split the columns); pass 2 keeps each key's running max.
+// Barriers: kfull/kempty per K stage, qfull/qempty per Q buffer, tfull/tempty per accumulator.
+// Every wait is bounded; a wait that gives up sets KVC_STATUS_TIMEOUT and a CTA-wide abort
+// flag, after which every role skips its work but still passes every named barrier.
+#include <cudaTypedefs.h>
+
+#include "kvc_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace kvc {
+
+constexpr int kEpiWarps = 8;
+constexpr int kFusedThreads = 64 + 32 * kEpiWarps;
+constexpr uint32_t kAccCols = 256;  // one TMEM accumulator (two of them: 512 columns)
+
+struct FusedMaps {
+  CUtensorMap k[KVC_MAX_LAYERS];  // per layer: dims {D, ncap, B*Hkv}, box {64, 128, 1}
+  CUtensorMap q;                  // observation rows: dims {D, heads*M_pad}, box {64, 128}
+};
+
+struct FusedPlan {
+  int group_size;      // CTAs per head
+  int ngroups;         // heads processed at once
+  int chunks_per_cta;  // key chunks per CTA per head
+  int stages;          // K ring depth
+  int qbytes;          // one observation tile: M_pad * D * 2
+};
+
+struct FusedXch {
+  float2* part;      // [2][ngroups][group_size][M_pad] per-row (max, sum) of each range, by round parity
+  unsigned* arrive;  // [ngroups] monotone arrival counters, zero at launch
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~(uintptr_t)1023);
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;\n" ::"n"(32 * kEpiWarps) : "memory"); }
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// mbarrier wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              int32_t* status) {
+  for (int round = 0; round < 64; ++round) {
+    if (*abort_flag) return false;
+    if (tc::mbar_wait(bar, parity, 1u << 18)) return true;
+  }
+  *abort_flag = 1;
+  status_or(status, KVC_STATUS_TIMEOUT);
+  return false;
+}
+
+// Tree reductions over a 32-value slice: five dependent steps instead of 32.
+__device__ __forceinline__ float tree_max32(const float (&x)[32]) {
+  float a[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = fmaxf(x[i], x[i + 16]);
+#pragma unroll
+  for (int w = 8; w; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) a[i] = fmaxf(a[i], a[i + w]);
+  return a[0];
+}
+__device__ __forceinline__ float tree_sum32(const float (&x)[32]) {
+  float a[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = x[i] + x[i + 16];
+#pragma unroll
+  for (int w = 8; w; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) a[i] += a[i + w];
+  return a[0];
+}
+
+// merge two (max, sum-of-exp2) states
+__device__ __forceinline__ float2 lse_merge(float2 x, float2 y) {
+  if (y.y <= 0.f) return x;
+  if (x.y <= 0.f) return y;
+  const float m = fmaxf(x.x, y.x);
+  return make_float2(m, x.y * exp2f(x.x - m) + y.y * exp2f(y.x - m));
+}
+
+template <int D, int MT>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    score_fused_kernel(const __grid_constant__ FusedMaps maps, ScoreArgs a, ScoreWs ws, FusedPlan p, FusedXch xch,
+                       float c2) {
+  constexpr int HALVES = D / 64;
+  constexpr int kStage = kChunk * D * 2;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* Qs = align1024(smraw);
+  uint8_t* Ks = Qs + 2 * p.qbytes;
+  const int S = p.stages;
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(Ks + S * kStage);
+  uint64_t* kempty = kfull + S;
+  uint64_t* qfull = kempty + S;
+  uint64_t* qempty = qfull + 2;
+  uint64_t* tfull = qempty + 2;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 1);
+  float* lse2s = reinterpret_cast<float*>(Ks + S * kStage + 512);  // [kMaxRows], 16-byte aligned
+  float2* merge = reinterpret_cast<float2*>(lse2s + kMaxRows);  // [kMaxRows]
+  float* pbest = reinterpret_cast<float*>(merge + kMaxRows);    // [2][kChunk]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&kfull[i], 1);
+      tc::mbar_init(&kempty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&qfull[i], 1);
+      tc::mbar_init(&qempty[i], 1);
+      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tempty[i], kEpiWarps);
+    }
+    *abort_flag = 0;
+    tc::mbar_fence_init();
+  }
+  if (warp == 1) tc::tmem_alloc(slot, 2 * kAccCols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *slot;
+
+  const int heads = a.g.L * a.g.B * a.g.Hkv;
+  const int group = blockIdx.x / p.group_size, rank = blockIdx.x % p.group_size;
+  const int c0 = rank * p.chunks_per_cta;
+  const int c1 = min(c0 + p.chunks_per_cta, a.nchunk);
+  const int qrow_bytes = a.M_pad * 128;  // one 64-column half of an observation tile
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t kc = 0;
+      for (int round = 0; !*abort_flag; ++round) {
+        const int head = group + round * p.ngroups;
+        if (head >= heads) break;
+        const int l = head / (a.g.B * a.g.Hkv), bh = head % (a.g.B * a.g.Hkv);
+        const int qb = round & 1;
+        if (round >= 2 && !wait_or_abort(&qempty[qb], ((round - 2) >> 1) & 1, abort_flag, a.status)) break;
+        uint8_t* qdst = Qs + qb * p.qbytes;
+        tc::mbar_expect_tx(&qfull[qb], (uint32_t)p.qbytes);
+        for (int h = 0; h < HALVES; ++h)
+          for (int mt = 0; mt < MT; ++mt)
+            tc::tma_load_2d(qdst + h * qrow_bytes + mt * 16384, &maps.q, &qfull[qb], h * 64,
+                            head * a.M_pad + mt * 128);
+        for (int pass = 0; pass < 2; ++pass)
+          for (int c = c0; c < c1; ++c, ++kc) {
+            const int s = kc % S;
+            if (kc >= (uint32_t)S && !wait_or_abort(&kempty[s], ((kc / S) - 1) & 1, abort_flag, a.status)) break;
+            tc::mbar_expect_tx(&kfull[s], (uint32_t)kStage);
+            for (int h = 0; h < HALVES; ++h)
+              tc::tma_load_3d(Ks + s * kStage + h * 16384, &maps.k[l], &kfull[s], h * 64, c * kChunk, bh);
+          }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t kc = 0;
+      const uint32_t id1 = tc::idesc_bf16(128, kChunk);
+      const uint32_t id2 = tc::idesc_bf16(128, a.M_n);
+      for (int round = 0; !*abort_flag; ++round) {
+        const int head = group + round * p.ngroups;
+        if (head >= heads) break;
+        const int qb = round & 1;
+        if (!wait_or_abort(&qfull[qb], (round >> 1) & 1, abort_flag, a.status)) break;
+        tc::fence_after_sync();
+        const uint32_t qaddr = tc::smem_u32(Qs + qb * p.qbytes);
+        bool ok = true;
+        for (int pass = 0; pass < 2 && ok; ++pass)
+          for (int c = c0; c < c1; ++c, ++kc) {
+            const int s = kc % S;
+            const uint32_t acc = kc & 1;
+            if (!wait_or_abort(&kfull[s], (kc / S) & 1, abort_flag, a.status) ||
+                (kc >= 2 && !wait_or_abort(&tempty[acc], ((kc >> 1) - 1) & 1, abort_flag, a.status))) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t kaddr = tc::smem_u32(Ks + s * kStage);
+            const uint32_t d = tmem + acc * kAccCols;
+            if (pass == 0) {
+              for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                  tc::umma_bf16(d + mt * kChunk, tc::desc_k_sw128(qaddr + (ks >> 2) * qrow_bytes + mt * 16384 + (ks & 3) * 32),
+                                tc::desc_k_sw128(kaddr + (ks >> 2) * 16384 + (ks & 3) * 32), id1, ks > 0);
+            } else {
+#pragma unroll
+              for (int ks = 0; ks < D / 16; ++ks)
+                tc::umma_bf16(d, tc::desc_k_sw128(kaddr + (ks >> 2) * 16384 + (ks & 3) * 32),
+                              tc::desc_k_sw128(qaddr + (ks >> 2) * qrow_bytes + (ks & 3) * 32), id2, ks > 0);
+            }
+            tc::umma_commit(&kempty[s]);
+            tc::umma_commit(&tfull[acc]);
+          }
+        if (!ok) break;
+        tc::umma_commit(&qempty[qb]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue ----------------
+    const int e = warp - 2;      // 0..7
+    const int q = warp & 3;      // TMEM lane quarter this warp may read
+    const int hf = e >> 2;       // which half of the columns
+    const int te = threadIdx.x - 64;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    uint32_t kc = 0;
+    for (int round = 0;; ++round) {
+      const int head = group + round * p.ngroups;
+      if (head >= heads) break;
+      // ---- pass 1: running (max, sum of exp2) of each row over this CTA's key range
+      float2 st[2] = {make_float2(-INFINITY, 0.f), make_float2(-INFINITY, 0.f)};
+      for (int c = c0; c < c1; ++c, ++kc) {
+        const uint32_t acc = kc & 1;
+        bool go = !*abort_flag && wait_or_abort(&tfull[acc], (kc >> 1) & 1, abort_flag, a.status);
+        if (__all_sync(kFull, go)) {  // tcgen05.ld is warp-collective: decide per warp
+          tc::fence_after_sync();
+          const int nvalid = min(kChunk, a.g.N - c * kChunk);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            float v0[32], v1[32];
+            const uint32_t col0 = (uint32_t)(mt * kChunk + hf * 64);
+            tc::tmem_ld32(tmem + acc * kAccCols + lane_off + col0, v0);
+            tc::tmem_ld32(tmem + acc * kAccCols + lane_off + col0 + 32, v1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              v0[i] = (hf * 64 + i < nvalid) ? v0[i] * c2 : -INFINITY;
+              v1[i] = (hf * 64 + 32 + i < nvalid) ? v1[i] * c2 : -INFINITY;
+            }
+            const float mx = fmaxf(tree_max32(v0), tree_max32(v1));
+            if (mx > -INFINITY) {
+              const float mn = fmaxf(st[mt].x, mx);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                v0[i] = exp2f(v0[i] - mn);
+                v1[i] = exp2f(v1[i] - mn);
+              }
+              st[mt] = make_float2(mn, st[mt].y * exp2f(st[mt].x - mn) + (tree_sum32(v0) + tree_sum32(v1)));
+            }
+          }
+          tc::fence_before_sync();
+        }
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&tempty[acc])) : "memory");
+      }
+      // ---- merge the two column halves, publish this range's partials, wait for the group
+      if (hf == 1)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) merge[mt * 128 + q * 32 + lane] = st[mt];
+      epi_bar();
+      float2* mine = xch.part + ((size_t)((round & 1) * p.ngroups + group) * p.group_size + rank) * a.M_pad;
+      if (hf == 0)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int r = mt * 128 + q * 32 + lane;
+          mine[r] = lse_merge(st[mt], merge[r]);
+        }
+      __threadfence();
+      epi_bar();
+      if (te == 0 && p.group_size > 1) {
+        atomicAdd(&xch.arrive[group], 1u);
+        const unsigned target = (unsigned)(round + 1) * (unsigned)p.group_size;
+        bool done = false;
+        for (uint32_t it = 0; it < (1u << 22) && !*abort_flag; ++it) {
+          if (ld_acquire(&xch.arrive[group]) >= target) {
+            done = true;
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (!done && !*abort_flag) {
+          *abort_flag = 1;
+          status_or(a.status, KVC_STATUS_TIMEOUT);
+        }
+        __threadfence();
+      }
+      epi_bar();
+      // ---- lse2 of every row of the head from the group's partials
+      const float2* grp = xch.part + ((size_t)((round & 1) * p.ngroups + group) * p.group_size) * a.M_pad;
+      for (int r = te; r < a.M_pad; r += 32 * kEpiWarps) {
+        float2 acc2 = make_float2(-INFINITY, 0.f);
+        for (int k = 0; k < p.group_size; ++k) acc2 = lse_merge(acc2, grp[(size_t)k * a.M_pad + r]);
+        const bool valid = ws.valid[(size_t)head * a.M_pad + r] != 0;
+        lse2s[r] = (valid && acc2.y > 0.f) ? acc2.x + log2f(acc2.y) : INFINITY;
+      }
+      epi_bar();
+      // ---- pass 2: each key's max over rows of s*c2 - lse2, then exp2
+      const int nslice = (a.M_n + 31) >> 5;
+      const int half_s = (nslice + 1) >> 1;
+      const int s_lo = hf == 0 ? 0 : half_s, s_hi = hf == 0 ? half_s : nslice;
+      const int key = q * 32 + lane;
+      for (int c = c0; c < c1; ++c, ++kc) {
+        const uint32_t acc = kc & 1;
+        float best = -INFINITY;
+        bool go = !*abort_flag && wait_or_abort(&tfull[acc], (kc >> 1) & 1, abort_flag, a.status);
+        if (__all_sync(kFull, go)) {  // tcgen05.ld is warp-collective: decide per warp
+          tc::fence_after_sync();
+          // rows past M_n read TMEM columns the MMA did not write; their lse2 is +inf, so the
+          // term is -inf or NaN, which fmaxf drops
+#pragma unroll 1
+          for (int cs = s_lo; cs < s_hi; ++cs) {
+            float v[32];
+            tc::tmem_ld32(tmem + acc * kAccCols + lane_off + (uint32_t)(cs * 32), v);
+            const float4* l4 = reinterpret_cast<const float4*>(lse2s + cs * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 lb = l4[i];
+              v[4 * i + 0] = fmaf(v[4 * i + 0], c2, -lb.x);
+              v[4 * i + 1] = fmaf(v[4 * i + 1], c2, -lb.y);
+              v[4 * i + 2] = fmaf(v[4 * i + 2], c2, -lb.z);
+              v[4 * i + 3] = fmaf(v[4 * i + 3], c2, -lb.w);
+            }
+            best = fmaxf(best, tree_max32(v));
+          }
+          tc::fence_before_sync();
+        }
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&tempty[acc])) : "memory");
+        float* pb = pbest + (kc & 1) * kChunk;
+        if (hf == 1) pb[key] = best;
+        epi_bar();
+        if (hf == 0 && !*abort_flag) {
+          best = fmaxf(best, pb[key]);
+          const int j = c * kChunk + key;
+          if (j < a.g.N) a.scores[(size_t)head * a.g.N + j] = exp2f(best);
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, 2 * kAccCols);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 fused_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;  // resolved once from the driver
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+static bool fused_maps(FusedMaps* m, const ScoreArgs& a, const ScoreWs& ws) {
+  auto enc = fused_encoder();
+  if (!enc) return false;
+  const int D = a.g.D;
+  const cuuint32_t es[3] = {1, 1, 1};
+  for (int l = 0; l < a.g.L; ++l) {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.g.ncap, (cuuint64_t)a.g.B * a.g.Hkv};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.g.ncap * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kChunk, 1};
+    if (enc(&m->k[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.K.p[l], dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  const int heads = a.g.L * a.g.B * a.g.Hkv;
+  const cuuint64_t qdims[2] = {(cuuint64_t)D, (cuuint64_t)heads * a.M_pad};
+  const cuuint64_t qstrides[1] = {(cuuint64_t)D * 2};
+  const cuuint32_t qbox[2] = {64, 128};
+  return enc(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws.obs, qdims, qstrides, qbox, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t fused_xch_bytes(int M_pad) {
+  return (size_t)2 * kMaxSMs * (size_t)M_pad * sizeof(float2) + (size_t)kMaxSMs * sizeof(unsigned) + 256;
+}
+
+int launch_score_fused(const ScoreArgs& a, const ScoreWs& ws, void* xch_base, cudaStream_t s) {
+  int dev = 0, nsm = 0, smem_optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return KVC_ERR_LAUNCH;
+  if (nsm > kMaxSMs) nsm = kMaxSMs;
+  const int D = a.g.D;
+  FusedPlan p;
+  // about eight 128-key chunks (1024 keys) per CTA, with the group size a divisor of the SM count
+  const int want = (a.nchunk + 7) / 8;
+  int gs = nsm;
+  for (int d = 1; d <= nsm; ++d)
+    if (nsm % d == 0 && d >= want) {
+      gs = d;
+      break;
+    }
+  p.group_size = gs;
+  p.ngroups = nsm / gs;
+  p.chunks_per_cta = (a.nchunk + gs - 1) / gs;
+  p.qbytes = a.M_pad * D * 2;
+  const int stage_bytes = kChunk * D * 2;
+  const int tail = 1024 + 64 * 8 + kMaxRows * 12 + 2 * kChunk * 4 + 256;
+  int stages = (smem_optin - 2 * p.qbytes - tail) / stage_bytes;
+  if (stages > 6) stages = 6;
+  if (stages < 2) return KVC_ERR_TOO_LARGE;
+  p.stages = stages;
+  const size_t smem = (size_t)tail + 2 * (size_t)p.qbytes + (size_t)stages * stage_bytes;
+
+  FusedXch xch;
+  xch.part = reinterpret_cast<float2*>(xch_base);
+  xch.arrive = reinterpret_cast<unsigned*>(static_cast<char*>(xch_base) +
+                                           (size_t)2 * kMaxSMs * (size_t)a.M_pad * sizeof(float2));
+  if (cudaMemsetAsync(xch.arrive, 0, sizeof(unsigned) * (size_t)p.ngroups, s) != cudaSuccess) return KVC_ERR_LAUNCH;
+
+  FusedMaps maps;
+  if (!fused_maps(&maps, a, ws)) return KVC_ERR_LAUNCH;
+  const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
+  void (*kern)(const FusedMaps, ScoreArgs, ScoreWs, FusedPlan, FusedXch, float) =
+      D == 128 ? (a.M_pad > 128 ? score_fused_kernel<128, 2> : score_fused_kernel<128, 1>)
+               : (a.M_pad > 128 ? score_fused_kernel<64, 2> : score_fused_kernel<64, 1>);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return KVC_ERR_LAUNCH;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFusedThreads, smem) != cudaSuccess ||
+      per_sm < 1)
+    return KVC_ERR_LAUNCH;
+  ScoreArgs aa = a;
+  ScoreWs wss = ws;
+  float cc = c2;
+  void* args[] = {(void*)&maps, (void*)&aa, (void*)&wss, (void*)&p, (void*)&xch, (void*)&cc};
+  if (cudaLaunchCooperativeKernel((const void*)kern, dim3(p.ngroups * p.group_size), dim3(kFusedThreads), args, smem,
+                                  s) != cudaSuccess)
+    return KVC_ERR_LAUNCH;
+  return KVC_OK;
+}
+
+}  // namespace kvc
