@@ -9,10 +9,10 @@
 // Work split. A head's keys are cut into G_s contiguous ranges of whole 128-key chunks, one
 // per CTA of a "group"; the grid is (#groups x G_s) CTAs, one per SM, launched cooperatively so
 // every CTA is resident. Group g handles heads g, g + #groups, ... in rounds. In a round a CTA
-// runs pass 1 over its range, publishes its per-row partials, waits (bounded) for the rest of
-// its group, merges the partials into lse2, and runs pass 2 over the same range. Pass 2's TMA
-// reads find the range in L2: it was read moments before and at most one range per SM
-// (~256 KB) is live at a time.
+// runs pass 1 over its range and publishes its per-row partials; once the whole group has
+// published, the partials merge into lse2 and the CTA runs pass 2 over the same range. Pass 1
+// of the next round is interleaved before pass 2 of the current one, so nobody waits for the
+// group. Pass 2's TMA reads find the range in L2: at most two ranges per SM (~512 KB) are live.
 //
 // Roles inside a CTA (all derive the same chunk sequence from blockIdx, so no queue is needed):
 //   warp 0      TMA producer: the round's observation tile Q into one of two Q buffers, then
@@ -21,7 +21,11 @@
 //               S = Q K^T (lane = row), pass 2 S^T = K Q^T (lane = key).
 //   warps 2-9   epilogue: pass 1 keeps each row's running (max, sum) in registers (two warps
 //               per TMEM lane quarter split the columns); pass 2 keeps each key's running max.
-// Barriers: kfull/kempty per K stage, qfull/qempty per Q buffer, tfull/tempty per accumulator.
+//   warp 10     exchange: waits until the group has published a round's partials and merges
+//               them into lse2 per row (double-buffered in shared memory), off the critical path.
+// Barriers: kfull/kempty per K stage, qfull/qempty per Q buffer, tfull/tempty per TMEM
+// accumulator (four of 128 columns when both passes fit, else two of 256), lfull/lempty per
+// lse2 buffer. Partials are published with one release add after a CTA-local barrier.
 // Every wait is bounded; a wait that gives up sets KVC_STATUS_TIMEOUT and a CTA-wide abort
 // flag, after which every role skips its work but still passes every named barrier.
 #include <cudaTypedefs.h>
@@ -32,8 +36,7 @@
 namespace kvc {
 
 constexpr int kEpiWarps = 8;
-constexpr int kFusedThreads = 64 + 32 * kEpiWarps;
-constexpr uint32_t kAccCols = 256;  // one TMEM accumulator (two of them: 512 columns)
+constexpr int kFusedThreads = 64 + 32 * kEpiWarps + 32;  // producer, MMA, epilogue warps, exchange warp
 
 struct FusedMaps {
   CUtensorMap k[KVC_MAX_LAYERS];  // per layer: dims {D, ncap, B*Hkv}, box {64, 128, 1}
@@ -49,8 +52,8 @@ struct FusedPlan {
 };
 
 struct FusedXch {
-  float2* part;      // [2][ngroups][group_size][M_pad] per-row (max, sum) of each range, by round parity
-  unsigned* arrive;  // [ngroups] monotone arrival counters, zero at launch
+  float2* part;      // [4][ngroups][group_size][M_pad] per-row (max, sum) of each range, slot = round % 4
+  unsigned* arrive;  // [4][ngroups] publications per exchange slot, zero at launch
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -99,6 +102,12 @@ __device__ __forceinline__ float tree_sum32(const float (&x)[32]) {
   return a[0];
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {  // MUFU.EX2; relative error about 2^-22
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // merge two (max, sum-of-exp2) states
 __device__ __forceinline__ float2 lse_merge(float2 x, float2 y) {
   if (y.y <= 0.f) return x;
@@ -107,12 +116,13 @@ __device__ __forceinline__ float2 lse_merge(float2 x, float2 y) {
   return make_float2(m, x.y * exp2f(x.x - m) + y.y * exp2f(y.x - m));
 }
 
-template <int D, int MT>
+template <int D, int MT, int NACC>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     score_fused_kernel(const __grid_constant__ FusedMaps maps, ScoreArgs a, ScoreWs ws, FusedPlan p, FusedXch xch,
                        float c2) {
   constexpr int HALVES = D / 64;
   constexpr int kStage = kChunk * D * 2;
+  constexpr uint32_t kAcc = 512u / NACC;  // TMEM columns per accumulator
   extern __shared__ uint8_t smraw[];
   uint8_t* Qs = align1024(smraw);
   uint8_t* Ks = Qs + 2 * p.qbytes;
@@ -122,12 +132,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   uint64_t* qfull = kempty + S;
   uint64_t* qempty = qfull + 2;
   uint64_t* tfull = qempty + 2;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tempty = tfull + NACC;
+  uint64_t* lfull = tempty + NACC;
+  uint64_t* lempty = lfull + 2;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(lempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 1);
-  float* lse2s = reinterpret_cast<float*>(Ks + S * kStage + 512);  // [kMaxRows], 16-byte aligned
-  float2* merge = reinterpret_cast<float2*>(lse2s + kMaxRows);  // [kMaxRows]
-  float* pbest = reinterpret_cast<float*>(merge + kMaxRows);    // [2][kChunk]
+  float* lse2s = reinterpret_cast<float*>(Ks + S * kStage + 512);  // [2][kMaxRows], 16-byte aligned
+  float2* merge = reinterpret_cast<float2*>(lse2s + 2 * kMaxRows);   // [kMaxRows]
+  float* pbest = reinterpret_cast<float*>(merge + kMaxRows);         // [2][kChunk]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -135,16 +147,20 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       tc::mbar_init(&kfull[i], 1);
       tc::mbar_init(&kempty[i], 1);
     }
+    for (int i = 0; i < NACC; ++i) {
+      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tempty[i], kEpiWarps);
+    }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&qfull[i], 1);
       tc::mbar_init(&qempty[i], 1);
-      tc::mbar_init(&tfull[i], 1);
-      tc::mbar_init(&tempty[i], kEpiWarps);
+      tc::mbar_init(&lfull[i], 1);
+      tc::mbar_init(&lempty[i], kEpiWarps);
     }
     *abort_flag = 0;
     tc::mbar_fence_init();
   }
-  if (warp == 1) tc::tmem_alloc(slot, 2 * kAccCols);
+  if (warp == 1) tc::tmem_alloc(slot, 512);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -152,34 +168,50 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
   const int heads = a.g.L * a.g.B * a.g.Hkv;
   const int group = blockIdx.x / p.group_size, rank = blockIdx.x % p.group_size;
+  const int rounds = group < heads ? (heads - group + p.ngroups - 1) / p.ngroups : 0;
   const int c0 = rank * p.chunks_per_cta;
   const int c1 = min(c0 + p.chunks_per_cta, a.nchunk);
   const int qrow_bytes = a.M_pad * 128;  // one 64-column half of an observation tile
 
+  // Chunk order, identical in every role: segment seg = pass 1 of round seg (if any), then
+  // pass 2 of round seg - 1 (if any). Pass 1 of the next round thus runs while the group's
+  // partials for the previous round are gathered.
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       uint32_t kc = 0;
-      for (int round = 0; !*abort_flag; ++round) {
-        const int head = group + round * p.ngroups;
-        if (head >= heads) break;
-        const int l = head / (a.g.B * a.g.Hkv), bh = head % (a.g.B * a.g.Hkv);
-        const int qb = round & 1;
-        if (round >= 2 && !wait_or_abort(&qempty[qb], ((round - 2) >> 1) & 1, abort_flag, a.status)) break;
-        uint8_t* qdst = Qs + qb * p.qbytes;
-        tc::mbar_expect_tx(&qfull[qb], (uint32_t)p.qbytes);
-        for (int h = 0; h < HALVES; ++h)
-          for (int mt = 0; mt < MT; ++mt)
-            tc::tma_load_2d(qdst + h * qrow_bytes + mt * 16384, &maps.q, &qfull[qb], h * 64,
-                            head * a.M_pad + mt * 128);
-        for (int pass = 0; pass < 2; ++pass)
-          for (int c = c0; c < c1; ++c, ++kc) {
+      const int n = c1 > c0 ? c1 - c0 : 0;
+      for (int seg = 0; seg <= rounds && !*abort_flag; ++seg) {
+        if (seg < rounds) {  // this round's observation tile, into the buffer its round parity names
+          const int round = seg, head = group + round * p.ngroups;
+          const int qb = round & 1;
+          if (round >= 2 && !wait_or_abort(&qempty[qb], ((round - 2) >> 1) & 1, abort_flag, a.status)) break;
+          uint8_t* qdst = Qs + qb * p.qbytes;
+          tc::mbar_expect_tx(&qfull[qb], (uint32_t)p.qbytes);
+          for (int h = 0; h < HALVES; ++h)
+            for (int mt = 0; mt < MT; ++mt)
+              tc::tma_load_2d(qdst + h * qrow_bytes + mt * 16384, &maps.q, &qfull[qb], h * 64,
+                              head * a.M_pad + mt * 128);
+        }
+        bool stop = false;
+        for (int j = 0; j < n + 2 && !stop; ++j)
+          for (int pass = 0; pass < 2; ++pass) {
+            const int round = seg - pass;
+            const int c = c0 + j - 2 * pass;
+            if (round < 0 || round >= rounds || c < c0 || c >= c1) continue;
+            const int head = group + round * p.ngroups;
+            const int l = head / (a.g.B * a.g.Hkv), bh = head % (a.g.B * a.g.Hkv);
             const int s = kc % S;
-            if (kc >= (uint32_t)S && !wait_or_abort(&kempty[s], ((kc / S) - 1) & 1, abort_flag, a.status)) break;
+            if (kc >= (uint32_t)S && !wait_or_abort(&kempty[s], ((kc / S) - 1) & 1, abort_flag, a.status)) {
+              stop = true;
+              break;
+            }
             tc::mbar_expect_tx(&kfull[s], (uint32_t)kStage);
             for (int h = 0; h < HALVES; ++h)
               tc::tma_load_3d(Ks + s * kStage + h * 16384, &maps.k[l], &kfull[s], h * 64, c * kChunk, bh);
+            ++kc;
           }
+        if (stop) break;
       }
     }
     __syncwarp();
@@ -189,31 +221,37 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       uint32_t kc = 0;
       const uint32_t id1 = tc::idesc_bf16(128, kChunk);
       const uint32_t id2 = tc::idesc_bf16(128, a.M_n);
-      for (int round = 0; !*abort_flag; ++round) {
-        const int head = group + round * p.ngroups;
-        if (head >= heads) break;
-        const int qb = round & 1;
-        if (!wait_or_abort(&qfull[qb], (round >> 1) & 1, abort_flag, a.status)) break;
-        tc::fence_after_sync();
-        const uint32_t qaddr = tc::smem_u32(Qs + qb * p.qbytes);
-        bool ok = true;
-        for (int pass = 0; pass < 2 && ok; ++pass)
-          for (int c = c0; c < c1; ++c, ++kc) {
+      const int n = c1 > c0 ? c1 - c0 : 0;
+      bool ok = true;
+      for (int seg = 0; seg <= rounds && ok && !*abort_flag; ++seg) {
+        if (seg < rounds) {
+          if (!wait_or_abort(&qfull[seg & 1], (seg >> 1) & 1, abort_flag, a.status)) break;
+          tc::fence_after_sync();
+        }
+        for (int j = 0; j < n + 2 && ok; ++j)
+          for (int pass = 0; pass < 2; ++pass) {
+            const int round = seg - pass;
+            const int c = c0 + j - 2 * pass;
+            if (round < 0 || round >= rounds || c < c0 || c >= c1) continue;
+            const uint32_t qaddr = tc::smem_u32(Qs + (round & 1) * p.qbytes);
             const int s = kc % S;
-            const uint32_t acc = kc & 1;
+            const uint32_t acc = kc % NACC;
             if (!wait_or_abort(&kfull[s], (kc / S) & 1, abort_flag, a.status) ||
-                (kc >= 2 && !wait_or_abort(&tempty[acc], ((kc >> 1) - 1) & 1, abort_flag, a.status))) {
+                (kc >= (uint32_t)NACC &&
+                 !wait_or_abort(&tempty[acc], ((kc / NACC) - 1) & 1, abort_flag, a.status))) {
               ok = false;
               break;
             }
             tc::fence_after_sync();
             const uint32_t kaddr = tc::smem_u32(Ks + s * kStage);
-            const uint32_t d = tmem + acc * kAccCols;
+            const uint32_t d = tmem + acc * kAcc;
             if (pass == 0) {
+#pragma unroll
               for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                  tc::umma_bf16(d + mt * kChunk, tc::desc_k_sw128(qaddr + (ks >> 2) * qrow_bytes + mt * 16384 + (ks & 3) * 32),
+                  tc::umma_bf16(d + mt * kChunk,
+                                tc::desc_k_sw128(qaddr + (ks >> 2) * qrow_bytes + mt * 16384 + (ks & 3) * 32),
                                 tc::desc_k_sw128(kaddr + (ks >> 2) * 16384 + (ks & 3) * 32), id1, ks > 0);
             } else {
 #pragma unroll
@@ -223,145 +261,236 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             }
             tc::umma_commit(&kempty[s]);
             tc::umma_commit(&tfull[acc]);
+            ++kc;
           }
-        if (!ok) break;
-        tc::umma_commit(&qempty[qb]);
+        // the previous round's tile is done once its pass 2 has been issued (n == 0 issues none)
+        if (ok && seg >= 1) tc::umma_commit(&qempty[(seg - 1) & 1]);
       }
     }
     __syncwarp();
+  } else if (warp == 2 + kEpiWarps) {
+    // ---------------- exchange warp: lse2 of every row once the group has published ----------------
+    for (int round = 0; round < rounds && !*abort_flag; ++round) {
+      const int b = round & 1;
+      if (round >= 2 && !wait_or_abort(&lempty[b], ((round - 2) >> 1) & 1, abort_flag, a.status)) break;
+      const int head = group + round * p.ngroups;
+      // Slot round % 4 has been published by the group (round >> 2) times before; a partner can
+      // only publish round + 4 into it after the whole group published round + 2, so reaching
+      // this count means every partner has published `round`.
+      if (lane == 0) {
+        const unsigned target = (unsigned)((round >> 2) + 1) * (unsigned)p.group_size;
+        const unsigned* ctr = &xch.arrive[(round & 3) * p.ngroups + group];
+        bool done = false;
+        for (uint32_t it = 0; it < (1u << 22) && !*abort_flag; ++it) {
+          if (ld_acquire(ctr) >= target) {
+            done = true;
+            break;
+          }
+          __nanosleep(32);
+        }
+        if (!done && !*abort_flag) {
+          *abort_flag = 1;
+          status_or(a.status, KVC_STATUS_TIMEOUT);
+        }
+      }
+      __syncwarp();
+      const float2* grp = xch.part + ((size_t)((round & 3) * p.ngroups + group) * p.group_size) * a.M_pad;
+      float* dst = lse2s + b * kMaxRows;
+      for (int r = lane; r < a.M_pad; r += kWarp) {
+        float2 acc2 = make_float2(-INFINITY, 0.f);
+        for (int k = 0; k < p.group_size; ++k) acc2 = lse_merge(acc2, grp[(size_t)k * a.M_pad + r]);
+        const bool valid = ws.valid[(size_t)head * a.M_pad + r] != 0;
+        dst[r] = (valid && acc2.y > 0.f) ? acc2.x + log2f(acc2.y) : INFINITY;
+      }
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&lfull[b])) : "memory");
+    }
   } else {
     // ---------------- epilogue ----------------
     const int e = warp - 2;      // 0..7
     const int q = warp & 3;      // TMEM lane quarter this warp may read
     const int hf = e >> 2;       // which half of the columns
-    const int te = threadIdx.x - 64;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const int key = q * 32 + lane;
+    const int nslice = (a.M_n + 31) >> 5;
+    const int half_s = (nslice + 1) >> 1;
+    const int s_lo = hf == 0 ? 0 : half_s, s_hi = hf == 0 ? half_s : nslice;
+    const int n = c1 > c0 ? c1 - c0 : 0;
     uint32_t kc = 0;
-    for (int round = 0;; ++round) {
-      const int head = group + round * p.ngroups;
-      if (head >= heads) break;
-      // ---- pass 1: running (max, sum of exp2) of each row over this CTA's key range
-      float2 st[2] = {make_float2(-INFINITY, 0.f), make_float2(-INFINITY, 0.f)};
-      for (int c = c0; c < c1; ++c, ++kc) {
-        const uint32_t acc = kc & 1;
-        bool go = !*abort_flag && wait_or_abort(&tfull[acc], (kc >> 1) & 1, abort_flag, a.status);
-        if (__all_sync(kFull, go)) {  // tcgen05.ld is warp-collective: decide per warp
-          tc::fence_after_sync();
-          const int nvalid = min(kChunk, a.g.N - c * kChunk);
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            float v0[32], v1[32];
-            const uint32_t col0 = (uint32_t)(mt * kChunk + hf * 64);
-            tc::tmem_ld32(tmem + acc * kAccCols + lane_off + col0, v0);
-            tc::tmem_ld32(tmem + acc * kAccCols + lane_off + col0 + 32, v1);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              v0[i] = (hf * 64 + i < nvalid) ? v0[i] * c2 : -INFINITY;
-              v1[i] = (hf * 64 + 32 + i < nvalid) ? v1[i] * c2 : -INFINITY;
-            }
-            const float mx = fmaxf(tree_max32(v0), tree_max32(v1));
-            if (mx > -INFINITY) {
-              const float mn = fmaxf(st[mt].x, mx);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                v0[i] = exp2f(v0[i] - mn);
-                v1[i] = exp2f(v1[i] - mn);
-              }
-              st[mt] = make_float2(mn, st[mt].y * exp2f(st[mt].x - mn) + (tree_sum32(v0) + tree_sum32(v1)));
-            }
-          }
-          tc::fence_before_sync();
-        }
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&tempty[acc])) : "memory");
-      }
-      // ---- merge the two column halves, publish this range's partials, wait for the group
+    float2 st[MT];
+    bool have = false;  // lse2 of the round whose pass 2 is running is in shared memory
+
+    // publish this CTA's partials of round `round` (slot = round % 4)
+    auto publish = [&](int round) {
       if (hf == 1)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) merge[mt * 128 + q * 32 + lane] = st[mt];
       epi_bar();
-      float2* mine = xch.part + ((size_t)((round & 1) * p.ngroups + group) * p.group_size + rank) * a.M_pad;
+      float2* mine = xch.part + ((size_t)((round & 3) * p.ngroups + group) * p.group_size + rank) * a.M_pad;
       if (hf == 0)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const int r = mt * 128 + q * 32 + lane;
           mine[r] = lse_merge(st[mt], merge[r]);
         }
-      __threadfence();
       epi_bar();
-      if (te == 0 && p.group_size > 1) {
-        atomicAdd(&xch.arrive[group], 1u);
-        const unsigned target = (unsigned)(round + 1) * (unsigned)p.group_size;
-        bool done = false;
-        for (uint32_t it = 0; it < (1u << 22) && !*abort_flag; ++it) {
-          if (ld_acquire(&xch.arrive[group]) >= target) {
-            done = true;
-            break;
+      // one release add after the CTA-local barrier publishes every epilogue thread's writes
+      if (e == 0 && lane == 0)
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(&xch.arrive[(round & 3) * p.ngroups + group])
+                     : "memory");
+    };
+    auto lse_wait = [&](int round) {
+      have = !*abort_flag && wait_or_abort(&lfull[round & 1], (round >> 1) & 1, abort_flag, a.status);
+    };
+    auto lse_release = [&](int round) {
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&lempty[round & 1])) : "memory");
+    };
+    auto free_acc = [&](uint32_t acc) {
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&tempty[acc])) : "memory");
+    };
+
+    // pass 1 chunk: fold this thread's row(s) into the running (max, sum of exp2)
+    auto pass1_chunk = [&](int c) {
+      const uint32_t acc = kc % NACC;
+      const bool go = !*abort_flag && wait_or_abort(&tfull[acc], (kc / NACC) & 1, abort_flag, a.status);
+      if (__all_sync(kFull, go)) {  // tcgen05.ld is warp-collective: decide per warp
+        tc::fence_after_sync();
+        const int nvalid = min(kChunk, a.g.N - c * kChunk);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t r0[32], r1[32];
+          const uint32_t col0 = (uint32_t)(mt * kChunk + hf * 64);
+          tc::tmem_ld32_async(tmem + acc * kAcc + lane_off + col0, r0);
+          tc::tmem_ld32_async(tmem + acc * kAcc + lane_off + col0 + 32, r1);
+          tc::tmem_wait();
+          tc::tmem_regs_ready(r0);
+          tc::tmem_regs_ready(r1);
+          if (mt == MT - 1) {  // the accumulator is free as soon as its last values are in registers
+            tc::fence_before_sync();
+            free_acc(acc);
           }
-          __nanosleep(64);
+          float v0[32], v1[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            v0[i] = __uint_as_float(r0[i]);
+            v1[i] = __uint_as_float(r1[i]);
+          }
+          if (nvalid < kChunk) {  // ragged last chunk only
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (hf * 64 + i >= nvalid) v0[i] = -INFINITY;
+              if (hf * 64 + 32 + i >= nvalid) v1[i] = -INFINITY;
+            }
+          }
+          const float mraw = fmaxf(tree_max32(v0), tree_max32(v1));  // c2 > 0: scale the max once
+          if (mraw > -INFINITY) {
+            const float mn = fmaxf(st[mt].x, mraw * c2);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              v0[i] = ex2_approx(fmaf(v0[i], c2, -mn));
+              v1[i] = ex2_approx(fmaf(v1[i], c2, -mn));
+            }
+            st[mt] = make_float2(mn, st[mt].y * ex2_approx(st[mt].x - mn) + (tree_sum32(v0) + tree_sum32(v1)));
+          }
         }
-        if (!done && !*abort_flag) {
-          *abort_flag = 1;
-          status_or(a.status, KVC_STATUS_TIMEOUT);
-        }
-        __threadfence();
+      } else {
+        free_acc(acc);
       }
-      epi_bar();
-      // ---- lse2 of every row of the head from the group's partials
-      const float2* grp = xch.part + ((size_t)((round & 1) * p.ngroups + group) * p.group_size) * a.M_pad;
-      for (int r = te; r < a.M_pad; r += 32 * kEpiWarps) {
-        float2 acc2 = make_float2(-INFINITY, 0.f);
-        for (int k = 0; k < p.group_size; ++k) acc2 = lse_merge(acc2, grp[(size_t)k * a.M_pad + r]);
-        const bool valid = ws.valid[(size_t)head * a.M_pad + r] != 0;
-        lse2s[r] = (valid && acc2.y > 0.f) ? acc2.x + log2f(acc2.y) : INFINITY;
-      }
-      epi_bar();
-      // ---- pass 2: each key's max over rows of s*c2 - lse2, then exp2
-      const int nslice = (a.M_n + 31) >> 5;
-      const int half_s = (nslice + 1) >> 1;
-      const int s_lo = hf == 0 ? 0 : half_s, s_hi = hf == 0 ? half_s : nslice;
-      const int key = q * 32 + lane;
-      for (int c = c0; c < c1; ++c, ++kc) {
-        const uint32_t acc = kc & 1;
-        float best = -INFINITY;
-        bool go = !*abort_flag && wait_or_abort(&tfull[acc], (kc >> 1) & 1, abort_flag, a.status);
-        if (__all_sync(kFull, go)) {  // tcgen05.ld is warp-collective: decide per warp
-          tc::fence_after_sync();
-          // rows past M_n read TMEM columns the MMA did not write; their lse2 is +inf, so the
-          // term is -inf or NaN, which fmaxf drops
+      ++kc;
+    };
+
+    // pass 2 chunk: each key's max over rows of s*c2 - lse2, then exp2
+    auto pass2_chunk = [&](int round, int c) {
+      const uint32_t acc = kc % NACC;
+      const int head = group + round * p.ngroups;
+      const float* L2 = lse2s + (round & 1) * kMaxRows;
+      float best = -INFINITY;
+      const bool go = have && !*abort_flag && wait_or_abort(&tfull[acc], (kc / NACC) & 1, abort_flag, a.status);
+      if (__all_sync(kFull, go)) {  // tcgen05.ld is warp-collective: decide per warp
+        tc::fence_after_sync();
+        // rows past M_n read TMEM columns the MMA did not write; their lse2 is +inf, so the term
+        // is -inf or NaN, which fmaxf drops
 #pragma unroll 1
-          for (int cs = s_lo; cs < s_hi; ++cs) {
-            float v[32];
-            tc::tmem_ld32(tmem + acc * kAccCols + lane_off + (uint32_t)(cs * 32), v);
-            const float4* l4 = reinterpret_cast<const float4*>(lse2s + cs * 32);
+        for (int cs = s_lo; cs < s_hi; cs += 2) {
+          uint32_t ra[32], rb[32];
+          const bool two = cs + 1 < s_hi;
+          tc::tmem_ld32_async(tmem + acc * kAcc + lane_off + (uint32_t)(cs * 32), ra);
+          if (two) tc::tmem_ld32_async(tmem + acc * kAcc + lane_off + (uint32_t)(cs * 32 + 32), rb);
+          tc::tmem_wait();
+          tc::tmem_regs_ready(ra);
+          tc::tmem_regs_ready(rb);
+          float v[32];
+          const float4* l4 = reinterpret_cast<const float4*>(L2 + cs * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 lb = l4[i];
+            v[4 * i + 0] = fmaf(__uint_as_float(ra[4 * i + 0]), c2, -lb.x);
+            v[4 * i + 1] = fmaf(__uint_as_float(ra[4 * i + 1]), c2, -lb.y);
+            v[4 * i + 2] = fmaf(__uint_as_float(ra[4 * i + 2]), c2, -lb.z);
+            v[4 * i + 3] = fmaf(__uint_as_float(ra[4 * i + 3]), c2, -lb.w);
+          }
+          best = fmaxf(best, tree_max32(v));
+          if (two) {
+            const float4* m4 = reinterpret_cast<const float4*>(L2 + cs * 32 + 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float4 lb = l4[i];
-              v[4 * i + 0] = fmaf(v[4 * i + 0], c2, -lb.x);
-              v[4 * i + 1] = fmaf(v[4 * i + 1], c2, -lb.y);
-              v[4 * i + 2] = fmaf(v[4 * i + 2], c2, -lb.z);
-              v[4 * i + 3] = fmaf(v[4 * i + 3], c2, -lb.w);
+              const float4 lb = m4[i];
+              v[4 * i + 0] = fmaf(__uint_as_float(rb[4 * i + 0]), c2, -lb.x);
+              v[4 * i + 1] = fmaf(__uint_as_float(rb[4 * i + 1]), c2, -lb.y);
+              v[4 * i + 2] = fmaf(__uint_as_float(rb[4 * i + 2]), c2, -lb.z);
+              v[4 * i + 3] = fmaf(__uint_as_float(rb[4 * i + 3]), c2, -lb.w);
             }
             best = fmaxf(best, tree_max32(v));
           }
-          tc::fence_before_sync();
         }
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&tempty[acc])) : "memory");
-        float* pb = pbest + (kc & 1) * kChunk;
-        if (hf == 1) pb[key] = best;
-        epi_bar();
-        if (hf == 0 && !*abort_flag) {
-          best = fmaxf(best, pb[key]);
-          const int j = c * kChunk + key;
-          if (j < a.g.N) a.scores[(size_t)head * a.g.N + j] = exp2f(best);
+        tc::fence_before_sync();
+      }
+      free_acc(acc);
+      float* pb = pbest + (kc & 1) * kChunk;
+      if (hf == 1) pb[key] = best;
+      epi_bar();
+      if (hf == 0 && !*abort_flag) {
+        best = fmaxf(best, pb[key]);
+        const int j = c * kChunk + key;
+        if (j < a.g.N) a.scores[(size_t)head * a.g.N + j] = exp2f(best);
+      }
+      ++kc;
+    };
+
+    // Same chunk order as the producer and MMA warps: in segment seg, pass-1 chunk j of round
+    // seg is followed by pass-2 chunk j - 2 of round seg - 1.
+    for (int seg = 0; seg <= rounds; ++seg) {
+      if (seg < rounds)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) st[mt] = make_float2(-INFINITY, 0.f);
+      if (n == 0) {  // no keys here: still take part in the group's exchange
+        if (seg < rounds) publish(seg);
+        if (seg >= 1) {
+          lse_wait(seg - 1);
+          lse_release(seg - 1);
+        }
+        continue;
+      }
+      for (int j = 0; j < n + 2; ++j) {
+        if (seg < rounds && j < n) {
+          pass1_chunk(c0 + j);
+          if (j == n - 1) publish(seg);
+        }
+        if (seg >= 1 && j >= 2) {
+          if (j == 2) lse_wait(seg - 1);
+          pass2_chunk(seg - 1, c0 + j - 2);
+          if (j == n + 1) lse_release(seg - 1);
         }
       }
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) tc::tmem_dealloc(tmem, 2 * kAccCols);
+  if (warp == 1) tc::tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -404,7 +533,7 @@ static bool fused_maps(FusedMaps* m, const ScoreArgs& a, const ScoreWs& ws) {
 }
 
 size_t fused_xch_bytes(int M_pad) {
-  return (size_t)2 * kMaxSMs * (size_t)M_pad * sizeof(float2) + (size_t)kMaxSMs * sizeof(unsigned) + 256;
+  return (size_t)4 * kMaxSMs * (size_t)M_pad * sizeof(float2) + (size_t)4 * kMaxSMs * sizeof(unsigned) + 256;
 }
 
 int launch_score_fused(const ScoreArgs& a, const ScoreWs& ws, void* xch_base, cudaStream_t s) {
@@ -429,7 +558,7 @@ int launch_score_fused(const ScoreArgs& a, const ScoreWs& ws, void* xch_base, cu
   p.chunks_per_cta = (a.nchunk + gs - 1) / gs;
   p.qbytes = a.M_pad * D * 2;
   const int stage_bytes = kChunk * D * 2;
-  const int tail = 1024 + 64 * 8 + kMaxRows * 12 + 2 * kChunk * 4 + 256;
+  const int tail = 1024 + 512 + kMaxRows * 16 + 2 * kChunk * 4 + 256;  // align slack, barriers, lse2 x2, merge, pbest
   int stages = (smem_optin - 2 * p.qbytes - tail) / stage_bytes;
   if (stages > 6) stages = 6;
   if (stages < 2) return KVC_ERR_TOO_LARGE;
@@ -439,15 +568,17 @@ int launch_score_fused(const ScoreArgs& a, const ScoreWs& ws, void* xch_base, cu
   FusedXch xch;
   xch.part = reinterpret_cast<float2*>(xch_base);
   xch.arrive = reinterpret_cast<unsigned*>(static_cast<char*>(xch_base) +
-                                           (size_t)2 * kMaxSMs * (size_t)a.M_pad * sizeof(float2));
-  if (cudaMemsetAsync(xch.arrive, 0, sizeof(unsigned) * (size_t)p.ngroups, s) != cudaSuccess) return KVC_ERR_LAUNCH;
+                                           (size_t)4 * kMaxSMs * (size_t)a.M_pad * sizeof(float2));
+  if (cudaMemsetAsync(xch.arrive, 0, sizeof(unsigned) * 4 * (size_t)p.ngroups, s) != cudaSuccess)
+    return KVC_ERR_LAUNCH;
 
   FusedMaps maps;
   if (!fused_maps(&maps, a, ws)) return KVC_ERR_LAUNCH;
   const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
+  // four 128-column accumulators when both passes fit in 128 columns, else two of 256
   void (*kern)(const FusedMaps, ScoreArgs, ScoreWs, FusedPlan, FusedXch, float) =
-      D == 128 ? (a.M_pad > 128 ? score_fused_kernel<128, 2> : score_fused_kernel<128, 1>)
-               : (a.M_pad > 128 ? score_fused_kernel<64, 2> : score_fused_kernel<64, 1>);
+      D == 128 ? (a.M_pad > 128 ? score_fused_kernel<128, 2, 2> : score_fused_kernel<128, 1, 4>)
+               : (a.M_pad > 128 ? score_fused_kernel<64, 2, 2> : score_fused_kernel<64, 1, 4>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   int per_sm = 0;
