@@ -84,6 +84,126 @@ __global__ void __launch_bounds__(kCpThreads) compact_kernel(CompactArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Bulk-copy version: one warp per (head, K-or-V), a ring of kRing 16 KB shared-memory tiles.
+// Each maximal run of consecutive kept rows inside a 32-row block is fetched with one
+// cp.async.bulk (completion counted on the tile's mbarrier); each tile goes back with one
+// contiguous bulk store. Ordering is the forward sweep's: a tile's store is issued after that
+// tile's loads have landed, earlier tiles' loads landed before their own stores, and later
+// tiles only read rows at or beyond this tile's destination end.
+// ---------------------------------------------------------------------------
+constexpr int kRing = 3;
+constexpr int kTileBytes = 16384;
+
+__device__ __forceinline__ uint32_t sm_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__global__ void __launch_bounds__(32) compact_bulk_kernel(CompactArgs a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kRing * kTileBytes);
+  const int lane = threadIdx.x;
+  const int head = blockIdx.x;
+  const int l = head / (a.g.B * a.g.Hkv), bh = head % (a.g.B * a.g.Hkv);
+  const int rb = a.rowbytes;
+  const int T = kTileBytes / rb;  // rows per tile: 32, 64 or 128
+  char* base = static_cast<char*>(blockIdx.y ? a.V.p[l] : a.K.p[l]) + (size_t)bh * a.g.ncap * rb;
+  const int32_t* src = a.kept_idx + (size_t)head * a.g.N;
+  const int len = a.kept_len[head];
+  const int N = a.g.N;
+  if (a.validate) {
+    bool bad = len < 0 || len > N;
+    if (!bad)
+      for (int k = lane; k < len; k += 32) {
+        const int v = src[k];
+        bad |= v < k || v >= N || (k > 0 && v <= src[k - 1]);
+      }
+    if (__any_sync(kFull, bad)) {
+      if (lane == 0 && blockIdx.y == 0) status_or(a.status, KVC_STATUS_BAD_INDEX);
+      return;
+    }
+  }
+  // first index that moves: smallest k with src[k] != k (src[k] - k never decreases)
+  int lo = 0, hi = len;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (src[mid] == mid) lo = mid + 1; else hi = mid;
+  }
+  const int first = lo;
+  if (first >= len) return;
+  const int ntiles = (len - first + T - 1) / T;
+  if (lane == 0) {
+    for (int i = 0; i < kRing; ++i) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(sm_u32(&bar[i])));
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncwarp();
+
+  auto issue_loads = [&](int i) {
+    const int s = i % kRing;
+    const int k0 = first + i * T;
+    const int nrows = min(T, len - k0);
+    uint8_t* dst = sm + s * kTileBytes;
+    if (lane == 0)
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(sm_u32(&bar[s])),
+                   "r"(nrows * rb)
+                   : "memory");
+    __syncwarp();
+    for (int r0 = 0; r0 < nrows; r0 += 32) {
+      const int r = r0 + lane;
+      const bool live = r < nrows;
+      const int sk = live ? src[k0 + r] : 0;
+      const int prev = (live && r > r0) ? src[k0 + r - 1] : -2;
+      const bool start = live && (r == r0 || prev + 1 != sk);
+      const unsigned starts = __ballot_sync(kFull, start);
+      if (start) {
+        const unsigned later = (lane < 31) ? (starts >> (lane + 1)) : 0u;
+        const int blk_end = min(r0 + 32, nrows);
+        const int end = later ? (r + 1 + __ffs(later) - 1) : blk_end;
+        const uint32_t bytes = (uint32_t)((end - r) * rb);
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                sm_u32(dst + r * rb)),
+            "l"(base + (size_t)sk * rb), "r"(bytes), "r"(sm_u32(&bar[s]))
+            : "memory");
+      }
+    }
+  };
+
+  const int pro = ntiles < kRing ? ntiles : kRing;
+  for (int i = 0; i < pro; ++i) issue_loads(i);
+  bool ok = true;
+  for (int i = 0; i < ntiles && ok; ++i) {
+    const int s = i % kRing;
+    const int k0 = first + i * T;
+    const int nrows = min(T, len - k0);
+    if (lane == 0) {
+      const uint32_t a0 = sm_u32(&bar[s]), par = (uint32_t)((i / kRing) & 1);
+      bool done = false;
+      for (uint32_t it = 0; it < (1u << 24) && !done; ++it) {
+        uint32_t d;
+        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(d)
+                     : "r"(a0), "r"(par)
+                     : "memory");
+        done = d != 0;
+      }
+      if (!done) {
+        status_or(a.status, KVC_STATUS_TIMEOUT);
+        ok = false;
+      } else {
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(base + (size_t)k0 * rb),
+                     "r"(sm_u32(sm + s * kTileBytes)), "r"(nrows * rb)
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+        // the stage is reusable once this store has read it
+        asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+      }
+    }
+    ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+    if (ok && i + kRing < ntiles) issue_loads(i + kRing);
+  }
+  if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+  __syncwarp();
+}
+
 int launch_compact(const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V, const int32_t* kept_idx,
                    const int32_t* kept_len, int32_t* status, bool validate, cudaStream_t s) {
   const int heads = g.L * g.B * g.Hkv;
@@ -97,7 +217,10 @@ int launch_compact(const CacheGeom& g, int dtype, const LayerPtrs& K, const Laye
   a.status = status;
   a.rowbytes = g.D * (dtype == KVC_BF16 ? 2 : 4);
   a.validate = validate ? 1 : 0;
-  compact_kernel<<<dim3(heads, 2), kCpThreads, 0, s>>>(a);
+  const size_t smem = (size_t)kRing * kTileBytes + 64;
+  if (cudaFuncSetAttribute(compact_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return KVC_ERR_LAUNCH;
+  compact_bulk_kernel<<<dim3(heads, 2), 32, smem, s>>>(a);
   return launch_ok();
 }
 
