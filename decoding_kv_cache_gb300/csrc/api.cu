@@ -220,4 +220,56 @@ int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void*
   return launch_compact(g, c->dtype, K, V, ki, kept_len, status, false, s);
 }
 
+// ---------------------------------------------------------------------------
+// kvc_score without a caller workspace: scratch lives in a fixed device region.
+// ---------------------------------------------------------------------------
 }  // extern "C"
+
+#include <mutex>
+
+namespace kvc {
+namespace {
+// The region every kvc_score_static call on a device uses (see kvc.h for sharing rules).
+static __device__ __align__(256) unsigned char g_score_scratch[KVC_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the region on the current device, looked up once per device with that
+// device current (the symbol's name is only a host-side stand-in). NULL on failure.
+void* static_scratch() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_score_scratch) != cudaSuccess) return nullptr;
+    g_scratch_addr[dev] = p;
+  }
+  return g_scratch_addr[dev];
+}
+}  // namespace
+}  // namespace kvc
+
+extern "C" int kvc_score_static(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf,
+                                const int32_t* count, int32_t qmax, int32_t n_b, int64_t t, double rope_theta,
+                                float* scores, int32_t* beacon_picks, void* stream) {
+  CacheGeom g;
+  LayerPtrs K, V;
+  int rc = check_cache(c, &g, &K, &V);
+  if (rc) return rc;
+  rc = check_queries(c, q_recent, n_r, qbuf, count, qmax, n_b, rope_theta);
+  if (rc) return rc;
+  if (!scores) return KVC_ERR_INVALID_ARG;
+  const size_t need = score_ws_bytes(g, c->dtype, n_r, n_b, nullptr, nullptr);
+  if (need > (size_t)KVC_STATIC_SCRATCH_BYTES) return KVC_ERR_WORKSPACE;
+  void* scratch = static_scratch();
+  if (!scratch) return KVC_ERR_LAUNCH;
+  ScoreWs ws;
+  score_ws_bytes(g, c->dtype, n_r, n_b, &ws, scratch);
+  ScoreArgs a;
+  fill_score_args(&a, g, c->dtype, K, q_recent, n_r, qbuf, count, qmax, n_b, t, rope_theta, scores, beacon_picks,
+                  nullptr);
+  return launch_score(a, ws, static_cast<cudaStream_t>(stream));
+}

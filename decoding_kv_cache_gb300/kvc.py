@@ -20,7 +20,9 @@ KVC_STATUS_BUDGET_RANGE, KVC_STATUS_COUNT_RANGE, KVC_STATUS_BAD_INDEX = 0x1, 0x2
 KVC_MAX_LAYERS = 128
 
 EXPORTED = ("kvc_fps_update", "kvc_score_workspace_size", "kvc_score", "kvc_select", "kvc_compact",
-            "kvc_evict_workspace_size", "kvc_evict", "kvc_evict_launch_count", "kvc_strerror", "kvc_abi_version")
+            "kvc_evict_workspace_size", "kvc_evict", "kvc_evict_launch_count", "kvc_strerror", "kvc_abi_version",
+            "kvc_score_static")
+KVC_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class KvcError(RuntimeError):
@@ -59,6 +61,7 @@ def lib():
         "kvc_evict": (C.c_int, [pc, vp, i32, vp, vp, i32, i32, i64, dbl, i32, i32, vp, i32, vp, vp, vp, vp, vp, sz,
                                 vp]),
         "kvc_evict_launch_count": (C.c_int, [pc, i32, i32]),
+        "kvc_score_static": (C.c_int, [pc, vp, i32, vp, vp, i32, i32, i64, dbl, vp, vp, vp]),
         "kvc_strerror": (C.c_char_p, [C.c_int]),
         "kvc_abi_version": (C.c_int, []),
     }
@@ -163,6 +166,16 @@ def kvc_score(cache: Cache, q_recent: torch.Tensor, qbuf: torch.Tensor, count: t
     ws = _workspace(kvc_score_workspace_size(cache, n_r, n_b), scores.device, workspace)
     _check(lib().kvc_score(cache.ref, _p(q_recent), n_r, _p(qbuf), _p(count), qmax, n_b, int(t), float(rope_theta),
                            _p(scores), _p(beacon_picks), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def kvc_score_static(cache: Cache, q_recent: torch.Tensor, qbuf: torch.Tensor, count: torch.Tensor, n_b: int,
+                     t: int, rope_theta: float, scores: torch.Tensor, beacon_picks: Optional[torch.Tensor] = None,
+                     stream=None):
+    """kvc_score with the library's fixed scratch region instead of a workspace (allocates nothing;
+    see kvc.h for the size limit and the sharing rules)."""
+    n_r, qmax = q_recent.shape[-2], qbuf.shape[-2]
+    _check(lib().kvc_score_static(cache.ref, _p(q_recent), n_r, _p(qbuf), _p(count), qmax, n_b, int(t),
+                                  float(rope_theta), _p(scores), _p(beacon_picks), _stream(stream)))
 
 
 def kvc_select(scores: torch.Tensor, prefix: int, recent: int, kept_idx: torch.Tensor, kept_len: torch.Tensor,

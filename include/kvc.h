@@ -197,6 +197,33 @@ KVC_API int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, con
               const int32_t* budget, int32_t budget_all, int32_t* kept_idx, int32_t* kept_len, float* scores,
               int32_t* status, void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * kvc_score_static -- kvc_score for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a deployment convenience of this library.
+ *
+ * Some callers cannot call cudaMalloc or hand the library a workspace: a serving
+ * runtime that reserves all device memory up front for weights and its KV pool, or
+ * code that runs where allocation is not allowed (inside an allocator callback or an
+ * out-of-memory recovery path). This entry point computes exactly what kvc_score
+ * computes (same arguments, same results) but takes its scratch from a fixed region
+ * of KVC_STATIC_SCRATCH_BYTES that the library reserves in device memory when it is
+ * loaded; every GPU that loads the library holds that region until the process exits.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * - Size limit: the call is rejected with KVC_ERR_WORKSPACE, before any launch, when
+ *   kvc_score_workspace_size() for these arguments exceeds KVC_STATIC_SCRATCH_BYTES
+ *   (the Qwen3-4B-shaped step, about 10.6 MB, fits; larger caches do not).
+ * - Set-up: the first call on a device looks up the region's device address with that
+ *   device current; make that first call before any CUDA stream capture.
+ * - Sharing: every call on a device uses the same region and leaves its contents behind
+ *   (the library clears what must start at zero). Calls whose kernels overlap on the GPU
+ *   (two streams, or two threads) race on the region: order them on one stream.
+ */
+#define KVC_STATIC_SCRATCH_BYTES (16u << 20)
+KVC_API int kvc_score_static(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf,
+                             const int32_t* count, int32_t qmax, int32_t n_b, int64_t t, double rope_theta,
+                             float* scores, int32_t* beacon_picks, void* stream);
+
 /* Number of kernels one kvc_evict call with these arguments launches (host only;
  * for accounting, e.g. counting launches inside a timed region). */
 KVC_API int kvc_evict_launch_count(const kvc_cache* c, int32_t n_r, int32_t n_b);
