@@ -34,25 +34,52 @@ __host__ __device__ constexpr size_t fps_scratch_bytes(int npad) {
 }
 
 // Copy rows [0, n) of x (global, 16-byte aligned) into xs[npad][LD]; rows [n, npad) become zero.
+// bf16 rows go straight to shared memory with asynchronous 16-byte copies (LD * 2 is a multiple
+// of 16 bytes): stage_rows_issue only starts them and stage_rows_wait completes them, so other
+// memory work can overlap. fp32 rows (odd LD) pass through registers in batches of eight loads
+// per lane, each batch in flight before its stores; they are complete when issue returns.
 template <typename T, int D>
-__device__ __forceinline__ void stage_rows(const T* __restrict__ x, int n, int npad, T* xs) {
+__device__ __forceinline__ void stage_rows_issue(const T* __restrict__ x, int n, int npad, T* xs) {
   const int lane = threadIdx.x & 31;
   constexpr int per = 16 / sizeof(T);
   constexpr int vpr = D / per;
   constexpr int LD = Staging<T, D>::LD;
   const uint4* src = reinterpret_cast<const uint4*>(x);
-  for (int e = lane; e < npad * vpr; e += kWarp) {
-    const int r = e / vpr, c0 = (e % vpr) * per;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r < n) v = src[e];
-    if constexpr (sizeof(T) == 2) {
-      *reinterpret_cast<uint4*>(xs + r * LD + c0) = v;  // LD*2 is a multiple of 16 bytes
-    } else {
-      const T* t = reinterpret_cast<const T*>(&v);
+  const int total = npad * vpr;
+  if constexpr (sizeof(T) == 2) {
+    for (int e = lane; e < total; e += kWarp) {
+      const int r = e / vpr, c0 = (e % vpr) * per;
+      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(xs + r * LD + c0);
+      const bool live = r < n;  // a zero source size fills the 16 bytes with zeros
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src + (live ? e : 0)),
+                   "r"(live ? 16 : 0)
+                   : "memory");
+    }
+  } else {
+    for (int e0 = 0; e0 < total; e0 += 8 * kWarp) {
+      uint4 v[8];
 #pragma unroll
-      for (int q = 0; q < per; ++q) xs[r * LD + c0 + q] = t[q];
+      for (int u = 0; u < 8; ++u) {
+        const int e = e0 + u * kWarp + lane;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < total && e / vpr < n) v[u] = src[e];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = e0 + u * kWarp + lane;
+        if (e < total) {
+          const int r = e / vpr, c0 = (e % vpr) * per;
+          const T* t = reinterpret_cast<const T*>(&v[u]);
+#pragma unroll
+          for (int k = 0; k < per; ++k) xs[r * LD + c0 + k] = t[k];
+        }
+      }
     }
   }
+}
+template <typename T>
+__device__ __forceinline__ void stage_rows_wait() {
+  if constexpr (sizeof(T) == 2) asm volatile("cp.async.wait_all;\n" ::: "memory");
   __syncwarp();
 }
 
@@ -70,32 +97,57 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// G[i][j] (ld = npad + 1) = row_i . row_j over the staged bf16 rows, npad a multiple of 16.
+// G[i][j] (ld = npad + 1) = row_i . row_j over the staged bf16 rows, npad a multiple of 16 (<= 64).
+// Only tiles on or above the diagonal are formed (the A fragment of a tile row is loaded once and
+// shared by that row's tiles); an off-diagonal tile is also written mirrored.
 template <int D>
 __device__ __forceinline__ void gram_rows(const __nv_bfloat16* xs, int npad, float* G) {
   const int lane = threadIdx.x & 31;
   constexpr int LD = Staging<__nv_bfloat16, D>::LD;
   const int ldg = npad + 1;
-  for (int mt = 0; mt < npad / 16; ++mt)
-    for (int np = 0; np < npad / 16; ++np) {
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  const int nt = npad / 16;
+  for (int mt = 0; mt < nt; ++mt) {
+    float acc[4][2][4];
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t af[4], bf[4];
-        ldsm_x4(af, xs + (mt * 16 + (lane & 15)) * LD + ks * 16 + (lane >> 4) * 8);
-        ldsm_x4(bf, xs + (np * 16 + ((lane >> 4) << 3) + (lane & 7)) * LD + ks * 16 + ((lane >> 3) & 1) * 8);
-        mma_16816(acc[0], af, bf[0], bf[1]);
-        mma_16816(acc[1], af, bf[2], bf[3]);
-      }
-      const int r0 = mt * 16 + (lane >> 2), cb = np * 16 + 2 * (lane & 3);
+    for (int t = 0; t < 4; ++t)
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        G[r0 * ldg + cb + 8 * t] = acc[t][0];
-        G[r0 * ldg + cb + 8 * t + 1] = acc[t][1];
-        G[(r0 + 8) * ldg + cb + 8 * t] = acc[t][2];
-        G[(r0 + 8) * ldg + cb + 8 * t + 1] = acc[t][3];
-      }
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[t][h][k] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t af[4];
+      ldsm_x4(af, xs + (mt * 16 + (lane & 15)) * LD + ks * 16 + (lane >> 4) * 8);
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (mt + t < nt) {
+          uint32_t bf[4];
+          ldsm_x4(bf, xs + ((mt + t) * 16 + ((lane >> 4) << 3) + (lane & 7)) * LD + ks * 16 + ((lane >> 3) & 1) * 8);
+          mma_16816(acc[t][0], af, bf[0], bf[1]);
+          mma_16816(acc[t][1], af, bf[2], bf[3]);
+        }
     }
+    const int r0 = mt * 16 + (lane >> 2);
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (mt + t < nt) {
+        const int cb = (mt + t) * 16 + 2 * (lane & 3);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = cb + 8 * h;
+          G[r0 * ldg + c] = acc[t][h][0];
+          G[r0 * ldg + c + 1] = acc[t][h][1];
+          G[(r0 + 8) * ldg + c] = acc[t][h][2];
+          G[(r0 + 8) * ldg + c + 1] = acc[t][h][3];
+          if (t > 0) {
+            G[c * ldg + r0] = acc[t][h][0];
+            G[(c + 1) * ldg + r0] = acc[t][h][1];
+            G[c * ldg + r0 + 8] = acc[t][h][2];
+            G[(c + 1) * ldg + r0 + 8] = acc[t][h][3];
+          }
+        }
+      }
+  }
   __syncwarp();
 }
 
@@ -115,6 +167,13 @@ __device__ __forceinline__ void gram_rows(const float* xs, int npad, float* G) {
       G[i * ldg + j] = s0 + s1;
     }
   __syncwarp();
+}
+
+// Unsigned key with the order of the float (NaN excluded); -0 is first made +0 so that equal
+// floats give equal keys.
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+  const uint32_t b = __float_as_uint(f + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
 // Greedy FPS from the Gram matrix of n <= 64 rows: m picks, written ascending to picks[0..m)
@@ -157,15 +216,11 @@ __device__ __forceinline__ void fps_gram(const float* G, int ldg, int n, int m, 
         bi = i;
       }
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, bv, o);
-      const int oi = __shfl_xor_sync(kFull, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
+    // warp argmax, ties to the lower row: the largest order-preserving key, then the lowest row
+    // among the lanes holding it (two warp reductions instead of a five-step shuffle tree)
+    const uint32_t key = ordered_key(bv);
+    const uint32_t kmax = __reduce_max_sync(kFull, key);
+    bi = (int)__reduce_min_sync(kFull, key == kmax ? (uint32_t)bi : 0xffffffffu);
     const float invj = inv_of(bi);
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
@@ -183,17 +238,21 @@ __device__ __forceinline__ void fps_gram(const float* G, int ldg, int n, int m, 
   __syncwarp();
 }
 
-// Stage rows [0, n) of x, form their Gram matrix and run FPS for m picks (all n rows are
-// picked when m >= n). Scratch layout: staged rows, then G, then picks (fps_scratch_bytes).
-// Returns the staged rows; *picks_out points at the picks.
+// FPS over a staged buffer. Scratch layout: staged rows, then G, then picks (fps_scratch_bytes).
+// fps_buffer_issue starts staging rows [0, n) of x; fps_buffer_finish completes it, forms the Gram
+// matrix and runs FPS for m picks (all n rows are picked when m >= n). finish returns the staged
+// rows; *picks_out points at the picks.
 template <typename T, int D>
-__device__ __forceinline__ T* fps_buffer(const T* __restrict__ x, int n, int m, int npad, void* scratch,
-                                         int** picks_out) {
+__device__ __forceinline__ void fps_buffer_issue(const T* __restrict__ x, int n, int npad, void* scratch) {
+  stage_rows_issue<T, D>(x, n, npad, reinterpret_cast<T*>(scratch));
+}
+template <typename T, int D>
+__device__ __forceinline__ T* fps_buffer_finish(int n, int m, int npad, void* scratch, int** picks_out) {
   T* xs = reinterpret_cast<T*>(scratch);
   float* G = reinterpret_cast<float*>(xs + (size_t)npad * Staging<T, D>::LD);
   int* picks = reinterpret_cast<int*>(G + (size_t)npad * (npad + 1));
   *picks_out = picks;
-  stage_rows<T, D>(x, n, npad, xs);
+  stage_rows_wait<T>();
   if (m < n) {
     gram_rows<D>(xs, npad, G);
     fps_gram(G, npad + 1, n, m, picks);
@@ -202,6 +261,12 @@ __device__ __forceinline__ T* fps_buffer(const T* __restrict__ x, int n, int m, 
     __syncwarp();
   }
   return xs;
+}
+template <typename T, int D>
+__device__ __forceinline__ T* fps_buffer(const T* __restrict__ x, int n, int m, int npad, void* scratch,
+                                         int** picks_out) {
+  fps_buffer_issue<T, D>(x, n, npad, scratch);
+  return fps_buffer_finish<T, D>(n, m, npad, scratch, picks_out);
 }
 
 }  // namespace kvc

@@ -74,6 +74,8 @@ struct ScoreArgs {
   int32_t* status;
   int M, M_pad, M_n, nchunk;  // rows, rows stored per head, rows rounded to 16, key chunks
   float2 rope[64];            // (cos, sin) of t * theta^(-2i/D), i < D/2, from fp64
+  unsigned long long* xch_zero;  // words the observation kernel zeroes for the scoring kernel, or null
+  long long xch_zero_words;
 };
 
 int obs_rows(int M, int dtype);
@@ -82,6 +84,18 @@ size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, ScoreWs* 
 int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s);
 size_t fused_xch_bytes(int M_pad);
 int launch_score_fused(const ScoreArgs& a, const ScoreWs& ws, void* xch_base, cudaStream_t s);
+// Single-read kernel (bf16, 128 observation rows, at most 256 keys per SM per head): the plan, or
+// false when it does not apply; the exchange words it needs zeroed (in ws.part); the launch.
+struct FusedPlan {
+  int group_size;      // CTAs per head
+  int ngroups;         // heads processed at once
+  int chunks_per_cta;  // key chunks per CTA per head
+  int stages;          // K ring depth
+  int qbytes;          // one observation tile: M_pad * D * 2
+};
+bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem);
+long long score_resident_words(const FusedPlan& p);
+int launch_score_resident(const ScoreArgs& a, const ScoreWs& ws, const FusedPlan& p, size_t smem, cudaStream_t s);
 
 int launch_select(const float* scores, int heads, int N, int P, int R, const int32_t* budget, int budget_all,
                   int32_t* kept_idx, int32_t* kept_len, int32_t* status, cudaStream_t s);

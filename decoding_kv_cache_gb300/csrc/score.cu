@@ -10,8 +10,11 @@
 //   (host)       cos/sin of t * theta^(-2i/D) in fp64, rounded to fp32, passed as a parameter
 //   build_obs    per KV head: copy recent rows, pick beacons (FPS when the buffer
 //                holds more than n_b), rotate them to t, round to storage type  (heads CTAs)
-//   bf16 caches: score_fused (score_fused.cu), both passes on the tensor cores in one
-//                persistent kernel
+//   bf16 caches: both passes on the tensor cores in one persistent kernel:
+//                score_resident (score_resident.cu) when the observation tile is one
+//                128-row MMA tile and a head spreads over at most one CTA per SM in
+//                256-key pieces (pass-1 logits kept in TMEM, every key read once);
+//                otherwise score_fused (score_fused.cu), which reads the keys twice
 //   fp32 caches: pass1 / combine / pass2 below on CUDA cores:
 //     pass1      per (key chunk, head): per-row chunk max and sum of exp2
 //     combine    per head: merge the partials into lse2 per row
@@ -41,43 +44,81 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
   const T* qrec = static_cast<const T*>(a.q_recent);
   const T* qbuf = static_cast<const T*>(a.qbuf);
 
+  // the scoring kernel's exchange words start at zero (this CTA's share of them)
+  if (a.xch_zero) {
+    const long long per = (a.xch_zero_words + gridDim.x - 1) / gridDim.x;
+    const long long lo = (long long)blockIdx.x * per;
+    const long long hi = lo + per < a.xch_zero_words ? lo + per : a.xch_zero_words;
+    for (long long w = lo + threadIdx.x; w < hi; w += blockDim.x) a.xch_zero[w] = 0ull;
+  }
+  // rotation table in shared memory (a per-lane index into the parameter block would serialize)
+  float2* rope_s = reinterpret_cast<float2*>(smem_raw + (size_t)nw * ((fps_scratch_bytes<T, D>(npad) + 15) & ~(size_t)15));
+  for (int i = threadIdx.x; i < hd; i += blockDim.x) rope_s[i] = a.rope[i];
+  __syncthreads();
+  // beacon rows are rotated lpr lanes per row, each lane `per` consecutive pairs (i, i + D/2):
+  // one 16-byte store per half-row and lane
+  constexpr int per = 16 / (int)sizeof(T);
+  constexpr int lpr = (D / 2) / per;
+  constexpr int rpi = kWarp / lpr;
+  const int i0 = (lane % lpr) * per, rsel = lane / lpr;
+
   for (int g = warp; g < G; g += nw) {
     const int hq = h * G + g;
     const size_t qh = ((size_t)l * B + b) * Hq + hq;
     T* orow = obs + (size_t)g * per_q * D;
-    // recent queries: already rotated to their own positions, copied as stored (16-byte vectors)
-    {
-      const uint4* qr = reinterpret_cast<const uint4*>(qrec + qh * a.n_r * D);
-      uint4* od = reinterpret_cast<uint4*>(orow);
-      const int nv = a.n_r * D * (int)sizeof(T) / 16;
-      for (int e = lane; e < nv; e += kWarp) od[e] = qr[e];
-    }
-    for (int r = lane; r < a.n_r; r += kWarp) valid[g * per_q + r] = 1;
-    // beacons: the buffer itself when it holds at most n_b rows, else FPS down to n_b
     int c = a.qmax > 0 ? a.count[qh] : 0;
     if (c < 0 || c > a.qmax) {
       if (lane == 0) status_or(a.status, KVC_STATUS_COUNT_RANGE);
       c = c < 0 ? 0 : a.qmax;
     }
+    // start staging the query buffer, then copy the recent queries while it is in flight
+    fps_buffer_issue<T, D>(qbuf + qh * a.qmax * D, c, npad, scratch);
+    // recent queries: already rotated to their own positions, copied as stored (16-byte vectors,
+    // eight loads per lane in flight before their stores)
+    {
+      const uint4* qr = reinterpret_cast<const uint4*>(qrec + qh * a.n_r * D);
+      uint4* od = reinterpret_cast<uint4*>(orow);
+      const int nv = a.n_r * D * (int)sizeof(T) / 16;
+      for (int e0 = 0; e0 < nv; e0 += 8 * kWarp) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (e0 + u * kWarp + lane < nv) v[u] = qr[e0 + u * kWarp + lane];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (e0 + u * kWarp + lane < nv) od[e0 + u * kWarp + lane] = v[u];
+      }
+    }
+    for (int r = lane; r < a.n_r; r += kWarp) valid[g * per_q + r] = 1;
+    // beacons: the buffer itself when it holds at most n_b rows, else FPS down to n_b
     int* pk;
-    const T* xs = fps_buffer<T, D>(qbuf + qh * a.qmax * D, c, a.n_b, npad, scratch, &pk);
+    const T* xs = fps_buffer_finish<T, D>(c, a.n_b, npad, scratch, &pk);
     const int nb = c < a.n_b ? c : a.n_b;
-    for (int k = 0; k < a.n_b; ++k) {
+    for (int k0 = 0; k0 < a.n_b; k0 += rpi) {
+      const int k = k0 + rsel;
+      if (k >= a.n_b) continue;
       T* dst = orow + (size_t)(a.n_r + k) * D;
+      alignas(16) T o1[per];
+      alignas(16) T o2[per];
       if (k < nb) {
         const T* src = xs + pk[k] * LD;
-        for (int i = lane; i < hd; i += kWarp) {
-          const float2 cs = a.rope[i];
+#pragma unroll
+        for (int u = 0; u < per; ++u) {
+          const int i = i0 + u;
+          const float2 cs = rope_s[i];
           const float x0 = to_f32(src[i]), x1 = to_f32(src[i + hd]);
           // each product and the sum rounded separately (no fused multiply-add), so the
           // rounding to the storage type below is a reproducible decision
-          dst[i] = from_f32<T>(__fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y)));
-          dst[i + hd] = from_f32<T>(__fadd_rn(__fmul_rn(x1, cs.x), __fmul_rn(x0, cs.y)));
+          o1[u] = from_f32<T>(__fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y)));
+          o2[u] = from_f32<T>(__fadd_rn(__fmul_rn(x1, cs.x), __fmul_rn(x0, cs.y)));
         }
       } else {
-        for (int i = lane; i < D; i += kWarp) dst[i] = from_f32<T>(0.f);
+#pragma unroll
+        for (int u = 0; u < per; ++u) o1[u] = o2[u] = from_f32<T>(0.f);
       }
-      if (lane == 0) valid[g * per_q + a.n_r + k] = k < nb ? 1 : 0;
+      *reinterpret_cast<uint4*>(dst + i0) = *reinterpret_cast<const uint4*>(o1);
+      *reinterpret_cast<uint4*>(dst + i0 + hd) = *reinterpret_cast<const uint4*>(o2);
+      if (i0 == 0) valid[g * per_q + a.n_r + k] = k < nb ? 1 : 0;
     }
     if (a.beacon_picks)
       for (int k = lane; k < a.n_b; k += kWarp) a.beacon_picks[qh * a.n_b + k] = k < nb ? pk[k] : -1;
@@ -216,8 +257,15 @@ static bool set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess;
 }
 
-int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s) {
+int launch_score(const ScoreArgs& a_in, const ScoreWs& ws, cudaStream_t s) {
+  ScoreArgs a = a_in;
   const int heads = a.g.L * a.g.B * a.g.Hkv;
+  // the single-read kernel's plan is fixed first: the observation kernel zeroes its exchange words
+  FusedPlan rp;
+  size_t rsmem = 0;
+  const bool resident = a.dtype == KVC_BF16 && score_resident_plan(a, &rp, &rsmem);
+  a.xch_zero = resident ? reinterpret_cast<unsigned long long*>(ws.part) : nullptr;
+  a.xch_zero_words = resident ? score_resident_words(rp) : 0;
   const int D = a.g.D;
   const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
   // observation rows: one warp per query head of the group
@@ -229,7 +277,7 @@ int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s) {
   const size_t per_warp = (raw + 15) & ~(size_t)15;
   int nw = G < 8 ? G : 8;
   while (nw > 1 && per_warp * nw > 200u * 1024u) --nw;
-  const size_t obs_smem = per_warp * nw;
+  const size_t obs_smem = per_warp * nw + 64 * sizeof(float2);  // + the rotation table
   {
     bool ok;
     if (a.dtype == KVC_BF16) {
@@ -247,6 +295,7 @@ int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s) {
 
   const dim3 grid(a.nchunk, heads);
   if (a.dtype == KVC_BF16) {
+    if (resident) return launch_score_resident(a, ws, rp, rsmem, s);
     return launch_score_fused(a, ws, ws.part, s);
   } else {
     const size_t sm1 = sizeof(float) * ((size_t)a.M_pad * (D + 1) + (size_t)kChunk * D);

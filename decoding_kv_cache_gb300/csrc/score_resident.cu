@@ -1,0 +1,514 @@
+// score_resident.cu -- bf16 scoring that reads every key once: pass-1 logits stay in tensor memory.
+//
+// What it computes is kvc_score's definition (BeaconKV write-up, "打分时的 RoPE 对齐": a key's
+// importance is the max over the observation rows of its softmax weight over all cached keys).
+// The softmax needs each row's log-sum-exp over ALL keys of the head before any score exists.
+// The two-pass kernel (score_fused.cu) loads every key twice for that; here the logits
+// S = Q K^T of pass 1 are kept in TMEM until the head's log-sum-exp is known, and pass 2
+// reads them back from TMEM. K crosses the memory system once.
+//
+// Capacity sets the shape. With an observation tile of 128 rows (one MMA tile: lane = row), a
+// 128-key chunk of logits is 128 TMEM columns, so an SM holds four chunks. Each CTA takes two
+// chunks of a head per round and double-buffers rounds: round r+1's MMAs and pass 1 run while
+// the group exchanges round r's partials. A head of N keys is spread over ceil(N / 256) CTAs
+// (a "group"); the grid is #groups x group size CTAs, at most one per SM, launched cooperatively
+// because group partners wait on one another.
+//
+// Roles (all derive the same chunk sequence from blockIdx; no queue):
+//   warp 0      TMA producer: each round's observation tile into one of two Q buffers, then the
+//               round's key chunks into a ring of K stages.
+//   warp 1      tcgen05.mma issuer (one thread): S = Q K^T per chunk into TMEM accumulator
+//               (round & 1) * 2 + j.
+//   warps 2-9   epilogue, two warps per TMEM lane quarter (one column half each), alternating:
+//               pass 1 of round r: each thread owns one row and folds its columns into the
+//               row's running (max, sum of exp2); the quarter's two warps merge and publish the
+//               row's partial. Pass 2 of round r - 1 (whose exchange ran meanwhile): a chunk's
+//               TMEM values are read in the 16x256b fragment shape (each thread: 4 of the
+//               warp's 32 rows x 2 columns per 8-column group) and its accumulator freed;
+//               s*c2 - lse2 and the max over the 4 rows in registers, then a 3-step
+//               reduce-scatter over the 8 lanes sharing a column pair leaves each lane one
+//               column's max over 32 rows (7 shuffles per 32 columns); the eight warps' maxima
+//               meet in shared memory and one thread per key writes exp2 of the max.
+//   warp 10     exchange: polls the group's partials of a round and merges them into lse2,
+//               all of a batch's loads in flight at once (the merge is on the critical path).
+// Exchange protocol: a partial is one 64-bit word, the row's log2-sum-exp2 over the CTA's keys
+// in the low half and round + 1 in the high half, written with one relaxed store; a reader
+// accepts a word once its tag matches, so data and "published" travel together and nobody
+// waits for a store to be acknowledged. The observation kernel that runs just before zeroes them.
+// Every wait is bounded; a wait that gives up sets KVC_STATUS_TIMEOUT and a CTA-wide abort flag,
+// after which every role skips its work but still passes every named barrier. Before exiting,
+// the producer waits (bounded) for its own loads in flight and the MMA thread for its MMAs.
+#include "score_tc.cuh"
+
+namespace kvc {
+
+constexpr int kResChunks = 2;    // key chunks per CTA per round
+constexpr int kResRows = 128;    // observation rows per head this kernel handles (one MMA tile)
+constexpr int kResAcc = 2 * kResChunks;
+
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Max-reduce-scatter over lane bits 4, 3, 2: on entry w[k] is this lane's value for slot k; on
+// exit w[0] holds the max, over the 8 lanes that differ only in those bits, of slot (lane >> 2) & 7.
+__device__ __forceinline__ void reduce_scatter_max8(float (&w)[8], int lane) {
+#pragma unroll
+  for (int h = 4, bit = 16; h; h >>= 1, bit >>= 1) {
+    const bool up = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? w[i] : w[i + h];
+      const float keep = up ? w[i + h] : w[i];
+      w[i] = fmaxf(keep, __shfl_xor_sync(kFull, send, bit));
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    score_resident_kernel(const __grid_constant__ FusedMaps maps, ScoreArgs a, ScoreWs ws, FusedPlan p, FusedXch xch,
+                          float c2) {
+  constexpr int HALVES = D / 64;
+  constexpr int kStage = kChunk * D * 2;
+  constexpr int kQBytes = kResRows * D * 2;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* Qs = align1024(smraw);
+  uint8_t* Ks = Qs + 2 * kQBytes;
+  const int S = p.stages;
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(Ks + S * kStage);
+  uint64_t* kempty = kfull + S;
+  uint64_t* qfull = kempty + S;
+  uint64_t* qempty = qfull + 2;
+  uint64_t* tfull = qempty + 2;
+  uint64_t* tempty = tfull + kResAcc;
+  uint64_t* lfull = tempty + kResAcc;
+  uint64_t* lempty = lfull + 2;
+  uint64_t* mdone = lempty + 2;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(mdone + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 1);
+  float* lse2s = reinterpret_cast<float*>(Ks + S * kStage + 512);  // [2][128]
+  float2* merge = reinterpret_cast<float2*>(lse2s + 2 * kResRows);  // [2][128]
+  float* pbest = reinterpret_cast<float*>(merge + 2 * kResRows);    // [2][2 chunks][4][128]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&kfull[i], 1);
+      tc::mbar_init(&kempty[i], 1);
+    }
+    for (int i = 0; i < kResAcc; ++i) {
+      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tempty[i], kEpiWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&qfull[i], 1);
+      tc::mbar_init(&qempty[i], 1);
+      tc::mbar_init(&lfull[i], 1);
+      tc::mbar_init(&lempty[i], kEpiWarps);
+    }
+    tc::mbar_init(mdone, 1);
+    *abort_flag = 0;
+    tc::mbar_fence_init();
+  }
+  if (warp == 1) tc::tmem_alloc(slot, 512);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *slot;
+
+  const int heads = a.g.L * a.g.B * a.g.Hkv;
+  const int group = blockIdx.x / p.group_size, rank = blockIdx.x % p.group_size;
+  const int rounds = group < heads ? (heads - group + p.ngroups - 1) / p.ngroups : 0;
+  const int c0 = rank * p.chunks_per_cta;
+  const int n = max(0, min(c0 + p.chunks_per_cta, a.nchunk) - c0);  // chunks per round, the same every round
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t kc = 0;
+      int qloads = 0;
+      for (int r = 0; r < rounds && !*abort_flag; ++r) {
+        const int head = group + r * p.ngroups;
+        const int qb = r & 1;
+        if (r >= 2 && !wait_or_abort(&qempty[qb], ((r - 2) >> 1) & 1, abort_flag, a.status)) break;
+        tc::mbar_expect_tx(&qfull[qb], (uint32_t)kQBytes);
+        for (int h = 0; h < HALVES; ++h)
+          tc::tma_load_2d(Qs + qb * kQBytes + h * (kResRows * 128), &maps.q, &qfull[qb], h * 64, head * kResRows);
+        qloads = r + 1;
+        const int l = head / (a.g.B * a.g.Hkv), bh = head % (a.g.B * a.g.Hkv);
+        bool stop = false;
+        for (int j = 0; j < n; ++j) {
+          const int s = kc % S;
+          if (kc >= (uint32_t)S && !wait_or_abort(&kempty[s], ((kc / S) - 1) & 1, abort_flag, a.status)) {
+            stop = true;
+            break;
+          }
+          tc::mbar_expect_tx(&kfull[s], (uint32_t)kStage);
+          for (int h = 0; h < HALVES; ++h)
+            tc::tma_load_3d(Ks + s * kStage + h * 16384, &maps.k[l], &kfull[s], h * 64, (c0 + j) * kChunk, bh);
+          ++kc;
+        }
+        if (stop) break;
+      }
+      // Drain: every issued load has landed before the CTA exits (immediate on the normal path).
+      const uint32_t tail = kc < (uint32_t)S ? kc : (uint32_t)S;
+      for (uint32_t k = kc - tail; k < kc; ++k)
+        if (!tc::mbar_wait(&kfull[k % S], (k / S) & 1)) status_or(a.status, KVC_STATUS_TIMEOUT);
+      for (int r = qloads - 2 < 0 ? 0 : qloads - 2; r < qloads; ++r)
+        if (!tc::mbar_wait(&qfull[r & 1], (r >> 1) & 1)) status_or(a.status, KVC_STATUS_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t kc = 0;
+      const uint32_t id = tc::idesc_bf16(128, kChunk);
+      bool ok = true, issued = false;
+      for (int r = 0; r < rounds && ok && !*abort_flag; ++r) {
+        const int qb = r & 1;
+        if (!wait_or_abort(&qfull[qb], (r >> 1) & 1, abort_flag, a.status)) break;
+        tc::fence_after_sync();
+        const uint32_t qaddr = tc::smem_u32(Qs + qb * kQBytes);
+        for (int j = 0; j < n; ++j) {
+          const int s = kc % S;
+          const uint32_t acc = (uint32_t)(qb * kResChunks + j);
+          if (!wait_or_abort(&kfull[s], (kc / S) & 1, abort_flag, a.status) ||
+              (r >= 2 && !wait_or_abort(&tempty[acc], ((r >> 1) - 1) & 1, abort_flag, a.status))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t kaddr = tc::smem_u32(Ks + s * kStage);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            tc::umma_bf16(tmem + acc * kChunk,
+                          tc::desc_k_sw128(qaddr + (ks >> 2) * (kResRows * 128) + (ks & 3) * 32),
+                          tc::desc_k_sw128(kaddr + (ks >> 2) * 16384 + (ks & 3) * 32), id, ks > 0);
+          tc::umma_commit(&kempty[s]);
+          tc::umma_commit(&tfull[acc]);
+          issued = true;
+          ++kc;
+        }
+        if (ok) tc::umma_commit(&qempty[qb]);
+      }
+      // every MMA has completed before TMEM is released
+      if (issued) {
+        tc::umma_commit(mdone);
+        if (!tc::mbar_wait(mdone, 0)) status_or(a.status, KVC_STATUS_TIMEOUT);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2 + kEpiWarps) {
+    // ---------------- exchange warp: lse2 of every row once the group has published ----------------
+    const uint64_t* words = reinterpret_cast<const uint64_t*>(xch.part);
+    for (int round = 0; round < rounds && !*abort_flag; ++round) {
+      const int b = round & 1;
+      if (round >= 2 && !wait_or_abort(&lempty[b], ((round - 2) >> 1) & 1, abort_flag, a.status)) break;
+      const int head = group + round * p.ngroups;
+      bool valid[kResRows / kWarp];  // written by the observation kernel: safe to read early
+#pragma unroll
+      for (int i = 0; i < kResRows / kWarp; ++i) valid[i] = ws.valid[(size_t)head * kResRows + i * kWarp + lane] != 0;
+      // Slot round % 4 last held round - 4. A partner overwrites it (round + 4) only after its
+      // pass 1 of round + 4, which needs its TMEM buffer back from pass 2 of round + 2, which
+      // needs the whole group's partials of round + 2, which each CTA publishes only after its
+      // own pass 2 of round, i.e. after this warp has read slot round % 4.
+      const uint32_t tag = (uint32_t)round + 1u;
+      const uint64_t* grp = words + ((size_t)((round & 3) * p.ngroups + group) * p.group_size) * kResRows;
+      float mx[kResRows / kWarp], sm[kResRows / kWarp];
+#pragma unroll
+      for (int i = 0; i < kResRows / kWarp; ++i) {
+        mx[i] = -INFINITY;
+        sm[i] = 0.f;
+      }
+      bool ok = true;
+      for (int k0 = 0; k0 < p.group_size && ok; k0 += 8) {
+        // all of a batch's loads are issued before any is used: one L2 round trip per poll
+        uint64_t w[kResRows / kWarp][8];
+#pragma unroll
+        for (int i = 0; i < kResRows / kWarp; ++i)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            w[i][kk] = k0 + kk < p.group_size ? ld_relaxed_u64(&grp[(size_t)(k0 + kk) * kResRows + i * kWarp + lane])
+                                              : ((uint64_t)tag << 32) | __float_as_uint(-INFINITY);
+        for (uint32_t it = 0;; ++it) {
+          unsigned need = 0u;
+#pragma unroll
+          for (int i = 0; i < kResRows / kWarp; ++i)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              if ((uint32_t)(w[i][kk] >> 32) != tag) need |= 1u << (i * 8 + kk);
+          if (!__any_sync(kFull, need != 0u)) break;
+          if (it >= (1u << 22) || *abort_flag) {
+            ok = false;
+            if (lane == 0 && !*abort_flag) {
+              *abort_flag = 1;
+              status_or(a.status, KVC_STATUS_TIMEOUT);
+            }
+            break;
+          }
+          __nanosleep(32);
+#pragma unroll
+          for (int i = 0; i < kResRows / kWarp; ++i)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              if (need & (1u << (i * 8 + kk))) w[i][kk] = ld_relaxed_u64(&grp[(size_t)(k0 + kk) * kResRows + i * kWarp + lane]);
+        }
+#pragma unroll
+        for (int i = 0; i < kResRows / kWarp; ++i) {
+          float v[8];
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) v[kk] = __uint_as_float((uint32_t)w[i][kk]);
+          float bm = v[0];
+#pragma unroll
+          for (int kk = 1; kk < 8; ++kk) bm = fmaxf(bm, v[kk]);
+          const float nm = fmaxf(mx[i], bm);
+          if (nm > -INFINITY) {
+            float acc = mx[i] > -INFINITY ? sm[i] * exp2f(mx[i] - nm) : 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) acc += exp2f(v[kk] - nm);  // -inf partials add 0
+            mx[i] = nm;
+            sm[i] = acc;
+          }
+        }
+      }
+      if (!ok) break;
+      float* dst = lse2s + b * kResRows;
+#pragma unroll
+      for (int i = 0; i < kResRows / kWarp; ++i)
+        dst[i * kWarp + lane] = (valid[i] && sm[i] > 0.f) ? mx[i] + log2f(sm[i]) : INFINITY;
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&lfull[b])) : "memory");
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int e = warp - 2;  // 0..7
+    const int q = warp & 3;  // TMEM lane quarter this warp may read: rows q*32 .. q*32+31
+    const int hf = e >> 2;   // which 64 of a chunk's 128 columns
+    const int row = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    uint64_t* words = reinterpret_cast<uint64_t*>(xch.part);
+    // after the pass-2 reduce-scatter a lane holds slot (lane >> 2) & 7 of each 32-column block
+    const int slot8 = (lane >> 2) & 7;
+    const int col_in = 8 * (slot8 >> 1) + 2 * (lane & 3) + (slot8 & 1);
+
+    // pass 1 of a round: fold this thread's row over its column half of every chunk into the
+    // running (max, sum of exp2); the accumulators stay allocated for pass 2
+    auto pass1 = [&](int round) {
+      float2 st = make_float2(-INFINITY, 0.f);
+      for (int j = 0; j < n; ++j) {
+        const uint32_t acc = (uint32_t)((round & 1) * kResChunks + j);
+        const int c = c0 + j;
+        const bool go = !*abort_flag && wait_or_abort(&tfull[acc], (round >> 1) & 1, abort_flag, a.status);
+        if (!__all_sync(kFull, go)) continue;  // tcgen05.ld is warp-collective: decide per warp
+        tc::fence_after_sync();
+        uint32_t r0[32], r1[32];
+        const uint32_t col0 = tmem + acc * kChunk + lane_off + (uint32_t)(hf * 64);
+        tc::tmem_ld32_async(col0, r0);
+        tc::tmem_ld32_async(col0 + 32, r1);
+        tc::tmem_wait();
+        tc::tmem_regs_ready(r0);
+        tc::tmem_regs_ready(r1);
+        float v0[32], v1[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v0[i] = __uint_as_float(r0[i]);
+          v1[i] = __uint_as_float(r1[i]);
+        }
+        const int nvalid = min(kChunk, a.g.N - c * kChunk);
+        if (nvalid < kChunk) {  // ragged last chunk only
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (hf * 64 + i >= nvalid) v0[i] = -INFINITY;
+            if (hf * 64 + 32 + i >= nvalid) v1[i] = -INFINITY;
+          }
+        }
+        const float mraw = fmaxf(tree_max32(v0), tree_max32(v1));  // c2 > 0: scale the max once
+        if (mraw > -INFINITY) {
+          const float mn = fmaxf(st.x, mraw * c2);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            v0[i] = ex2_approx(fmaf(v0[i], c2, -mn));
+            v1[i] = ex2_approx(fmaf(v1[i], c2, -mn));
+          }
+          st = make_float2(mn, st.y * ex2_approx(st.x - mn) + (tree_sum32(v0) + tree_sum32(v1)));
+        }
+      }
+      // The two warps of a lane quarter merge their column halves; the hf == 0 warp publishes
+      // the row's log2-sum-exp2 over this CTA's keys as one tagged word (no fence). merge is
+      // double-buffered by round parity: pass 2 of round r, with its CTA-wide barrier, lies
+      // between publishing r and r + 2.
+      float2* mg = merge + (round & 1) * kResRows;
+      if (hf == 1) mg[row] = st;
+      asm volatile("bar.sync %0, 64;\n" ::"r"(2 + q) : "memory");
+      if (hf == 0) {
+        const float2 m = lse_merge(st, mg[row]);
+        const float part = m.y > 0.f ? m.x + log2f(m.y) : -INFINITY;
+        st_relaxed_u64(words + ((size_t)((round & 3) * p.ngroups + group) * p.group_size + rank) * kResRows + row,
+                       ((uint64_t)((uint32_t)round + 1u) << 32) | __float_as_uint(part));
+      }
+    };
+
+    // pass 2 of a round: per key, the max over rows of s*c2 - lse2, from the logits still in TMEM;
+    // each chunk's accumulator is freed as soon as its values are in registers.
+    auto pass2 = [&](int round) {
+      const bool have = !*abort_flag && wait_or_abort(&lfull[round & 1], (round >> 1) & 1, abort_flag, a.status);
+      float lse4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};  // rows q*32 + lane/4 + 8k
+      if (have)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) lse4[k] = lse2s[(round & 1) * kResRows + q * 32 + (lane >> 2) + 8 * k];
+      __syncwarp();
+      if (lane == 0)  // lse2 is in registers now: the exchange warp may refill the buffer
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&lempty[round & 1])) : "memory");
+      const int head = group + round * p.ngroups;
+      float best[kResChunks][2];
+#pragma unroll
+      for (int j = 0; j < kResChunks; ++j) best[j][0] = best[j][1] = -INFINITY;
+      if (__all_sync(kFull, have && !*abort_flag)) {
+        // this warp's pass 1 waited on every accumulator of the round, and lse2 exists only after
+        // this CTA published, so the MMAs are complete; the fence orders the reads after them
+        tc::fence_after_sync();
+#pragma unroll
+        for (int j = 0; j < kResChunks; ++j) {
+          if (j >= n) break;
+          const uint32_t acc = (uint32_t)((round & 1) * kResChunks + j);
+          const uint32_t base = tmem + acc * kChunk + lane_off + (uint32_t)(hf * 64);
+          uint32_t ra[2][16], rb[2][16];  // [block] x rows (t/4, t/4+8) and (t/4+16, t/4+24)
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb) {
+            tc::tmem_ld16x256_x4_async(base + (uint32_t)(cb * 32), ra[cb]);
+            tc::tmem_ld16x256_x4_async(base + (16u << 16) + (uint32_t)(cb * 32), rb[cb]);
+          }
+          tc::tmem_wait();
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb) {
+            tc::tmem_regs_ready(ra[cb]);
+            tc::tmem_regs_ready(rb[cb]);
+          }
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0)  // the accumulator is free as soon as its values are in registers
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&tempty[acc])) : "memory");
+          // a row without observations has lse2 = +inf, so its terms are -inf and drop out of the max
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb) {
+            float w[8];  // slot 2i + cc: column 8i + 2*(lane%4) + cc of the block, max over 4 rows
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                const float x0 = fmaf(__uint_as_float(ra[cb][4 * i + cc]), c2, -lse4[0]);
+                const float x1 = fmaf(__uint_as_float(ra[cb][4 * i + 2 + cc]), c2, -lse4[1]);
+                const float x2 = fmaf(__uint_as_float(rb[cb][4 * i + cc]), c2, -lse4[2]);
+                const float x3 = fmaf(__uint_as_float(rb[cb][4 * i + 2 + cc]), c2, -lse4[3]);
+                w[2 * i + cc] = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+              }
+            reduce_scatter_max8(w, lane);
+            best[j][cb] = w[0];
+          }
+        }
+      } else {
+        __syncwarp();
+        if (lane == 0)
+          for (int j = 0; j < n; ++j)
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(
+                             tc::smem_u32(&tempty[(round & 1) * kResChunks + j]))
+                         : "memory");
+      }
+      // pbest[buffer][chunk][quarter][column]; buffer = round parity (pass 2 of round r + 1 and its
+      // barrier lie between two uses)
+      float* pb = pbest + (round & 1) * (kResChunks * 4 * kChunk);
+#pragma unroll
+      for (int j = 0; j < kResChunks; ++j)
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) pb[(j * 4 + q) * kChunk + hf * 64 + cb * 32 + col_in] = best[j][cb];
+      epi_bar();
+      const int idx = e * 32 + lane;  // 256 threads: chunk idx / 128, key idx % 128
+      const int j = idx >> 7, col = idx & (kChunk - 1);
+      if (j < n && !*abort_flag) {
+        const float* pj = pb + j * 4 * kChunk;
+        const float m = fmaxf(fmaxf(pj[col], pj[kChunk + col]), fmaxf(pj[2 * kChunk + col], pj[3 * kChunk + col]));
+        const int key = (c0 + j) * kChunk + col;
+        if (key < a.g.N) a.scores[(size_t)head * a.g.N + key] = exp2f(m);
+      }
+    };
+
+    // Segment seg: pass 1 of round seg and its publication, then pass 2 of round seg - 1, whose
+    // exchange ran meanwhile.
+    for (int seg = 0; seg <= rounds; ++seg) {
+      if (seg < rounds) pass1(seg);
+      if (seg >= 1) pass2(seg - 1);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+// Shared memory: align slack, barriers, lse2 x2, merge x2, pbest x2; then two Q tiles and the ring.
+static int resident_tail_bytes() { return 1024 + 512 + 2 * kResRows * 4 + 2 * kResRows * 8 + 2 * kResChunks * 4 * kChunk * 4; }
+
+bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem) {
+  if (a.dtype != KVC_BF16 || a.M_pad != kResRows) return false;
+  int dev = 0, nsm = 0, smem_optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return false;
+  if (nsm > kMaxSMs) nsm = kMaxSMs;
+  const int D = a.g.D;
+  const int heads = a.g.L * a.g.B * a.g.Hkv;
+  p->chunks_per_cta = a.nchunk >= kResChunks ? kResChunks : 1;
+  p->group_size = (a.nchunk + p->chunks_per_cta - 1) / p->chunks_per_cta;
+  if (p->group_size > nsm) return false;
+  p->ngroups = nsm / p->group_size;
+  if (p->ngroups > heads) p->ngroups = heads;
+  p->qbytes = kResRows * D * 2;
+  const int stage_bytes = kChunk * D * 2;
+  int stages = (smem_optin - resident_tail_bytes() - 2 * p->qbytes) / stage_bytes;
+  if (stages > 6) stages = 6;
+  if (stages < 2) return false;
+  p->stages = stages;
+  *smem = (size_t)resident_tail_bytes() + 2 * (size_t)p->qbytes + (size_t)stages * stage_bytes;
+  return true;
+}
+
+// tagged partial words [4][ngroups][group_size][128]; zero, so no tag of an earlier launch matches
+long long score_resident_words(const FusedPlan& p) { return 4LL * p.ngroups * p.group_size * kResRows; }
+
+int launch_score_resident(const ScoreArgs& a, const ScoreWs& ws, const FusedPlan& p, size_t smem, cudaStream_t s) {
+  const int D = a.g.D;
+  FusedXch xch;
+  xch.part = ws.part;
+  xch.arrive = nullptr;
+  FusedMaps maps;
+  if (!fused_maps(&maps, a, ws)) return KVC_ERR_LAUNCH;
+  const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
+  void (*kern)(const FusedMaps, ScoreArgs, ScoreWs, FusedPlan, FusedXch, float) =
+      D == 128 ? score_resident_kernel<128> : score_resident_kernel<64>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return KVC_ERR_LAUNCH;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFusedThreads, smem) != cudaSuccess ||
+      per_sm < 1)
+    return KVC_ERR_LAUNCH;
+  ScoreArgs aa = a;
+  ScoreWs wss = ws;
+  FusedPlan pp = p;
+  float cc = c2;
+  void* args[] = {(void*)&maps, (void*)&aa, (void*)&wss, (void*)&pp, (void*)&xch, (void*)&cc};
+  if (cudaLaunchCooperativeKernel((const void*)kern, dim3(p.ngroups * p.group_size), dim3(kFusedThreads), args, smem,
+                                  s) != cudaSuccess)
+    return KVC_ERR_LAUNCH;
+  return KVC_OK;
+}
+
+}  // namespace kvc

@@ -24,6 +24,10 @@ CASES = [
     ("llama8b-planted", dict(L=1, B=2, N=700)),
     ("qwen7b-reasonalloc", dict(L=2, B=2, N=1500)),
     ("qwen3-14b-long", dict(L=1, B=1, N=2100)),
+    # 512 heads over 76 groups of 2 CTAs: 7 rounds, so the exchange slots and TMEM buffers wrap
+    ("qwen3-4b", dict(L=8, B=8, N=300, D=64)),
+    # a 128-row tile whose keys exceed 256 per SM: the two-pass kernel takes it
+    ("qwen3-4b", dict(L=1, Hq=4, Hkv=1, N=50000)),
 ]
 
 
