@@ -66,13 +66,15 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
     const int hq = h * G + g;
     const size_t qh = ((size_t)l * B + b) * Hq + hq;
     T* orow = obs + (size_t)g * per_q * D;
+    // Start staging the whole query buffer at once (rows at or past its count are staged too but
+    // never read: FPS and the Gram entries it uses involve live rows only), read the count and
+    // copy the recent queries while the copies are in flight.
+    fps_buffer_issue<T, D>(qbuf + qh * a.qmax * D, a.qmax, npad, scratch);
     int c = a.qmax > 0 ? a.count[qh] : 0;
     if (c < 0 || c > a.qmax) {
       if (lane == 0) status_or(a.status, KVC_STATUS_COUNT_RANGE);
       c = c < 0 ? 0 : a.qmax;
     }
-    // start staging the query buffer, then copy the recent queries while it is in flight
-    fps_buffer_issue<T, D>(qbuf + qh * a.qmax * D, c, npad, scratch);
     // recent queries: already rotated to their own positions, copied as stored (16-byte vectors,
     // eight loads per lane in flight before their stores)
     {

@@ -19,17 +19,19 @@
 //               round's key chunks into a ring of K stages.
 //   warp 1      tcgen05.mma issuer (one thread): S = Q K^T per chunk into TMEM accumulator
 //               (round & 1) * 2 + j.
-//   warps 2-9   epilogue, two warps per TMEM lane quarter (one column half each), alternating:
-//               pass 1 of round r: each thread owns one row and folds its columns into the
-//               row's running (max, sum of exp2); the quarter's two warps merge and publish the
-//               row's partial. Pass 2 of round r - 1 (whose exchange ran meanwhile): a chunk's
+//   warps 2-9   pass 1, two warps per TMEM lane quarter (one column half each): each thread owns
+//               one row and folds its columns into the row's running (max, sum of exp2); the
+//               quarter's two warps merge and publish the row's partial. Two warps per SM
+//               sub-partition keep the MUFU (exp2) pipe busy while one waits on it.
+//   warps 10-17 pass 2, laid out the same way and running concurrently with pass 1 of the next
+//               round, once the round's lse2 exists: a chunk's
 //               TMEM values are read in the 16x256b fragment shape (each thread: 4 of the
 //               warp's 32 rows x 2 columns per 8-column group) and its accumulator freed;
 //               s*c2 - lse2 and the max over the 4 rows in registers, then a 3-step
 //               reduce-scatter over the 8 lanes sharing a column pair leaves each lane one
 //               column's max over 32 rows (7 shuffles per 32 columns); the eight warps' maxima
 //               meet in shared memory and one thread per key writes exp2 of the max.
-//   warp 10     exchange: polls the group's partials of a round and merges them into lse2,
+//   warp 18     exchange: polls the group's partials of a round and merges them into lse2,
 //               all of a batch's loads in flight at once (the merge is on the critical path).
 // Exchange protocol: a partial is one 64-bit word, the row's log2-sum-exp2 over the CTA's keys
 // in the low half and round + 1 in the high half, written with one relaxed store; a reader
@@ -45,6 +47,16 @@ namespace kvc {
 constexpr int kResChunks = 2;    // key chunks per CTA per round
 constexpr int kResRows = 128;    // observation rows per head this kernel handles (one MMA tile)
 constexpr int kResAcc = 2 * kResChunks;
+constexpr int kP1Warps = 8;  // warps 2-9: pass 1, two per TMEM lane quarter (one column half each)
+constexpr int kP2Warps = 8;  // warps 10-17: pass 2, likewise
+constexpr int kQWarp = 2 + kP1Warps + kP2Warps;              // warp 18: observation-tile producer
+constexpr int kResThreads = 32 * (kQWarp + 1);
+// Observation-tile buffers: two, so that the tile of round r + 1 is in place before round r's
+// MMAs have completed (one buffer put the tile's load latency on the MMA's path).
+constexpr int kQBuf = 2;
+
+// named barrier among the pass-2 warps only
+__device__ __forceinline__ void p2_bar() { asm volatile("bar.sync 1, %0;\n" ::"n"(32 * kP2Warps) : "memory"); }
 
 __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
@@ -71,7 +83,7 @@ __device__ __forceinline__ void reduce_scatter_max8(float (&w)[8], int lane) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kFusedThreads, 1)
+__global__ void __launch_bounds__(kResThreads, 1)
     score_resident_kernel(const __grid_constant__ FusedMaps maps, ScoreArgs a, ScoreWs ws, FusedPlan p, FusedXch xch,
                           float c2) {
   constexpr int HALVES = D / 64;
@@ -79,17 +91,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   constexpr int kQBytes = kResRows * D * 2;
   extern __shared__ uint8_t smraw[];
   uint8_t* Qs = align1024(smraw);
-  uint8_t* Ks = Qs + 2 * kQBytes;
+  uint8_t* Ks = Qs + kQBuf * kQBytes;
   const int S = p.stages;
   uint64_t* kfull = reinterpret_cast<uint64_t*>(Ks + S * kStage);
   uint64_t* kempty = kfull + S;
   uint64_t* qfull = kempty + S;
-  uint64_t* qempty = qfull + 2;
-  uint64_t* tfull = qempty + 2;
+  uint64_t* qempty = qfull + kQBuf;
+  uint64_t* tfull = qempty + kQBuf;
   uint64_t* tempty = tfull + kResAcc;
-  uint64_t* lfull = tempty + kResAcc;
-  uint64_t* lempty = lfull + 2;
-  uint64_t* mdone = lempty + 2;
+  uint64_t* mdone = tempty + kResAcc;
   uint32_t* slot = reinterpret_cast<uint32_t*>(mdone + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 1);
   float* lse2s = reinterpret_cast<float*>(Ks + S * kStage + 512);  // [2][128]
@@ -104,13 +114,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     for (int i = 0; i < kResAcc; ++i) {
       tc::mbar_init(&tfull[i], 1);
-      tc::mbar_init(&tempty[i], kEpiWarps);
+      tc::mbar_init(&tempty[i], kP2Warps);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kQBuf; ++i) {
       tc::mbar_init(&qfull[i], 1);
       tc::mbar_init(&qempty[i], 1);
-      tc::mbar_init(&lfull[i], 1);
-      tc::mbar_init(&lempty[i], kEpiWarps);
     }
     tc::mbar_init(mdone, 1);
     *abort_flag = 0;
@@ -129,18 +137,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int n = max(0, min(c0 + p.chunks_per_cta, a.nchunk) - c0);  // chunks per round, the same every round
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer: key chunks ----------------
     if (lane == 0) {
       uint32_t kc = 0;
-      int qloads = 0;
       for (int r = 0; r < rounds && !*abort_flag; ++r) {
         const int head = group + r * p.ngroups;
-        const int qb = r & 1;
-        if (r >= 2 && !wait_or_abort(&qempty[qb], ((r - 2) >> 1) & 1, abort_flag, a.status)) break;
-        tc::mbar_expect_tx(&qfull[qb], (uint32_t)kQBytes);
-        for (int h = 0; h < HALVES; ++h)
-          tc::tma_load_2d(Qs + qb * kQBytes + h * (kResRows * 128), &maps.q, &qfull[qb], h * 64, head * kResRows);
-        qloads = r + 1;
         const int l = head / (a.g.B * a.g.Hkv), bh = head % (a.g.B * a.g.Hkv);
         bool stop = false;
         for (int j = 0; j < n; ++j) {
@@ -160,8 +161,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const uint32_t tail = kc < (uint32_t)S ? kc : (uint32_t)S;
       for (uint32_t k = kc - tail; k < kc; ++k)
         if (!tc::mbar_wait(&kfull[k % S], (k / S) & 1)) status_or(a.status, KVC_STATUS_TIMEOUT);
-      for (int r = qloads - 2 < 0 ? 0 : qloads - 2; r < qloads; ++r)
-        if (!tc::mbar_wait(&qfull[r & 1], (r >> 1) & 1)) status_or(a.status, KVC_STATUS_TIMEOUT);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -171,13 +170,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const uint32_t id = tc::idesc_bf16(128, kChunk);
       bool ok = true, issued = false;
       for (int r = 0; r < rounds && ok && !*abort_flag; ++r) {
-        const int qb = r & 1;
-        if (!wait_or_abort(&qfull[qb], (r >> 1) & 1, abort_flag, a.status)) break;
+        const int qb = r % kQBuf;
+        if (!wait_or_abort(&qfull[qb], (r / kQBuf) & 1, abort_flag, a.status)) break;
         tc::fence_after_sync();
         const uint32_t qaddr = tc::smem_u32(Qs + qb * kQBytes);
         for (int j = 0; j < n; ++j) {
           const int s = kc % S;
-          const uint32_t acc = (uint32_t)(qb * kResChunks + j);
+          const uint32_t acc = (uint32_t)((r & 1) * kResChunks + j);
           if (!wait_or_abort(&kfull[s], (kc / S) & 1, abort_flag, a.status) ||
               (r >= 2 && !wait_or_abort(&tempty[acc], ((r >> 1) - 1) & 1, abort_flag, a.status))) {
             ok = false;
@@ -204,90 +203,27 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 2 + kEpiWarps) {
-    // ---------------- exchange warp: lse2 of every row once the group has published ----------------
-    const uint64_t* words = reinterpret_cast<const uint64_t*>(xch.part);
-    for (int round = 0; round < rounds && !*abort_flag; ++round) {
-      const int b = round & 1;
-      if (round >= 2 && !wait_or_abort(&lempty[b], ((round - 2) >> 1) & 1, abort_flag, a.status)) break;
-      const int head = group + round * p.ngroups;
-      bool valid[kResRows / kWarp];  // written by the observation kernel: safe to read early
-#pragma unroll
-      for (int i = 0; i < kResRows / kWarp; ++i) valid[i] = ws.valid[(size_t)head * kResRows + i * kWarp + lane] != 0;
-      // Slot round % 4 last held round - 4. A partner overwrites it (round + 4) only after its
-      // pass 1 of round + 4, which needs its TMEM buffer back from pass 2 of round + 2, which
-      // needs the whole group's partials of round + 2, which each CTA publishes only after its
-      // own pass 2 of round, i.e. after this warp has read slot round % 4.
-      const uint32_t tag = (uint32_t)round + 1u;
-      const uint64_t* grp = words + ((size_t)((round & 3) * p.ngroups + group) * p.group_size) * kResRows;
-      float mx[kResRows / kWarp], sm[kResRows / kWarp];
-#pragma unroll
-      for (int i = 0; i < kResRows / kWarp; ++i) {
-        mx[i] = -INFINITY;
-        sm[i] = 0.f;
+  } else if (warp == kQWarp) {
+    // ---------------- TMA producer: observation tiles ----------------
+    if (lane == 0) {
+      int qloads = 0;
+      for (int r = 0; r < rounds && !*abort_flag; ++r) {
+        const int head = group + r * p.ngroups;
+        const int qb = r % kQBuf, use = r / kQBuf;
+        if (use >= 1 && !wait_or_abort(&qempty[qb], (use - 1) & 1, abort_flag, a.status)) break;
+        tc::mbar_expect_tx(&qfull[qb], (uint32_t)kQBytes);
+        for (int h = 0; h < HALVES; ++h)
+          tc::tma_load_2d(Qs + qb * kQBytes + h * (kResRows * 128), &maps.q, &qfull[qb], h * 64, head * kResRows);
+        qloads = r + 1;
       }
-      bool ok = true;
-      for (int k0 = 0; k0 < p.group_size && ok; k0 += 8) {
-        // all of a batch's loads are issued before any is used: one L2 round trip per poll
-        uint64_t w[kResRows / kWarp][8];
-#pragma unroll
-        for (int i = 0; i < kResRows / kWarp; ++i)
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            w[i][kk] = k0 + kk < p.group_size ? ld_relaxed_u64(&grp[(size_t)(k0 + kk) * kResRows + i * kWarp + lane])
-                                              : ((uint64_t)tag << 32) | __float_as_uint(-INFINITY);
-        for (uint32_t it = 0;; ++it) {
-          unsigned need = 0u;
-#pragma unroll
-          for (int i = 0; i < kResRows / kWarp; ++i)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              if ((uint32_t)(w[i][kk] >> 32) != tag) need |= 1u << (i * 8 + kk);
-          if (!__any_sync(kFull, need != 0u)) break;
-          if (it >= (1u << 22) || *abort_flag) {
-            ok = false;
-            if (lane == 0 && !*abort_flag) {
-              *abort_flag = 1;
-              status_or(a.status, KVC_STATUS_TIMEOUT);
-            }
-            break;
-          }
-          __nanosleep(32);
-#pragma unroll
-          for (int i = 0; i < kResRows / kWarp; ++i)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              if (need & (1u << (i * 8 + kk))) w[i][kk] = ld_relaxed_u64(&grp[(size_t)(k0 + kk) * kResRows + i * kWarp + lane]);
-        }
-#pragma unroll
-        for (int i = 0; i < kResRows / kWarp; ++i) {
-          float v[8];
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) v[kk] = __uint_as_float((uint32_t)w[i][kk]);
-          float bm = v[0];
-#pragma unroll
-          for (int kk = 1; kk < 8; ++kk) bm = fmaxf(bm, v[kk]);
-          const float nm = fmaxf(mx[i], bm);
-          if (nm > -INFINITY) {
-            float acc = mx[i] > -INFINITY ? sm[i] * exp2f(mx[i] - nm) : 0.f;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) acc += exp2f(v[kk] - nm);  // -inf partials add 0
-            mx[i] = nm;
-            sm[i] = acc;
-          }
-        }
-      }
-      if (!ok) break;
-      float* dst = lse2s + b * kResRows;
-#pragma unroll
-      for (int i = 0; i < kResRows / kWarp; ++i)
-        dst[i * kWarp + lane] = (valid[i] && sm[i] > 0.f) ? mx[i] + log2f(sm[i]) : INFINITY;
-      __syncwarp();
-      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&lfull[b])) : "memory");
+      for (int r = qloads - kQBuf < 0 ? 0 : qloads - kQBuf; r < qloads; ++r)
+        if (!tc::mbar_wait(&qfull[r % kQBuf], (r / kQBuf) & 1)) status_or(a.status, KVC_STATUS_TIMEOUT);
     }
+    __syncwarp();
   } else {
-    // ---------------- epilogue ----------------
-    const int e = warp - 2;  // 0..7
+    // ---------------- pass-1 warps (2-9) and pass-2 warps (10-17) ----------------
+    const bool is_p1 = warp < 2 + kP1Warps;
+    const int e = is_p1 ? warp - 2 : warp - 2 - kP1Warps;  // 0..7 within the group
     const int q = warp & 3;  // TMEM lane quarter this warp may read: rows q*32 .. q*32+31
     const int hf = e >> 2;   // which 64 of a chunk's 128 columns
     const int row = q * 32 + lane;
@@ -307,42 +243,46 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const bool go = !*abort_flag && wait_or_abort(&tfull[acc], (round >> 1) & 1, abort_flag, a.status);
         if (!__all_sync(kFull, go)) continue;  // tcgen05.ld is warp-collective: decide per warp
         tc::fence_after_sync();
-        uint32_t r0[32], r1[32];
-        const uint32_t col0 = tmem + acc * kChunk + lane_off + (uint32_t)(hf * 64);
-        tc::tmem_ld32_async(col0, r0);
-        tc::tmem_ld32_async(col0 + 32, r1);
-        tc::tmem_wait();
-        tc::tmem_regs_ready(r0);
-        tc::tmem_regs_ready(r1);
-        float v0[32], v1[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v0[i] = __uint_as_float(r0[i]);
-          v1[i] = __uint_as_float(r1[i]);
-        }
         const int nvalid = min(kChunk, a.g.N - c * kChunk);
-        if (nvalid < kChunk) {  // ragged last chunk only
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (hf * 64 + i >= nvalid) v0[i] = -INFINITY;
-            if (hf * 64 + 32 + i >= nvalid) v1[i] = -INFINITY;
-          }
-        }
-        const float mraw = fmaxf(tree_max32(v0), tree_max32(v1));  // c2 > 0: scale the max once
-        if (mraw > -INFINITY) {
-          const float mn = fmaxf(st.x, mraw * c2);
+        for (int h32 = 0; h32 < 2; ++h32) {  // 32 columns at a time
+          uint32_t r0[32];
+          const int cbase = hf * 64 + h32 * 32;
+          tc::tmem_ld32_async(tmem + acc * kChunk + lane_off + (uint32_t)cbase, r0);
+          tc::tmem_wait();
+          tc::tmem_regs_ready(r0);
+          float v0[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            v0[i] = ex2_approx(fmaf(v0[i], c2, -mn));
-            v1[i] = ex2_approx(fmaf(v1[i], c2, -mn));
+          for (int i = 0; i < 32; ++i) v0[i] = __uint_as_float(r0[i]);
+          if (nvalid < kChunk) {  // ragged last chunk only
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (cbase + i >= nvalid) v0[i] = -INFINITY;
           }
-          st = make_float2(mn, st.y * ex2_approx(st.x - mn) + (tree_sum32(v0) + tree_sum32(v1)));
+          const float mraw = tree_max32_3(v0);  // c2 > 0: scale the max once
+          if (mraw > -INFINITY) {
+            const float mn = fmaxf(st.x, mraw * c2);
+            // s*c2 - mn two lanes at a time (packed fp32 FMA), exp2 on the MUFU, packed sum tree
+            const float2 c2v = make_float2(c2, c2), nmv = make_float2(-mn, -mn);
+            float2 sum2[8];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 x = __ffma2_rn(make_float2(v0[2 * i], v0[2 * i + 1]), c2v, nmv);
+              const float2 e2 = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              sum2[i & 7] = i < 8 ? e2 : __fadd2_rn(sum2[i & 7], e2);
+            }
+#pragma unroll
+            for (int w = 4; w; w >>= 1)
+#pragma unroll
+              for (int i = 0; i < w; ++i) sum2[i] = __fadd2_rn(sum2[i], sum2[i + w]);
+            st = make_float2(mn, st.y * ex2_approx(st.x - mn) + (sum2[0].x + sum2[0].y));
+          }
         }
       }
       // The two warps of a lane quarter merge their column halves; the hf == 0 warp publishes
       // the row's log2-sum-exp2 over this CTA's keys as one tagged word (no fence). merge is
-      // double-buffered by round parity: pass 2 of round r, with its CTA-wide barrier, lies
-      // between publishing r and r + 2.
+      // double-buffered by round parity: the pair passes round r + 1's barrier before hf == 1
+      // writes the buffer of round r again.
       float2* mg = merge + (round & 1) * kResRows;
       if (hf == 1) mg[row] = st;
       asm volatile("bar.sync %0, 64;\n" ::"r"(2 + q) : "memory");
@@ -357,21 +297,83 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // pass 2 of a round: per key, the max over rows of s*c2 - lse2, from the logits still in TMEM;
     // each chunk's accumulator is freed as soon as its values are in registers.
     auto pass2 = [&](int round) {
-      const bool have = !*abort_flag && wait_or_abort(&lfull[round & 1], (round >> 1) & 1, abort_flag, a.status);
-      float lse4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};  // rows q*32 + lane/4 + 8k
-      if (have)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) lse4[k] = lse2s[(round & 1) * kResRows + q * 32 + (lane >> 2) + 8 * k];
-      __syncwarp();
-      if (lane == 0)  // lse2 is in registers now: the exchange warp may refill the buffer
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&lempty[round & 1])) : "memory");
       const int head = group + round * p.ngroups;
+      // ---- exchange: lse2 of every row from the group's tagged partials. Thread t of the group
+      // polls row t/2 of partners t%2, t%2 + 2, ... (four words in flight at a time) and merges
+      // them; the two threads of a row combine with one shuffle.
+      const int gt = e * 32 + lane;  // 0..255
+      const int xrow = gt >> 1, xpar = gt & 1;
+      const bool xvalid = ws.valid[(size_t)head * kResRows + xrow] != 0;
+      // Slot round % 4 last held round - 4. A partner overwrites it (round + 4) only after its
+      // pass 1 of round + 4, which needs its TMEM buffer back from its pass 2 of round + 2, which
+      // follows the whole group's partials of round + 2, which this CTA publishes only after its
+      // pass 2 of round has freed the TMEM buffer, i.e. after this read.
+      const uint32_t tag = (uint32_t)round + 1u;
+      const uint64_t* grp = words + ((size_t)((round & 3) * p.ngroups + group) * p.group_size) * kResRows + xrow;
+      float mx = -INFINITY, sm = 0.f;
+      bool ok = !*abort_flag;
+      for (int u0 = 0; ok && xpar + 2 * u0 < p.group_size; u0 += 4) {
+        uint64_t w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int k = xpar + 2 * (u0 + u);
+          w[u] = k < p.group_size ? ld_relaxed_u64(grp + (size_t)k * kResRows)
+                                  : ((uint64_t)tag << 32) | __float_as_uint(-INFINITY);
+        }
+        for (uint32_t it = 0;; ++it) {
+          unsigned need = 0u;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if ((uint32_t)(w[u] >> 32) != tag) need |= 1u << u;
+          if (need == 0u) break;
+          if (it >= (1u << 22) || *abort_flag) {
+            ok = false;
+            if (!*abort_flag) {
+              *abort_flag = 1;
+              status_or(a.status, KVC_STATUS_TIMEOUT);
+            }
+            break;
+          }
+          __nanosleep(32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (need & (1u << u)) w[u] = ld_relaxed_u64(grp + (size_t)(xpar + 2 * (u0 + u)) * kResRows);
+        }
+        float bm = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) bm = fmaxf(bm, __uint_as_float((uint32_t)w[u]));
+        const float nm = fmaxf(mx, bm);
+        if (nm > -INFINITY) {
+          float accs = mx > -INFINITY ? sm * exp2f(mx - nm) : 0.f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) accs += exp2f(__uint_as_float((uint32_t)w[u]) - nm);  // -inf adds 0
+          mx = nm;
+          sm = accs;
+        }
+      }
+      {
+        const float om = __shfl_xor_sync(kFull, mx, 1), os = __shfl_xor_sync(kFull, sm, 1);
+        const float2 m2 = lse_merge(make_float2(mx, sm), make_float2(om, os));
+        if (xpar == 0)
+          lse2s[(round & 1) * kResRows + xrow] = (xvalid && m2.y > 0.f) ? m2.x + log2f(m2.y) : INFINITY;
+      }
+      p2_bar();
+      const bool have = !*abort_flag;
+      float2 nl[4];  // -lse2 of rows q*32 + lane/4 + 8k, twice (packed operands)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float l2 = lse2s[(round & 1) * kResRows + q * 32 + (lane >> 2) + 8 * k];
+        nl[k] = make_float2(-l2, -l2);
+      }
+      const float2 c2v = make_float2(c2, c2);
+      // ---- per key, the max over rows of s*c2 - lse2, from the logits still in TMEM
       float best[kResChunks][2];
 #pragma unroll
       for (int j = 0; j < kResChunks; ++j) best[j][0] = best[j][1] = -INFINITY;
-      if (__all_sync(kFull, have && !*abort_flag)) {
-        // this warp's pass 1 waited on every accumulator of the round, and lse2 exists only after
-        // this CTA published, so the MMAs are complete; the fence orders the reads after them
+      if (__all_sync(kFull, have)) {
+        // lse2 exists only after this CTA's pass 1 published, so the round's MMAs are complete;
+        // waiting on their (completed) phases orders this warp's TMEM reads after them
+        for (int j = 0; j < n; ++j) wait_or_abort(&tfull[(round & 1) * kResChunks + j], (round >> 1) & 1, abort_flag, a.status);
         tc::fence_after_sync();
 #pragma unroll
         for (int j = 0; j < kResChunks; ++j) {
@@ -394,20 +396,25 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           __syncwarp();
           if (lane == 0)  // the accumulator is free as soon as its values are in registers
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&tempty[acc])) : "memory");
-          // a row without observations has lse2 = +inf, so its terms are -inf and drop out of the max
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb) {
-            float w[8];  // slot 2i + cc: column 8i + 2*(lane%4) + cc of the block, max over 4 rows
+            // a row without observations has lse2 = +inf, so its terms are -inf and drop out of the max
+            // slot 2i + cc: column 8i + 2*(lane%4) + cc of the block, max over 4 rows; the two
+            // columns of a pair share each row's lse2, so s*c2 - lse2 is one packed FMA per row
+            float w[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-              for (int cc = 0; cc < 2; ++cc) {
-                const float x0 = fmaf(__uint_as_float(ra[cb][4 * i + cc]), c2, -lse4[0]);
-                const float x1 = fmaf(__uint_as_float(ra[cb][4 * i + 2 + cc]), c2, -lse4[1]);
-                const float x2 = fmaf(__uint_as_float(rb[cb][4 * i + cc]), c2, -lse4[2]);
-                const float x3 = fmaf(__uint_as_float(rb[cb][4 * i + 2 + cc]), c2, -lse4[3]);
-                w[2 * i + cc] = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-              }
+            for (int i = 0; i < 4; ++i) {
+              const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(ra[cb][4 * i]), __uint_as_float(ra[cb][4 * i + 1])),
+                                           c2v, nl[0]);
+              const float2 x1 = __ffma2_rn(
+                  make_float2(__uint_as_float(ra[cb][4 * i + 2]), __uint_as_float(ra[cb][4 * i + 3])), c2v, nl[1]);
+              const float2 x2 = __ffma2_rn(make_float2(__uint_as_float(rb[cb][4 * i]), __uint_as_float(rb[cb][4 * i + 1])),
+                                           c2v, nl[2]);
+              const float2 x3 = __ffma2_rn(
+                  make_float2(__uint_as_float(rb[cb][4 * i + 2]), __uint_as_float(rb[cb][4 * i + 3])), c2v, nl[3]);
+              w[2 * i] = fmaxf(max3f(x0.x, x1.x, x2.x), x3.x);
+              w[2 * i + 1] = fmaxf(max3f(x0.y, x1.y, x2.y), x3.y);
+            }
             reduce_scatter_max8(w, lane);
             best[j][cb] = w[0];
           }
@@ -420,16 +427,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                              tc::smem_u32(&tempty[(round & 1) * kResChunks + j]))
                          : "memory");
       }
-      // pbest[buffer][chunk][quarter][column]; buffer = round parity (pass 2 of round r + 1 and its
-      // barrier lie between two uses)
+      // pbest[buffer][chunk][quarter][column]; buffer = round parity (the group's barriers of
+      // round r + 1 lie between two uses)
       float* pb = pbest + (round & 1) * (kResChunks * 4 * kChunk);
 #pragma unroll
       for (int j = 0; j < kResChunks; ++j)
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) pb[(j * 4 + q) * kChunk + hf * 64 + cb * 32 + col_in] = best[j][cb];
-      epi_bar();
-      const int idx = e * 32 + lane;  // 256 threads: chunk idx / 128, key idx % 128
-      const int j = idx >> 7, col = idx & (kChunk - 1);
+      p2_bar();
+      const int j = gt >> 7, col = gt & (kChunk - 1);  // 256 threads: one key each
       if (j < n && !*abort_flag) {
         const float* pj = pb + j * 4 * kChunk;
         const float m = fmaxf(fmaxf(pj[col], pj[kChunk + col]), fmaxf(pj[2 * kChunk + col], pj[3 * kChunk + col]));
@@ -438,12 +444,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     };
 
-    // Segment seg: pass 1 of round seg and its publication, then pass 2 of round seg - 1, whose
-    // exchange ran meanwhile.
-    for (int seg = 0; seg <= rounds; ++seg) {
-      if (seg < rounds) pass1(seg);
-      if (seg >= 1) pass2(seg - 1);
-    }
+    // The two groups run concurrently: pass 1 of round r + 1 overlaps pass 2 of round r.
+    if (is_p1)
+      for (int round = 0; round < rounds; ++round) pass1(round);
+    else
+      for (int round = 0; round < rounds; ++round) pass2(round);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -453,7 +458,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// Shared memory: align slack, barriers, lse2 x2, merge x2, pbest x2; then two Q tiles and the ring.
+// Shared memory: align slack, barriers, lse2 x2, merge x2, pbest x2; then the Q tile(s) and the ring.
 static int resident_tail_bytes() { return 1024 + 512 + 2 * kResRows * 4 + 2 * kResRows * 8 + 2 * kResChunks * 4 * kChunk * 4; }
 
 bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem) {
@@ -473,11 +478,11 @@ bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem) {
   if (p->ngroups > heads) p->ngroups = heads;
   p->qbytes = kResRows * D * 2;
   const int stage_bytes = kChunk * D * 2;
-  int stages = (smem_optin - resident_tail_bytes() - 2 * p->qbytes) / stage_bytes;
+  int stages = (smem_optin - resident_tail_bytes() - kQBuf * p->qbytes) / stage_bytes;
   if (stages > 6) stages = 6;
   if (stages < 2) return false;
   p->stages = stages;
-  *smem = (size_t)resident_tail_bytes() + 2 * (size_t)p->qbytes + (size_t)stages * stage_bytes;
+  *smem = (size_t)resident_tail_bytes() + kQBuf * (size_t)p->qbytes + (size_t)stages * stage_bytes;
   return true;
 }
 
@@ -497,7 +502,7 @@ int launch_score_resident(const ScoreArgs& a, const ScoreWs& ws, const FusedPlan
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFusedThreads, smem) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kResThreads, smem) != cudaSuccess ||
       per_sm < 1)
     return KVC_ERR_LAUNCH;
   ScoreArgs aa = a;
@@ -505,7 +510,7 @@ int launch_score_resident(const ScoreArgs& a, const ScoreWs& ws, const FusedPlan
   FusedPlan pp = p;
   float cc = c2;
   void* args[] = {(void*)&maps, (void*)&aa, (void*)&wss, (void*)&pp, (void*)&xch, (void*)&cc};
-  if (cudaLaunchCooperativeKernel((const void*)kern, dim3(p.ngroups * p.group_size), dim3(kFusedThreads), args, smem,
+  if (cudaLaunchCooperativeKernel((const void*)kern, dim3(p.ngroups * p.group_size), dim3(kResThreads), args, smem,
                                   s) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   return KVC_OK;

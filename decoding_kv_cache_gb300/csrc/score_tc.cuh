@@ -69,6 +69,22 @@ __device__ __forceinline__ float tree_sum32(const float (&x)[32]) {
   return a[0];
 }
 
+// max of three (a NaN operand is ignored, as with fmaxf)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// max of 32 values with three-input max steps: 17 instructions instead of 31
+__device__ __forceinline__ float tree_max32_3(const float (&x)[32]) {
+  float a[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) a[i] = max3f(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  a[10] = fmaxf(x[30], x[31]);
+  const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]), b2 = max3f(a[6], a[7], a[8]);
+  return fmaxf(max3f(b0, b1, b2), fmaxf(a[9], a[10]));
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {  // MUFU.EX2; relative error about 2^-22
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
