@@ -119,25 +119,27 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inwin)}
 
 
-def src_hash() -> str:
-    """Hash of the CUDA sources; ncu traffic figures are only reported for the build they came from."""
+def src_hash(files=None) -> str:
+    """Hash of CUDA sources (the given files under csrc/, else all of them); an ncu traffic figure is
+    only reported while the sources of the kernel it was taken from are unchanged."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "decoding_kv_cache_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    names = sorted(files) if files else sorted(f for f in os.listdir(d) if f.endswith((".cu", ".cuh")))
+    for f in names:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config: str, kernel: str):
+def recorded_traffic(config: str, phase: str):
+    """DRAM bytes (read + write) per launch of the phase's dominant kernel, from profiles/traffic.json."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(config, {}).get(kernel)
-    if not e or e.get("src_hash") != src_hash():
+    e = d.get(config, {}).get(phase)
+    if not e or e.get("src_hash") != src_hash(e.get("sources")):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -175,7 +177,8 @@ def gpu_arm(args, rank, world, local_rank):
         kbuild.build()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    inp = make_inputs(args.config, device=dev)
+    over = {"L": args.layers} if args.layers else {}
+    inp = make_inputs(args.config, device=dev, **over)
     stream = torch.cuda.current_stream(dev)
     K0, V0 = inp.K.clone(), inp.V.clone()
     cache = kvc.Cache(inp.K, inp.V, inp.Hq)
@@ -296,7 +299,7 @@ def gpu_arm(args, rank, world, local_rank):
         "algorithmic_bytes_per_step": {"k_read": k_read, "kv_moved": moved_bytes, "moved_tokens": moved},
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_source": pk_kind,
-                     "traffic": recorded_traffic(args.config, dom)},
+                     "traffic": None if args.layers else recorded_traffic(args.config, dom)},
         "phases_ms": phase_ms,
         "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -369,6 +372,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling aid: run the workload with only this many layers (0 = all)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
