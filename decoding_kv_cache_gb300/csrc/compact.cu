@@ -12,13 +12,11 @@
 // src[k] == k needs no move and is skipped (found by binary search: src[k] - k is
 // non-decreasing).
 //
-// One CTA per (head, K-or-V). 16-byte vectors, register double buffering across tiles.
+// One warp per (head, K-or-V). Each tile of kept rows is fetched with one bulk copy per run of
+// consecutive sources into a 3-stage shared-memory ring and written back with one bulk store.
 #include "kvc_internal.cuh"
 
 namespace kvc {
-
-constexpr int kCpThreads = 256;
-constexpr int kCpVec = 4;  // 16-byte vectors per thread per tile
 
 struct CompactArgs {
   CacheGeom g;
@@ -30,68 +28,6 @@ struct CompactArgs {
   int validate;
 };
 
-__global__ void __launch_bounds__(kCpThreads) compact_kernel(CompactArgs a) {
-  const int head = blockIdx.x;
-  const int l = head / (a.g.B * a.g.Hkv), bh = head % (a.g.B * a.g.Hkv);
-  char* base = static_cast<char*>(blockIdx.y ? a.V.p[l] : a.K.p[l]) + (size_t)bh * a.g.ncap * a.rowbytes;
-  const int32_t* src = a.kept_idx + (size_t)head * a.g.N;
-  const int len = a.kept_len[head];
-  const int N = a.g.N;
-  if (a.validate) {
-    bool bad = len < 0 || len > N;
-    if (!bad)
-      for (int k = threadIdx.x; k < len; k += blockDim.x) {
-        const int v = src[k];
-        bad |= v < k || v >= N || (k > 0 && v <= src[k - 1]);
-      }
-    if (__syncthreads_or(bad)) {
-      if (threadIdx.x == 0 && blockIdx.y == 0) status_or(a.status, KVC_STATUS_BAD_INDEX);
-      return;
-    }
-  }
-  // first index that moves: smallest k with src[k] != k
-  int lo = 0, hi = len;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (src[mid] == mid) lo = mid + 1; else hi = mid;
-  }
-  const int first = lo;
-  if (first >= len) return;
-  const int vpr = a.rowbytes / 16;
-  const int tile_rows = kCpThreads * kCpVec / vpr;
-  uint4 cur[kCpVec], nxt[kCpVec];
-
-  auto load = [&](int t0, uint4 (&v)[kCpVec]) {
-#pragma unroll
-    for (int q = 0; q < kCpVec; ++q) {
-      const int e = threadIdx.x + q * kCpThreads;
-      const int k = t0 + e / vpr;
-      if (k < len) v[q] = reinterpret_cast<const uint4*>(base + (size_t)src[k] * a.rowbytes)[e % vpr];
-    }
-  };
-  load(first, cur);
-  for (int t0 = first; t0 < len; t0 += tile_rows) {
-    if (t0 + tile_rows < len) load(t0 + tile_rows, nxt);
-    __syncthreads();  // every load of this tile (and all earlier ones) has been performed
-#pragma unroll
-    for (int q = 0; q < kCpVec; ++q) {
-      const int e = threadIdx.x + q * kCpThreads;
-      const int k = t0 + e / vpr;
-      if (k < len) reinterpret_cast<uint4*>(base + (size_t)k * a.rowbytes)[e % vpr] = cur[q];
-    }
-#pragma unroll
-    for (int q = 0; q < kCpVec; ++q) cur[q] = nxt[q];
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Bulk-copy version: one warp per (head, K-or-V), a ring of kRing 16 KB shared-memory tiles.
-// Each maximal run of consecutive kept rows inside a 32-row block is fetched with one
-// cp.async.bulk (completion counted on the tile's mbarrier); each tile goes back with one
-// contiguous bulk store. Ordering is the forward sweep's: a tile's store is issued after that
-// tile's loads have landed, earlier tiles' loads landed before their own stores, and later
-// tiles only read rows at or beyond this tile's destination end.
-// ---------------------------------------------------------------------------
 constexpr int kRing = 3;
 constexpr int kTileBytes = 16384;
 
@@ -107,6 +43,7 @@ __global__ void __launch_bounds__(32) compact_bulk_kernel(CompactArgs a) {
   const int T = kTileBytes / rb;  // rows per tile: 32, 64 or 128
   char* base = static_cast<char*>(blockIdx.y ? a.V.p[l] : a.K.p[l]) + (size_t)bh * a.g.ncap * rb;
   const int32_t* src = a.kept_idx + (size_t)head * a.g.N;
+  griddep_wait();  // the kept lists come from the previous kernel
   const int len = a.kept_len[head];
   const int N = a.g.N;
   if (a.validate) {
@@ -220,8 +157,8 @@ int launch_compact(const CacheGeom& g, int dtype, const LayerPtrs& K, const Laye
   const size_t smem = (size_t)kRing * kTileBytes + 64;
   if (cudaFuncSetAttribute(compact_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
-  compact_bulk_kernel<<<dim3(heads, 2), 32, smem, s>>>(a);
-  return launch_ok();
+  if (launch_pdl(compact_bulk_kernel, dim3(heads, 2), dim3(32), smem, s, false, a) != cudaSuccess) return KVC_ERR_LAUNCH;
+  return KVC_OK;
 }
 
 }  // namespace kvc

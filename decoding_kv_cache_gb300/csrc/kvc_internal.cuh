@@ -35,6 +35,45 @@ __device__ __forceinline__ void status_or(int32_t* status, unsigned bits) {
   if (status) atomicOr(reinterpret_cast<unsigned*>(status), bits);
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// A kernel launched with programmatic stream serialisation may start while the previous
+// kernel in the stream is still running; griddep_wait() returns once that kernel has
+// completed and its memory operations are visible (immediately when launched normally).
+// griddep_launch_dependents() lets the next such kernel be scheduled early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+// Launch with programmatic stream serialisation (and cooperatively if asked); when the
+// runtime refuses the attribute, launch again without it.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool coop,
+                              Args... args) {
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (coop) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  }
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    cfg.numAttrs = na - 1;
+    e = cudaLaunchKernelEx(&cfg, kern, args...);
+  }
+  return e;
+}
+
 // ---- per-layer pointer tables passed by value -------------------------------
 struct LayerPtrs {
   void* p[KVC_MAX_LAYERS];

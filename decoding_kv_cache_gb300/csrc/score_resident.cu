@@ -37,6 +37,8 @@
 // in the low half and round + 1 in the high half, written with one relaxed store; a reader
 // accepts a word once its tag matches, so data and "published" travel together and nobody
 // waits for a store to be acknowledged. The observation kernel that runs just before zeroes them.
+// Launched with programmatic stream serialisation: the key producer and the MMA thread may start
+// before the observation kernel has finished; every role that reads its output waits for it.
 // Every wait is bounded; a wait that gives up sets KVC_STATUS_TIMEOUT and a CTA-wide abort flag,
 // after which every role skips its work but still passes every named barrier. Before exiting,
 // the producer waits (bounded) for its own loads in flight and the MMA thread for its MMAs.
@@ -129,6 +131,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *slot;
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   const int heads = a.g.L * a.g.B * a.g.Hkv;
   const int group = blockIdx.x / p.group_size, rank = blockIdx.x % p.group_size;
@@ -140,9 +143,13 @@ __global__ void __launch_bounds__(kResThreads, 1)
     // ---------------- TMA producer: key chunks ----------------
     if (lane == 0) {
       uint32_t kc = 0;
+      const int bhkv = a.g.B * a.g.Hkv;
+      // a round usually moves to another layer's tensor map: fetch the next rounds' maps early
+      for (int r = 0; r < 2 && r < rounds; ++r) tc::prefetch_tensormap(&maps.k[(group + r * p.ngroups) / bhkv]);
       for (int r = 0; r < rounds && !*abort_flag; ++r) {
         const int head = group + r * p.ngroups;
-        const int l = head / (a.g.B * a.g.Hkv), bh = head % (a.g.B * a.g.Hkv);
+        const int l = head / bhkv, bh = head % bhkv;
+        if (r + 2 < rounds) tc::prefetch_tensormap(&maps.k[(head + 2 * p.ngroups) / bhkv]);
         bool stop = false;
         for (int j = 0; j < n; ++j) {
           const int s = kc % S;
@@ -206,6 +213,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
   } else if (warp == kQWarp) {
     // ---------------- TMA producer: observation tiles ----------------
     if (lane == 0) {
+      griddep_wait();  // the tiles come from the observation kernel
       int qloads = 0;
       for (int r = 0; r < rounds && !*abort_flag; ++r) {
         const int head = group + r * p.ngroups;
@@ -222,6 +230,9 @@ __global__ void __launch_bounds__(kResThreads, 1)
     __syncwarp();
   } else {
     // ---------------- pass-1 warps (2-9) and pass-2 warps (10-17) ----------------
+    // the exchange words and row flags come from the observation kernel (the key producer and
+    // the MMA thread start without waiting: the keys are the caller's cache)
+    griddep_wait();
     const bool is_p1 = warp < 2 + kP1Warps;
     const int e = is_p1 ? warp - 2 : warp - 2 - kP1Warps;  // 0..7 within the group
     const int q = warp & 3;  // TMEM lane quarter this warp may read: rows q*32 .. q*32+31
@@ -509,9 +520,8 @@ int launch_score_resident(const ScoreArgs& a, const ScoreWs& ws, const FusedPlan
   ScoreWs wss = ws;
   FusedPlan pp = p;
   float cc = c2;
-  void* args[] = {(void*)&maps, (void*)&aa, (void*)&wss, (void*)&pp, (void*)&xch, (void*)&cc};
-  if (cudaLaunchCooperativeKernel((const void*)kern, dim3(p.ngroups * p.group_size), dim3(kResThreads), args, smem,
-                                  s) != cudaSuccess)
+  if (launch_pdl(kern, dim3(p.ngroups * p.group_size), dim3(kResThreads), smem, s, true, maps, aa, wss, pp, xch, cc) !=
+      cudaSuccess)
     return KVC_ERR_LAUNCH;
   return KVC_OK;
 }

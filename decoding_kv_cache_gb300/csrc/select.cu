@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
   __shared__ int wsum[33];
   __shared__ unsigned s_digit, s_k;
   const int head = blockIdx.x, tid = threadIdx.x;
+  griddep_wait();  // the scores come from the previous kernel
+  griddep_launch_dependents();
   const float* sc = scores + (size_t)head * N;
   int32_t* out = kept_idx + (size_t)head * N;
   const int b = budget ? budget[head] : budget_all;
@@ -145,9 +147,10 @@ int launch_select(const float* scores, int heads, int N, int P, int R, const int
   const size_t smem = use_smem ? bytes : 0;
   if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
-  select_kernel<<<heads, kSelThreads, smem, s>>>(scores, N, P, R, budget, budget_all, kept_idx, kept_len, status,
-                                                 use_smem);
-  return launch_ok();
+  if (launch_pdl(select_kernel, dim3(heads), dim3(kSelThreads), smem, s, false, scores, N, P, R, budget, budget_all,
+                 kept_idx, kept_len, status, use_smem) != cudaSuccess)
+    return KVC_ERR_LAUNCH;
+  return KVC_OK;
 }
 
 }  // namespace kvc

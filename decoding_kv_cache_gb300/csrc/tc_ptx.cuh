@@ -51,6 +51,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Bring a tensor map (here a __grid_constant__ kernel parameter) into the TMA unit's
+// descriptor cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"(map) : "memory");
+}
+
 // ---- tensor memory -------------------------------------------------------------------
 // One full warp allocates ncols (a power of two >= 32) columns; the TMEM address lands in *slot.
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
