@@ -39,9 +39,10 @@ __device__ __forceinline__ void status_or(int32_t* status, unsigned bits) {
 // A kernel launched with programmatic stream serialisation may start while the previous
 // kernel in the stream is still running; griddep_wait() returns once that kernel has
 // completed and its memory operations are visible (immediately when launched normally).
-// griddep_launch_dependents() lets the next such kernel be scheduled early.
+// No kernel here signals early completion: dependents are released when their predecessor
+// exits (an early signal let waiting CTAs sit beside the scoring kernel and slowed it), so
+// the overlap is the launch's own latency and the waiting roles' prologue.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
 // Launch with programmatic stream serialisation (and cooperatively if asked); when the
 // runtime refuses the attribute, launch again without it.

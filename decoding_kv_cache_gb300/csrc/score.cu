@@ -43,7 +43,6 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
   void* scratch = smem_raw + warp * ((fps_scratch_bytes<T, D>(npad) + 15) & ~(size_t)15);
   const T* qrec = static_cast<const T*>(a.q_recent);
   const T* qbuf = static_cast<const T*>(a.qbuf);
-  if (threadIdx.x == 0) griddep_launch_dependents();  // the scoring kernel waits where it reads our output
 
   // the scoring kernel's exchange words start at zero (this CTA's share of them)
   if (a.xch_zero) {

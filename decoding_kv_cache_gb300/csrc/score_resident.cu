@@ -131,7 +131,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *slot;
-  if (threadIdx.x == 0) griddep_launch_dependents();
 
   const int heads = a.g.L * a.g.B * a.g.Hkv;
   const int group = blockIdx.x / p.group_size, rank = blockIdx.x % p.group_size;

@@ -52,7 +52,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
   __shared__ unsigned s_digit, s_k;
   const int head = blockIdx.x, tid = threadIdx.x;
   griddep_wait();  // the scores come from the previous kernel
-  griddep_launch_dependents();
   const float* sc = scores + (size_t)head * N;
   int32_t* out = kept_idx + (size_t)head * N;
   const int b = budget ? budget[head] : budget_all;
