@@ -44,57 +44,68 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
   const T* qrec = static_cast<const T*>(a.q_recent);
   const T* qbuf = static_cast<const T*>(a.qbuf);
 
-  // the scoring kernel's exchange words start at zero (this CTA's share of them)
-  if (a.xch_zero) {
-    const long long per = (a.xch_zero_words + gridDim.x - 1) / gridDim.x;
-    const long long lo = (long long)blockIdx.x * per;
-    const long long hi = lo + per < a.xch_zero_words ? lo + per : a.xch_zero_words;
-    for (long long w = lo + threadIdx.x; w < hi; w += blockDim.x) a.xch_zero[w] = 0ull;
-  }
-  // rotation table in shared memory (a per-lane index into the parameter block would serialize)
-  float2* rope_s = reinterpret_cast<float2*>(smem_raw + (size_t)nw * ((fps_scratch_bytes<T, D>(npad) + 15) & ~(size_t)15));
-  for (int i = threadIdx.x; i < hd; i += blockDim.x) rope_s[i] = a.rope[i];
-  __syncthreads();
-  // beacon rows are rotated lpr lanes per row, each lane `per` consecutive pairs (i, i + D/2):
-  // one 16-byte store per half-row and lane
   constexpr int per = 16 / (int)sizeof(T);
-  constexpr int lpr = (D / 2) / per;
+  constexpr int lpr = (D / 2) / per;  // rotation: lanes per beacon row, `per` pairs (i, i + D/2) each
   constexpr int rpi = kWarp / lpr;
   const int i0 = (lane % lpr) * per, rsel = lane / lpr;
+  float2* rope_s = reinterpret_cast<float2*>(smem_raw + (size_t)nw * ((fps_scratch_bytes<T, D>(npad) + 15) & ~(size_t)15));
+  fps_stage_init<T, D>(scratch, npad);
+  uint32_t stage_phase = 0;
 
-  for (int g = warp; g < G; g += nw) {
+  // every warp has at least one query head (nw <= G), so the CTA-wide step in the first
+  // iteration is reached by all threads
+  for (int g = warp, it = 0; g < G; g += nw, ++it) {
     const int hq = h * G + g;
     const size_t qh = ((size_t)l * B + b) * Hq + hq;
     T* orow = obs + (size_t)g * per_q * D;
-    // Start staging the whole query buffer at once (rows at or past its count are staged too but
-    // never read: FPS and the Gram entries it uses involve live rows only), read the count and
-    // copy the recent queries while the copies are in flight.
+    // Issue this query head's global reads first: stage the whole buffer (rows at or past its
+    // count are staged too but never read: FPS and the Gram entries it uses involve live rows
+    // only), the count, and the first batch of recent rows.
     fps_buffer_issue<T, D>(qbuf + qh * a.qmax * D, a.qmax, npad, scratch);
     int c = a.qmax > 0 ? a.count[qh] : 0;
+    const uint4* qr = reinterpret_cast<const uint4*>(qrec + qh * a.n_r * D);
+    uint4* od = reinterpret_cast<uint4*>(orow);
+    const int nv = a.n_r * D * (int)sizeof(T) / 16;  // recent rows, 16-byte vectors
+    uint4 rv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (u * kWarp + lane < nv) rv[u] = qr[u * kWarp + lane];
+    if (it == 0) {
+      // while those are in flight: this CTA's share of the scoring kernel's exchange words (they
+      // start at zero) and the rotation table in shared memory (a per-lane index into the
+      // parameter block would serialise)
+      if (a.xch_zero) {
+        const long long share = (a.xch_zero_words + gridDim.x - 1) / gridDim.x;
+        const long long lo = (long long)blockIdx.x * share;
+        const long long hi = lo + share < a.xch_zero_words ? lo + share : a.xch_zero_words;
+        for (long long w = lo + threadIdx.x; w < hi; w += blockDim.x) a.xch_zero[w] = 0ull;
+      }
+      for (int i = threadIdx.x; i < hd; i += blockDim.x) rope_s[i] = a.rope[i];
+      __syncthreads();
+    }
     if (c < 0 || c > a.qmax) {
       if (lane == 0) status_or(a.status, KVC_STATUS_COUNT_RANGE);
       c = c < 0 ? 0 : a.qmax;
     }
-    // recent queries: already rotated to their own positions, copied as stored (16-byte vectors,
-    // eight loads per lane in flight before their stores)
-    {
-      const uint4* qr = reinterpret_cast<const uint4*>(qrec + qh * a.n_r * D);
-      uint4* od = reinterpret_cast<uint4*>(orow);
-      const int nv = a.n_r * D * (int)sizeof(T) / 16;
-      for (int e0 = 0; e0 < nv; e0 += 8 * kWarp) {
-        uint4 v[8];
+    // recent queries: already rotated to their own positions, copied as stored
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (e0 + u * kWarp + lane < nv) v[u] = qr[e0 + u * kWarp + lane];
+    for (int u = 0; u < 8; ++u)
+      if (u * kWarp + lane < nv) od[u * kWarp + lane] = rv[u];
+    for (int e0 = 8 * kWarp; e0 < nv; e0 += 8 * kWarp) {  // more than 8 vectors per lane: further batches
+      uint4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (e0 + u * kWarp + lane < nv) od[e0 + u * kWarp + lane] = v[u];
-      }
+      for (int u = 0; u < 8; ++u)
+        if (e0 + u * kWarp + lane < nv) v[u] = qr[e0 + u * kWarp + lane];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (e0 + u * kWarp + lane < nv) od[e0 + u * kWarp + lane] = v[u];
     }
     for (int r = lane; r < a.n_r; r += kWarp) valid[g * per_q + r] = 1;
     // beacons: the buffer itself when it holds at most n_b rows, else FPS down to n_b
     int* pk;
-    const T* xs = fps_buffer_finish<T, D>(c, a.n_b, npad, scratch, &pk);
+    bool staged;
+    const T* xs = fps_buffer_finish<T, D>(c, a.n_b, npad, scratch, stage_phase++, &pk, &staged);
+    if (!staged && lane == 0) status_or(a.status, KVC_STATUS_TIMEOUT);
     const int nb = c < a.n_b ? c : a.n_b;
     for (int k0 = 0; k0 < a.n_b; k0 += rpi) {
       const int k = k0 + rsel;
