@@ -3,6 +3,7 @@
 // Every check happens on the host before the first launch of a call, so a rejected call
 // has touched nothing. Conditions that only the device can see are OR-ed into the
 // caller's status word by the kernels (see kvc.h).
+#include <atomic>
 #include <math.h>
 #include <string.h>
 
@@ -55,10 +56,15 @@ int check_queries(const kvc_cache* c, const void* q_recent, int n_r, const void*
   return KVC_OK;
 }
 
+namespace {
+std::atomic<int> g_debug_fault{0};  // test-only fault switch, read at each scoring launch
+}
+
 void fill_score_args(ScoreArgs* a, const CacheGeom& g, int dtype, const LayerPtrs& K, const void* q_recent, int n_r,
                      const void* qbuf, const int32_t* count, int qmax, int n_b, int64_t t, double theta,
                      float* scores, int32_t* beacon_picks, int32_t* status) {
   a->g = g;
+  a->debug_fault = g_debug_fault.load();
   a->dtype = dtype;
   a->K = K;
   a->q_recent = q_recent;
@@ -95,6 +101,12 @@ using namespace kvc;
 extern "C" {
 
 int kvc_abi_version(void) { return KVC_ABI_VERSION; }
+
+int kvc_debug_fault(int32_t mode) {
+  if (mode < 0 || mode > 1) return KVC_ERR_INVALID_ARG;
+  g_debug_fault.store(mode);
+  return KVC_OK;
+}
 
 int kvc_evict_launch_count(const kvc_cache* c, int32_t n_r, int32_t n_b) {
   (void)n_r;

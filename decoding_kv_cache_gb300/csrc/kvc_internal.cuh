@@ -116,6 +116,7 @@ struct ScoreArgs {
   float2 rope[64];            // (cos, sin) of t * theta^(-2i/D), i < D/2, from fp64
   unsigned long long* xch_zero;  // words the observation kernel zeroes for the scoring kernel, or null
   long long xch_zero_words;
+  int debug_fault;               // kvc_debug_fault mode at launch (0 in normal use)
 };
 
 int obs_rows(int M, int dtype);

@@ -15,24 +15,24 @@
 // because group partners wait on one another.
 //
 // Roles (all derive the same chunk sequence from blockIdx; no queue):
-//   warp 0      TMA producer: each round's observation tile into one of two Q buffers, then the
-//               round's key chunks into a ring of K stages.
+//   warp 0      TMA producer of key chunks: each round's chunks into a ring of K stages.
 //   warp 1      tcgen05.mma issuer (one thread): S = Q K^T per chunk into TMEM accumulator
 //               (round & 1) * 2 + j.
+//   warp 18     TMA producer of observation tiles: each round's tile into one of two Q buffers
+//               (a separate warp, so key loads never wait behind a tile buffer).
 //   warps 2-9   pass 1, two warps per TMEM lane quarter (one column half each): each thread owns
 //               one row and folds its columns into the row's running (max, sum of exp2); the
 //               quarter's two warps merge and publish the row's partial. Two warps per SM
 //               sub-partition keep the MUFU (exp2) pipe busy while one waits on it.
 //   warps 10-17 pass 2, laid out the same way and running concurrently with pass 1 of the next
-//               round, once the round's lse2 exists: a chunk's
-//               TMEM values are read in the 16x256b fragment shape (each thread: 4 of the
-//               warp's 32 rows x 2 columns per 8-column group) and its accumulator freed;
+//               round. First the exchange: the 256 threads poll the group's partials of the
+//               round (four words each in flight at once) and merge them into lse2. Then a
+//               chunk's TMEM values are read in the 16x256b fragment shape (each thread: 4 of
+//               the warp's 32 rows x 2 columns per 8-column group) and its accumulator freed;
 //               s*c2 - lse2 and the max over the 4 rows in registers, then a 3-step
 //               reduce-scatter over the 8 lanes sharing a column pair leaves each lane one
 //               column's max over 32 rows (7 shuffles per 32 columns); the eight warps' maxima
 //               meet in shared memory and one thread per key writes exp2 of the max.
-//   warp 18     exchange: polls the group's partials of a round and merges them into lse2,
-//               all of a batch's loads in flight at once (the merge is on the critical path).
 // Exchange protocol: a partial is one 64-bit word, the row's log2-sum-exp2 over the CTA's keys
 // in the low half and round + 1 in the high half, written with one relaxed store; a reader
 // accepts a word once its tag matches, so data and "published" travel together and nobody
@@ -49,6 +49,13 @@ namespace kvc {
 constexpr int kResChunks = 2;    // key chunks per CTA per round
 constexpr int kResRows = 128;    // observation rows per head this kernel handles (one MMA tile)
 constexpr int kResAcc = 2 * kResChunks;
+constexpr unsigned long long kExchangeTimeoutNs = 50ull * 1000 * 1000;  // a partner's word: ~1 us normally
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
+  return t;
+}
 constexpr int kP1Warps = 8;  // warps 2-9: pass 1, two per TMEM lane quarter (one column half each)
 constexpr int kP2Warps = 8;  // warps 10-17: pass 2, likewise
 constexpr int kQWarp = 2 + kP1Warps + kP2Warps;              // warp 18: observation-tile producer
@@ -296,7 +303,9 @@ __global__ void __launch_bounds__(kResThreads, 1)
       float2* mg = merge + (round & 1) * kResRows;
       if (hf == 1) mg[row] = st;
       asm volatile("bar.sync %0, 64;\n" ::"r"(2 + q) : "memory");
-      if (hf == 0) {
+      // test-only fault (kvc_debug_fault 1): the first CTA never publishes, so its group's
+      // bounded exchange waits run out
+      if (hf == 0 && !(a.debug_fault == 1 && blockIdx.x == 0)) {
         const float2 m = lse_merge(st, mg[row]);
         const float part = m.y > 0.f ? m.x + log2f(m.y) : -INFINITY;
         st_relaxed_u64(words + ((size_t)((round & 3) * p.ngroups + group) * p.group_size + rank) * kResRows + row,
@@ -330,13 +339,15 @@ __global__ void __launch_bounds__(kResThreads, 1)
           w[u] = k < p.group_size ? ld_relaxed_u64(grp + (size_t)k * kResRows)
                                   : ((uint64_t)tag << 32) | __float_as_uint(-INFINITY);
         }
+        unsigned long long t_start = 0;
         for (uint32_t it = 0;; ++it) {
           unsigned need = 0u;
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             if ((uint32_t)(w[u] >> 32) != tag) need |= 1u << u;
           if (need == 0u) break;
-          if (it >= (1u << 22) || *abort_flag) {
+          if (it == 0) t_start = global_ns();
+          if (it >= (1u << 22) || *abort_flag || global_ns() - t_start > kExchangeTimeoutNs) {
             ok = false;
             if (!*abort_flag) {
               *abort_flag = 1;

@@ -16,12 +16,12 @@ import torch
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvc.so")
 
 KVC_BF16, KVC_F32 = 0, 1
-KVC_STATUS_BUDGET_RANGE, KVC_STATUS_COUNT_RANGE, KVC_STATUS_BAD_INDEX = 0x1, 0x2, 0x4
+KVC_STATUS_BUDGET_RANGE, KVC_STATUS_COUNT_RANGE, KVC_STATUS_BAD_INDEX, KVC_STATUS_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 KVC_MAX_LAYERS = 128
 
 EXPORTED = ("kvc_fps_update", "kvc_score_workspace_size", "kvc_score", "kvc_select", "kvc_compact",
             "kvc_evict_workspace_size", "kvc_evict", "kvc_evict_launch_count", "kvc_strerror", "kvc_abi_version",
-            "kvc_score_static")
+            "kvc_score_static", "kvc_debug_fault")
 KVC_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -64,6 +64,7 @@ def lib():
         "kvc_score_static": (C.c_int, [pc, vp, i32, vp, vp, i32, i32, i64, dbl, vp, vp, vp]),
         "kvc_strerror": (C.c_char_p, [C.c_int]),
         "kvc_abi_version": (C.c_int, []),
+        "kvc_debug_fault": (C.c_int, [i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -151,6 +152,11 @@ def kvc_evict_workspace_size(cache: Cache, n_r: int, n_b: int) -> int:
 
 def kvc_evict_launch_count(cache: Cache, n_r: int, n_b: int) -> int:
     return int(lib().kvc_evict_launch_count(cache.ref, n_r, n_b))
+
+
+def kvc_debug_fault(mode: int) -> None:
+    """Test-only fault switch (see include/kvc.h): 1 makes the scoring exchange wait run out."""
+    _check(lib().kvc_debug_fault(int(mode)))
 
 
 def _workspace(nbytes: int, device, workspace):

@@ -234,6 +234,15 @@ KVC_API const char* kvc_strerror(int code);
 /* KVC_ABI_VERSION of the loaded library. */
 KVC_API int kvc_abi_version(void);
 
+/* Test-only fault switch for the failure-detection path; none of the pages has a counterpart.
+ * mode 1: from the next scoring launch on, the first CTA of the single-read scoring kernel
+ * (bf16 caches with 128-row observation tiles) withholds its exchange partials, so its group's
+ * bounded waits give up after about 50 ms: those heads' scores are left unset,
+ * KVC_STATUS_TIMEOUT is raised in the status word of kvc_evict, and the launch still returns.
+ * mode 0 restores normal behaviour. Process-wide, not thread-safe against concurrent calls.
+ * Returns KVC_OK or KVC_ERR_INVALID_ARG for any other mode. */
+KVC_API int kvc_debug_fault(int32_t mode);
+
 #ifdef __cplusplus
 }
 #endif

@@ -45,6 +45,12 @@ def test_header_compiles_as_c():
     assert r.returncode == 0, r.stderr
 
 
+def test_fault_switch_takes_only_known_modes(lib):
+    assert lib.kvc_debug_fault(7) == -1
+    assert lib.kvc_debug_fault(-1) == -1
+    assert lib.kvc_debug_fault(0) == 0
+
+
 def test_strerror(lib):
     assert lib.kvc_strerror(0) == b"ok"
     assert b"head dimension" in lib.kvc_strerror(-3)
