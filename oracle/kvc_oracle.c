@@ -28,6 +28,16 @@
  *   score      BeaconKV page, same section: score_j = max over observation
  *              queries r of softmax_r(q_r . k_j / sqrt(D)) over all cached keys;
  *              the max also runs over the query heads sharing KV head h.
+ *   variants   BeaconKV page, section "实验", the max-vs-mean ablation: the
+ *              weights of one query head's observation rows may be averaged
+ *              instead of maxed; the query heads of a group may be summed
+ *              instead of maxed (oracle_score_agg_f64). The same function
+ *              returns the head's normalised attention entropy (mean over its
+ *              rows of -sum p ln p / ln N), the ReasonAlloc page's head utility
+ *              signal ("Key Concepts": low entropy = focused = more budget).
+ *   budget     ReasonAlloc page, "Core Mechanism": each layer's preallocated
+ *              total is redistributed over its heads by utility, the total held
+ *              fixed (oracle_head_budget states the rule; the page gives none).
  *   select     BeaconKV page, same section, last paragraph: prefix tokens and the
  *              most recent tokens are always kept; the rest of the budget goes
  *              to the top scores (ties: lower index). Section "实验": on reaching
@@ -274,6 +284,172 @@ void oracle_score_f64(const double* q, int M, const double* k, int N, int D, dou
 }
 
 /* ------------------------------------------------------------------------- */
+/* Aggregation variants and attention entropy.                                 */
+/* BeaconKV page, section "实验" (the max-vs-mean ablation): the softmax        */
+/* weights of the observation queries may be averaged instead of maxed.        */
+/* ReasonAlloc page, "Key Concepts" (Head Utility): a head's utility is its    */
+/* normalised attention entropy; low entropy = focused = more useful.          */
+/* ------------------------------------------------------------------------- */
+
+#define AGG_MAX 0
+#define AGG_MEAN 1
+#define AGG_SUM 2
+
+/* q[M][D] observation rows, row_head[M] the query head (0..G-1) each row
+ * belongs to, k[N][D] keys (fp64). With p_rj = softmax over all N keys of
+ * q_r . k_j / sqrt(D):
+ *   A_g(j)  = max over the rows of head g of p_rj          (row_agg AGG_MAX)
+ *           = mean over the rows of head g of p_rj         (row_agg AGG_MEAN)
+ *   out[j]  = max over heads g of A_g(j)                    (group_agg AGG_MAX)
+ *           = sum over heads g of A_g(j)                    (group_agg AGG_SUM)
+ * Heads without rows take no part. entropy (may be NULL) receives the mean over
+ * all M rows of H_r / ln N, H_r = -sum_j p_rj ln p_rj (0 when N = 1 or M = 0).
+ * Returns 0, or -1 for an unknown mode or a row_head entry out of range. */
+int oracle_score_agg_f64(const double* q, const int* row_head, int M, int G, const double* k, int N, int D,
+                         int row_agg, int group_agg, double* out, double* entropy) {
+  if ((row_agg != AGG_MAX && row_agg != AGG_MEAN) || (group_agg != AGG_MAX && group_agg != AGG_SUM)) return -1;
+  for (int r = 0; r < M; ++r)
+    if (row_head[r] < 0 || row_head[r] >= G) return -1;
+  double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+  double* A = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+  const double scale = 1.0 / sqrt((double)D);
+  double hsum = 0.0;
+  for (int j = 0; j < N; ++j) out[j] = 0.0;
+  for (int g = 0; g < G; ++g) {
+    int Mg = 0;
+    for (int j = 0; j < N; ++j) A[j] = 0.0;
+    for (int r = 0; r < M; ++r) {
+      if (row_head[r] != g) continue;
+      ++Mg;
+      double mx = -INFINITY;
+      for (int j = 0; j < N; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += q[(int64_t)r * D + d] * k[(int64_t)j * D + d];
+        s[j] = acc * scale;
+        if (s[j] > mx) mx = s[j];
+      }
+      double sum = 0.0;
+      for (int j = 0; j < N; ++j) sum += exp(s[j] - mx);
+      const double l = mx + log(sum);
+      double h = 0.0;
+      for (int j = 0; j < N; ++j) {
+        const double p = exp(s[j] - l);
+        if (row_agg == AGG_MAX) {
+          if (p > A[j]) A[j] = p;
+        } else {
+          A[j] += p;
+        }
+        if (p > 0.0) h -= p * log(p);
+      }
+      hsum += h;
+    }
+    if (Mg == 0) continue;
+    for (int j = 0; j < N; ++j) {
+      const double a = row_agg == AGG_MEAN ? A[j] / Mg : A[j];
+      if (group_agg == AGG_SUM) out[j] += a;
+      else if (a > out[j]) out[j] = a;
+    }
+  }
+  if (entropy) *entropy = (M > 0 && N > 1) ? hsum / M / log((double)N) : 0.0;
+  free(s);
+  free(A);
+  return 0;
+}
+
+/* Online head-wise budgets for the H KV heads of one layer of one sequence
+ * (ReasonAlloc page, "Core Mechanism": budget moves from low-utility to
+ * high-utility heads within a layer while the layer's preallocated total
+ * stays fixed; "Key Concepts": utility from normalised attention entropy, low
+ * entropy gets more). The page fixes no formula; the rule here:
+ *   total  T = sum_h min(given_h, N)            (the layer's preallocation)
+ *   floor  f = P + R, cap c = N - f             (every head keeps its windows)
+ *   utility u_h = 1 - ent_h, clipped to [0, 1]  (ent_h = normalised entropy)
+ *   the E = T - H f slots beyond the floors are shared in proportion to u
+ *   (equally when all active u are 0); a head whose share exceeds c gets c
+ *   and leaves, and the rest is shared again among the others (water-filling);
+ *   integer shares by largest remainder (floors, then one more slot each to the
+ *   largest fractional parts, ties to the lower head index);
+ *   out_h = f + share_h.
+ * Arithmetic in fp64 with each operation rounded on its own (no fused
+ * multiply-add), in head order. Returns 0, or -1 if some given_h < P + R (the
+ * caller keeps the given budgets then). If N <= f or T >= H N every head gets
+ * min(given_h, N) unchanged. */
+int oracle_head_budget(const float* ent, int H, int N, int P, int R, const int32_t* given, int32_t* out) {
+  const int f = P + R;
+  int64_t T = 0;
+  for (int h = 0; h < H; ++h) {
+    if (given[h] < f) return -1;
+    T += given[h] < N ? given[h] : N;
+  }
+  if (N <= f || T >= (int64_t)H * N) {
+    for (int h = 0; h < H; ++h) out[h] = given[h] < N ? given[h] : N;
+    return 0;
+  }
+  const int cap = N - f;
+  const int64_t E = T - (int64_t)H * f;
+  double u[64], share[64];
+  int active[64], x[64], bonus[64];
+  if (H > 64) return -1;
+  for (int h = 0; h < H; ++h) {
+    const double e = (double)ent[h];
+    double v = 1.0 - e;
+    if (!(v > 0.0)) v = 0.0; /* also catches NaN */
+    if (v > 1.0) v = 1.0;
+    u[h] = v;
+    active[h] = 1;
+    share[h] = 0.0;
+  }
+  double Erem = (double)E;
+  for (;;) {
+    double U = 0.0;
+    int na = 0;
+    for (int h = 0; h < H; ++h)
+      if (active[h]) {
+        U += u[h];
+        ++na;
+      }
+    if (na == 0) break;
+    int capped = 0;
+    for (int h = 0; h < H; ++h) {
+      if (!active[h]) continue;
+      share[h] = U > 0.0 ? (Erem * u[h]) / U : Erem / (double)na;
+    }
+    for (int h = 0; h < H; ++h)
+      if (active[h] && share[h] > (double)cap) {
+        share[h] = (double)cap;
+        active[h] = 0;
+        Erem -= (double)cap;
+        capped = 1;
+      }
+    if (!capped) break;
+  }
+  int64_t given_out = 0;
+  for (int h = 0; h < H; ++h) {
+    x[h] = active[h] ? (int)floor(share[h]) : cap;
+    if (x[h] > cap) x[h] = cap;
+    bonus[h] = 0;
+    given_out += x[h];
+  }
+  for (int64_t left = E - given_out; left > 0; --left) {
+    int best = -1;
+    double bf = -1.0;
+    for (int h = 0; h < H; ++h) {
+      if (bonus[h] || x[h] >= cap) continue;
+      const double fr = share[h] - (double)x[h];
+      if (fr > bf) {
+        bf = fr;
+        best = h;
+      }
+    }
+    if (best < 0) break; /* every head full: cannot happen while E < H * cap */
+    bonus[best] = 1;
+    x[best] += 1;
+  }
+  for (int h = 0; h < H; ++h) out[h] = f + x[h];
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Selection (BeaconKV page, end of "打分时的 RoPE 对齐"; section "实验").       */
 /* ------------------------------------------------------------------------- */
 
@@ -337,6 +513,11 @@ typedef struct {
   const int32_t* count;     /* [L,B,Hq] */
   const int32_t* budget;    /* [L,B,Hkv] or NULL -> budget_all */
   const int32_t* forced_picks; /* [L,B,Hq,n_b] beacon rows to use instead of FPS, or NULL */
+  int32_t row_agg;          /* AGG_MAX or AGG_MEAN over a query head's observation rows */
+  int32_t group_agg;        /* AGG_MAX or AGG_SUM over the query heads of a KV head */
+  int32_t head_budget;      /* 0: budgets as given; 1: reallocated within each layer by entropy */
+  int32_t pad_;
+  const float* forced_entropy; /* [L,B,Hkv] entropies for the reallocation instead of the oracle's, or NULL */
 } oracle_problem;
 
 typedef struct {
@@ -347,6 +528,8 @@ typedef struct {
   void* V_out;          /* [L,B,Hkv,N,D] or NULL */
   int32_t* beacon_picks;/* [L,B,Hq,n_b] or NULL: buffer rows used as beacons (-1 = none) */
   int32_t* error;       /* [L,B,Hkv] or NULL: 0, or -1 when the head's budget was out of range */
+  float* entropy;       /* [L,B,Hkv] or NULL: normalised attention entropy of the head's rows */
+  int32_t* budget_used; /* [L,B,Hkv] or NULL: the budget each head was selected with */
 } oracle_outputs;
 
 /* Beacon rows of one query head: the buffer's first `count` rows if there are
@@ -383,17 +566,17 @@ static void store_elem(void* base, int dtype, int64_t i, const void* src_base, i
   else ((float*)base)[i] = ((const float*)src_base)[si];
 }
 
-static void evict_head(const oracle_problem* p, const oracle_outputs* o, int64_t head) {
+/* Scores (and the entropy) of one KV head. */
+static void score_head(const oracle_problem* p, const oracle_outputs* o, int64_t head, float* scf, double* ent) {
   const int D = p->D, N = p->N, G = p->Hq / p->Hkv;
   const int l = (int)(head / ((int64_t)p->B * p->Hkv));
   const int b = (int)((head / p->Hkv) % p->B);
   const int h = (int)(head % p->Hkv);
   const int maxrows = G * (p->n_r + p->n_b);
   double* q = (double*)malloc(sizeof(double) * (size_t)(maxrows > 0 ? maxrows : 1) * D);
+  int* row_head = (int*)malloc(sizeof(int) * (size_t)(maxrows > 0 ? maxrows : 1));
   double* k = (double*)malloc(sizeof(double) * (size_t)N * D);
   double* sc = (double*)malloc(sizeof(double) * (size_t)N);
-  float* scf = (float*)malloc(sizeof(float) * (size_t)N);
-  int32_t* kept = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
   int* rows = (int*)malloc(sizeof(int) * (size_t)(p->qmax > 0 ? p->qmax : 1));
   float* tmp = (float*)malloc(sizeof(float) * (size_t)D);
   float* rot = (float*)malloc(sizeof(float) * (size_t)D);
@@ -404,13 +587,16 @@ static void evict_head(const oracle_problem* p, const oracle_outputs* o, int64_t
   for (int g = 0; g < G; ++g) {
     const int hq = h * G + g;
     const int64_t qh = ((int64_t)l * p->B + b) * p->Hq + hq;
-    for (int r = 0; r < p->n_r; ++r, ++M)
+    for (int r = 0; r < p->n_r; ++r, ++M) {
+      row_head[M] = g;
       for (int d = 0; d < D; ++d)
         q[(int64_t)M * D + d] = load_elem(p->q_recent, p->dtype, (qh * p->n_r + r) * D + d);
+    }
     int nb = beacon_rows(p, qh, rows);
     if (o->beacon_picks)
       for (int kk = 0; kk < p->n_b; ++kk) o->beacon_picks[qh * p->n_b + kk] = kk < nb ? rows[kk] : -1;
     for (int kk = 0; kk < nb; ++kk, ++M) {
+      row_head[M] = g;
       for (int d = 0; d < D; ++d) tmp[d] = (float)load_elem(p->qbuf, p->dtype, (qh * p->qmax + rows[kk]) * D + d);
       oracle_rope_f32(tmp, D, (long long)p->t, p->theta, rot);
       for (int d = 0; d < D; ++d) q[(int64_t)M * D + d] = round_to_storage((double)rot[d], p->dtype);
@@ -418,11 +604,23 @@ static void evict_head(const oracle_problem* p, const oracle_outputs* o, int64_t
   }
   const int64_t kbase = head * (int64_t)N * D;
   for (int64_t i = 0; i < (int64_t)N * D; ++i) k[i] = load_elem(p->K, p->dtype, kbase + i);
-  oracle_score_f64(q, M, k, N, D, sc, NULL);
+  if (p->row_agg == AGG_MAX && p->group_agg == AGG_MAX && !o->entropy && !p->head_budget) {
+    oracle_score_f64(q, M, k, N, D, sc, NULL);
+    *ent = 0.0;
+  } else {
+    oracle_score_agg_f64(q, row_head, M, G, k, N, D, p->row_agg, p->group_agg, sc, ent);
+  }
   for (int j = 0; j < N; ++j) scf[j] = (float)sc[j];
   if (o->scores) memcpy(&o->scores[head * N], scf, sizeof(float) * (size_t)N);
+  if (o->entropy) o->entropy[head] = (float)*ent;
+  free(q); free(row_head); free(k); free(sc); free(rows); free(tmp); free(rot);
+}
 
-  int budget = p->budget ? p->budget[head] : p->budget_all;
+/* Selection and compaction of one KV head with the given budget. */
+static void keep_head(const oracle_problem* p, const oracle_outputs* o, int64_t head, const float* scf, int budget) {
+  const int D = p->D, N = p->N;
+  int32_t* kept = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+  if (o->budget_used) o->budget_used[head] = budget;
   int len = oracle_select(scf, N, p->prefix, p->recent, budget, kept);
   if (o->error) o->error[head] = len < 0 ? -1 : 0;
   if (len < 0) { /* out-of-range budget: the head is left whole */
@@ -433,29 +631,63 @@ static void evict_head(const oracle_problem* p, const oracle_outputs* o, int64_t
   if (o->kept_idx)
     for (int j = 0; j < N; ++j) o->kept_idx[head * N + j] = j < len ? kept[j] : -1;
   /* compaction: out-of-place gather into the output copies */
+  const int64_t kbase = head * (int64_t)N * D;
   if (o->K_out)
     for (int j = 0; j < len; ++j)
       for (int d = 0; d < D; ++d) store_elem(o->K_out, p->dtype, kbase + (int64_t)j * D + d, p->K, kbase + (int64_t)kept[j] * D + d);
   if (o->V_out)
     for (int j = 0; j < len; ++j)
       for (int d = 0; d < D; ++d) store_elem(o->V_out, p->dtype, kbase + (int64_t)j * D + d, p->V, kbase + (int64_t)kept[j] * D + d);
-  free(q); free(k); free(sc); free(scf); free(kept); free(rows); free(tmp); free(rot);
+  free(kept);
 }
 
-/* The eviction step for every (l, b, h_kv). K_out / V_out must already hold a
- * copy of K / V (slots past the kept count are left as they are). heads /
- * nheads (optional) restrict the work to the listed flat head ids
- * (l*B + b)*Hkv + h. Returns 0, or -1 on bad sizes. */
+/* The eviction step for every (l, b, h_kv), in three steps: the scores (and
+ * entropy) of each head; with head_budget = 1 the budgets of each layer of each
+ * sequence (oracle_head_budget over its Hkv heads); then selection and
+ * compaction of each head. K_out / V_out must already hold a copy of K / V
+ * (slots past the kept count are left as they are). heads / nheads (optional)
+ * restrict the work to the listed flat head ids (l*B + b)*Hkv + h; with
+ * head_budget = 1 the other heads of each listed head's layer are scored too,
+ * since its budget depends on them. Returns 0, or -1 on bad sizes or modes. */
 int oracle_evict(const oracle_problem* p, const oracle_outputs* o, const int64_t* heads, int64_t nheads) {
   if (!p || !o || p->L < 1 || p->B < 1 || p->Hkv < 1 || p->Hq < p->Hkv || p->Hq % p->Hkv) return -1;
   if (p->D < 2 || p->D % 2 || p->N < 1 || p->n_r < 0 || p->n_b < 0 || p->qmax < 0) return -1;
+  if ((p->row_agg != AGG_MAX && p->row_agg != AGG_MEAN) || (p->group_agg != AGG_MAX && p->group_agg != AGG_SUM) ||
+      p->head_budget < 0 || p->head_budget > 1 || p->Hkv > 64)
+    return -1;
   const int64_t total = (int64_t)p->L * p->B * p->Hkv;
-  const int64_t n = heads ? nheads : total;
-#pragma omp parallel for schedule(dynamic, 1)
-  for (int64_t i = 0; i < n; ++i) {
-    int64_t head = heads ? heads[i] : i;
-    if (head >= 0 && head < total) evict_head(p, o, head);
+  const int N = p->N, Hkv = p->Hkv;
+  /* which heads to score (want = 1) and to keep (want = 2) */
+  char* want = (char*)calloc((size_t)total, 1);
+  for (int64_t i = 0; i < (heads ? nheads : total); ++i) {
+    const int64_t head = heads ? heads[i] : i;
+    if (head < 0 || head >= total) continue;
+    want[head] = 2;
+    if (p->head_budget)
+      for (int64_t g = head - head % Hkv; g < head - head % Hkv + Hkv; ++g)
+        if (!want[g]) want[g] = 1;
   }
+  float* scf = (float*)malloc(sizeof(float) * (size_t)total * N);
+  double* ent = (double*)calloc((size_t)total, sizeof(double));
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t head = 0; head < total; ++head)
+    if (want[head]) score_head(p, o, head, scf + head * N, &ent[head]);
+  int32_t* bud = (int32_t*)malloc(sizeof(int32_t) * (size_t)total);
+  for (int64_t head = 0; head < total; ++head) bud[head] = p->budget ? p->budget[head] : p->budget_all;
+  if (p->head_budget)
+    for (int64_t lb = 0; lb < total / Hkv; ++lb) {
+      if (!want[lb * Hkv]) continue;
+      float e[64];
+      int32_t out[64];
+      for (int h = 0; h < Hkv; ++h)
+        e[h] = p->forced_entropy ? p->forced_entropy[lb * Hkv + h] : (float)ent[lb * Hkv + h];
+      if (oracle_head_budget(e, Hkv, N, p->prefix, p->recent, bud + lb * Hkv, out) == 0)
+        memcpy(bud + lb * Hkv, out, sizeof(int32_t) * (size_t)Hkv);
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t head = 0; head < total; ++head)
+    if (want[head] == 2) keep_head(p, o, head, scf + head * N, bud[head]);
+  free(want); free(scf); free(ent); free(bud);
   return 0;
 }
 

@@ -39,13 +39,15 @@ class _Problem(C.Structure):
                 ("n_b", C.c_int32), ("qmax", C.c_int32), ("prefix", C.c_int32), ("recent", C.c_int32),
                 ("budget_all", C.c_int32), ("t", C.c_int64), ("theta", C.c_double),
                 ("K", C.c_void_p), ("V", C.c_void_p), ("q_recent", C.c_void_p), ("qbuf", C.c_void_p),
-                ("count", C.c_void_p), ("budget", C.c_void_p), ("forced_picks", C.c_void_p)]
+                ("count", C.c_void_p), ("budget", C.c_void_p), ("forced_picks", C.c_void_p),
+                ("row_agg", C.c_int32), ("group_agg", C.c_int32), ("head_budget", C.c_int32), ("pad_", C.c_int32),
+                ("forced_entropy", C.c_void_p)]
 
 
 class _Outputs(C.Structure):
     _fields_ = [("scores", C.c_void_p), ("kept_idx", C.c_void_p), ("kept_len", C.c_void_p),
                 ("K_out", C.c_void_p), ("V_out", C.c_void_p), ("beacon_picks", C.c_void_p),
-                ("error", C.c_void_p)]
+                ("error", C.c_void_p), ("entropy", C.c_void_p), ("budget_used", C.c_void_p)]
 
 
 def lib():
@@ -65,6 +67,11 @@ def lib():
         L.oracle_rope_f32.argtypes = [C.c_void_p, C.c_int, C.c_longlong, C.c_double, C.c_void_p]
         L.oracle_score_f64.restype = None
         L.oracle_score_f64.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
+        L.oracle_score_agg_f64.restype = C.c_int
+        L.oracle_score_agg_f64.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_int,
+                                           C.c_int, C.c_int, C.c_void_p, C.c_void_p]
+        L.oracle_head_budget.restype = C.c_int
+        L.oracle_head_budget.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         L.oracle_select.restype = C.c_int
         L.oracle_select.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p]
         L.oracle_evict.restype = C.c_int
@@ -155,6 +162,40 @@ def score(q, k, with_lse: bool = False):
     return (out, lse[:M]) if with_lse else out
 
 
+ROW_AGG = {"max": 0, "mean": 1}
+GROUP_AGG = {"max": 0, "sum": 2}
+HEAD_BUDGET = {"given": 0, "entropy": 1}
+
+
+def score_agg(q, row_head, G: int, k, row_agg: str = "max", group_agg: str = "max"):
+    """Scores under the aggregation variants and the normalised entropy, fp64.
+
+    q [M, D] rows, row_head [M] query head of each row (0..G-1), k [N, D] keys. Returns
+    (scores [N], entropy) where entropy = mean over rows of H_r / ln N."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    rh = np.ascontiguousarray(row_head, dtype=np.int32)
+    M, D = q.shape
+    N = k.shape[0]
+    out = np.zeros(N, dtype=np.float64)
+    ent = np.zeros(1, dtype=np.float64)
+    rc = lib().oracle_score_agg_f64(_ptr(q), _ptr(rh), M, G, _ptr(k), N, D, ROW_AGG[row_agg], GROUP_AGG[group_agg],
+                                    _ptr(out), _ptr(ent))
+    if rc:
+        raise ValueError("oracle_score_agg_f64: bad mode or row_head")
+    return out, float(ent[0])
+
+
+def head_budget(entropy, N: int, prefix: int, recent: int, given):
+    """Budgets of one layer's heads reallocated by entropy (see oracle_head_budget), or None when a
+    given budget is below prefix + recent."""
+    e = np.ascontiguousarray(entropy, dtype=np.float32)
+    g = np.ascontiguousarray(given, dtype=np.int32)
+    out = np.zeros(len(e), dtype=np.int32)
+    rc = lib().oracle_head_budget(_ptr(e), len(e), int(N), int(prefix), int(recent), _ptr(g), _ptr(out))
+    return None if rc else out
+
+
 def select(scores, prefix: int, recent: int, budget: int):
     """Kept indices (ascending) or None when the budget cannot hold prefix + recent."""
     s = np.ascontiguousarray(scores, dtype=np.float32)
@@ -180,12 +221,17 @@ def _np_storage(t):
     raise TypeError(t.dtype)
 
 
-def evict(inp, heads: Optional[Sequence[int]] = None, forced_picks=None, threads: int = 0):
+def evict(inp, heads: Optional[Sequence[int]] = None, forced_picks=None, threads: int = 0, row_agg: str = "max",
+          group_agg: str = "max", head_budget: str = "given", forced_entropy=None):
     """Run the oracle's eviction step on ``inp`` (an ``EvictInputs`` with CPU tensors).
 
     Returns a dict of numpy arrays: scores [L,B,Hkv,N] f32, kept_idx [L,B,Hkv,N] (-1 past kept_len),
     kept_len [L,B,Hkv], K_out/V_out (storage bits, compacted copies), beacon_picks [L,B,Hq,n_b],
-    error [L,B,Hkv]. ``heads`` restricts the work to flat head ids (others stay zero / copied).
+    error [L,B,Hkv], entropy [L,B,Hkv] (normalised attention entropy), budget_used [L,B,Hkv].
+    ``heads`` restricts the work to flat head ids (others stay zero / copied). ``row_agg`` /
+    ``group_agg`` pick the aggregation variant, ``head_budget="entropy"`` reallocates each layer's
+    budget over its heads by entropy (``forced_entropy`` [L,B,Hkv] replaces the oracle's entropies
+    in that decision).
     """
     if threads:
         set_threads(threads)
@@ -196,16 +242,20 @@ def evict(inp, heads: Optional[Sequence[int]] = None, forced_picks=None, threads
     cnt = _np_storage(inp.count.to(dtype=__import__("torch").int32))
     bud = None if inp.budget is None else _np_storage(inp.budget.to(dtype=__import__("torch").int32))
     fp = None if forced_picks is None else np.ascontiguousarray(forced_picks, dtype=np.int32)
+    fe = None if forced_entropy is None else np.ascontiguousarray(forced_entropy, dtype=np.float32)
     L, B, Hq, Hkv, N = inp.L, inp.B, inp.Hq, inp.Hkv, inp.N
     p = _Problem(dtype=0 if inp.dtype == "bf16" else 1, L=L, B=B, Hq=Hq, Hkv=Hkv, D=inp.D, N=N,
                  n_r=inp.n_r, n_b=inp.n_b, qmax=inp.qmax, prefix=inp.prefix, recent=inp.recent,
                  budget_all=inp.budget_all, t=inp.t, theta=inp.theta, K=_ptr(K).value, V=_ptr(V).value,
                  q_recent=_ptr(qr).value, qbuf=_ptr(qb).value, count=_ptr(cnt).value,
                  budget=None if bud is None else _ptr(bud).value,
-                 forced_picks=None if fp is None else _ptr(fp).value)
+                 forced_picks=None if fp is None else _ptr(fp).value, row_agg=ROW_AGG[row_agg],
+                 group_agg=GROUP_AGG[group_agg], head_budget=HEAD_BUDGET[head_budget], pad_=0,
+                 forced_entropy=None if fe is None else _ptr(fe).value)
     out = dict(scores=np.zeros((L, B, Hkv, N), np.float32), kept_idx=np.full((L, B, Hkv, N), -1, np.int32),
                kept_len=np.zeros((L, B, Hkv), np.int32), K_out=K.copy(), V_out=V.copy(),
-               beacon_picks=np.full((L, B, Hq, inp.n_b), -1, np.int32), error=np.zeros((L, B, Hkv), np.int32))
+               beacon_picks=np.full((L, B, Hq, inp.n_b), -1, np.int32), error=np.zeros((L, B, Hkv), np.int32),
+               entropy=np.zeros((L, B, Hkv), np.float32), budget_used=np.zeros((L, B, Hkv), np.int32))
     o = _Outputs(**{k: _ptr(v).value for k, v in out.items()})
     hv = None if heads is None else np.ascontiguousarray(heads, dtype=np.int64)
     rc = lib().oracle_evict(C.byref(p), C.byref(o), None if hv is None else _ptr(hv), 0 if hv is None else len(hv))
