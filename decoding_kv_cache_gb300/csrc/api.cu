@@ -43,15 +43,40 @@ int check_cache(const kvc_cache* c, CacheGeom* g, LayerPtrs* K, LayerPtrs* V) {
   return KVC_OK;
 }
 
+// The options of one call, checked; ext = the extended scoring epilogue is needed.
+struct Opts {
+  bool ext;
+  int row_agg, group_agg, head_budget;
+  float* entropy;  // the caller's entropy output, or null
+};
+
+int check_opts(const kvc_opts* o, bool evict, Opts* out) {
+  *out = Opts{false, KVC_AGG_MAX, KVC_AGG_MAX, KVC_BUDGET_GIVEN, nullptr};
+  if (!o) return KVC_OK;
+  if ((o->row_agg != KVC_AGG_MAX && o->row_agg != KVC_AGG_MEAN) ||
+      (o->group_agg != KVC_AGG_MAX && o->group_agg != KVC_AGG_SUM) ||
+      (o->head_budget != KVC_BUDGET_GIVEN && o->head_budget != KVC_BUDGET_ENTROPY) || o->reserved != 0)
+    return KVC_ERR_INVALID_ARG;
+  if (!evict && o->head_budget != KVC_BUDGET_GIVEN) return KVC_ERR_INVALID_ARG;
+  if (o->entropy && (reinterpret_cast<uintptr_t>(o->entropy) & 3u)) return KVC_ERR_ALIGNMENT;
+  out->row_agg = o->row_agg;
+  out->group_agg = o->group_agg;
+  out->head_budget = o->head_budget;
+  out->entropy = o->entropy;
+  out->ext = o->row_agg != KVC_AGG_MAX || o->group_agg != KVC_AGG_MAX || o->entropy ||
+             o->head_budget == KVC_BUDGET_ENTROPY;
+  return KVC_OK;
+}
+
 int check_queries(const kvc_cache* c, const void* q_recent, int n_r, const void* qbuf, const int32_t* count,
-                  int qmax, int n_b, double theta) {
+                  int qmax, int n_b, double theta, bool ext) {
   if (n_r < 0 || n_r > 64 || qmax < 0 || qmax > kMaxQmax || n_b < 0 || n_b > qmax || n_r + n_b < 1)
     return KVC_ERR_INVALID_ARG;
   if (n_r > 0 && !q_recent) return KVC_ERR_INVALID_ARG;
   if (qmax > 0 && (!qbuf || !count)) return KVC_ERR_INVALID_ARG;
   if (!(theta > 1.0) || !isfinite(theta)) return KVC_ERR_INVALID_ARG;
   const int G = c->Hq / c->Hkv;
-  if ((long long)G * (n_r + n_b) > kMaxRows) return KVC_ERR_TOO_LARGE;
+  if ((long long)(G - 1) * obs_qstride(n_r, n_b, ext) + n_r + n_b > kMaxRows) return KVC_ERR_TOO_LARGE;
   if ((q_recent && !aligned16(q_recent)) || (qbuf && !aligned16(qbuf))) return KVC_ERR_ALIGNMENT;
   return KVC_OK;
 }
@@ -62,8 +87,13 @@ std::atomic<int> g_debug_fault{0};  // test-only fault switch, read at each scor
 
 void fill_score_args(ScoreArgs* a, const CacheGeom& g, int dtype, const LayerPtrs& K, const void* q_recent, int n_r,
                      const void* qbuf, const int32_t* count, int qmax, int n_b, int64_t t, double theta,
-                     float* scores, int32_t* beacon_picks, int32_t* status) {
+                     float* scores, int32_t* beacon_picks, int32_t* status, const Opts& o, float* entropy) {
   a->g = g;
+  a->ext = o.ext ? 1 : 0;
+  a->qstride = obs_qstride(n_r, n_b, o.ext);
+  a->row_agg = o.row_agg;
+  a->group_agg = o.group_agg;
+  a->entropy = entropy;
   a->debug_fault = g_debug_fault.load();
   a->dtype = dtype;
   a->K = K;
@@ -78,7 +108,7 @@ void fill_score_args(ScoreArgs* a, const CacheGeom& g, int dtype, const LayerPtr
   a->scores = scores;
   a->beacon_picks = beacon_picks;
   a->status = status;
-  a->M = (g.Hq / g.Hkv) * (n_r + n_b);
+  a->M = obs_rows_used(g.Hq / g.Hkv, n_r, n_b, o.ext);
   a->M_pad = obs_rows(a->M, dtype);
   a->M_n = (a->M + 15) / 16 * 16;
   // Rotary angles of the current step in fp64 (BeaconKV write-up, "打分时的 RoPE 对齐":
@@ -106,6 +136,19 @@ int kvc_debug_fault(int32_t mode) {
   if (mode < 0 || mode > 1) return KVC_ERR_INVALID_ARG;
   g_debug_fault.store(mode);
   return KVC_OK;
+}
+
+int kvc_head_budget(const float* entropy, int32_t L, int32_t B, int32_t Hkv, int32_t N, int32_t prefix,
+                    int32_t recent, const int32_t* budget, int32_t budget_all, int32_t* budget_out, int32_t* status,
+                    void* stream) {
+  if (!entropy || !budget_out || L < 1 || B < 1 || Hkv < 1 || N < 1 || prefix < 0 || recent < 0)
+    return KVC_ERR_INVALID_ARG;
+  if (Hkv > 64) return KVC_ERR_TOO_LARGE;
+  const long long groups = (long long)L * B;
+  if (groups > (1LL << 31) - 1) return KVC_ERR_TOO_LARGE;
+  if (!budget && budget_all < prefix + recent && budget_all < N) return KVC_ERR_BUDGET_RANGE;
+  return launch_head_budget(entropy, (int)groups, Hkv, N, prefix, recent, budget, budget_all, budget_out, status,
+                            static_cast<cudaStream_t>(stream));
 }
 
 int kvc_evict_launch_count(const kvc_cache* c, int32_t n_r, int32_t n_b) {
@@ -149,26 +192,32 @@ size_t kvc_score_workspace_size(const kvc_cache* c, int32_t n_r, int32_t n_b) {
   if (!c || n_r < 0 || n_b < 0) return 0;
   kvc_cache probe = *c;
   if (check_cache(&probe, &g, &K, &V)) return 0;
-  return score_ws_bytes(g, c->dtype, n_r, n_b, nullptr, nullptr);
+  // enough for either row layout (the extended one may need more rows)
+  const size_t a = score_ws_bytes(g, c->dtype, n_r, n_b, false, nullptr, nullptr);
+  const size_t b = score_ws_bytes(g, c->dtype, n_r, n_b, true, nullptr, nullptr);
+  return a > b ? a : b;
 }
 
 int kvc_score(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf, const int32_t* count,
               int32_t qmax, int32_t n_b, int64_t t, double rope_theta, float* scores, int32_t* beacon_picks,
-              void* workspace, size_t ws_bytes, void* stream) {
+              const kvc_opts* opts, void* workspace, size_t ws_bytes, void* stream) {
   CacheGeom g;
   LayerPtrs K, V;
+  Opts o;
   int rc = check_cache(c, &g, &K, &V);
   if (rc) return rc;
-  rc = check_queries(c, q_recent, n_r, qbuf, count, qmax, n_b, rope_theta);
+  rc = check_opts(opts, false, &o);
+  if (rc) return rc;
+  rc = check_queries(c, q_recent, n_r, qbuf, count, qmax, n_b, rope_theta, o.ext);
   if (rc) return rc;
   if (!scores) return KVC_ERR_INVALID_ARG;
-  const size_t need = score_ws_bytes(g, c->dtype, n_r, n_b, nullptr, nullptr);
+  const size_t need = score_ws_bytes(g, c->dtype, n_r, n_b, o.ext, nullptr, nullptr);
   if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return KVC_ERR_WORKSPACE;
   ScoreWs ws;
-  score_ws_bytes(g, c->dtype, n_r, n_b, &ws, workspace);
+  score_ws_bytes(g, c->dtype, n_r, n_b, o.ext, &ws, workspace);
   ScoreArgs a;
   fill_score_args(&a, g, c->dtype, K, q_recent, n_r, qbuf, count, qmax, n_b, t, rope_theta, scores, beacon_picks,
-                  nullptr);
+                  nullptr, o, o.entropy);
   return launch_score(a, ws, static_cast<cudaStream_t>(stream));
 }
 
@@ -180,8 +229,8 @@ int kvc_select(const float* scores, int32_t L, int32_t B, int32_t Hkv, int32_t N
   const long long heads = (long long)L * B * Hkv;
   if (heads > (1LL << 31) - 1 || (long long)N > (1LL << 30)) return KVC_ERR_TOO_LARGE;
   if (!budget && budget_all < prefix + recent && budget_all < N) return KVC_ERR_BUDGET_RANGE;
-  return launch_select(scores, (int)heads, N, prefix, recent, budget, budget_all, kept_idx, kept_len, status,
-                       static_cast<cudaStream_t>(stream));
+  return launch_select(scores, (int)heads, N, prefix, recent, budget, budget_all, nullptr, 1, kept_idx, kept_len,
+                       status, static_cast<cudaStream_t>(stream));
 }
 
 int kvc_compact(const kvc_cache* c, const int32_t* kept_idx, const int32_t* kept_len, int32_t* status,
@@ -204,30 +253,38 @@ size_t kvc_evict_workspace_size(const kvc_cache* c, int32_t n_r, int32_t n_b) {
 int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf, const int32_t* count,
               int32_t qmax, int32_t n_b, int64_t t, double rope_theta, int32_t prefix, int32_t recent,
               const int32_t* budget, int32_t budget_all, int32_t* kept_idx, int32_t* kept_len, float* scores,
-              int32_t* status, void* workspace, size_t ws_bytes, void* stream) {
+              int32_t* status, const kvc_opts* opts, void* workspace, size_t ws_bytes, void* stream) {
   CacheGeom g;
   LayerPtrs K, V;
+  Opts o;
   int rc = check_cache(c, &g, &K, &V);
   if (rc) return rc;
-  rc = check_queries(c, q_recent, n_r, qbuf, count, qmax, n_b, rope_theta);
+  rc = check_opts(opts, true, &o);
+  if (rc) return rc;
+  rc = check_queries(c, q_recent, n_r, qbuf, count, qmax, n_b, rope_theta, o.ext);
   if (rc) return rc;
   if (!kept_len || prefix < 0 || recent < 0) return KVC_ERR_INVALID_ARG;
   if (!budget && budget_all < prefix + recent && budget_all < c->N) return KVC_ERR_BUDGET_RANGE;
-  const size_t sw = score_ws_bytes(g, c->dtype, n_r, n_b, nullptr, nullptr);
+  if (o.head_budget == KVC_BUDGET_ENTROPY && g.Hkv > 64) return KVC_ERR_TOO_LARGE;
+  const size_t sw = score_ws_bytes(g, c->dtype, n_r, n_b, o.ext, nullptr, nullptr);
   const size_t per = align256((size_t)g.L * g.B * g.Hkv * (size_t)g.N * 4);
   if (!workspace || ws_bytes < sw + 2 * per || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return KVC_ERR_WORKSPACE;
   char* wb = static_cast<char*>(workspace);
   ScoreWs ws;
-  score_ws_bytes(g, c->dtype, n_r, n_b, &ws, wb);
+  score_ws_bytes(g, c->dtype, n_r, n_b, o.ext, &ws, wb);
   float* sc = scores ? scores : reinterpret_cast<float*>(wb + sw);
   int32_t* ki = kept_idx ? kept_idx : reinterpret_cast<int32_t*>(wb + sw + per);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the entropy goes to the caller's array, else (when the budgets need it) to the workspace's
+  float* ent = o.entropy ? o.entropy : (o.head_budget == KVC_BUDGET_ENTROPY ? ws.ent : nullptr);
   ScoreArgs a;
-  fill_score_args(&a, g, c->dtype, K, q_recent, n_r, qbuf, count, qmax, n_b, t, rope_theta, sc, nullptr, status);
+  fill_score_args(&a, g, c->dtype, K, q_recent, n_r, qbuf, count, qmax, n_b, t, rope_theta, sc, nullptr, status, o,
+                  ent);
   rc = launch_score(a, ws, s);
   if (rc) return rc;
-  rc = launch_select(sc, g.L * g.B * g.Hkv, g.N, prefix, recent, budget, budget_all, ki, kept_len, status, s);
+  rc = launch_select(sc, g.L * g.B * g.Hkv, g.N, prefix, recent, budget, budget_all,
+                     o.head_budget == KVC_BUDGET_ENTROPY ? ent : nullptr, g.Hkv, ki, kept_len, status, s);
   if (rc) return rc;
   return launch_compact(g, c->dtype, K, V, ki, kept_len, status, false, s);
 }
@@ -266,22 +323,25 @@ void* static_scratch() {
 
 extern "C" int kvc_score_static(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf,
                                 const int32_t* count, int32_t qmax, int32_t n_b, int64_t t, double rope_theta,
-                                float* scores, int32_t* beacon_picks, void* stream) {
+                                float* scores, int32_t* beacon_picks, const kvc_opts* opts, void* stream) {
   CacheGeom g;
   LayerPtrs K, V;
+  Opts o;
   int rc = check_cache(c, &g, &K, &V);
   if (rc) return rc;
-  rc = check_queries(c, q_recent, n_r, qbuf, count, qmax, n_b, rope_theta);
+  rc = check_opts(opts, false, &o);
+  if (rc) return rc;
+  rc = check_queries(c, q_recent, n_r, qbuf, count, qmax, n_b, rope_theta, o.ext);
   if (rc) return rc;
   if (!scores) return KVC_ERR_INVALID_ARG;
-  const size_t need = score_ws_bytes(g, c->dtype, n_r, n_b, nullptr, nullptr);
+  const size_t need = score_ws_bytes(g, c->dtype, n_r, n_b, o.ext, nullptr, nullptr);
   if (need > (size_t)KVC_STATIC_SCRATCH_BYTES) return KVC_ERR_WORKSPACE;
   void* scratch = static_scratch();
   if (!scratch) return KVC_ERR_LAUNCH;
   ScoreWs ws;
-  score_ws_bytes(g, c->dtype, n_r, n_b, &ws, scratch);
+  score_ws_bytes(g, c->dtype, n_r, n_b, o.ext, &ws, scratch);
   ScoreArgs a;
   fill_score_args(&a, g, c->dtype, K, q_recent, n_r, qbuf, count, qmax, n_b, t, rope_theta, scores, beacon_picks,
-                  nullptr);
+                  nullptr, o, o.entropy);
   return launch_score(a, ws, static_cast<cudaStream_t>(stream));
 }

@@ -96,6 +96,9 @@ struct ScoreWs {            // carved out of the caller's workspace
   uint8_t* valid;           // [heads][M_pad]
   float2* part;             // fp32: [heads][nchunk][M_pad] partial (max, sum) in base 2; bf16: fused exchange
   float* lse2;              // [heads][M_pad] log2-sum-exp2, +inf for unused rows
+  float* rw;                // [heads][M_pad] row weight of a mean over the query head's rows (0: no row)
+  float* escale;            // [heads] 1 / (valid rows * log2 N): entropy in bits -> normalised mean
+  float* ent;               // [heads] entropy accumulator when the caller keeps none (kvc_evict)
 };
 
 struct ScoreArgs {
@@ -117,11 +120,22 @@ struct ScoreArgs {
   unsigned long long* xch_zero;  // words the observation kernel zeroes for the scoring kernel, or null
   long long xch_zero_words;
   int debug_fault;               // kvc_debug_fault mode at launch (0 in normal use)
+  // Variants: an aggregation other than max/max or an entropy output runs the kernels'
+  // extended epilogue (ext = 1). Rows of query head g then start at g * qstride, a multiple
+  // of 16, so every 16-row block of the tile belongs to one query head.
+  int ext;
+  int qstride;                   // rows per query head in the tile (n_r + n_b, or rounded up to 16)
+  int row_agg, group_agg;        // KVC_AGG_* (ext only)
+  float* entropy;                // [heads] normalised entropy, accumulated (zeroed by build_obs), or null
 };
+
+// Row stride of a query head and row count of the observation tile for a mode.
+inline int obs_qstride(int n_r, int n_b, bool ext) { return ext ? (n_r + n_b + 15) / 16 * 16 : n_r + n_b; }
+inline int obs_rows_used(int G, int n_r, int n_b, bool ext) { return (G - 1) * obs_qstride(n_r, n_b, ext) + n_r + n_b; }
 
 int obs_rows(int M, int dtype);
 
-size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, ScoreWs* carve, void* base);
+size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext, ScoreWs* carve, void* base);
 int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s);
 size_t fused_xch_bytes(int M_pad);
 int launch_score_fused(const ScoreArgs& a, const ScoreWs& ws, void* xch_base, cudaStream_t s);
@@ -138,8 +152,12 @@ bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem);
 long long score_resident_words(const FusedPlan& p);
 int launch_score_resident(const ScoreArgs& a, const ScoreWs& ws, const FusedPlan& p, size_t smem, cudaStream_t s);
 
+// entropy non-null: each (layer, sequence)'s budgets are reallocated over its Hkv heads first
 int launch_select(const float* scores, int heads, int N, int P, int R, const int32_t* budget, int budget_all,
-                  int32_t* kept_idx, int32_t* kept_len, int32_t* status, cudaStream_t s);
+                  const float* entropy, int Hkv, int32_t* kept_idx, int32_t* kept_len, int32_t* status,
+                  cudaStream_t s);
+int launch_head_budget(const float* entropy, int groups, int Hkv, int N, int P, int R, const int32_t* budget,
+                       int budget_all, int32_t* budget_out, int32_t* status, cudaStream_t s);
 
 int launch_compact(const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V, const int32_t* kept_idx,
                    const int32_t* kept_len, int32_t* status, bool validate, cudaStream_t s);

@@ -35,6 +35,7 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
   const int head = blockIdx.x;
   const int l = head / (B * Hkv), b = (head / Hkv) % B, h = head % Hkv;
   const int G = Hq / Hkv, per_q = a.n_r + a.n_b, hd = D / 2;
+  const int qs = a.qstride;  // rows of query head g start at g * qs
   constexpr int LD = Staging<T, D>::LD;
   T* obs = static_cast<T*>(ws.obs) + (size_t)head * a.M_pad * D;
   uint8_t* valid = ws.valid + (size_t)head * a.M_pad;
@@ -51,13 +52,15 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
   float2* rope_s = reinterpret_cast<float2*>(smem_raw + (size_t)nw * ((fps_scratch_bytes<T, D>(npad) + 15) & ~(size_t)15));
   fps_stage_init<T, D>(scratch, npad);
   uint32_t stage_phase = 0;
+  __shared__ int s_nvalid;  // valid observation rows of this KV head (for the entropy's mean)
+  const bool mean_w = a.ext && a.row_agg == KVC_AGG_MEAN;
 
   // every warp has at least one query head (nw <= G), so the CTA-wide step in the first
   // iteration is reached by all threads
   for (int g = warp, it = 0; g < G; g += nw, ++it) {
     const int hq = h * G + g;
     const size_t qh = ((size_t)l * B + b) * Hq + hq;
-    T* orow = obs + (size_t)g * per_q * D;
+    T* orow = obs + (size_t)g * qs * D;
     // Issue this query head's global reads first: stage the whole buffer (rows at or past its
     // count are staged too but never read: FPS and the Gram entries it uses involve live rows
     // only), the count, and the first batch of recent rows.
@@ -81,6 +84,7 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
         for (long long w = lo + threadIdx.x; w < hi; w += blockDim.x) a.xch_zero[w] = 0ull;
       }
       for (int i = threadIdx.x; i < hd; i += blockDim.x) rope_s[i] = a.rope[i];
+      if (threadIdx.x == 0) s_nvalid = 0;
       __syncthreads();
     }
     if (c < 0 || c > a.qmax) {
@@ -100,13 +104,26 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
       for (int u = 0; u < 8; ++u)
         if (e0 + u * kWarp + lane < nv) od[e0 + u * kWarp + lane] = v[u];
     }
-    for (int r = lane; r < a.n_r; r += kWarp) valid[g * per_q + r] = 1;
+    for (int r = lane; r < a.n_r; r += kWarp) valid[g * qs + r] = 1;
     // beacons: the buffer itself when it holds at most n_b rows, else FPS down to n_b
     int* pk;
     bool staged;
     const T* xs = fps_buffer_finish<T, D>(c, a.n_b, npad, scratch, stage_phase++, &pk, &staged);
     if (!staged && lane == 0) status_or(a.status, KVC_STATUS_TIMEOUT);
     const int nb = c < a.n_b ? c : a.n_b;
+    if (a.ext) {
+      if (lane == 0) atomicAdd(&s_nvalid, a.n_r + nb);
+      // the mean over this query head's rows weighs each valid row 1 / (its valid rows)
+      if (mean_w) {
+        const float w = a.n_r + nb > 0 ? 1.f / (float)(a.n_r + nb) : 0.f;
+        for (int r = lane; r < qs && g * qs + r < a.M_pad; r += kWarp)
+          ws.rw[(size_t)head * a.M_pad + g * qs + r] = r < a.n_r + nb ? w : 0.f;
+      }
+      // rows between this query head's last row and the next head's first
+      if (g + 1 < G)
+        for (int e = lane; e < (qs - per_q) * D; e += kWarp) orow[(size_t)per_q * D + e] = from_f32<T>(0.f);
+      for (int r = per_q + lane; r < qs && g + 1 < G; r += kWarp) valid[g * qs + r] = 0;
+    }
     for (int k0 = 0; k0 < a.n_b; k0 += rpi) {
       const int k = k0 + rsel;
       if (k >= a.n_b) continue;
@@ -131,7 +148,7 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
       }
       *reinterpret_cast<uint4*>(dst + i0) = *reinterpret_cast<const uint4*>(o1);
       *reinterpret_cast<uint4*>(dst + i0 + hd) = *reinterpret_cast<const uint4*>(o2);
-      if (i0 == 0) valid[g * per_q + a.n_r + k] = k < nb ? 1 : 0;
+      if (i0 == 0) valid[g * qs + a.n_r + k] = k < nb ? 1 : 0;
     }
     if (a.beacon_picks)
       for (int k = lane; k < a.n_b; k += kWarp) a.beacon_picks[qh * a.n_b + k] = k < nb ? pk[k] : -1;
@@ -140,6 +157,17 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
   // padding rows up to the stored row count
   for (int e = threadIdx.x; e < (a.M_pad - a.M) * D; e += blockDim.x) obs[(size_t)a.M * D + e] = from_f32<T>(0.f);
   for (int r = a.M + threadIdx.x; r < a.M_pad; r += blockDim.x) valid[r] = 0;
+  if (a.ext) {
+    if (mean_w)
+      for (int r = (G - 1) * qs + qs + threadIdx.x; r < a.M_pad; r += blockDim.x) ws.rw[(size_t)head * a.M_pad + r] = 0.f;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      // the scoring kernel adds -sum p log2 p of its rows and keys, times this scale, into entropy
+      const int nv = s_nvalid;
+      ws.escale[head] = (nv > 0 && a.g.N > 1) ? 1.f / ((float)nv * log2f((float)a.g.N)) : 0.f;
+      if (a.entropy) a.entropy[head] = 0.f;
+    }
+  }
 }
 
 struct HeadLoc {
@@ -189,25 +217,63 @@ __global__ void __launch_bounds__(128) pass2_f32_kernel(ScoreArgs a, ScoreWs ws,
   float* Qs = smf;                  // [M_pad][D]
   float* Ks = Qs + a.M_pad * D;     // [kChunk][D+1]
   float* L2s = Ks + kChunk * LK;    // [M_pad]
+  float* RWs = L2s + a.M_pad;       // [M_pad] row weights (extended epilogue, mean over rows)
   const int chunk = blockIdx.x, head = blockIdx.y;
   const HeadLoc hl = head_loc(a.g, head);
   const float* Kh = static_cast<const float*>(a.K.p[hl.l]) + (size_t)hl.bh * a.g.ncap * D;
   const int j0 = chunk * kChunk;
   const int nvalid = min(kChunk, a.g.N - j0);
   const float* obs = static_cast<const float*>(ws.obs) + (size_t)head * a.M_pad * D;
+  const bool mean = a.ext && a.row_agg == KVC_AGG_MEAN;
   for (int e = threadIdx.x; e < a.M_pad * D; e += blockDim.x) Qs[e] = obs[e];
   for (int e = threadIdx.x; e < nvalid * D; e += blockDim.x) Ks[(e / D) * LK + e % D] = Kh[(size_t)j0 * D + e];
-  for (int r = threadIdx.x; r < a.M_pad; r += blockDim.x) L2s[r] = ws.lse2[(size_t)head * a.M_pad + r];
+  for (int r = threadIdx.x; r < a.M_pad; r += blockDim.x) {
+    L2s[r] = ws.lse2[(size_t)head * a.M_pad + r];
+    if (mean) RWs[r] = ws.rw[(size_t)head * a.M_pad + r];
+  }
   __syncthreads();
   const int j = threadIdx.x;
-  if (j >= nvalid) return;
-  float best = -INFINITY;
-  for (int r = 0; r < a.M_pad; ++r) {
-    float dot = 0.f;
-    for (int d = 0; d < D; ++d) dot = fmaf(Qs[r * D + d], Ks[j * LK + d], dot);
-    best = fmaxf(best, dot * c2 - L2s[r]);
+  if (!a.ext) {
+    if (j >= nvalid) return;
+    float best = -INFINITY;
+    for (int r = 0; r < a.M_pad; ++r) {
+      float dot = 0.f;
+      for (int d = 0; d < D; ++d) dot = fmaf(Qs[r * D + d], Ks[j * LK + d], dot);
+      best = fmaxf(best, dot * c2 - L2s[r]);
+    }
+    a.scores[(size_t)head * a.g.N + j0 + j] = exp2f(best);
+    return;
   }
-  a.scores[(size_t)head * a.g.N + j0 + j] = exp2f(best);
+  // Extended epilogue: p = exp2(s*c2 - lse2) per row; the max (or row-weighted sum) over each
+  // query head's rows (rows of head g start at g * qstride), then the max or sum over heads;
+  // -sum p log2 p over rows and keys for the entropy.
+  const bool gsum = a.group_agg == KVC_AGG_SUM;
+  float hacc = 0.f, gacc = 0.f, cv = 0.f;  // values >= 0: 0 is the identity of max and sum
+  int cur = -1;
+  if (j < nvalid) {
+    for (int r = 0; r < a.M_pad; ++r) {
+      float dot = 0.f;
+      for (int d = 0; d < D; ++d) dot = fmaf(Qs[r * D + d], Ks[j * LK + d], dot);
+      const float y = dot * c2 - fminf(L2s[r], 1e30f);  // unused rows: p = 0, p * log2 p = 0
+      const float e = exp2f(y);
+      hacc = fmaf(e, y, hacc);
+      const int sg = r / a.qstride;
+      const float v = mean ? RWs[r] * e : e;
+      if (sg != cur) {
+        if (cur >= 0) gacc = gsum ? gacc + cv : fmaxf(gacc, cv);
+        cur = sg;
+        cv = v;
+      } else {
+        cv = mean ? cv + v : fmaxf(cv, v);
+      }
+    }
+    gacc = gsum ? gacc + cv : fmaxf(gacc, cv);
+    a.scores[(size_t)head * a.g.N + j0 + j] = gacc;
+  }
+  if (a.entropy) {
+    const float h = warp_sum(hacc);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&a.entropy[head], -h * ws.escale[head]);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -241,11 +307,11 @@ int obs_rows(int M, int dtype) {
   return (M + 15) / 16 * 16;
 }
 
-size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, ScoreWs* carve, void* base) {
+size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext, ScoreWs* carve, void* base) {
   const size_t es = dtype == KVC_BF16 ? 2 : 4;
   const size_t heads = (size_t)g.L * g.B * g.Hkv;
   const int G = g.Hq / g.Hkv;
-  const int M = G * (n_r + n_b);
+  const int M = obs_rows_used(G, n_r, n_b, ext);
   const size_t M_pad = (size_t)obs_rows(M, dtype);
   const size_t nchunk = (size_t)(g.N + kChunk - 1) / kChunk;
   size_t off = 0;
@@ -255,12 +321,18 @@ size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, ScoreWs* 
   const size_t part_bytes = dtype == KVC_BF16 ? fused_xch_bytes((int)M_pad) : heads * nchunk * M_pad * sizeof(float2);
   const size_t o_part = off;  off += align256(part_bytes);
   const size_t o_lse = off;   off += align256(heads * M_pad * sizeof(float));
+  const size_t o_rw = off;    off += ext ? align256(heads * M_pad * sizeof(float)) : 0;
+  const size_t o_esc = off;   off += ext ? align256(heads * sizeof(float)) : 0;
+  const size_t o_ent = off;   off += ext ? align256(heads * sizeof(float)) : 0;
   if (carve) {
     char* b = static_cast<char*>(base);
     carve->obs = b + o_obs;
     carve->valid = reinterpret_cast<uint8_t*>(b + o_valid);
     carve->part = reinterpret_cast<float2*>(b + o_part);
     carve->lse2 = reinterpret_cast<float*>(b + o_lse);
+    carve->rw = ext ? reinterpret_cast<float*>(b + o_rw) : nullptr;
+    carve->escale = ext ? reinterpret_cast<float*>(b + o_esc) : nullptr;
+    carve->ent = ext ? reinterpret_cast<float*>(b + o_ent) : nullptr;
   }
   return off;
 }
@@ -312,7 +384,7 @@ int launch_score(const ScoreArgs& a_in, const ScoreWs& ws, cudaStream_t s) {
     return launch_score_fused(a, ws, ws.part, s);
   } else {
     const size_t sm1 = sizeof(float) * ((size_t)a.M_pad * (D + 1) + (size_t)kChunk * D);
-    const size_t sm2 = sizeof(float) * ((size_t)a.M_pad * D + (size_t)kChunk * (D + 1) + a.M_pad);
+    const size_t sm2 = sizeof(float) * ((size_t)a.M_pad * D + (size_t)kChunk * (D + 1) + 2 * (size_t)a.M_pad);
     if (!set_smem(pass1_f32_kernel, sm1) || !set_smem(pass2_f32_kernel, sm2)) return KVC_ERR_LAUNCH;
     pass1_f32_kernel<<<grid, 128, sm1, s>>>(a, ws, c2);
     if (launch_ok()) return KVC_ERR_LAUNCH;

@@ -32,7 +32,8 @@
 
 namespace kvc {
 
-template <int D, int MT, int NACC>
+// kExt: the extended epilogue (aggregation variants and the entropy); otherwise max/max only.
+template <int D, int MT, int NACC, bool kExt>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     score_fused_kernel(const __grid_constant__ FusedMaps maps, ScoreArgs a, ScoreWs ws, FusedPlan p, FusedXch xch,
                        float c2) {
@@ -56,6 +57,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   float* lse2s = reinterpret_cast<float*>(Ks + S * kStage + 512);  // [2][kMaxRows], 16-byte aligned
   float2* merge = reinterpret_cast<float2*>(lse2s + 2 * kMaxRows);   // [kMaxRows]
   float* pbest = reinterpret_cast<float*>(merge + kMaxRows);         // [2][kChunk]
+  float* rws = pbest + 2 * kChunk;                                    // kExt: [2][kMaxRows] row weights
+  float* pext = rws + 2 * kMaxRows;                                   // kExt: [2][5][kChunk] half partials
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -212,11 +215,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       __syncwarp();
       const float2* grp = xch.part + ((size_t)((round & 3) * p.ngroups + group) * p.group_size) * a.M_pad;
       float* dst = lse2s + b * kMaxRows;
+      // unused rows: +inf drops them from a max; the extended epilogue takes a large finite value
+      // instead, so that p = 0 and p * log2 p = 0 there (no inf * 0)
+      const float none = kExt ? 1e30f : INFINITY;
+      const bool mean_w = kExt && a.row_agg == KVC_AGG_MEAN;
       for (int r = lane; r < a.M_pad; r += kWarp) {
         float2 acc2 = make_float2(-INFINITY, 0.f);
         for (int k = 0; k < p.group_size; ++k) acc2 = lse_merge(acc2, grp[(size_t)k * a.M_pad + r]);
         const bool valid = ws.valid[(size_t)head * a.M_pad + r] != 0;
-        dst[r] = (valid && acc2.y > 0.f) ? acc2.x + log2f(acc2.y) : INFINITY;
+        dst[r] = (valid && acc2.y > 0.f) ? acc2.x + log2f(acc2.y) : none;
+        if (mean_w) rws[b * kMaxRows + r] = ws.rw[(size_t)head * a.M_pad + r];
       }
       __syncwarp();
       if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&lfull[b])) : "memory");
@@ -324,6 +332,95 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const uint32_t acc = kc % NACC;
       const int head = group + round * p.ngroups;
       const float* L2 = lse2s + (round & 1) * kMaxRows;
+      if constexpr (kExt) {
+        // Extended epilogue: p = exp2(s*c2 - lse2) per logit; per 16-row half-slice the max
+        // (or the row-weighted sum) of p; the half-slices fold by query head (rows of head g
+        // start at g * qstride, a multiple of 16) into the max or sum over the group. A thread
+        // sees its column half's rows in order, so it keeps its first and last head's partial
+        // apart; the two halves' partials meet in shared memory. -sum p log2 p is summed too.
+        const float* RW = rws + (round & 1) * kMaxRows;
+        const bool mean = a.row_agg == KVC_AGG_MEAN, gsum = a.group_agg == KVC_AGG_SUM;
+        const bool kvalid = c * kChunk + key < a.g.N;
+        int fseg = -1, cur = -1;  // first head (if a later one followed) and current head
+        float fval = 0.f, cv = 0.f, gacc = 0.f, hacc = 0.f;  // values >= 0: 0 is the identity
+        const bool go = have && !*abort_flag && wait_or_abort(&tfull[acc], (kc / NACC) & 1, abort_flag, a.status);
+        if (__all_sync(kFull, go)) {
+          tc::fence_after_sync();
+#pragma unroll 1
+          for (int cs = s_lo; cs < s_hi; ++cs) {
+            uint32_t ra[32];
+            tc::tmem_ld32_async(tmem + acc * kAcc + lane_off + (uint32_t)(cs * 32), ra);
+            tc::tmem_wait();
+            tc::tmem_regs_ready(ra);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int r0 = cs * 32 + hh * 16;
+              if (r0 >= a.M_n) break;  // columns the MMA did not write (M_n is a multiple of 16)
+              float v = 0.f;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float y = fmaf(__uint_as_float(ra[hh * 16 + i]), c2, -L2[r0 + i]);
+                const float e = ex2_approx(y);
+                hacc = fmaf(e, y, hacc);
+                v = mean ? fmaf(RW[r0 + i], e, v) : fmaxf(v, e);
+              }
+              const int sg = r0 / a.qstride;
+              if (sg != cur) {
+                if (cur >= 0) {
+                  if (fseg < 0) {
+                    fseg = cur;
+                    fval = cv;
+                  } else {
+                    gacc = gsum ? gacc + cv : fmaxf(gacc, cv);
+                  }
+                }
+                cur = sg;
+                cv = v;
+              } else {
+                cv = mean ? cv + v : fmaxf(cv, v);
+              }
+            }
+          }
+          tc::fence_before_sync();
+          if (a.entropy) {
+            const float h = warp_sum(kvalid ? hacc : 0.f);
+            if (lane == 0) atomicAdd(&a.entropy[head], -h * ws.escale[head]);
+          }
+        }
+        free_acc(acc);
+        float* px = pext + (kc & 1) * 5 * kChunk;
+        if (hf == 1) {
+          px[key] = __int_as_float(fseg);
+          px[kChunk + key] = fval;
+          px[2 * kChunk + key] = gacc;
+          px[3 * kChunk + key] = __int_as_float(cur);
+          px[4 * kChunk + key] = cv;
+        }
+        epi_bar();
+        if (hf == 0 && !*abort_flag) {
+          const int fsegB = __float_as_int(px[key]), curB = __float_as_int(px[3 * kChunk + key]);
+          const float fvalB = px[kChunk + key], gaccB = px[2 * kChunk + key], cvB = px[4 * kChunk + key];
+          auto gop = [&](float x, float y) { return gsum ? x + y : fmaxf(x, y); };
+          float tot = gacc;
+          if (fseg >= 0) tot = gop(tot, fval);
+          const int bfs = fsegB >= 0 ? fsegB : curB;  // the other half's first head
+          const float bfv = fsegB >= 0 ? fvalB : cvB;
+          if (cur >= 0 && cur == bfs) {
+            tot = gop(tot, mean ? cv + bfv : fmaxf(cv, bfv));
+          } else {
+            if (cur >= 0) tot = gop(tot, cv);
+            if (bfs >= 0) tot = gop(tot, bfv);
+          }
+          if (fsegB >= 0) {
+            tot = gop(tot, gaccB);
+            tot = gop(tot, cvB);
+          }
+          const int j = c * kChunk + key;
+          if (j < a.g.N) a.scores[(size_t)head * a.g.N + j] = tot;
+        }
+        ++kc;
+        return;
+      }
       float best = -INFINITY;
       const bool go = have && !*abort_flag && wait_or_abort(&tfull[acc], (kc / NACC) & 1, abort_flag, a.status);
       if (__all_sync(kFull, go)) {  // tcgen05.ld is warp-collective: decide per warp
@@ -474,7 +571,9 @@ int launch_score_fused(const ScoreArgs& a, const ScoreWs& ws, void* xch_base, cu
   p.chunks_per_cta = (a.nchunk + gs - 1) / gs;
   p.qbytes = a.M_pad * D * 2;
   const int stage_bytes = kChunk * D * 2;
-  const int tail = 1024 + 512 + kMaxRows * 16 + 2 * kChunk * 4 + 256;  // align slack, barriers, lse2 x2, merge, pbest
+  // align slack, barriers, lse2 x2, merge, pbest; with the extended epilogue row weights x2 and
+  // the half partials x2
+  const int tail = 1024 + 512 + kMaxRows * 16 + 2 * kChunk * 4 + 256 + (a.ext ? 2 * kMaxRows * 4 + 10 * kChunk * 4 : 0);
   int stages = (smem_optin - 2 * p.qbytes - tail) / stage_bytes;
   if (stages > 6) stages = 6;
   if (stages < 2) return KVC_ERR_TOO_LARGE;
@@ -492,9 +591,13 @@ int launch_score_fused(const ScoreArgs& a, const ScoreWs& ws, void* xch_base, cu
   if (!fused_maps(&maps, a, ws)) return KVC_ERR_LAUNCH;
   const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
   // four 128-column accumulators when both passes fit in 128 columns, else two of 256
-  void (*kern)(const FusedMaps, ScoreArgs, ScoreWs, FusedPlan, FusedXch, float) =
-      D == 128 ? (a.M_pad > 128 ? score_fused_kernel<128, 2, 2> : score_fused_kernel<128, 1, 4>)
-               : (a.M_pad > 128 ? score_fused_kernel<64, 2, 2> : score_fused_kernel<64, 1, 4>);
+  void (*kern)(const FusedMaps, ScoreArgs, ScoreWs, FusedPlan, FusedXch, float);
+  if (a.ext)
+    kern = D == 128 ? (a.M_pad > 128 ? score_fused_kernel<128, 2, 2, true> : score_fused_kernel<128, 1, 4, true>)
+                    : (a.M_pad > 128 ? score_fused_kernel<64, 2, 2, true> : score_fused_kernel<64, 1, 4, true>);
+  else
+    kern = D == 128 ? (a.M_pad > 128 ? score_fused_kernel<128, 2, 2, false> : score_fused_kernel<128, 1, 4, false>)
+                    : (a.M_pad > 128 ? score_fused_kernel<64, 2, 2, false> : score_fused_kernel<64, 1, 4, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   int per_sm = 0;

@@ -91,7 +91,24 @@ __device__ __forceinline__ void reduce_scatter_max8(float (&w)[8], int lane) {
   }
 }
 
-template <int D>
+// Reduce-scatter like reduce_scatter_max8, with a sum (kSum) or a max.
+template <bool kSum>
+__device__ __forceinline__ void reduce_scatter8(float (&w)[8], int lane) {
+#pragma unroll
+  for (int h = 4, bit = 16; h; h >>= 1, bit >>= 1) {
+    const bool up = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? w[i] : w[i + h];
+      const float keep = up ? w[i + h] : w[i];
+      const float other = __shfl_xor_sync(kFull, send, bit);
+      w[i] = kSum ? keep + other : fmaxf(keep, other);
+    }
+  }
+}
+
+// kExt: the extended epilogue (aggregation variants and the entropy); otherwise max/max only.
+template <int D, bool kExt>
 __global__ void __launch_bounds__(kResThreads, 1)
     score_resident_kernel(const __grid_constant__ FusedMaps maps, ScoreArgs a, ScoreWs ws, FusedPlan p, FusedXch xch,
                           float c2) {
@@ -113,7 +130,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 1);
   float* lse2s = reinterpret_cast<float*>(Ks + S * kStage + 512);  // [2][128]
   float2* merge = reinterpret_cast<float2*>(lse2s + 2 * kResRows);  // [2][128]
-  float* pbest = reinterpret_cast<float*>(merge + 2 * kResRows);    // [2][2 chunks][4][128]
+  float* pbest = reinterpret_cast<float*>(merge + 2 * kResRows);    // [2][2 chunks][4 quarters, or 8 halves][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -380,88 +397,224 @@ __global__ void __launch_bounds__(kResThreads, 1)
       }
       p2_bar();
       const bool have = !*abort_flag;
-      float2 nl[4];  // -lse2 of rows q*32 + lane/4 + 8k, twice (packed operands)
+      if constexpr (kExt) {
+        // ---- extended epilogue: p = exp2(s*c2 - lse2) per logit; per 16-row half of each lane
+        // quarter the max (or the row-weighted sum) over its rows, per key; the halves meet in
+        // shared memory, where one thread per key folds them by query head (rows of head g start
+        // at g * qstride, a multiple of 16) into the max or sum over the group. -sum p log2 p of
+        // the rows and keys is summed on the way for the entropy.
+        const bool mean = a.row_agg == KVC_AGG_MEAN;
+        float2 nl[4];
+        float wr[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float l2 = lse2s[(round & 1) * kResRows + q * 32 + (lane >> 2) + 8 * k];
-        nl[k] = make_float2(-l2, -l2);
-      }
-      const float2 c2v = make_float2(c2, c2);
-      // ---- per key, the max over rows of s*c2 - lse2, from the logits still in TMEM
-      float best[kResChunks][2];
+        for (int k = 0; k < 4; ++k) {
+          const int r = q * 32 + (lane >> 2) + 8 * k;
+          // unused rows: a large finite lse2 makes p = 0 and p * log2 p = 0 (no inf * 0)
+          const float l2 = fminf(lse2s[(round & 1) * kResRows + r], 1e30f);
+          nl[k] = make_float2(-l2, -l2);
+          wr[k] = mean ? ws.rw[(size_t)head * kResRows + r] : 0.f;
+        }
+        const float2 c2v = make_float2(c2, c2);
+        float2 hacc = make_float2(0.f, 0.f);
+        float bestA[kResChunks][2], bestB[kResChunks][2];
 #pragma unroll
-      for (int j = 0; j < kResChunks; ++j) best[j][0] = best[j][1] = -INFINITY;
-      if (__all_sync(kFull, have)) {
-        // lse2 exists only after this CTA's pass 1 published, so the round's MMAs are complete;
-        // waiting on their (completed) phases orders this warp's TMEM reads after them
-        for (int j = 0; j < n; ++j) wait_or_abort(&tfull[(round & 1) * kResChunks + j], (round >> 1) & 1, abort_flag, a.status);
-        tc::fence_after_sync();
+        for (int j = 0; j < kResChunks; ++j) bestA[j][0] = bestA[j][1] = bestB[j][0] = bestB[j][1] = 0.f;
+        if (__all_sync(kFull, have)) {
+          for (int j = 0; j < n; ++j) wait_or_abort(&tfull[(round & 1) * kResChunks + j], (round >> 1) & 1, abort_flag, a.status);
+          tc::fence_after_sync();
 #pragma unroll
-        for (int j = 0; j < kResChunks; ++j) {
-          if (j >= n) break;
-          const uint32_t acc = (uint32_t)((round & 1) * kResChunks + j);
-          const uint32_t base = tmem + acc * kChunk + lane_off + (uint32_t)(hf * 64);
-          uint32_t ra[2][16], rb[2][16];  // [block] x rows (t/4, t/4+8) and (t/4+16, t/4+24)
+          for (int j = 0; j < kResChunks; ++j) {
+            if (j >= n) break;
+            const uint32_t acc = (uint32_t)((round & 1) * kResChunks + j);
+            const uint32_t base = tmem + acc * kChunk + lane_off + (uint32_t)(hf * 64);
+            const int key0 = (c0 + j) * kChunk + hf * 64 + 2 * (lane & 3);
+            const bool ragged = (c0 + j + 1) * kChunk > a.g.N;
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb) {
-            tc::tmem_ld16x256_x4_async(base + (uint32_t)(cb * 32), ra[cb]);
-            tc::tmem_ld16x256_x4_async(base + (16u << 16) + (uint32_t)(cb * 32), rb[cb]);
-          }
-          tc::tmem_wait();
+            for (int cb = 0; cb < 2; ++cb) {
+              uint32_t ra[16], rb[16];  // rows (t/4, t/4+8) and (t/4+16, t/4+24) of 32 columns
+              tc::tmem_ld16x256_x4_async(base + (uint32_t)(cb * 32), ra);
+              tc::tmem_ld16x256_x4_async(base + (16u << 16) + (uint32_t)(cb * 32), rb);
+              tc::tmem_wait();
+              tc::tmem_regs_ready(ra);
+              tc::tmem_regs_ready(rb);
+              if (cb == 1) {  // the accumulator is free once its last values are in registers
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&tempty[acc])) : "memory");
+              }
+              float wA[8], wB[8];  // slot 2i + cc: column 8i + 2*(lane%4) + cc; A rows k0,k1, B rows k2,k3
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb) {
-            tc::tmem_regs_ready(ra[cb]);
-            tc::tmem_regs_ready(rb[cb]);
-          }
-          tc::fence_before_sync();
-          __syncwarp();
-          if (lane == 0)  // the accumulator is free as soon as its values are in registers
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&tempty[acc])) : "memory");
+              for (int i = 0; i < 4; ++i) {
+                float2 y[4], e[4];
+                y[0] = __ffma2_rn(make_float2(__uint_as_float(ra[4 * i]), __uint_as_float(ra[4 * i + 1])), c2v, nl[0]);
+                y[1] = __ffma2_rn(make_float2(__uint_as_float(ra[4 * i + 2]), __uint_as_float(ra[4 * i + 3])), c2v, nl[1]);
+                y[2] = __ffma2_rn(make_float2(__uint_as_float(rb[4 * i]), __uint_as_float(rb[4 * i + 1])), c2v, nl[2]);
+                y[3] = __ffma2_rn(make_float2(__uint_as_float(rb[4 * i + 2]), __uint_as_float(rb[4 * i + 3])), c2v, nl[3]);
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb) {
-            // a row without observations has lse2 = +inf, so its terms are -inf and drop out of the max
-            // slot 2i + cc: column 8i + 2*(lane%4) + cc of the block, max over 4 rows; the two
-            // columns of a pair share each row's lse2, so s*c2 - lse2 is one packed FMA per row
-            float w[8];
+                for (int k = 0; k < 4; ++k) e[k] = make_float2(ex2_approx(y[k].x), ex2_approx(y[k].y));
+                if (a.entropy) {
+                  if (ragged) {  // keys past N (zero-filled loads) take no part
+                    const int kk = key0 + cb * 32 + 8 * i;
+                    const float2 m = make_float2(kk < a.g.N ? 1.f : 0.f, kk + 1 < a.g.N ? 1.f : 0.f);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(ra[cb][4 * i]), __uint_as_float(ra[cb][4 * i + 1])),
-                                           c2v, nl[0]);
-              const float2 x1 = __ffma2_rn(
-                  make_float2(__uint_as_float(ra[cb][4 * i + 2]), __uint_as_float(ra[cb][4 * i + 3])), c2v, nl[1]);
-              const float2 x2 = __ffma2_rn(make_float2(__uint_as_float(rb[cb][4 * i]), __uint_as_float(rb[cb][4 * i + 1])),
-                                           c2v, nl[2]);
-              const float2 x3 = __ffma2_rn(
-                  make_float2(__uint_as_float(rb[cb][4 * i + 2]), __uint_as_float(rb[cb][4 * i + 3])), c2v, nl[3]);
-              w[2 * i] = fmaxf(max3f(x0.x, x1.x, x2.x), x3.x);
-              w[2 * i + 1] = fmaxf(max3f(x0.y, x1.y, x2.y), x3.y);
+                    for (int k = 0; k < 4; ++k) hacc = __ffma2_rn(__fmul2_rn(e[k], m), y[k], hacc);
+                  } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) hacc = __ffma2_rn(e[k], y[k], hacc);
+                  }
+                }
+                if (mean) {
+                  wA[2 * i] = fmaf(wr[1], e[1].x, wr[0] * e[0].x);
+                  wA[2 * i + 1] = fmaf(wr[1], e[1].y, wr[0] * e[0].y);
+                  wB[2 * i] = fmaf(wr[3], e[3].x, wr[2] * e[2].x);
+                  wB[2 * i + 1] = fmaf(wr[3], e[3].y, wr[2] * e[2].y);
+                } else {
+                  wA[2 * i] = fmaxf(e[0].x, e[1].x);
+                  wA[2 * i + 1] = fmaxf(e[0].y, e[1].y);
+                  wB[2 * i] = fmaxf(e[2].x, e[3].x);
+                  wB[2 * i + 1] = fmaxf(e[2].y, e[3].y);
+                }
+              }
+              if (mean) {
+                reduce_scatter8<true>(wA, lane);
+                reduce_scatter8<true>(wB, lane);
+              } else {
+                reduce_scatter8<false>(wA, lane);
+                reduce_scatter8<false>(wB, lane);
+              }
+              bestA[j][cb] = wA[0];
+              bestB[j][cb] = wB[0];
             }
-            reduce_scatter_max8(w, lane);
-            best[j][cb] = w[0];
           }
+        } else {
+          __syncwarp();
+          if (lane == 0)
+            for (int j = 0; j < n; ++j)
+              asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(
+                               tc::smem_u32(&tempty[(round & 1) * kResChunks + j]))
+                           : "memory");
+        }
+        if (a.entropy) {
+          const float h = warp_sum(hacc.x + hacc.y);
+          if (lane == 0 && !*abort_flag) atomicAdd(&a.entropy[head], -h * ws.escale[head]);
+        }
+        // pbest[buffer][chunk][half h = 2 * quarter + (0: rows +0..15, 1: rows +16..31)][column]
+        float* pb = pbest + (round & 1) * (kResChunks * 8 * kChunk);
+#pragma unroll
+        for (int j = 0; j < kResChunks; ++j)
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb) {
+            pb[(j * 8 + 2 * q) * kChunk + hf * 64 + cb * 32 + col_in] = bestA[j][cb];
+            pb[(j * 8 + 2 * q + 1) * kChunk + hf * 64 + cb * 32 + col_in] = bestB[j][cb];
+          }
+        p2_bar();
+        const int j = gt >> 7, col = gt & (kChunk - 1);  // 256 threads: one key each
+        if (j < n && !*abort_flag) {
+          const float* pj = pb + j * 8 * kChunk;
+          const bool gsum = a.group_agg == KVC_AGG_SUM;
+          float gacc = 0.f, cur = 0.f;  // every value is >= 0: 0 is the identity of max and sum
+          int cs = -1;
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            const int sg = (16 * h) / a.qstride;
+            const float v = pj[h * kChunk + col];
+            if (sg != cs) {
+              if (cs >= 0) gacc = gsum ? gacc + cur : fmaxf(gacc, cur);
+              cs = sg;
+              cur = v;
+            } else {
+              cur = mean ? cur + v : fmaxf(cur, v);
+            }
+          }
+          gacc = gsum ? gacc + cur : fmaxf(gacc, cur);
+          const int key = (c0 + j) * kChunk + col;
+          if (key < a.g.N) a.scores[(size_t)head * a.g.N + key] = gacc;
         }
       } else {
-        __syncwarp();
-        if (lane == 0)
-          for (int j = 0; j < n; ++j)
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(
-                             tc::smem_u32(&tempty[(round & 1) * kResChunks + j]))
-                         : "memory");
-      }
-      // pbest[buffer][chunk][quarter][column]; buffer = round parity (the group's barriers of
-      // round r + 1 lie between two uses)
-      float* pb = pbest + (round & 1) * (kResChunks * 4 * kChunk);
+        float2 nl[4];  // -lse2 of rows q*32 + lane/4 + 8k, twice (packed operands)
 #pragma unroll
-      for (int j = 0; j < kResChunks; ++j)
+        for (int k = 0; k < 4; ++k) {
+          const float l2 = lse2s[(round & 1) * kResRows + q * 32 + (lane >> 2) + 8 * k];
+          nl[k] = make_float2(-l2, -l2);
+        }
+        const float2 c2v = make_float2(c2, c2);
+        // ---- per key, the max over rows of s*c2 - lse2, from the logits still in TMEM
+        float best[kResChunks][2];
 #pragma unroll
-        for (int cb = 0; cb < 2; ++cb) pb[(j * 4 + q) * kChunk + hf * 64 + cb * 32 + col_in] = best[j][cb];
-      p2_bar();
-      const int j = gt >> 7, col = gt & (kChunk - 1);  // 256 threads: one key each
-      if (j < n && !*abort_flag) {
-        const float* pj = pb + j * 4 * kChunk;
-        const float m = fmaxf(fmaxf(pj[col], pj[kChunk + col]), fmaxf(pj[2 * kChunk + col], pj[3 * kChunk + col]));
-        const int key = (c0 + j) * kChunk + col;
-        if (key < a.g.N) a.scores[(size_t)head * a.g.N + key] = exp2f(m);
+        for (int j = 0; j < kResChunks; ++j) best[j][0] = best[j][1] = -INFINITY;
+        if (__all_sync(kFull, have)) {
+          // lse2 exists only after this CTA's pass 1 published, so the round's MMAs are complete;
+          // waiting on their (completed) phases orders this warp's TMEM reads after them
+          for (int j = 0; j < n; ++j) wait_or_abort(&tfull[(round & 1) * kResChunks + j], (round >> 1) & 1, abort_flag, a.status);
+          tc::fence_after_sync();
+#pragma unroll
+          for (int j = 0; j < kResChunks; ++j) {
+            if (j >= n) break;
+            const uint32_t acc = (uint32_t)((round & 1) * kResChunks + j);
+            const uint32_t base = tmem + acc * kChunk + lane_off + (uint32_t)(hf * 64);
+            uint32_t ra[2][16], rb[2][16];  // [block] x rows (t/4, t/4+8) and (t/4+16, t/4+24)
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+              tc::tmem_ld16x256_x4_async(base + (uint32_t)(cb * 32), ra[cb]);
+              tc::tmem_ld16x256_x4_async(base + (16u << 16) + (uint32_t)(cb * 32), rb[cb]);
+            }
+            tc::tmem_wait();
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+              tc::tmem_regs_ready(ra[cb]);
+              tc::tmem_regs_ready(rb[cb]);
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0)  // the accumulator is free as soon as its values are in registers
+              asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(&tempty[acc])) : "memory");
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+              // a row without observations has lse2 = +inf, so its terms are -inf and drop out of the max
+              // slot 2i + cc: column 8i + 2*(lane%4) + cc of the block, max over 4 rows; the two
+              // columns of a pair share each row's lse2, so s*c2 - lse2 is one packed FMA per row
+              float w[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(ra[cb][4 * i]), __uint_as_float(ra[cb][4 * i + 1])),
+                                             c2v, nl[0]);
+                const float2 x1 = __ffma2_rn(
+                    make_float2(__uint_as_float(ra[cb][4 * i + 2]), __uint_as_float(ra[cb][4 * i + 3])), c2v, nl[1]);
+                const float2 x2 = __ffma2_rn(make_float2(__uint_as_float(rb[cb][4 * i]), __uint_as_float(rb[cb][4 * i + 1])),
+                                             c2v, nl[2]);
+                const float2 x3 = __ffma2_rn(
+                    make_float2(__uint_as_float(rb[cb][4 * i + 2]), __uint_as_float(rb[cb][4 * i + 3])), c2v, nl[3]);
+                w[2 * i] = fmaxf(max3f(x0.x, x1.x, x2.x), x3.x);
+                w[2 * i + 1] = fmaxf(max3f(x0.y, x1.y, x2.y), x3.y);
+              }
+              reduce_scatter_max8(w, lane);
+              best[j][cb] = w[0];
+            }
+          }
+        } else {
+          __syncwarp();
+          if (lane == 0)
+            for (int j = 0; j < n; ++j)
+              asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(
+                               tc::smem_u32(&tempty[(round & 1) * kResChunks + j]))
+                           : "memory");
+        }
+        // pbest[buffer][chunk][quarter][column]; buffer = round parity (the group's barriers of
+        // round r + 1 lie between two uses)
+        float* pb = pbest + (round & 1) * (kResChunks * 4 * kChunk);
+#pragma unroll
+        for (int j = 0; j < kResChunks; ++j)
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb) pb[(j * 4 + q) * kChunk + hf * 64 + cb * 32 + col_in] = best[j][cb];
+        p2_bar();
+        const int j = gt >> 7, col = gt & (kChunk - 1);  // 256 threads: one key each
+        if (j < n && !*abort_flag) {
+          const float* pj = pb + j * 4 * kChunk;
+          const float m = fmaxf(fmaxf(pj[col], pj[kChunk + col]), fmaxf(pj[2 * kChunk + col], pj[3 * kChunk + col]));
+          const int key = (c0 + j) * kChunk + col;
+          if (key < a.g.N) a.scores[(size_t)head * a.g.N + key] = exp2f(m);
+        }
       }
     };
 
@@ -480,7 +633,9 @@ __global__ void __launch_bounds__(kResThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 // Shared memory: align slack, barriers, lse2 x2, merge x2, pbest x2; then the Q tile(s) and the ring.
-static int resident_tail_bytes() { return 1024 + 512 + 2 * kResRows * 4 + 2 * kResRows * 8 + 2 * kResChunks * 4 * kChunk * 4; }
+static int resident_tail_bytes(bool ext) {
+  return 1024 + 512 + 2 * kResRows * 4 + 2 * kResRows * 8 + 2 * kResChunks * (ext ? 8 : 4) * kChunk * 4;
+}
 
 bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem) {
   if (a.dtype != KVC_BF16 || a.M_pad != kResRows) return false;
@@ -499,11 +654,11 @@ bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem) {
   if (p->ngroups > heads) p->ngroups = heads;
   p->qbytes = kResRows * D * 2;
   const int stage_bytes = kChunk * D * 2;
-  int stages = (smem_optin - resident_tail_bytes() - kQBuf * p->qbytes) / stage_bytes;
+  int stages = (smem_optin - resident_tail_bytes(a.ext != 0) - kQBuf * p->qbytes) / stage_bytes;
   if (stages > 6) stages = 6;
   if (stages < 2) return false;
   p->stages = stages;
-  *smem = (size_t)resident_tail_bytes() + kQBuf * (size_t)p->qbytes + (size_t)stages * stage_bytes;
+  *smem = (size_t)resident_tail_bytes(a.ext != 0) + kQBuf * (size_t)p->qbytes + (size_t)stages * stage_bytes;
   return true;
 }
 
@@ -519,7 +674,8 @@ int launch_score_resident(const ScoreArgs& a, const ScoreWs& ws, const FusedPlan
   if (!fused_maps(&maps, a, ws)) return KVC_ERR_LAUNCH;
   const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
   void (*kern)(const FusedMaps, ScoreArgs, ScoreWs, FusedPlan, FusedXch, float) =
-      D == 128 ? score_resident_kernel<128> : score_resident_kernel<64>;
+      a.ext ? (D == 128 ? score_resident_kernel<128, true> : score_resident_kernel<64, true>)
+            : (D == 128 ? score_resident_kernel<128, false> : score_resident_kernel<64, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   int per_sm = 0;

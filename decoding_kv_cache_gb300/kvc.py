@@ -21,7 +21,13 @@ KVC_MAX_LAYERS = 128
 
 EXPORTED = ("kvc_fps_update", "kvc_score_workspace_size", "kvc_score", "kvc_select", "kvc_compact",
             "kvc_evict_workspace_size", "kvc_evict", "kvc_evict_launch_count", "kvc_strerror", "kvc_abi_version",
-            "kvc_score_static", "kvc_debug_fault")
+            "kvc_score_static", "kvc_debug_fault", "kvc_head_budget")
+KVC_ABI_VERSION = 2
+KVC_AGG_MAX, KVC_AGG_MEAN, KVC_AGG_SUM = 0, 1, 2
+KVC_BUDGET_GIVEN, KVC_BUDGET_ENTROPY = 0, 1
+ROW_AGG = {"max": KVC_AGG_MAX, "mean": KVC_AGG_MEAN}
+GROUP_AGG = {"max": KVC_AGG_MAX, "sum": KVC_AGG_SUM}
+HEAD_BUDGET = {"given": KVC_BUDGET_GIVEN, "entropy": KVC_BUDGET_ENTROPY}
 KVC_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -35,6 +41,11 @@ class kvc_cache(C.Structure):
     _fields_ = [("dtype", C.c_int32), ("L", C.c_int32), ("B", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32),
                 ("D", C.c_int32), ("N", C.c_int32), ("pad_", C.c_int32), ("ncap", C.c_int64),
                 ("K", C.POINTER(C.c_void_p)), ("V", C.POINTER(C.c_void_p))]
+
+
+class kvc_opts(C.Structure):
+    _fields_ = [("row_agg", C.c_int32), ("group_agg", C.c_int32), ("head_budget", C.c_int32),
+                ("reserved", C.c_int32), ("entropy", C.c_void_p)]
 
 
 _lib = None
@@ -51,17 +62,19 @@ def lib():
     L = C.CDLL(LIB_PATH)
     vp, i32, i64, dbl, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_double, C.c_size_t
     pc = C.POINTER(kvc_cache)
+    po = C.POINTER(kvc_opts)
     sig = {
         "kvc_fps_update": (C.c_int, [i32, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp]),
         "kvc_score_workspace_size": (sz, [pc, i32, i32]),
-        "kvc_score": (C.c_int, [pc, vp, i32, vp, vp, i32, i32, i64, dbl, vp, vp, vp, sz, vp]),
+        "kvc_score": (C.c_int, [pc, vp, i32, vp, vp, i32, i32, i64, dbl, vp, vp, po, vp, sz, vp]),
         "kvc_select": (C.c_int, [vp, i32, i32, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp]),
         "kvc_compact": (C.c_int, [pc, vp, vp, vp, vp]),
         "kvc_evict_workspace_size": (sz, [pc, i32, i32]),
-        "kvc_evict": (C.c_int, [pc, vp, i32, vp, vp, i32, i32, i64, dbl, i32, i32, vp, i32, vp, vp, vp, vp, vp, sz,
-                                vp]),
+        "kvc_evict": (C.c_int, [pc, vp, i32, vp, vp, i32, i32, i64, dbl, i32, i32, vp, i32, vp, vp, vp, vp, po, vp,
+                                sz, vp]),
         "kvc_evict_launch_count": (C.c_int, [pc, i32, i32]),
-        "kvc_score_static": (C.c_int, [pc, vp, i32, vp, vp, i32, i32, i64, dbl, vp, vp, vp]),
+        "kvc_score_static": (C.c_int, [pc, vp, i32, vp, vp, i32, i32, i64, dbl, vp, vp, po, vp]),
+        "kvc_head_budget": (C.c_int, [vp, i32, i32, i32, i32, i32, i32, vp, i32, vp, vp, vp]),
         "kvc_strerror": (C.c_char_p, [C.c_int]),
         "kvc_abi_version": (C.c_int, []),
         "kvc_debug_fault": (C.c_int, [i32]),
@@ -159,6 +172,19 @@ def kvc_debug_fault(mode: int) -> None:
     _check(lib().kvc_debug_fault(int(mode)))
 
 
+def make_opts(row_agg: str = "max", group_agg: str = "max", head_budget: str = "given",
+              entropy: Optional[torch.Tensor] = None):
+    """A ``kvc_opts`` (see kvc.h), or None for the defaults (max/max, budgets as given, no entropy)."""
+    if row_agg == "max" and group_agg == "max" and head_budget == "given" and entropy is None:
+        return None
+    return kvc_opts(row_agg=ROW_AGG[row_agg], group_agg=GROUP_AGG[group_agg], head_budget=HEAD_BUDGET[head_budget],
+                    reserved=0, entropy=_p(entropy))
+
+
+def _opts_ref(o):
+    return None if o is None else C.byref(o)
+
+
 def _workspace(nbytes: int, device, workspace):
     if workspace is not None:
         return workspace
@@ -167,21 +193,27 @@ def _workspace(nbytes: int, device, workspace):
 
 def kvc_score(cache: Cache, q_recent: torch.Tensor, qbuf: torch.Tensor, count: torch.Tensor, n_b: int, t: int,
               rope_theta: float, scores: torch.Tensor, beacon_picks: Optional[torch.Tensor] = None,
-              workspace: Optional[torch.Tensor] = None, stream=None):
+              workspace: Optional[torch.Tensor] = None, stream=None, row_agg: str = "max", group_agg: str = "max",
+              entropy: Optional[torch.Tensor] = None):
+    """Scores of every cached key; ``row_agg``/``group_agg``/``entropy`` select the variants of kvc_opts."""
     n_r, qmax = q_recent.shape[-2], qbuf.shape[-2]
     ws = _workspace(kvc_score_workspace_size(cache, n_r, n_b), scores.device, workspace)
+    o = make_opts(row_agg, group_agg, "given", entropy)
     _check(lib().kvc_score(cache.ref, _p(q_recent), n_r, _p(qbuf), _p(count), qmax, n_b, int(t), float(rope_theta),
-                           _p(scores), _p(beacon_picks), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+                           _p(scores), _p(beacon_picks), _opts_ref(o), _p(ws), ws.numel() * ws.element_size(),
+                           _stream(stream)))
 
 
 def kvc_score_static(cache: Cache, q_recent: torch.Tensor, qbuf: torch.Tensor, count: torch.Tensor, n_b: int,
                      t: int, rope_theta: float, scores: torch.Tensor, beacon_picks: Optional[torch.Tensor] = None,
-                     stream=None):
+                     stream=None, row_agg: str = "max", group_agg: str = "max",
+                     entropy: Optional[torch.Tensor] = None):
     """kvc_score with the library's fixed scratch region instead of a workspace (allocates nothing;
     see kvc.h for the size limit and the sharing rules)."""
     n_r, qmax = q_recent.shape[-2], qbuf.shape[-2]
+    o = make_opts(row_agg, group_agg, "given", entropy)
     _check(lib().kvc_score_static(cache.ref, _p(q_recent), n_r, _p(qbuf), _p(count), qmax, n_b, int(t),
-                                  float(rope_theta), _p(scores), _p(beacon_picks), _stream(stream)))
+                                  float(rope_theta), _p(scores), _p(beacon_picks), _opts_ref(o), _stream(stream)))
 
 
 def kvc_select(scores: torch.Tensor, prefix: int, recent: int, kept_idx: torch.Tensor, kept_len: torch.Tensor,
@@ -201,10 +233,22 @@ def kvc_evict(cache: Cache, q_recent: torch.Tensor, qbuf: torch.Tensor, count: t
               rope_theta: float, prefix: int, recent: int, kept_len: torch.Tensor,
               budget: Optional[torch.Tensor] = None, budget_all: int = 0, kept_idx: Optional[torch.Tensor] = None,
               scores: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-              workspace: Optional[torch.Tensor] = None, stream=None):
-    """The whole eviction step (beacons, scores, selection, in-place compaction) on one stream."""
+              workspace: Optional[torch.Tensor] = None, stream=None, row_agg: str = "max", group_agg: str = "max",
+              head_budget: str = "given", entropy: Optional[torch.Tensor] = None):
+    """The whole eviction step (beacons, scores, selection, in-place compaction) on one stream.
+    ``row_agg``/``group_agg``/``head_budget``/``entropy`` select the variants of kvc_opts."""
     n_r, qmax = q_recent.shape[-2], qbuf.shape[-2]
     ws = _workspace(kvc_evict_workspace_size(cache, n_r, n_b), kept_len.device, workspace)
+    o = make_opts(row_agg, group_agg, head_budget, entropy)
     _check(lib().kvc_evict(cache.ref, _p(q_recent), n_r, _p(qbuf), _p(count), qmax, n_b, int(t), float(rope_theta),
                            prefix, recent, _p(budget), int(budget_all), _p(kept_idx), _p(kept_len), _p(scores),
-                           _p(status), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+                           _p(status), _opts_ref(o), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def kvc_head_budget(entropy: torch.Tensor, N: int, prefix: int, recent: int, budget_out: torch.Tensor,
+                    budget: Optional[torch.Tensor] = None, budget_all: int = 0, status: Optional[torch.Tensor] = None,
+                    stream=None):
+    """Each (layer, sequence)'s budgets reallocated over its heads by entropy (see kvc.h)."""
+    L, B, Hkv = entropy.shape
+    _check(lib().kvc_head_budget(_p(entropy), L, B, Hkv, int(N), int(prefix), int(recent), _p(budget),
+                                 int(budget_all), _p(budget_out), _p(status), _stream(stream)))

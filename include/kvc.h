@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 1
+#define KVC_ABI_VERSION 2
 #define KVC_MAX_LAYERS 128
 
 #if defined(__GNUC__)
@@ -70,6 +70,42 @@ enum {
 #define KVC_STATUS_COUNT_RANGE 0x2u  /* a query-buffer count < 0 or > qmax: head left alone */
 #define KVC_STATUS_BAD_INDEX 0x4u    /* kvc_compact: kept list not strictly increasing in [k, N) */
 #define KVC_STATUS_TIMEOUT 0x8u      /* a bounded device-side wait gave up; that work was skipped */
+
+/*
+ * Scoring and budget options (kvc_score, kvc_score_static, kvc_evict). A NULL
+ * options pointer, or one that is all zero, selects the default step: max over
+ * rows, max over the GQA group, budgets as given, no entropy output.
+ *
+ * Aggregation (BeaconKV write-up, "实验": the ablation of max against mean
+ * aggregation of the observation queries' weights). With p_rj the softmax
+ * weight of observation row r on key j, and the rows of query head g:
+ *   A_g(j) = max_r p_rj             row_agg KVC_AGG_MAX
+ *          = (1/M_g) sum_r p_rj     row_agg KVC_AGG_MEAN (M_g = g's valid rows)
+ *   score_j = max_g A_g(j)          group_agg KVC_AGG_MAX
+ *           = sum_g A_g(j)          group_agg KVC_AGG_SUM
+ * Query heads without rows (no recent queries, empty buffer) take no part.
+ *
+ * Entropy (ReasonAlloc note, "Key Concepts": head utility from normalised
+ * attention entropy): entropy[l,b,h] = mean over the KV head's valid rows of
+ * H_r / ln N, H_r = -sum_j p_rj ln p_rj, in [0, 1]; 0 when N = 1.
+ *
+ * Head budgets (ReasonAlloc note, "Core Mechanism": budget moves from low- to
+ * high-utility heads within a layer, the layer total fixed), kvc_evict only:
+ * with KVC_BUDGET_ENTROPY each (layer, sequence)'s budgets are replaced by
+ * kvc_head_budget's reallocation of their total by the heads' entropies.
+ */
+#define KVC_AGG_MAX 0
+#define KVC_AGG_MEAN 1 /* row_agg only */
+#define KVC_AGG_SUM 2  /* group_agg only */
+#define KVC_BUDGET_GIVEN 0
+#define KVC_BUDGET_ENTROPY 1
+typedef struct {
+  int32_t row_agg;     /* KVC_AGG_MAX or KVC_AGG_MEAN */
+  int32_t group_agg;   /* KVC_AGG_MAX or KVC_AGG_SUM */
+  int32_t head_budget; /* KVC_BUDGET_GIVEN or KVC_BUDGET_ENTROPY (kvc_evict only) */
+  int32_t reserved;    /* must be 0 */
+  float* entropy;      /* [L,B,Hkv] fp32 (device, out) or NULL */
+} kvc_opts;
 
 /* One KV cache: every layer's K and V. */
 typedef struct {
@@ -135,13 +171,18 @@ KVC_API int kvc_fps_update(int32_t dtype, int32_t L, int32_t B, int32_t Hq, int3
  *   scores       [L,B,Hkv,N] fp32 (device, out)
  *   beacon_picks [L,B,Hq,n_b] int32 (device, out, may be NULL): buffer rows used
  *                as beacons, ascending, -1 padded
+ *   opts         NULL or the aggregation variant / entropy output (see kvc_opts;
+ *                head_budget must be KVC_BUDGET_GIVEN here). A variant other than
+ *                max/max, or an entropy output, stores each query head's rows from
+ *                a 16-row boundary; G * that stride must stay within 256 rows
+ *                (else KVC_ERR_TOO_LARGE).
  *   workspace    device scratch of at least kvc_score_workspace_size() bytes,
  *                256-byte aligned; contents on entry do not matter
  */
 KVC_API size_t kvc_score_workspace_size(const kvc_cache* c, int32_t n_r, int32_t n_b);
 KVC_API int kvc_score(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf, const int32_t* count,
               int32_t qmax, int32_t n_b, int64_t t, double rope_theta, float* scores, int32_t* beacon_picks,
-              void* workspace, size_t ws_bytes, void* stream);
+              const kvc_opts* opts, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * kvc_select -- which tokens each head keeps.
@@ -189,13 +230,16 @@ KVC_API int kvc_compact(const kvc_cache* c, const int32_t* kept_idx, const int32
  *   scores       [L,B,Hkv,N] fp32 (device, out) or NULL
  *   kept_idx     [L,B,Hkv,N] int32 (device, out) or NULL
  *   kept_len     [L,B,Hkv] int32 (device, out), required
+ *   opts         NULL or options (see kvc_opts); with KVC_BUDGET_ENTROPY the budgets
+ *                (budget or budget_all) are each layer's preallocation, reallocated
+ *                over its heads as kvc_head_budget does before selection
  *   workspace    at least kvc_evict_workspace_size() bytes, 256-byte aligned
  */
 KVC_API size_t kvc_evict_workspace_size(const kvc_cache* c, int32_t n_r, int32_t n_b);
 KVC_API int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf, const int32_t* count,
               int32_t qmax, int32_t n_b, int64_t t, double rope_theta, int32_t prefix, int32_t recent,
               const int32_t* budget, int32_t budget_all, int32_t* kept_idx, int32_t* kept_len, float* scores,
-              int32_t* status, void* workspace, size_t ws_bytes, void* stream);
+              int32_t* status, const kvc_opts* opts, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * kvc_score_static -- kvc_score for callers that cannot allocate device memory.
@@ -222,7 +266,33 @@ KVC_API int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, con
 #define KVC_STATIC_SCRATCH_BYTES (16u << 20)
 KVC_API int kvc_score_static(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf,
                              const int32_t* count, int32_t qmax, int32_t n_b, int64_t t, double rope_theta,
-                             float* scores, int32_t* beacon_picks, void* stream);
+                             float* scores, int32_t* beacon_picks, const kvc_opts* opts, void* stream);
+
+/*
+ * kvc_head_budget -- online head-wise budgets from attention entropy.
+ * ReasonAlloc note, "Core Mechanism": each layer's preallocated budget is moved
+ * from low-utility to high-utility heads, the layer total held fixed; "Key
+ * Concepts": utility from normalised attention entropy, low entropy gets more.
+ * The note states no formula; per (layer, sequence) with H = Hkv heads:
+ *   T = sum_h min(given_h, N); f = prefix + recent; cap = N - f;
+ *   u_h = 1 - entropy_h clipped to [0, 1];
+ *   the E = T - H f slots above the floors are shared in proportion to u
+ *   (equally if every remaining u is 0); a share above cap is cut to cap and
+ *   the rest shared again among the other heads (water-filling);
+ *   integer shares by largest remainder, ties to the lower head;
+ *   budget_out_h = f + share_h.
+ * fp64, every operation rounded on its own, heads in order. If N <= f or
+ * T >= H N, budget_out_h = min(given_h, N). A given_h < f sets
+ * KVC_STATUS_BUDGET_RANGE and that (layer, sequence) keeps its given budgets.
+ *
+ *   entropy      [L,B,Hkv] fp32 (device), e.g. kvc_opts.entropy of kvc_score
+ *   budget       [L,B,Hkv] int32 (device) or NULL to use budget_all for all heads
+ *   budget_out   [L,B,Hkv] int32 (device, out); may alias budget
+ *   status       device int32 or NULL
+ */
+KVC_API int kvc_head_budget(const float* entropy, int32_t L, int32_t B, int32_t Hkv, int32_t N, int32_t prefix,
+                            int32_t recent, const int32_t* budget, int32_t budget_all, int32_t* budget_out,
+                            int32_t* status, void* stream);
 
 /* Number of kernels one kvc_evict call with these arguments launches (host only;
  * for accounting, e.g. counting launches inside a timed region). */

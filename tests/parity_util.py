@@ -1,6 +1,7 @@
 """Helpers for comparing the CUDA path (through the C ABI) with the CPU oracle.
 
-Tolerances: scores |gpu - oracle| <= 1e-3 * |oracle| + 1e-30; kept sets identical except
+Tolerances: scores |gpu - oracle| <= 1e-3 * |oracle| + 1e-30 (every aggregation variant);
+normalised entropy |gpu - oracle| <= 1e-4 absolute; kept sets identical except
 where both swapped indices' oracle scores lie within 1e-5 (relative) of the oracle's
 threshold score; FPS picks identical except at distance near-ties within 1e-5; compacted
 K/V bit-exact against a gather with the GPU's own kept indices.
@@ -16,38 +17,48 @@ SCORE_RTOL = 1e-3
 SCORE_FLOOR = 1e-30
 TIE_RTOL = 1e-5
 FPS_TOL = 1e-5
+# The entropy is a mean over rows of -sum p log2 p / log2 N, a number in [0, 1]. The kernels
+# take p from exp2 of fp32 logits (relative error ~1e-6 in s and lse2 against fp64, ~2^-22 in
+# exp2) and sum ~1e5 to 1e7 terms in fp32 per head; 1e-4 absolute covers both with margin.
+ENTROPY_ATOL = 1e-4
 
 
 def storage_to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().double().numpy()
 
 
-def run_evict(inp, dev, with_scores=True):
-    """kvc_evict on a device copy of ``inp``; returns numpy results and the compacted cache."""
+def run_evict(inp, dev, with_scores=True, row_agg="max", group_agg="max", head_budget="given", entropy=False):
+    """kvc_evict on a device copy of ``inp``; returns numpy results and the compacted cache.
+    ``entropy=True`` also returns the per-head normalised entropy output."""
     from decoding_kv_cache_gb300 import kvc
     g = inp.to(dev)
     cache = kvc.Cache(g.K, g.V, g.Hq)
     kept_len = torch.full((g.L, g.B, g.Hkv), -7, dtype=torch.int32, device=dev)
     kept_idx = torch.full((g.L, g.B, g.Hkv, g.N), -7, dtype=torch.int32, device=dev)
     scores = torch.full((g.L, g.B, g.Hkv, g.N), -1.0, dtype=torch.float32, device=dev) if with_scores else None
+    ent = torch.full((g.L, g.B, g.Hkv), -1.0, dtype=torch.float32, device=dev) if entropy else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     kvc.kvc_evict(cache, g.q_recent, g.qbuf, g.count, g.n_b, g.t, g.theta, g.prefix, g.recent, kept_len,
-                  budget=g.budget, budget_all=g.budget_all, kept_idx=kept_idx, scores=scores, status=status)
+                  budget=g.budget, budget_all=g.budget_all, kept_idx=kept_idx, scores=scores, status=status,
+                  row_agg=row_agg, group_agg=group_agg, head_budget=head_budget, entropy=ent)
     torch.cuda.synchronize()
     return dict(kept_len=kept_len.cpu().numpy(), kept_idx=kept_idx.cpu().numpy(),
                 scores=None if scores is None else scores.cpu().numpy(), status=int(status.item()),
-                K=g.K.cpu(), V=g.V.cpu())
+                K=g.K.cpu(), V=g.V.cpu(), entropy=None if ent is None else ent.cpu().numpy())
 
 
-def run_score(inp, dev):
+def run_score(inp, dev, row_agg="max", group_agg="max", entropy=False):
     from decoding_kv_cache_gb300 import kvc
     g = inp.to(dev)
     cache = kvc.Cache(g.K, g.V, g.Hq)
     scores = torch.full((g.L, g.B, g.Hkv, g.N), -1.0, dtype=torch.float32, device=dev)
     picks = torch.full((g.L, g.B, g.Hq, max(g.n_b, 1)), -7, dtype=torch.int32, device=dev)[..., :g.n_b].contiguous()
+    ent = torch.full((g.L, g.B, g.Hkv), -1.0, dtype=torch.float32, device=dev) if entropy else None
     kvc.kvc_score(cache, g.q_recent, g.qbuf, g.count, g.n_b, g.t, g.theta, scores,
-                  beacon_picks=picks if g.n_b else None)
+                  beacon_picks=picks if g.n_b else None, row_agg=row_agg, group_agg=group_agg, entropy=ent)
     torch.cuda.synchronize()
+    if entropy:
+        return scores.cpu().numpy(), picks.cpu().numpy(), ent.cpu().numpy()
     return scores.cpu().numpy(), picks.cpu().numpy()
 
 
@@ -81,11 +92,11 @@ def check_beacon_picks(inp, gpu_picks: np.ndarray, ora_picks: np.ndarray):
     return differ
 
 
-def check_kept(inp, gpu, ora, gpu_scores):
+def check_kept(inp, gpu, ora, gpu_scores, budgets=None):
     """Kept lists: invariants against the GPU's own scores (exact) and agreement with the oracle
-    up to near-ties."""
+    up to near-ties. ``budgets`` [L,B,Hkv] overrides the input's (reallocated budgets)."""
     N, P, R = inp.N, inp.prefix, inp.recent
-    budgets = inp.budgets().cpu().numpy()
+    budgets = inp.budgets().cpu().numpy() if budgets is None else budgets
     L, B, Hkv = inp.L, inp.B, inp.Hkv
     for l in range(L):
         for b in range(B):

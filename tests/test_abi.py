@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
     exported = set(re.findall(r"\bT (kvc_\w+)", out))
     assert set(_declared()) <= exported
     assert set(kvc.EXPORTED) == set(_declared())
-    assert lib.kvc_abi_version() == 1
+    assert lib.kvc_abi_version() == kvc.KVC_ABI_VERSION == 2
 
 
 def test_header_compiles_as_c():
@@ -88,7 +88,7 @@ def test_evict_rejects_bad_cache_before_launch(lib, kw, code):
     from decoding_kv_cache_gb300 import kvc
     c, _keep = _cache(kvc, **kw)
     rc = lib.kvc_evict(C.byref(c), 0x1000, 16, 0x1000, 0x1000, 32, 16, 1023, 1e6, 4, 16, None, 896, None, 0x1000,
-                       None, None, 0x100000, 1 << 40, None)
+                       None, None, None, 0x100000, 1 << 40, None)
     assert rc == code
 
 
@@ -98,7 +98,7 @@ def test_evict_rejects_bad_query_and_budget_args(lib):
     call = lambda **kw: lib.kvc_evict(
         C.byref(c), kw.get("qr", 0x1000), kw.get("n_r", 16), 0x1000, 0x1000, kw.get("qmax", 32), kw.get("n_b", 16),
         1023, kw.get("theta", 1e6), 4, 16, None, kw.get("budget_all", 896), None, kw.get("kept_len", 0x1000), None,
-        None, kw.get("ws", 0x100000), kw.get("wsb", 1 << 40), None)
+        None, kw.get("opts"), kw.get("ws", 0x100000), kw.get("wsb", 1 << 40), None)
     assert call(n_b=40) == -1                 # more beacons than the buffer holds
     assert call(qmax=65, n_b=16) == -1         # buffer larger than supported
     assert call(n_r=0, n_b=0) == -1            # no observation rows
@@ -109,6 +109,32 @@ def test_evict_rejects_bad_query_and_budget_args(lib):
     assert call(ws=0x100010) == -7             # workspace not 256-byte aligned
     assert call(qr=0x1004) == -8               # misaligned query pointer
     assert call(n_r=64, n_b=32, qmax=64) == -9  # 4 * 96 observation rows > 256
+    o = lambda **kw: C.byref(kvc.kvc_opts(**{**dict(row_agg=0, group_agg=0, head_budget=0, reserved=0), **kw}))
+    assert call(opts=o(row_agg=2)) == -1        # sum is not a row aggregation
+    assert call(opts=o(group_agg=1)) == -1      # nor mean a group aggregation
+    assert call(opts=o(head_budget=2)) == -1
+    assert call(opts=o(reserved=1)) == -1
+    assert call(opts=o(entropy=0x1002)) == -8   # entropy output not 4-byte aligned
+    assert call(opts=o(head_budget=1, entropy=0x1004), wsb=16) == -7  # options fine: reaches the workspace check
+
+
+def test_variant_row_layout_limit(lib):
+    """The variants start each query head's rows on a 16-row boundary: 3 heads of 81 rows fit the
+    256-row tile (243) but not once padded (96 + 96 + 81 = 273)."""
+    from decoding_kv_cache_gb300 import kvc
+    c, _keep = _cache(kvc, Hq=6)
+    call = lambda opts: lib.kvc_evict(C.byref(c), 0x1000, 64, 0x1000, 0x1000, 18, 17, 1023, 1e6, 4, 16, None, 896,
+                                      None, 0x1000, None, None, opts, 0x100000, 16, None)
+    assert call(None) == -7  # accepted up to the (too small) workspace
+    o = kvc.kvc_opts(row_agg=1, group_agg=0, head_budget=0, reserved=0, entropy=None)
+    assert call(C.byref(o)) == -9
+    assert lib.kvc_score_workspace_size(C.byref(c), 64, 17) > 0
+
+
+def test_head_budget_rejects_bad_args(lib):
+    assert lib.kvc_head_budget(None, 1, 1, 4, 100, 4, 16, None, 60, 0x1000, None, None) == -1
+    assert lib.kvc_head_budget(0x1000, 1, 1, 65, 100, 4, 16, None, 60, 0x1000, None, None) == -9
+    assert lib.kvc_head_budget(0x1000, 1, 1, 4, 100, 4, 16, None, 19, 0x1000, None, None) == -4
 
 
 def test_select_and_fps_reject_bad_args(lib):
