@@ -2,6 +2,7 @@
 """Benchmark of the eviction step (one kvc_evict over the whole cache) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+                    [--row-agg max|mean] [--group-agg max|sum] [--head-budget given|entropy] [--entropy]
 
 Prints ONE JSON line. A step is one pass of the whole hot path (beacons, scores, selection,
 in-place compaction) over every (layer, sequence, KV head) of the workload. Inputs are
@@ -148,10 +149,25 @@ def recorded_traffic(config: str, phase: str):
 # the GPU arm
 # ---------------------------------------------------------------------------
 
-def workload_desc(inp):
+def variant_of(args) -> str:
+    """'' for the default step, else e.g. 'mean,sum' / 'max,max+entropy' / 'max,max+entropy-budgets'."""
+    v = f"{args.row_agg},{args.group_agg}"
+    if args.head_budget == "entropy":
+        v += "+entropy-budgets"
+    elif args.entropy:
+        v += "+entropy"
+    return "" if v == "max,max" else v
+
+
+def workload_desc(inp, variant=""):
     keep = "per-head budgets" if inp.budget is not None else f"{inp.budget_all}"
-    return (f"{inp.name} eviction step: L{inp.L} B{inp.B} Hq{inp.Hq} Hkv{inp.Hkv} D{inp.D} {inp.dtype} "
-            f"N{inp.N}->{keep}, obs {inp.n_r} recent + {inp.n_b} beacons (buffer {inp.qmax})")
+    d = (f"{inp.name} eviction step: L{inp.L} B{inp.B} Hq{inp.Hq} Hkv{inp.Hkv} D{inp.D} {inp.dtype} "
+         f"N{inp.N}->{keep}, obs {inp.n_r} recent + {inp.n_b} beacons (buffer {inp.qmax})")
+    if variant:
+        d += (f"; aggregation {variant.split('+')[0]} (rows, GQA group)" +
+              ("; budgets reallocated per layer by attention entropy" if "budgets" in variant else "") +
+              ("; entropy output" if variant.endswith("+entropy") else ""))
+    return d
 
 
 def algorithmic_bytes(inp, kept_idx, kept_len):
@@ -195,10 +211,15 @@ def gpu_arm(args, rank, world, local_rank):
         inp.V.copy_(V0)
         flush.zero_()
 
+    variant = variant_of(args)
+    ent = torch.zeros(shape, dtype=torch.float32, device=dev) if (args.entropy or args.head_budget == "entropy") \
+        else None
+    vkw = dict(row_agg=args.row_agg, group_agg=args.group_agg)
+
     def evict():
         kvc.kvc_evict(cache, inp.q_recent, inp.qbuf, inp.count, inp.n_b, inp.t, inp.theta, inp.prefix, inp.recent,
                       kept_len, budget=inp.budget, budget_all=inp.budget_all, kept_idx=kept_idx, scores=None,
-                      status=status, workspace=ws)
+                      status=status, workspace=ws, head_budget=args.head_budget, entropy=ent, **vkw)
 
     for _ in range(args.warmup):
         reset()
@@ -236,15 +257,20 @@ def gpu_arm(args, rank, world, local_rank):
     phase_ms = {"kvc_score": 0.0, "kvc_select": 0.0, "kvc_compact": 0.0}
     nph = max(3, min(args.steps, 50))
     sc_ws = torch.empty(kvc.kvc_score_workspace_size(cache, inp.n_r, inp.n_b), dtype=torch.uint8, device=dev)
+    hb_out = torch.zeros(shape, dtype=torch.int32, device=dev)
     evs = []
     for i in range(nph):
         reset()
         e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         e[0].record(stream)
-        kvc.kvc_score(cache, inp.q_recent, inp.qbuf, inp.count, inp.n_b, inp.t, inp.theta, scores, workspace=sc_ws)
+        kvc.kvc_score(cache, inp.q_recent, inp.qbuf, inp.count, inp.n_b, inp.t, inp.theta, scores, workspace=sc_ws,
+                      entropy=ent, **vkw)
         e[1].record(stream)
-        kvc.kvc_select(scores, inp.prefix, inp.recent, kept_idx, kept_len, budget=inp.budget,
-                       budget_all=inp.budget_all)
+        if args.head_budget == "entropy":  # the reallocation runs inside the selection kernel in kvc_evict
+            kvc.kvc_head_budget(ent, inp.N, inp.prefix, inp.recent, hb_out, budget=inp.budget,
+                                budget_all=inp.budget_all)
+        kvc.kvc_select(scores, inp.prefix, inp.recent, kept_idx, kept_len,
+                       budget=hb_out if args.head_budget == "entropy" else inp.budget, budget_all=inp.budget_all)
         e[2].record(stream)
         kvc.kvc_compact(cache, kept_idx, kept_len, status=status)
         e[3].record(stream)
@@ -291,7 +317,7 @@ def gpu_arm(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": inp.dtype, "data": "synthetic",
-        "config": {"workload": workload_desc(inp), "l2": "flushed between steps (512 MB write), cache restored "
+        "config": {"workload": workload_desc(inp, variant), "l2": "flushed between steps (512 MB write), cache restored "
                    "from a pristine copy between steps; both untimed", "parallelism": f"replicas x{world}",
                    "timing": "CUDA events around each kvc_evict on the launch stream"},
         "head_tokens_per_s": world * inp.heads * inp.N * args.steps / (total_ms / 1e3),
@@ -299,7 +325,8 @@ def gpu_arm(args, rank, world, local_rank):
         "algorithmic_bytes_per_step": {"k_read": k_read, "kv_moved": moved_bytes, "moved_tokens": moved},
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_source": pk_kind,
-                     "traffic": None if args.layers else recorded_traffic(args.config, dom)},
+                     "traffic": None if args.layers else recorded_traffic(args.config + (f"/{variant}" if variant
+                                                                                          else ""), dom)},
         "phases_ms": phase_ms,
         "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -313,8 +340,9 @@ def gpu_arm(args, rank, world, local_rank):
 # CPU oracle (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(config: str, budget_s: float = 12.0):
-    """Time the oracle, as it stands, on a bounded sample of the workload's heads.
+def oracle_sample(config: str, budget_s: float = 12.0, **variant):
+    """Time the oracle, as it stands, on a bounded sample of the workload's heads (``variant``:
+    the oracle's row_agg / group_agg / head_budget keywords).
     Returns (tokens/s scaled to the full step, cores, sample description, seconds)."""
     from decoding_kv_cache_gb300.inputs import make_inputs
     from oracle import oracle as O
@@ -325,7 +353,7 @@ def oracle_sample(config: str, budget_s: float = 12.0):
     # one layer of one sequence first, to size the sample
     probe = make_inputs(config, L=1, B=1)
     t0 = time.perf_counter()
-    O.evict(probe)
+    O.evict(probe, **variant)
     dt = time.perf_counter() - t0
     per_head = dt / probe.heads
     want_heads = max(probe.heads, min(heads_full, int(budget_s / max(per_head, 1e-9))))
@@ -333,7 +361,7 @@ def oracle_sample(config: str, budget_s: float = 12.0):
     B = spec["B"] if L > 1 else max(1, min(spec["B"], want_heads // spec["Hkv"]))
     samp = make_inputs(config, L=L, B=B)
     t0 = time.perf_counter()
-    O.evict(samp)
+    O.evict(samp, **variant)
     dt = time.perf_counter() - t0
     full_s = dt * heads_full / samp.heads
     tok = spec["B"] * spec["N"] / full_s
@@ -342,14 +370,19 @@ def oracle_sample(config: str, budget_s: float = 12.0):
     return tok, cores, desc, dt
 
 
+def oracle_variant(args):
+    return dict(row_agg=args.row_agg, group_agg=args.group_agg, head_budget=args.head_budget)
+
+
 def reference_arm(args, rank, world):
     if rank != 0:
         return None
     vals, descs = [], []
     if args.warmup > 0:
-        oracle_sample(args.config, budget_s=2.0)
+        oracle_sample(args.config, budget_s=2.0, **oracle_variant(args))
     for _ in range(args.steps):
-        tok, cores, desc, _ = oracle_sample(args.config, budget_s=min(12.0, 120.0 / max(args.steps, 1)))
+        tok, cores, desc, _ = oracle_sample(args.config, budget_s=min(12.0, 120.0 / max(args.steps, 1)),
+                                            **oracle_variant(args))
         vals.append(tok)
         descs.append(desc)
     value = statistics.mean(vals)
@@ -359,7 +392,8 @@ def reference_arm(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": spec["B"] * spec["N"] / value * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.config}, "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores,
+            "config": {"workload": args.config + (f" ({variant_of(args)})" if variant_of(args) else "")},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores,
                                                                  "kind": "oracle", "sample": descs[-1]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -374,6 +408,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run the workload with only this many layers (0 = all)")
+    ap.add_argument("--row-agg", default="max", choices=["max", "mean"],
+                    help="aggregation over a query head's observation rows")
+    ap.add_argument("--group-agg", default="max", choices=["max", "sum"],
+                    help="aggregation over the query heads of a KV head")
+    ap.add_argument("--head-budget", default="given", choices=["given", "entropy"],
+                    help="entropy: reallocate each layer's budget over its heads by attention entropy")
+    ap.add_argument("--entropy", action="store_true", help="also output each head's attention entropy")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -393,7 +434,7 @@ def main():
     res, _ = gpu_arm(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            tok, cores, desc, _ = oracle_sample(args.config)
+            tok, cores, desc, _ = oracle_sample(args.config, **oracle_variant(args))
             res["cpu_baseline"] = {"value": tok, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -149,7 +149,7 @@ struct FusedPlan {
   int qbytes;          // one observation tile: M_pad * D * 2
 };
 bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem);
-long long score_resident_words(const FusedPlan& p);
+long long score_resident_words(const FusedPlan& p, bool entropy);
 int launch_score_resident(const ScoreArgs& a, const ScoreWs& ws, const FusedPlan& p, size_t smem, cudaStream_t s);
 
 // entropy non-null: each (layer, sequence)'s budgets are reallocated over its Hkv heads first

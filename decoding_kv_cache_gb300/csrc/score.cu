@@ -318,7 +318,9 @@ size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext,
   const size_t o_obs = off;   off += align256(heads * M_pad * g.D * es);
   const size_t o_valid = off; off += align256(heads * M_pad);
   // fp32 caches keep per-chunk partials; bf16 caches exchange per-range partials in the fused kernel
-  const size_t part_bytes = dtype == KVC_BF16 ? fused_xch_bytes((int)M_pad) : heads * nchunk * M_pad * sizeof(float2);
+  // (twice that with the extended options: the single-read kernel then also publishes each row's mean logit)
+  const size_t part_bytes = dtype == KVC_BF16 ? fused_xch_bytes((int)M_pad) * (ext ? 2 : 1)
+                                              : heads * nchunk * M_pad * sizeof(float2);
   const size_t o_part = off;  off += align256(part_bytes);
   const size_t o_lse = off;   off += align256(heads * M_pad * sizeof(float));
   const size_t o_rw = off;    off += ext ? align256(heads * M_pad * sizeof(float)) : 0;
@@ -350,7 +352,7 @@ int launch_score(const ScoreArgs& a_in, const ScoreWs& ws, cudaStream_t s) {
   size_t rsmem = 0;
   const bool resident = a.dtype == KVC_BF16 && score_resident_plan(a, &rp, &rsmem);
   a.xch_zero = resident ? reinterpret_cast<unsigned long long*>(ws.part) : nullptr;
-  a.xch_zero_words = resident ? score_resident_words(rp) : 0;
+  a.xch_zero_words = resident ? score_resident_words(rp, a.entropy != nullptr) : 0;
   const int D = a.g.D;
   const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
   // observation rows: one warp per query head of the group

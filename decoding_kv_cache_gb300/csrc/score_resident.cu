@@ -107,8 +107,9 @@ __device__ __forceinline__ void reduce_scatter8(float (&w)[8], int lane) {
   }
 }
 
-// kExt: the extended epilogue (aggregation variants and the entropy); otherwise max/max only.
-template <int D, bool kExt>
+// kExt: the extended epilogue (the aggregation variants); otherwise max/max. kEnt: the rows'
+// attention entropy is accumulated too (pass 1 keeps each row's mean logit; pass 2 merges).
+template <int D, bool kExt, bool kEnt>
 __global__ void __launch_bounds__(kResThreads, 1)
     score_resident_kernel(const __grid_constant__ FusedMaps maps, ScoreArgs a, ScoreWs ws, FusedPlan p, FusedXch xch,
                           float c2) {
@@ -130,7 +131,8 @@ __global__ void __launch_bounds__(kResThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 1);
   float* lse2s = reinterpret_cast<float*>(Ks + S * kStage + 512);  // [2][128]
   float2* merge = reinterpret_cast<float2*>(lse2s + 2 * kResRows);  // [2][128]
-  float* pbest = reinterpret_cast<float*>(merge + 2 * kResRows);    // [2][2 chunks][4 quarters, or 8 halves][128]
+  float* mtau = reinterpret_cast<float*>(merge + 2 * kResRows);     // [2][128] (kEnt)
+  float* pbest = mtau + 2 * kResRows;                                // [2][2 chunks][4 quarters, or 8 halves][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -263,14 +265,19 @@ __global__ void __launch_bounds__(kResThreads, 1)
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     uint64_t* words = reinterpret_cast<uint64_t*>(xch.part);
+    // with kEnt a second set of words (the rows' mean logits) follows the first
+    const size_t words_per_set = (size_t)4 * p.ngroups * p.group_size * kResRows;
     // after the pass-2 reduce-scatter a lane holds slot (lane >> 2) & 7 of each 32-column block
     const int slot8 = (lane >> 2) & 7;
     const int col_in = 8 * (slot8 >> 1) + 2 * (lane & 3) + (slot8 & 1);
 
     // pass 1 of a round: fold this thread's row over its column half of every chunk into the
-    // running (max, sum of exp2); the accumulators stay allocated for pass 2
+    // running (max, sum of exp2); the accumulators stay allocated for pass 2. With kEnt also
+    // tau = sum of exp2(x - max) * (x - max), x = s*c2, which gives the row's mean logit under
+    // this CTA's softmax (for the entropy) without a second exponential.
     auto pass1 = [&](int round) {
       float2 st = make_float2(-INFINITY, 0.f);
+      float tau = 0.f;
       for (int j = 0; j < n; ++j) {
         const uint32_t acc = (uint32_t)((round & 1) * kResChunks + j);
         const int c = c0 + j;
@@ -289,44 +296,66 @@ __global__ void __launch_bounds__(kResThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v0[i] = __uint_as_float(r0[i]);
           if (nvalid < kChunk) {  // ragged last chunk only
+            if (kEnt && cbase >= nvalid) continue;
+            // with kEnt a finite stand-in, so that exp2 gives 0 and 0 * x stays 0
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (cbase + i >= nvalid) v0[i] = -INFINITY;
+              if (cbase + i >= nvalid) v0[i] = kEnt ? -3.0e38f : -INFINITY;
           }
           const float mraw = tree_max32_3(v0);  // c2 > 0: scale the max once
           if (mraw > -INFINITY) {
             const float mn = fmaxf(st.x, mraw * c2);
             // s*c2 - mn two lanes at a time (packed fp32 FMA), exp2 on the MUFU, packed sum tree
             const float2 c2v = make_float2(c2, c2), nmv = make_float2(-mn, -mn);
-            float2 sum2[8];
+            float2 sum2[8], t2[2];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float2 x = __ffma2_rn(make_float2(v0[2 * i], v0[2 * i + 1]), c2v, nmv);
               const float2 e2 = make_float2(ex2_approx(x.x), ex2_approx(x.y));
               sum2[i & 7] = i < 8 ? e2 : __fadd2_rn(sum2[i & 7], e2);
+              if constexpr (kEnt) t2[i & 1] = i < 2 ? __fmul2_rn(e2, x) : __ffma2_rn(e2, x, t2[i & 1]);
             }
 #pragma unroll
             for (int w = 4; w; w >>= 1)
 #pragma unroll
               for (int i = 0; i < w; ++i) sum2[i] = __fadd2_rn(sum2[i], sum2[i + w]);
-            st = make_float2(mn, st.y * ex2_approx(st.x - mn) + (sum2[0].x + sum2[0].y));
+            const float alpha = ex2_approx(st.x - mn);
+            if constexpr (kEnt) {
+              const float tb = (t2[0].x + t2[0].y) + (t2[1].x + t2[1].y);
+              tau = (st.y > 0.f ? alpha * fmaf(st.x - mn, st.y, tau) : 0.f) + tb;
+            }
+            st = make_float2(mn, st.y * alpha + (sum2[0].x + sum2[0].y));
           }
         }
       }
       // The two warps of a lane quarter merge their column halves; the hf == 0 warp publishes
-      // the row's log2-sum-exp2 over this CTA's keys as one tagged word (no fence). merge is
-      // double-buffered by round parity: the pair passes round r + 1's barrier before hf == 1
-      // writes the buffer of round r again.
+      // the row's log2-sum-exp2 over this CTA's keys as one tagged word (no fence), and with
+      // kEnt the row's mean logit in a second one. merge is double-buffered by round parity:
+      // the pair passes round r + 1's barrier before hf == 1 writes the buffer of round r again.
       float2* mg = merge + (round & 1) * kResRows;
-      if (hf == 1) mg[row] = st;
+      float* mt = mtau + (round & 1) * kResRows;
+      if (hf == 1) {
+        mg[row] = st;
+        if constexpr (kEnt) mt[row] = tau;
+      }
       asm volatile("bar.sync %0, 64;\n" ::"r"(2 + q) : "memory");
       // test-only fault (kvc_debug_fault 1): the first CTA never publishes, so its group's
       // bounded exchange waits run out
       if (hf == 0 && !(a.debug_fault == 1 && blockIdx.x == 0)) {
-        const float2 m = lse_merge(st, mg[row]);
+        const float2 o = mg[row];
+        const float2 m = lse_merge(st, o);
         const float part = m.y > 0.f ? m.x + log2f(m.y) : -INFINITY;
-        st_relaxed_u64(words + ((size_t)((round & 3) * p.ngroups + group) * p.group_size + rank) * kResRows + row,
-                       ((uint64_t)((uint32_t)round + 1u) << 32) | __float_as_uint(part));
+        const size_t widx = ((size_t)((round & 3) * p.ngroups + group) * p.group_size + rank) * kResRows + row;
+        const uint64_t tag = (uint64_t)((uint32_t)round + 1u) << 32;
+        st_relaxed_u64(words + widx, tag | __float_as_uint(part));
+        if constexpr (kEnt) {
+          // both halves' tau relative to the merged max, then mean logit = max + tau / sum
+          float tt = 0.f;
+          if (st.y > 0.f) tt += exp2f(st.x - m.x) * fmaf(st.x - m.x, st.y, tau);
+          if (o.y > 0.f) tt += exp2f(o.x - m.x) * fmaf(o.x - m.x, o.y, mt[row]);
+          const float mu = m.y > 0.f ? m.x + tt / m.y : 0.f;
+          st_relaxed_u64(words + words_per_set + widx, tag | __float_as_uint(mu));
+        }
       }
     };
 
@@ -340,6 +369,13 @@ __global__ void __launch_bounds__(kResThreads, 1)
       const int gt = e * 32 + lane;  // 0..255
       const int xrow = gt >> 1, xpar = gt & 1;
       const bool xvalid = ws.valid[(size_t)head * kResRows + xrow] != 0;
+      // extended epilogue: the weights of this thread's rows in a mean, fetched before the exchange
+      float wr[4];
+      if constexpr (kExt) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          wr[k] = a.row_agg == KVC_AGG_MEAN ? ws.rw[(size_t)head * kResRows + q * 32 + (lane >> 2) + 8 * k] : 0.f;
+      }
       // Slot round % 4 last held round - 4. A partner overwrites it (round + 4) only after its
       // pass 1 of round + 4, which needs its TMEM buffer back from its pass 2 of round + 2, which
       // follows the whole group's partials of round + 2, which this CTA publishes only after its
@@ -392,8 +428,31 @@ __global__ void __launch_bounds__(kResThreads, 1)
       {
         const float om = __shfl_xor_sync(kFull, mx, 1), os = __shfl_xor_sync(kFull, sm, 1);
         const float2 m2 = lse_merge(make_float2(mx, sm), make_float2(om, os));
-        if (xpar == 0)
-          lse2s[(round & 1) * kResRows + xrow] = (xvalid && m2.y > 0.f) ? m2.x + log2f(m2.y) : INFINITY;
+        const float l2 = (xvalid && m2.y > 0.f) ? m2.x + log2f(m2.y) : INFINITY;
+        if (xpar == 0) lse2s[(round & 1) * kResRows + xrow] = l2;
+        if constexpr (kEnt) {
+          // Entropy in bits of a row: lse2 - sum_j p_j x_j, and sum_j p_j x_j = sum over the group's
+          // CTAs of exp2(part - lse2) * (that CTA's mean logit). This CTA adds its term for each
+          // valid row (the group's first CTA adds lse2 too), from its own two published words.
+          float d = 0.f;
+          if (xpar == 0 && xvalid && ok && l2 < INFINITY) {
+            const size_t widx = ((size_t)((round & 3) * p.ngroups + group) * p.group_size + rank) * kResRows + xrow;
+            uint64_t wp = ld_relaxed_u64(words + widx), wm = ld_relaxed_u64(words + words_per_set + widx);
+            for (uint32_t it = 0; ((uint32_t)(wp >> 32) != tag || (uint32_t)(wm >> 32) != tag) && it < (1u << 20); ++it) {
+              __nanosleep(32);
+              wp = ld_relaxed_u64(words + widx);
+              wm = ld_relaxed_u64(words + words_per_set + widx);
+            }
+            if ((uint32_t)(wp >> 32) == tag && (uint32_t)(wm >> 32) == tag) {
+              d = (rank == 0 ? l2 : 0.f) - exp2f(__uint_as_float((uint32_t)wp) - l2) * __uint_as_float((uint32_t)wm);
+            } else if (!*abort_flag) {
+              *abort_flag = 1;
+              status_or(a.status, KVC_STATUS_TIMEOUT);
+            }
+          }
+          d = warp_sum(d);
+          if (lane == 0 && d != 0.f && !*abort_flag) atomicAdd(&a.entropy[head], d * ws.escale[head]);
+        }
       }
       p2_bar();
       const bool have = !*abort_flag;
@@ -401,21 +460,16 @@ __global__ void __launch_bounds__(kResThreads, 1)
         // ---- extended epilogue: p = exp2(s*c2 - lse2) per logit; per 16-row half of each lane
         // quarter the max (or the row-weighted sum) over its rows, per key; the halves meet in
         // shared memory, where one thread per key folds them by query head (rows of head g start
-        // at g * qstride, a multiple of 16) into the max or sum over the group. -sum p log2 p of
-        // the rows and keys is summed on the way for the entropy.
+        // at g * qstride, a multiple of 16) into the max or sum over the group.
         const bool mean = a.row_agg == KVC_AGG_MEAN;
         float2 nl[4];
-        float wr[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int r = q * 32 + (lane >> 2) + 8 * k;
-          // unused rows: a large finite lse2 makes p = 0 and p * log2 p = 0 (no inf * 0)
-          const float l2 = fminf(lse2s[(round & 1) * kResRows + r], 1e30f);
+          const float l2 = lse2s[(round & 1) * kResRows + r];  // unused rows: +inf, so p = 0
           nl[k] = make_float2(-l2, -l2);
-          wr[k] = mean ? ws.rw[(size_t)head * kResRows + r] : 0.f;
         }
         const float2 c2v = make_float2(c2, c2);
-        float2 hacc = make_float2(0.f, 0.f);
         float bestA[kResChunks][2], bestB[kResChunks][2];
 #pragma unroll
         for (int j = 0; j < kResChunks; ++j) bestA[j][0] = bestA[j][1] = bestB[j][0] = bestB[j][1] = 0.f;
@@ -427,8 +481,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
             if (j >= n) break;
             const uint32_t acc = (uint32_t)((round & 1) * kResChunks + j);
             const uint32_t base = tmem + acc * kChunk + lane_off + (uint32_t)(hf * 64);
-            const int key0 = (c0 + j) * kChunk + hf * 64 + 2 * (lane & 3);
-            const bool ragged = (c0 + j + 1) * kChunk > a.g.N;
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
               uint32_t ra[16], rb[16];  // rows (t/4, t/4+8) and (t/4+16, t/4+24) of 32 columns
@@ -453,17 +505,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 y[3] = __ffma2_rn(make_float2(__uint_as_float(rb[4 * i + 2]), __uint_as_float(rb[4 * i + 3])), c2v, nl[3]);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) e[k] = make_float2(ex2_approx(y[k].x), ex2_approx(y[k].y));
-                if (a.entropy) {
-                  if (ragged) {  // keys past N (zero-filled loads) take no part
-                    const int kk = key0 + cb * 32 + 8 * i;
-                    const float2 m = make_float2(kk < a.g.N ? 1.f : 0.f, kk + 1 < a.g.N ? 1.f : 0.f);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) hacc = __ffma2_rn(__fmul2_rn(e[k], m), y[k], hacc);
-                  } else {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) hacc = __ffma2_rn(e[k], y[k], hacc);
-                  }
-                }
                 if (mean) {
                   wA[2 * i] = fmaf(wr[1], e[1].x, wr[0] * e[0].x);
                   wA[2 * i + 1] = fmaf(wr[1], e[1].y, wr[0] * e[0].y);
@@ -494,10 +535,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
               asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(
                                tc::smem_u32(&tempty[(round & 1) * kResChunks + j]))
                            : "memory");
-        }
-        if (a.entropy) {
-          const float h = warp_sum(hacc.x + hacc.y);
-          if (lane == 0 && !*abort_flag) atomicAdd(&a.entropy[head], -h * ws.escale[head]);
         }
         // pbest[buffer][chunk][half h = 2 * quarter + (0: rows +0..15, 1: rows +16..31)][column]
         float* pb = pbest + (round & 1) * (kResChunks * 8 * kChunk);
@@ -632,9 +669,9 @@ __global__ void __launch_bounds__(kResThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// Shared memory: align slack, barriers, lse2 x2, merge x2, pbest x2; then the Q tile(s) and the ring.
+// Shared memory: align slack, barriers, lse2 x2, merge x2, tau x2, pbest x2; then the Q tile(s) and the ring.
 static int resident_tail_bytes(bool ext) {
-  return 1024 + 512 + 2 * kResRows * 4 + 2 * kResRows * 8 + 2 * kResChunks * (ext ? 8 : 4) * kChunk * 4;
+  return 1024 + 512 + 2 * kResRows * 4 + 2 * kResRows * 8 + 2 * kResRows * 4 + 2 * kResChunks * (ext ? 8 : 4) * kChunk * 4;
 }
 
 bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem) {
@@ -662,8 +699,11 @@ bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem) {
   return true;
 }
 
-// tagged partial words [4][ngroups][group_size][128]; zero, so no tag of an earlier launch matches
-long long score_resident_words(const FusedPlan& p) { return 4LL * p.ngroups * p.group_size * kResRows; }
+// tagged partial words [4][ngroups][group_size][128], and as many again for the rows' mean
+// logits when the entropy is wanted; zero, so no tag of an earlier launch matches
+long long score_resident_words(const FusedPlan& p, bool entropy) {
+  return (entropy ? 2LL : 1LL) * 4LL * p.ngroups * p.group_size * kResRows;
+}
 
 int launch_score_resident(const ScoreArgs& a, const ScoreWs& ws, const FusedPlan& p, size_t smem, cudaStream_t s) {
   const int D = a.g.D;
@@ -673,9 +713,15 @@ int launch_score_resident(const ScoreArgs& a, const ScoreWs& ws, const FusedPlan
   FusedMaps maps;
   if (!fused_maps(&maps, a, ws)) return KVC_ERR_LAUNCH;
   const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
-  void (*kern)(const FusedMaps, ScoreArgs, ScoreWs, FusedPlan, FusedXch, float) =
-      a.ext ? (D == 128 ? score_resident_kernel<128, true> : score_resident_kernel<64, true>)
-            : (D == 128 ? score_resident_kernel<128, false> : score_resident_kernel<64, false>);
+  using Kern = void (*)(const FusedMaps, ScoreArgs, ScoreWs, FusedPlan, FusedXch, float);
+  // [D == 128][extended epilogue][entropy]
+  static const Kern table[2][2][2] = {
+      {{score_resident_kernel<64, false, false>, score_resident_kernel<64, false, true>},
+       {score_resident_kernel<64, true, false>, score_resident_kernel<64, true, true>}},
+      {{score_resident_kernel<128, false, false>, score_resident_kernel<128, false, true>},
+       {score_resident_kernel<128, true, false>, score_resident_kernel<128, true, true>}}};
+  const bool variant = a.row_agg != KVC_AGG_MAX || a.group_agg != KVC_AGG_MAX;
+  Kern kern = table[D == 128][variant][a.entropy != nullptr];
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   int per_sm = 0;

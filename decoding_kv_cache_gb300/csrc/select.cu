@@ -21,106 +21,100 @@ constexpr int kSelThreads = 1024;
 constexpr int kMaxBudgetHeads = 64;
 
 // Reallocation of one (layer, sequence)'s budget total over its H heads by normalised entropy
-// (low entropy, more budget): floors f = P + R, the T - H f slots above them in proportion to
-// u = 1 - entropy (clipped to [0, 1]; equal shares when every remaining u is 0), shares above
-// the cap N - f cut to it and the rest shared again (water-filling), then integers by largest
-// remainder with ties to the lower head. fp64 with every operation rounded on its own, heads in
-// order, so the integer outcome is a fixed function of the fp32 entropies. Returns false (out
+// (low entropy, more budget). Floors f = P + R; the E = T - H f slots above them go in
+// proportion to the utility u = 1 - entropy (clipped to [0, 1]) held as the 24-bit fixed-point
+// integer w = floor(u * 2^24) (equal shares when every remaining w is 0); a share above the cap
+// N - f is cut to it and the rest shared again (water-filling); integers by largest remainder,
+// ties to the lower head. After w everything is exact integer arithmetic (E <= 2^36, w <= 2^24,
+// so E w and cap W stay below 2^61), so the result is a fixed function of the fp32 entropies.
+// One warp: lanes hold heads lane and lane + 32 (H <= 64, N <= 2^30). Returns false (out
 // untouched) when some given budget is below f; with N <= f or T >= H N, out = min(given, N).
-// One thread; H <= kMaxBudgetHeads; u and share are H doubles of scratch (shared memory).
-__device__ bool head_budget_alloc(const float* ent, const int32_t* given, int given_all, int H, int N, int P, int R,
-                                  double* u, double* share, int32_t* out) {
-  const int f = P + R;
-  long long T = 0;
-  for (int h = 0; h < H; ++h) {
-    const int g = given ? given[h] : given_all;
-    if (g < f) return false;
-    T += g < N ? g : N;
-  }
+__device__ __forceinline__ long long warp_sum64(long long v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ bool head_budget_warp(const float* ent, const int32_t* given, int given_all, int H, int N, int P, int R,
+                                 int32_t* out) {
+  const int lane = threadIdx.x & 31, f = P + R;
+  const int h0 = lane, h1 = lane + 32;
+  const bool in0 = h0 < H, in1 = h1 < H;
+  const int g0 = in0 ? (given ? given[h0] : given_all) : f, g1 = in1 ? (given ? given[h1] : given_all) : f;
+  if (__any_sync(kFull, g0 < f || g1 < f)) return false;
+  const long long T = warp_sum64((in0 ? (g0 < N ? g0 : N) : 0) + (in1 ? (g1 < N ? g1 : N) : 0));
   if (N <= f || T >= (long long)H * N) {
-    for (int h = 0; h < H; ++h) {
-      const int g = given ? given[h] : given_all;
-      out[h] = g < N ? g : N;
-    }
+    if (in0) out[h0] = g0 < N ? g0 : N;
+    if (in1) out[h1] = g1 < N ? g1 : N;
     return true;
   }
-  const int cap = N - f;
-  const long long E = T - (long long)H * f;
-  uint64_t active = 0;
-  for (int h = 0; h < H; ++h) {
-    double v = __dsub_rn(1.0, (double)ent[h]);
-    if (!(v > 0.0)) v = 0.0;  // NaN too
-    if (v > 1.0) v = 1.0;
-    u[h] = v;
-    share[h] = 0.0;
-    active |= 1ull << h;
-  }
-  double Erem = (double)E;
-  for (int pass = 0; pass <= H; ++pass) {  // each pass caps a head or ends
-    double U = 0.0;
-    int na = 0;
-    for (int h = 0; h < H; ++h)
-      if (active >> h & 1) {
-        U = __dadd_rn(U, u[h]);
-        ++na;
-      }
+  const unsigned long long cap = (unsigned long long)(N - f), E = (unsigned long long)(T - (long long)H * f);
+  auto weight = [&](int h) -> unsigned long long {
+    double u = __dsub_rn(1.0, (double)ent[h]);
+    if (!(u > 0.0)) u = 0.0;  // NaN too
+    if (u > 1.0) u = 1.0;
+    return (unsigned long long)floor(__dmul_rn(u, 16777216.0));
+  };
+  const unsigned long long w0 = in0 ? weight(h0) : 0ull, w1 = in1 ? weight(h1) : 0ull;
+  bool a0 = in0, a1 = in1;  // still sharing (not capped)
+  unsigned long long Erem = E;
+  for (int pass = 0; pass <= H; ++pass) {
+    const unsigned long long W = (unsigned long long)warp_sum64((long long)((a0 ? w0 : 0ull) + (a1 ? w1 : 0ull)));
+    const int na = __popc(__ballot_sync(kFull, a0)) + __popc(__ballot_sync(kFull, a1));
     if (na == 0) break;
-    for (int h = 0; h < H; ++h)
-      if (active >> h & 1) share[h] = U > 0.0 ? __ddiv_rn(__dmul_rn(Erem, u[h]), U) : __ddiv_rn(Erem, (double)na);
-    bool capped = false;
-    for (int h = 0; h < H; ++h)
-      if ((active >> h & 1) && share[h] > (double)cap) {
-        share[h] = (double)cap;
-        active &= ~(1ull << h);
-        Erem = __dsub_rn(Erem, (double)cap);
-        capped = true;
-      }
-    if (!capped) break;
+    // share > cap  <=>  Erem w > cap W (or Erem > cap na for the equal split)
+    const bool o0 = a0 && (W > 0 ? Erem * w0 > cap * W : Erem > cap * (unsigned long long)na);
+    const bool o1 = a1 && (W > 0 ? Erem * w1 > cap * W : Erem > cap * (unsigned long long)na);
+    const int nc = __popc(__ballot_sync(kFull, o0)) + __popc(__ballot_sync(kFull, o1));
+    if (nc == 0) break;
+    a0 = a0 && !o0;
+    a1 = a1 && !o1;
+    const int ncap_all = H - (__popc(__ballot_sync(kFull, a0)) + __popc(__ballot_sync(kFull, a1)));
+    Erem = E - (unsigned long long)ncap_all * cap;
   }
-  long long sum = 0;
-  for (int h = 0; h < H; ++h) {  // out holds the integer shares until the end
-    int x = (active >> h & 1) ? (int)floor(share[h]) : cap;
-    if (x > cap) x = cap;
-    out[h] = x;
-    sum += x;
+  const unsigned long long W = (unsigned long long)warp_sum64((long long)((a0 ? w0 : 0ull) + (a1 ? w1 : 0ull)));
+  const unsigned long long na = (unsigned long long)(__popc(__ballot_sync(kFull, a0)) + __popc(__ballot_sync(kFull, a1)));
+  unsigned long long x0 = in0 ? cap : 0ull, x1 = in1 ? cap : 0ull, r0 = 0ull, r1 = 0ull;
+  if (a0) {
+    const unsigned long long num = W > 0 ? Erem * w0 : Erem, den = W > 0 ? W : na;
+    x0 = num / den;
+    r0 = num % den;  // the active heads' remainders share the denominator
   }
-  uint64_t bonus = 0;
-  for (long long left = E - sum; left > 0; --left) {  // largest remainders, ties to the lower head
-    int best = -1;
-    double bf = -1.0;
-    for (int h = 0; h < H; ++h) {
-      if ((bonus >> h & 1) || out[h] >= cap) continue;
-      const double fr = __dsub_rn(share[h], (double)out[h]);
-      if (fr > bf) {
-        bf = fr;
-        best = h;
-      }
-    }
-    if (best < 0) break;
-    bonus |= 1ull << best;
-    out[best] += 1;
+  if (a1) {
+    const unsigned long long num = W > 0 ? Erem * w1 : Erem, den = W > 0 ? W : na;
+    x1 = num / den;
+    r1 = num % den;
   }
-  for (int h = 0; h < H; ++h) out[h] += f;
+  const long long left = (long long)E - warp_sum64((long long)((in0 ? x0 : 0ull) + (in1 ? x1 : 0ull)));
+  // one more slot for the `left` eligible heads ranked first by (remainder desc, head asc)
+  const bool e0 = a0 && x0 < cap, e1 = a1 && x1 < cap;
+  int rank0 = 0, rank1 = 0;
+  for (int src = 0; src < 32; ++src) {
+    const unsigned long long q0 = __shfl_sync(kFull, r0, src), q1 = __shfl_sync(kFull, r1, src);
+    const bool f0 = __shfl_sync(kFull, e0, src), f1 = __shfl_sync(kFull, e1, src);
+    // head src (rank before every head above it on a tie) and head src + 32
+    rank0 += (f0 && (q0 > r0 || (q0 == r0 && src < h0))) + (f1 && (q1 > r0 || (q1 == r0 && src + 32 < h0)));
+    rank1 += (f0 && (q0 > r1 || (q0 == r1 && src < h1))) + (f1 && (q1 > r1 || (q1 == r1 && src + 32 < h1)));
+  }
+  if (in0) out[h0] = f + (int)(x0 + (e0 && rank0 < left ? 1 : 0));
+  if (in1) out[h1] = f + (int)(x1 + (e1 && rank1 < left ? 1 : 0));
   return true;
 }
 
-// kvc_head_budget: one warp per (layer, sequence), its first thread allocates (budget_out may
-// alias budget: a warp reads its slice before writing it).
+// kvc_head_budget: one warp per (layer, sequence) (budget_out may alias budget: the warp reads
+// its slice before writing it).
 __global__ void head_budget_kernel(const float* __restrict__ entropy, int Hkv, int N, int P, int R,
-                                   const int32_t* budget, int budget_all, int32_t* budget_out,
-                                   int32_t* status) {
-  __shared__ double su[kMaxBudgetHeads], sshare[kMaxBudgetHeads];
+                                   const int32_t* budget, int budget_all, int32_t* budget_out, int32_t* status) {
   __shared__ int32_t sout[kMaxBudgetHeads];
   griddep_wait();
   const int lb = blockIdx.x;
   const int32_t* given = budget ? budget + (size_t)lb * Hkv : nullptr;
-  if (threadIdx.x == 0 &&
-      !head_budget_alloc(entropy + (size_t)lb * Hkv, given, budget_all, Hkv, N, P, R, su, sshare, sout)) {
-    status_or(status, KVC_STATUS_BUDGET_RANGE);
-    for (int h = 0; h < Hkv; ++h) sout[h] = given ? given[h] : budget_all;
+  if (!head_budget_warp(entropy + (size_t)lb * Hkv, given, budget_all, Hkv, N, P, R, sout)) {
+    if (threadIdx.x == 0) status_or(status, KVC_STATUS_BUDGET_RANGE);
+    for (int h = threadIdx.x; h < Hkv; h += 32) sout[h] = given ? given[h] : budget_all;
   }
   __syncwarp();
-  for (int h = threadIdx.x; h < Hkv; h += blockDim.x) budget_out[(size_t)lb * Hkv + h] = sout[h];
+  for (int h = threadIdx.x; h < Hkv; h += 32) budget_out[(size_t)lb * Hkv + h] = sout[h];
 }
 
 // Block-wide exclusive prefix count of a flag, in thread order. Returns this thread's
@@ -159,24 +153,19 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
   __shared__ unsigned hist[256];
   __shared__ int wsum[33];
   __shared__ unsigned s_digit, s_k;
-  __shared__ int s_budget;
-  __shared__ double s_u[kMaxBudgetHeads], s_share[kMaxBudgetHeads];
   __shared__ int32_t s_alloc[kMaxBudgetHeads];
   const int head = blockIdx.x, tid = threadIdx.x;
   griddep_wait();  // the scores (and entropies) come from the previous kernel
   const float* sc = scores + (size_t)head * N;
   int32_t* out = kept_idx + (size_t)head * N;
   int b = budget ? budget[head] : budget_all;
-  if (entropy) {  // this head's share of its (layer, sequence)'s reallocated total
-    if (tid == 0) {
-      const int lb = head / Hkv, h = head % Hkv;
-      s_budget = head_budget_alloc(entropy + (size_t)lb * Hkv, budget ? budget + (size_t)lb * Hkv : nullptr,
-                                   budget_all, Hkv, N, P, R, s_u, s_share, s_alloc)
-                     ? s_alloc[h]
-                     : b;
-    }
+  if (entropy) {  // this head's share of its (layer, sequence)'s reallocated total (warp 0)
+    const int lb = head / Hkv, h = head % Hkv;
+    if (tid < 32 && !head_budget_warp(entropy + (size_t)lb * Hkv, budget ? budget + (size_t)lb * Hkv : nullptr,
+                                      budget_all, Hkv, N, P, R, s_alloc) && tid == 0)
+      s_alloc[h] = b;  // a given budget below prefix + recent: the given budgets stand
     __syncthreads();
-    b = s_budget;
+    b = s_alloc[h];
   }
   if (b >= N || b < P + R) {  // keep everything (out-of-range budgets are flagged)
     if (b < N && tid == 0) status_or(status, KVC_STATUS_BUDGET_RANGE);

@@ -363,19 +363,22 @@ int oracle_score_agg_f64(const double* q, const int* row_head, int M, int G, con
  * entropy gets more). The page fixes no formula; the rule here:
  *   total  T = sum_h min(given_h, N)            (the layer's preallocation)
  *   floor  f = P + R, cap c = N - f             (every head keeps its windows)
- *   utility u_h = 1 - ent_h, clipped to [0, 1]  (ent_h = normalised entropy)
- *   the E = T - H f slots beyond the floors are shared in proportion to u
- *   (equally when all active u are 0); a head whose share exceeds c gets c
+ *   utility u_h = 1 - ent_h clipped to [0, 1], held as the integer
+ *           w_h = floor(u_h * 2^24)              (24-bit fixed point)
+ *   the E = T - H f slots beyond the floors are shared in proportion to w
+ *   (equally when all active w are 0); a head whose share exceeds c gets c
  *   and leaves, and the rest is shared again among the others (water-filling);
  *   integer shares by largest remainder (floors, then one more slot each to the
  *   largest fractional parts, ties to the lower head index);
  *   out_h = f + share_h.
- * Arithmetic in fp64 with each operation rounded on its own (no fused
- * multiply-add), in head order. Returns 0, or -1 if some given_h < P + R (the
- * caller keeps the given budgets then). If N <= f or T >= H N every head gets
- * min(given_h, N) unchanged. */
+ * After w, everything is exact integer arithmetic: share_h = E_A w_h / W_A
+ * with W_A = sum of the active w, compared and floored as integers. Returns 0,
+ * or -1 if some given_h < P + R (the caller keeps the given budgets then). If
+ * N <= f or T >= H N every head gets min(given_h, N) unchanged. H <= 64,
+ * N <= 2^30. */
 int oracle_head_budget(const float* ent, int H, int N, int P, int R, const int32_t* given, int32_t* out) {
   const int f = P + R;
+  if (H < 1 || H > 64) return -1;
   int64_t T = 0;
   for (int h = 0; h < H; ++h) {
     if (given[h] < f) return -1;
@@ -385,67 +388,79 @@ int oracle_head_budget(const float* ent, int H, int N, int P, int R, const int32
     for (int h = 0; h < H; ++h) out[h] = given[h] < N ? given[h] : N;
     return 0;
   }
-  const int cap = N - f;
-  const int64_t E = T - (int64_t)H * f;
-  double u[64], share[64];
-  int active[64], x[64], bonus[64];
-  if (H > 64) return -1;
+  const int64_t cap = N - f;
+  uint64_t w[64];
+  int active[64];
+  int64_t x[64];
   for (int h = 0; h < H; ++h) {
-    const double e = (double)ent[h];
-    double v = 1.0 - e;
-    if (!(v > 0.0)) v = 0.0; /* also catches NaN */
-    if (v > 1.0) v = 1.0;
-    u[h] = v;
+    double u = 1.0 - (double)ent[h];
+    if (!(u > 0.0)) u = 0.0; /* also catches NaN */
+    if (u > 1.0) u = 1.0;
+    w[h] = (uint64_t)floor(u * 16777216.0);
     active[h] = 1;
-    share[h] = 0.0;
+    x[h] = 0;
   }
-  double Erem = (double)E;
+  /* water-filling: cap every head whose exact share E w_h / W exceeds c */
+  uint64_t Erem = (uint64_t)(T - (int64_t)H * f);
   for (;;) {
-    double U = 0.0;
+    uint64_t W = 0;
     int na = 0;
     for (int h = 0; h < H; ++h)
       if (active[h]) {
-        U += u[h];
+        W += w[h];
         ++na;
       }
     if (na == 0) break;
     int capped = 0;
     for (int h = 0; h < H; ++h) {
       if (!active[h]) continue;
-      share[h] = U > 0.0 ? (Erem * u[h]) / U : Erem / (double)na;
-    }
-    for (int h = 0; h < H; ++h)
-      if (active[h] && share[h] > (double)cap) {
-        share[h] = (double)cap;
+      /* share > cap  <=>  Erem w_h > cap W (or Erem > cap na for the equal split) */
+      const int over = W > 0 ? Erem * w[h] > (uint64_t)cap * W : Erem > (uint64_t)cap * (uint64_t)na;
+      if (over) {
         active[h] = 0;
-        Erem -= (double)cap;
+        x[h] = cap;
         capped = 1;
       }
-    if (!capped) break;
-  }
-  int64_t given_out = 0;
-  for (int h = 0; h < H; ++h) {
-    x[h] = active[h] ? (int)floor(share[h]) : cap;
-    if (x[h] > cap) x[h] = cap;
-    bonus[h] = 0;
-    given_out += x[h];
-  }
-  for (int64_t left = E - given_out; left > 0; --left) {
-    int best = -1;
-    double bf = -1.0;
-    for (int h = 0; h < H; ++h) {
-      if (bonus[h] || x[h] >= cap) continue;
-      const double fr = share[h] - (double)x[h];
-      if (fr > bf) {
-        bf = fr;
-        best = h;
-      }
     }
-    if (best < 0) break; /* every head full: cannot happen while E < H * cap */
+    if (!capped) break;
+    /* the capped heads take their caps out of what is shared again */
+    Erem = (uint64_t)(T - (int64_t)H * f);
+    for (int h = 0; h < H; ++h)
+      if (!active[h]) Erem -= (uint64_t)cap;
+  }
+  /* floors and remainders of the active heads' exact shares */
+  uint64_t W = 0;
+  int na = 0;
+  for (int h = 0; h < H; ++h)
+    if (active[h]) {
+      W += w[h];
+      ++na;
+    }
+  uint64_t rem[64];
+  uint64_t given_out = 0;
+  for (int h = 0; h < H; ++h) {
+    if (!active[h]) {
+      rem[h] = 0;
+      given_out += (uint64_t)x[h];
+      continue;
+    }
+    const uint64_t num = W > 0 ? Erem * w[h] : Erem, den = W > 0 ? W : (uint64_t)na;
+    x[h] = (int64_t)(num / den);
+    rem[h] = num % den; /* remainders share the denominator: compare them directly */
+    given_out += (uint64_t)x[h];
+  }
+  int bonus[64] = {0};
+  for (uint64_t left = (uint64_t)(T - (int64_t)H * f) - given_out; left > 0; --left) {
+    int best = -1;
+    for (int h = 0; h < H; ++h) {
+      if (!active[h] || bonus[h] || x[h] >= cap) continue;
+      if (best < 0 || rem[h] > rem[best]) best = h;
+    }
+    if (best < 0) break; /* cannot happen: the remainders sum to fewer slots than active heads */
     bonus[best] = 1;
     x[best] += 1;
   }
-  for (int h = 0; h < H; ++h) out[h] = f + x[h];
+  for (int h = 0; h < H; ++h) out[h] = f + (int32_t)x[h];
   return 0;
 }
 

@@ -141,35 +141,44 @@ def test_head_budget_handworked(case):
         assert out.tolist() == case["budget"]
 
 
-def _waterfill(u, E, cap):
-    """Shares s_h = min(cap, lam * u_h) with sum E (bisection on lam), or an equal split of what
-    the capped heads leave when the rest have zero utility."""
-    u = np.asarray(u, dtype=np.float64)
-    if u.sum() == 0:
-        return np.full(len(u), E / len(u))
-    lo, hi = 0.0, 1.0
-    while np.minimum(cap, hi * u).sum() < E:
-        hi *= 2
-        if hi > 1e300:
-            break
-    for _ in range(200):
-        mid = (lo + hi) / 2
-        if np.minimum(cap, mid * u).sum() < E:
-            lo = mid
-        else:
-            hi = mid
-    s = np.minimum(cap, hi * u)
-    z = u == 0
-    if z.any() and s.sum() < E - 1e-9:  # zero-utility heads share what is left equally
-        s[z] = (E - s[~z].sum()) / z.sum()
-    return s
+def _weights(ent):
+    """The rule's utilities as 24-bit fixed point: floor((1 - entropy) * 2^24), clipped to [0, 1]."""
+    u = np.clip(1.0 - np.asarray(ent, dtype=np.float32).astype(np.float64), 0.0, 1.0)
+    return [int(math.floor(v * 2 ** 24)) for v in u]
+
+
+def _waterfill(w, E, cap):
+    """Exact shares s_h = min(cap, lam * w_h) with sum E, as Fractions: lam from the breakpoints
+    (independent of the oracle's iteration); zero-weight heads share what the others leave."""
+    H = len(w)
+    if sum(w) == 0:
+        return [Fraction(E, H)] * H
+    # lam is where sum_h min(cap, lam w_h) = E: try the heads capped in order of decreasing weight
+    order = sorted(range(H), key=lambda h: -w[h])
+    for k in range(H + 1):
+        capped = set(order[:k])
+        rest = [h for h in range(H) if h not in capped]
+        Wr = sum(w[h] for h in rest)
+        left = E - cap * k
+        if Wr == 0:
+            s = [Fraction(cap) if h in capped else Fraction(0) for h in range(H)]
+            z = [h for h in rest if w[h] == 0]
+            for h in z:
+                s[h] = Fraction(left, len(z))
+            if all(v <= cap for v in s):
+                return s
+            continue
+        lam = Fraction(left, Wr)
+        if all(lam * w[h] <= cap for h in rest) and all(lam * w[h] >= cap for h in capped):
+            return [Fraction(cap) if h in capped else lam * w[h] for h in range(H)]
+    raise AssertionError("no water level")
 
 
 @pytest.mark.parametrize("seed", range(30))
 def test_head_budget_brute_force(seed):
     """The integer budgets minimise sum (x - s)^2 over all integer vectors with the same total
-    and bounds, s being the water-filled real shares; among minimisers the lower heads get the
-    extra slots (lexicographically largest)."""
+    and bounds, s being the exact water-filled shares of the fixed-point weights; among
+    minimisers the lower heads get the extra slots (lexicographically largest)."""
     rng = np.random.default_rng(seed)
     H = int(rng.integers(2, 5))
     N, P, R = int(rng.integers(24, 34)), 2, 3
@@ -184,14 +193,13 @@ def test_head_budget_brute_force(seed):
     if T >= H * N:
         return
     E = T - H * f
-    u = np.clip(1.0 - ent.astype(np.float64), 0, 1)
-    s = _waterfill(u, E, cap)
+    s = _waterfill(_weights(ent), E, cap)
     best, best_x = None, None
     for x in itertools.product(range(cap + 1), repeat=H):
         if sum(x) != E:
             continue
-        d = float(np.sum((np.array(x) - s) ** 2))
-        if best is None or d < best - 1e-9 or (abs(d - best) <= 1e-9 and x > best_x):
+        d = sum((Fraction(xi) - si) ** 2 for xi, si in zip(x, s))
+        if best is None or d < best or (d == best and x > best_x):
             best, best_x = d, x
     assert (out - f).tolist() == list(best_x), (ent, given, s)
 
