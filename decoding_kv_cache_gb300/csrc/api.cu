@@ -94,6 +94,7 @@ void fill_score_args(ScoreArgs* a, const CacheGeom& g, int dtype, const LayerPtr
   a->row_agg = o.row_agg;
   a->group_agg = o.group_agg;
   a->entropy = entropy;
+  a->tiles = 1;  // launch_score may split 256-row tiles
   a->debug_fault = g_debug_fault.load();
   a->dtype = dtype;
   a->K = K;

@@ -127,6 +127,8 @@ struct ScoreArgs {
   int qstride;                   // rows per query head in the tile (n_r + n_b, or rounded up to 16)
   int row_agg, group_agg;        // KVC_AGG_* (ext only)
   float* entropy;                // [heads] normalised entropy, accumulated (zeroed by build_obs), or null
+  int tiles;                     // 128-row tiles scored apart per head by the single-read kernel (1 or 2);
+                                 // with 2, build_obs zeroes the scores and the tiles combine atomically
 };
 
 // Row stride of a query head and row count of the observation tile for a mode.

@@ -84,6 +84,9 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
         for (long long w = lo + threadIdx.x; w < hi; w += blockDim.x) a.xch_zero[w] = 0ull;
       }
       for (int i = threadIdx.x; i < hd; i += blockDim.x) rope_s[i] = a.rope[i];
+      // the scoring kernel combines a head's tiles into its scores with atomics: start at zero
+      if (a.tiles > 1)
+        for (int j = threadIdx.x; j < a.g.N; j += blockDim.x) a.scores[(size_t)head * a.g.N + j] = 0.f;
       if (threadIdx.x == 0) s_nvalid = 0;
       __syncthreads();
     }
@@ -347,10 +350,21 @@ static bool set_smem(K kernel, size_t bytes) {
 int launch_score(const ScoreArgs& a_in, const ScoreWs& ws, cudaStream_t s) {
   ScoreArgs a = a_in;
   const int heads = a.g.L * a.g.B * a.g.Hkv;
-  // the single-read kernel's plan is fixed first: the observation kernel zeroes its exchange words
+  // the single-read kernel's plan is fixed first: the observation kernel zeroes its exchange words.
+  // A 256-row observation tile goes to it as two 128-row tiles when no query head's rows cross the
+  // tile boundary (or the aggregation is max over everything, where heads do not matter).
   FusedPlan rp;
   size_t rsmem = 0;
-  const bool resident = a.dtype == KVC_BF16 && score_resident_plan(a, &rp, &rsmem);
+  a.tiles = 1;
+  if (a.dtype == KVC_BF16 && a.M_pad == 2 * 128) {
+    bool straddle = false;
+    const int per_q = a.n_r + a.n_b, G = a.g.Hq / a.g.Hkv;
+    if (a.row_agg != KVC_AGG_MAX || a.group_agg != KVC_AGG_MAX)
+      for (int g = 0; g < G; ++g) straddle |= (g * a.qstride) / 128 != (g * a.qstride + per_q - 1) / 128;
+    if (!straddle) a.tiles = 2;
+  }
+  bool resident = a.dtype == KVC_BF16 && score_resident_plan(a, &rp, &rsmem);
+  if (!resident) a.tiles = 1;
   a.xch_zero = resident ? reinterpret_cast<unsigned long long*>(ws.part) : nullptr;
   a.xch_zero_words = resident ? score_resident_words(rp, a.entropy != nullptr) : 0;
   const int D = a.g.D;

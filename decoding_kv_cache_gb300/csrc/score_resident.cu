@@ -26,7 +26,7 @@
 //               sub-partition keep the MUFU (exp2) pipe busy while one waits on it.
 //   warps 10-17 pass 2, laid out the same way and running concurrently with pass 1 of the next
 //               round. First the exchange: the 256 threads poll the group's partials of the
-//               round (four words each in flight at once) and merge them into lse2. Then a
+//               round (sixteen words each in flight at once) and merge them into lse2. Then a
 //               chunk's TMEM values are read in the 16x256b fragment shape (each thread: 4 of
 //               the warp's 32 rows x 2 columns per 8-column group) and its accumulator freed;
 //               s*c2 - lse2 and the max over the 4 rows in registers, then a 3-step
@@ -50,6 +50,10 @@ constexpr int kResChunks = 2;    // key chunks per CTA per round
 constexpr int kResRows = 128;    // observation rows per head this kernel handles (one MMA tile)
 constexpr int kResAcc = 2 * kResChunks;
 constexpr unsigned long long kExchangeTimeoutNs = 50ull * 1000 * 1000;  // a partner's word: ~1 us normally
+// Partner words each exchange thread keeps in flight (the kernel's kXB): a head spread over g CTAs
+// needs g/2 words per thread, so with 32 or 128 CTAs per head (8k or 32k keys) narrow batches
+// serialise round trips, while with 8 (2k keys) a wide batch only costs registers.
+constexpr int kXchNarrow = 4, kXchWide = 16;
 
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
@@ -109,7 +113,7 @@ __device__ __forceinline__ void reduce_scatter8(float (&w)[8], int lane) {
 
 // kExt: the extended epilogue (the aggregation variants); otherwise max/max. kEnt: the rows'
 // attention entropy is accumulated too (pass 1 keeps each row's mean logit; pass 2 merges).
-template <int D, bool kExt, bool kEnt>
+template <int D, bool kExt, bool kEnt, int kXchBatch>
 __global__ void __launch_bounds__(kResThreads, 1)
     score_resident_kernel(const __grid_constant__ FusedMaps maps, ScoreArgs a, ScoreWs ws, FusedPlan p, FusedXch xch,
                           float c2) {
@@ -158,9 +162,12 @@ __global__ void __launch_bounds__(kResThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *slot;
 
-  const int heads = a.g.L * a.g.B * a.g.Hkv;
+  // A unit is one 128-row observation tile of a head (a.tiles of them per head: the rows of a
+  // head are independent in the softmax, so its tiles are scored apart and their per-key
+  // values combined with atomics into the zeroed scores).
+  const int units = a.g.L * a.g.B * a.g.Hkv * a.tiles;
   const int group = blockIdx.x / p.group_size, rank = blockIdx.x % p.group_size;
-  const int rounds = group < heads ? (heads - group + p.ngroups - 1) / p.ngroups : 0;
+  const int rounds = group < units ? (units - group + p.ngroups - 1) / p.ngroups : 0;
   const int c0 = rank * p.chunks_per_cta;
   const int n = max(0, min(c0 + p.chunks_per_cta, a.nchunk) - c0);  // chunks per round, the same every round
 
@@ -170,11 +177,11 @@ __global__ void __launch_bounds__(kResThreads, 1)
       uint32_t kc = 0;
       const int bhkv = a.g.B * a.g.Hkv;
       // a round usually moves to another layer's tensor map: fetch the next rounds' maps early
-      for (int r = 0; r < 2 && r < rounds; ++r) tc::prefetch_tensormap(&maps.k[(group + r * p.ngroups) / bhkv]);
+      for (int r = 0; r < 2 && r < rounds; ++r) tc::prefetch_tensormap(&maps.k[(group + r * p.ngroups) / a.tiles / bhkv]);
       for (int r = 0; r < rounds && !*abort_flag; ++r) {
-        const int head = group + r * p.ngroups;
+        const int head = (group + r * p.ngroups) / a.tiles;
         const int l = head / bhkv, bh = head % bhkv;
-        if (r + 2 < rounds) tc::prefetch_tensormap(&maps.k[(head + 2 * p.ngroups) / bhkv]);
+        if (r + 2 < rounds) tc::prefetch_tensormap(&maps.k[(group + (r + 2) * p.ngroups) / a.tiles / bhkv]);
         bool stop = false;
         for (int j = 0; j < n; ++j) {
           const int s = kc % S;
@@ -241,12 +248,12 @@ __global__ void __launch_bounds__(kResThreads, 1)
       griddep_wait();  // the tiles come from the observation kernel
       int qloads = 0;
       for (int r = 0; r < rounds && !*abort_flag; ++r) {
-        const int head = group + r * p.ngroups;
+        const int unit = group + r * p.ngroups;
         const int qb = r % kQBuf, use = r / kQBuf;
         if (use >= 1 && !wait_or_abort(&qempty[qb], (use - 1) & 1, abort_flag, a.status)) break;
         tc::mbar_expect_tx(&qfull[qb], (uint32_t)kQBytes);
         for (int h = 0; h < HALVES; ++h)
-          tc::tma_load_2d(Qs + qb * kQBytes + h * (kResRows * 128), &maps.q, &qfull[qb], h * 64, head * kResRows);
+          tc::tma_load_2d(Qs + qb * kQBytes + h * (kResRows * 128), &maps.q, &qfull[qb], h * 64, unit * kResRows);
         qloads = r + 1;
       }
       for (int r = qloads - kQBuf < 0 ? 0 : qloads - kQBuf; r < qloads; ++r)
@@ -362,19 +369,20 @@ __global__ void __launch_bounds__(kResThreads, 1)
     // pass 2 of a round: per key, the max over rows of s*c2 - lse2, from the logits still in TMEM;
     // each chunk's accumulator is freed as soon as its values are in registers.
     auto pass2 = [&](int round) {
-      const int head = group + round * p.ngroups;
+      const int unit = group + round * p.ngroups;
+      const int head = unit / a.tiles, tile = unit % a.tiles;
       // ---- exchange: lse2 of every row from the group's tagged partials. Thread t of the group
       // polls row t/2 of partners t%2, t%2 + 2, ... (four words in flight at a time) and merges
       // them; the two threads of a row combine with one shuffle.
       const int gt = e * 32 + lane;  // 0..255
       const int xrow = gt >> 1, xpar = gt & 1;
-      const bool xvalid = ws.valid[(size_t)head * kResRows + xrow] != 0;
+      const bool xvalid = ws.valid[(size_t)unit * kResRows + xrow] != 0;
       // extended epilogue: the weights of this thread's rows in a mean, fetched before the exchange
       float wr[4];
       if constexpr (kExt) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          wr[k] = a.row_agg == KVC_AGG_MEAN ? ws.rw[(size_t)head * kResRows + q * 32 + (lane >> 2) + 8 * k] : 0.f;
+          wr[k] = a.row_agg == KVC_AGG_MEAN ? ws.rw[(size_t)unit * kResRows + q * 32 + (lane >> 2) + 8 * k] : 0.f;
       }
       // Slot round % 4 last held round - 4. A partner overwrites it (round + 4) only after its
       // pass 1 of round + 4, which needs its TMEM buffer back from its pass 2 of round + 2, which
@@ -384,10 +392,10 @@ __global__ void __launch_bounds__(kResThreads, 1)
       const uint64_t* grp = words + ((size_t)((round & 3) * p.ngroups + group) * p.group_size) * kResRows + xrow;
       float mx = -INFINITY, sm = 0.f;
       bool ok = !*abort_flag;
-      for (int u0 = 0; ok && xpar + 2 * u0 < p.group_size; u0 += 4) {
-        uint64_t w[4];
+      for (int u0 = 0; ok && xpar + 2 * u0 < p.group_size; u0 += kXchBatch) {
+        uint64_t w[kXchBatch];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kXchBatch; ++u) {
           const int k = xpar + 2 * (u0 + u);
           w[u] = k < p.group_size ? ld_relaxed_u64(grp + (size_t)k * kResRows)
                                   : ((uint64_t)tag << 32) | __float_as_uint(-INFINITY);
@@ -396,7 +404,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
         for (uint32_t it = 0;; ++it) {
           unsigned need = 0u;
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
+          for (int u = 0; u < kXchBatch; ++u)
             if ((uint32_t)(w[u] >> 32) != tag) need |= 1u << u;
           if (need == 0u) break;
           if (it == 0) t_start = global_ns();
@@ -410,17 +418,17 @@ __global__ void __launch_bounds__(kResThreads, 1)
           }
           __nanosleep(32);
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
+          for (int u = 0; u < kXchBatch; ++u)
             if (need & (1u << u)) w[u] = ld_relaxed_u64(grp + (size_t)(xpar + 2 * (u0 + u)) * kResRows);
         }
         float bm = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) bm = fmaxf(bm, __uint_as_float((uint32_t)w[u]));
+        for (int u = 0; u < kXchBatch; ++u) bm = fmaxf(bm, __uint_as_float((uint32_t)w[u]));
         const float nm = fmaxf(mx, bm);
         if (nm > -INFINITY) {
           float accs = mx > -INFINITY ? sm * exp2f(mx - nm) : 0.f;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) accs += exp2f(__uint_as_float((uint32_t)w[u]) - nm);  // -inf adds 0
+          for (int u = 0; u < kXchBatch; ++u) accs += exp2f(__uint_as_float((uint32_t)w[u]) - nm);  // -inf adds 0
           mx = nm;
           sm = accs;
         }
@@ -554,7 +562,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
           int cs = -1;
 #pragma unroll
           for (int h = 0; h < 8; ++h) {
-            const int sg = (16 * h) / a.qstride;
+            const int sg = (tile * kResRows + 16 * h) / a.qstride;
             const float v = pj[h * kChunk + col];
             if (sg != cs) {
               if (cs >= 0) gacc = gsum ? gacc + cur : fmaxf(gacc, cur);
@@ -566,7 +574,15 @@ __global__ void __launch_bounds__(kResThreads, 1)
           }
           gacc = gsum ? gacc + cur : fmaxf(gacc, cur);
           const int key = (c0 + j) * kChunk + col;
-          if (key < a.g.N) a.scores[(size_t)head * a.g.N + key] = gacc;
+          if (key < a.g.N) {
+            float* dst = a.scores + (size_t)head * a.g.N + key;
+            if (a.tiles == 1)
+              *dst = gacc;
+            else if (gsum)  // two tiles: a + b either way round, so the sum is deterministic
+              atomicAdd(dst, gacc);
+            else  // non-negative floats order like their bit patterns
+              atomicMax(reinterpret_cast<unsigned*>(dst), __float_as_uint(gacc));
+          }
         }
       } else {
         float2 nl[4];  // -lse2 of rows q*32 + lane/4 + 8k, twice (packed operands)
@@ -650,7 +666,13 @@ __global__ void __launch_bounds__(kResThreads, 1)
           const float* pj = pb + j * 4 * kChunk;
           const float m = fmaxf(fmaxf(pj[col], pj[kChunk + col]), fmaxf(pj[2 * kChunk + col], pj[3 * kChunk + col]));
           const int key = (c0 + j) * kChunk + col;
-          if (key < a.g.N) a.scores[(size_t)head * a.g.N + key] = exp2f(m);
+          if (key < a.g.N) {
+            float* dst = a.scores + (size_t)head * a.g.N + key;
+            if (a.tiles == 1)
+              *dst = exp2f(m);
+            else  // non-negative floats order like their bit patterns
+              atomicMax(reinterpret_cast<unsigned*>(dst), __float_as_uint(exp2f(m)));
+          }
         }
       }
     };
@@ -675,7 +697,7 @@ static int resident_tail_bytes(bool ext) {
 }
 
 bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem) {
-  if (a.dtype != KVC_BF16 || a.M_pad != kResRows) return false;
+  if (a.dtype != KVC_BF16 || a.M_pad != kResRows * a.tiles) return false;
   int dev = 0, nsm = 0, smem_optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -683,7 +705,7 @@ bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem) {
     return false;
   if (nsm > kMaxSMs) nsm = kMaxSMs;
   const int D = a.g.D;
-  const int heads = a.g.L * a.g.B * a.g.Hkv;
+  const int heads = a.g.L * a.g.B * a.g.Hkv * a.tiles;  // units
   p->chunks_per_cta = a.nchunk >= kResChunks ? kResChunks : 1;
   p->group_size = (a.nchunk + p->chunks_per_cta - 1) / p->chunks_per_cta;
   if (p->group_size > nsm) return false;
@@ -714,14 +736,17 @@ int launch_score_resident(const ScoreArgs& a, const ScoreWs& ws, const FusedPlan
   if (!fused_maps(&maps, a, ws)) return KVC_ERR_LAUNCH;
   const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
   using Kern = void (*)(const FusedMaps, ScoreArgs, ScoreWs, FusedPlan, FusedXch, float);
-  // [D == 128][extended epilogue][entropy]
-  static const Kern table[2][2][2] = {
-      {{score_resident_kernel<64, false, false>, score_resident_kernel<64, false, true>},
-       {score_resident_kernel<64, true, false>, score_resident_kernel<64, true, true>}},
-      {{score_resident_kernel<128, false, false>, score_resident_kernel<128, false, true>},
-       {score_resident_kernel<128, true, false>, score_resident_kernel<128, true, true>}}};
+  // [D == 128][extended epilogue][entropy][wide exchange batch]
+#define KVC_RES_K(d, x, e) {score_resident_kernel<d, x, e, kXchNarrow>, score_resident_kernel<d, x, e, kXchWide>}
+  static const Kern table[2][2][2][2] = {
+      {{KVC_RES_K(64, false, false), KVC_RES_K(64, false, true)}, {KVC_RES_K(64, true, false), KVC_RES_K(64, true, true)}},
+      {{KVC_RES_K(128, false, false), KVC_RES_K(128, false, true)},
+       {KVC_RES_K(128, true, false), KVC_RES_K(128, true, true)}}};
+#undef KVC_RES_K
   const bool variant = a.row_agg != KVC_AGG_MAX || a.group_agg != KVC_AGG_MAX;
-  Kern kern = table[D == 128][variant][a.entropy != nullptr];
+  // wide batches once a thread would need more than two narrow ones (group_size / 2 partners each)
+  const bool wide = p.group_size / 2 > 2 * kXchNarrow;
+  Kern kern = table[D == 128][variant][a.entropy != nullptr][wide];
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   int per_sm = 0;

@@ -28,6 +28,8 @@ CASES = [
     ("qwen3-4b", dict(L=8, B=8, N=300, D=64)),
     # a 128-row tile whose keys exceed 256 per SM: the two-pass kernel takes it
     ("qwen3-4b", dict(L=1, Hq=4, Hkv=1, N=50000)),
+    # 224 rows as two 128-row tiles over 20 CTAs per head (the wide exchange batch)
+    ("qwen7b-reasonalloc", dict(L=1, B=1, N=5000)),
 ]
 
 

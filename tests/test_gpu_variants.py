@@ -1,8 +1,9 @@
 """Parity of the aggregation variants, the entropy output and the entropy-driven head budgets
 (CUDA path through the C ABI) with the CPU oracle.
 
-Cases cover every scoring kernel: the single-read kernel (128-row tiles), the two-pass kernel
-(256-row tiles, and a 128-row tile over 50k keys), the fp32 path, a row count that is not a
+Cases cover every scoring kernel: the single-read kernel (128-row tiles, and 224-row tiles split
+in two), the two-pass kernel (48-row query heads crossing the 128-row boundary, and a 128-row tile
+over 50k keys), the fp32 path, a row count that is not a
 multiple of 16 (each query head's rows then start on a 16-row boundary) and buffers holding
 fewer rows than n_b (query heads with different row counts, so the mean's weights differ).
 """
@@ -22,8 +23,10 @@ CASES = [
     ("qwen3-4b", dict(L=2, N=1000)),                        # single-read kernel
     ("qwen3-4b", dict(L=1, N=700, n_b=8, qmax=16)),         # 24 rows per query head, stride 32
     ("qwen3-4b", dict(L=2, N=600, count=10)),               # 26 valid rows per query head
-    ("qwen7b-reasonalloc", dict(L=1, B=2, N=1500)),          # 224 rows: two-pass kernel
-    ("qwen3-14b-long", dict(L=1, B=1, N=2100)),              # 48 rows per query head across tiles
+    ("qwen7b-reasonalloc", dict(L=1, B=2, N=1500)),          # 224 rows: two 128-row tiles
+    ("qwen7b-reasonalloc", dict(L=1, B=1, N=5000)),          # two tiles, 20 CTAs per head
+    ("qwen3-14b-long", dict(L=1, B=1, N=2100)),              # 48 rows per query head: variants cross
+                                                             # tiles (two-pass kernel), max/max is tiled
     ("qwen3-4b", dict(L=1, Hq=4, Hkv=1, N=50000)),           # two-pass kernel, many keys per SM
     ("tiny", dict(N=1000, D=128)),                           # fp32 path
     ("tiny", dict(N=300, count=5)),                          # fp32, short buffers
