@@ -44,6 +44,9 @@
  *              B_KV^max, evict 1/8 so the cache drops to 7/8 B_KV^max. ReasonAlloc
  *              page, "Core Mechanism": a per-head budget B_{L_i,H_j} caps each
  *              head instead.
+ *   append     BeaconKV page, "Continual FPS" and "观察 query 集": one decode step's
+ *              pre-RoPE query joins its head's buffer (compressed by FPS as soon as
+ *              it is full) and its post-RoPE query joins the recent ring.
  *   compact    The kept tokens' K and V rows, in original order, at the head's
  *              front (out-of-place gather here); slots past the kept count keep
  *              their old contents.
@@ -740,6 +743,87 @@ int oracle_fps_update(int32_t dtype, int32_t nheads_q, int32_t D, void* qbuf, in
     free(x);
     free(sel);
     done += 1;
+  }
+  return done;
+}
+
+/* Compress one full buffer (qmax rows at base) to qmax/2 survivors in time order;
+ * sel receives the survivors' old rows. */
+static void compress_one(int32_t dtype, int32_t D, void* qbuf, int64_t base, int32_t qmax, int* sel) {
+  const int m = qmax / 2;
+  double* x = (double*)malloc(sizeof(double) * (size_t)qmax * D);
+  for (int i = 0; i < qmax; ++i)
+    for (int d = 0; d < D; ++d) x[(int64_t)i * D + d] = load_elem(qbuf, dtype, base + (int64_t)i * D + d);
+  oracle_fps_f64(x, qmax, D, m, sel, NULL, NULL);
+  for (int k = 0; k < m; ++k)
+    for (int d = 0; d < D; ++d) store_elem(qbuf, dtype, base + (int64_t)k * D + d, qbuf, base + (int64_t)sel[k] * D + d);
+  free(x);
+}
+
+/* One decode step's queries into the observation state (BeaconKV page, "Continual FPS": the
+ * buffer of pre-RoPE queries grows to B_Q^max and is then cut back to B_Q^min; "观察 query 集":
+ * the recent queries are the latest n_r at their own positions). For every query head:
+ *   - a buffer already full on entry (count == qmax) is compressed first;
+ *   - the new pre-RoPE query q_pre goes to buffer row count, count += 1;
+ *   - a buffer that has just become full is compressed (FPS to qmax/2, time order);
+ *   - ring row t mod n_r of q_recent receives q_post, or when q_post is NULL the binary32
+ *     rotation of q_pre to position t rounded to the storage type (as for beacons).
+ * A count outside [0, qmax] leaves that head's buffer alone (error[qh] = -1); its ring row is
+ * still written. picks [nheads_q, qmax/2] (may be NULL) receives the old rows of the last
+ * compression in this call, -1 when none. Returns the number of compressions, or -1 on bad
+ * sizes. */
+int oracle_append(int32_t dtype, int32_t nheads_q, int32_t D, const void* q_pre, const void* q_post, int64_t t,
+                  double theta, void* qbuf, int32_t qmax, int32_t* count, void* q_recent, int32_t n_r,
+                  int32_t* picks, int32_t* error) {
+  if (nheads_q < 0 || D < 2 || D % 2 || qmax < 2 || qmax % 2 || n_r < 0 || t < 0) return -1;
+  const int m = qmax / 2;
+  int done = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : done)
+  for (int64_t qh = 0; qh < nheads_q; ++qh) {
+    int* sel = (int*)malloc(sizeof(int) * (size_t)m);
+    float* tmp = (float*)malloc(sizeof(float) * (size_t)D);
+    float* rot = (float*)malloc(sizeof(float) * (size_t)D);
+    int compressed = 0;
+    if (error) error[qh] = 0;
+    if (n_r > 0) {
+      const int64_t dst = (qh * n_r + t % n_r) * (int64_t)D;
+      if (q_post) {
+        for (int d = 0; d < D; ++d) store_elem(q_recent, dtype, dst + d, q_post, qh * (int64_t)D + d);
+      } else {
+        for (int d = 0; d < D; ++d) tmp[d] = (float)load_elem(q_pre, dtype, qh * (int64_t)D + d);
+        oracle_rope_f32(tmp, D, (long long)t, theta, rot);
+        for (int d = 0; d < D; ++d) {
+          const double v = round_to_storage((double)rot[d], dtype);
+          if (dtype == DT_BF16) ((uint16_t*)q_recent)[dst + d] = oracle_f64_to_bf16(v);
+          else ((float*)q_recent)[dst + d] = (float)v;
+        }
+      }
+    }
+    int c = count[qh];
+    const int64_t base = qh * (int64_t)qmax * D;
+    if (c < 0 || c > qmax) {
+      if (error) error[qh] = -1;
+    } else {
+      if (c == qmax) {
+        compress_one(dtype, D, qbuf, base, qmax, sel);
+        c = m;
+        compressed = 1;
+      }
+      for (int d = 0; d < D; ++d) store_elem(qbuf, dtype, base + (int64_t)c * D + d, q_pre, qh * (int64_t)D + d);
+      c += 1;
+      if (c == qmax) {
+        compress_one(dtype, D, qbuf, base, qmax, sel);
+        c = m;
+        compressed += 1;
+      }
+      count[qh] = c;
+    }
+    if (picks)
+      for (int k = 0; k < m; ++k) picks[qh * m + k] = compressed ? sel[k] : -1;
+    done += compressed;
+    free(sel);
+    free(tmp);
+    free(rot);
   }
   return done;
 }

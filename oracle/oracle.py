@@ -79,6 +79,9 @@ def lib():
         L.oracle_fps_update.restype = C.c_int
         L.oracle_fps_update.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p,
                                         C.c_void_p]
+        L.oracle_append.restype = C.c_int
+        L.oracle_append.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_double,
+                                    C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]
         L.oracle_set_threads.restype = C.c_int
         L.oracle_set_threads.argtypes = [C.c_int]
         _lib = L
@@ -277,3 +280,26 @@ def fps_update(qbuf_bits: np.ndarray, count: np.ndarray, qmax: int, dtype: str, 
     if rc < 0:
         raise ValueError("oracle_fps_update: bad sizes")
     return qb, cnt, picks.reshape(count.shape + (qmax // 2,))
+
+
+def append(q_pre_bits: np.ndarray, q_post_bits, t: int, theta: float, qbuf_bits: np.ndarray, count: np.ndarray,
+           q_recent_bits: np.ndarray, dtype: str, threads: int = 0):
+    """One decode step's append (see oracle_append) on copies; returns (qbuf, count, q_recent, picks,
+    error). Arrays hold storage bits (uint16 for bf16), flattened over query heads in front:
+    q_pre [nq, D], q_post [nq, D] or None, qbuf [nq, qmax, D], count [nq], q_recent [nq, n_r, D]."""
+    if threads:
+        set_threads(threads)
+    qb = np.ascontiguousarray(qbuf_bits).copy()
+    cnt = np.ascontiguousarray(count, dtype=np.int32).copy()
+    qr = np.ascontiguousarray(q_recent_bits).copy()
+    qp = np.ascontiguousarray(q_pre_bits)
+    qo = None if q_post_bits is None else np.ascontiguousarray(q_post_bits)
+    nq, qmax, D = qb.shape[0], qb.shape[1], qb.shape[2]
+    n_r = qr.shape[1]
+    picks = np.full((nq, qmax // 2), -1, np.int32)
+    err = np.zeros(nq, np.int32)
+    rc = lib().oracle_append(0 if dtype == "bf16" else 1, nq, D, _ptr(qp), _ptr(qo), int(t), float(theta), _ptr(qb),
+                             qmax, _ptr(cnt), _ptr(qr), n_r, _ptr(picks), _ptr(err))
+    if rc < 0:
+        raise ValueError("oracle_append: bad sizes")
+    return qb, cnt, qr, picks, err
