@@ -183,6 +183,48 @@ def algorithmic_bytes(inp, kept_idx, kept_len):
     return k_read, moved * 4 * row, moved
 
 
+def append_timing(inp, dev, stream, cycles: int = 3):
+    """Per-decode-step kvc_append over every query head of the workload (the step that feeds the
+    eviction's observation state), on copies of its buffers: `cycles` fill/compress cycles, one call
+    per step, each bracketed by CUDA events. Calls that fill the buffers (and so run FPS) are
+    reported apart from plain appends; their bytes are the rows read and written."""
+    import torch
+    from decoding_kv_cache_gb300 import kvc
+    qb, cnt, ring = inp.qbuf.clone(), inp.count.clone(), inp.q_recent.clone()
+    nq = inp.L * inp.B * inp.Hq
+    g = torch.Generator(device=dev).manual_seed(1234)
+    pool = [torch.randn((inp.L, inp.B, inp.Hq, inp.D), generator=g, device=dev).to(inp.K.dtype) for _ in range(8)]
+    m = inp.qmax // 2
+    cnt.fill_(m)
+    steps = cycles * m
+    evs, fills = [], []
+    t0 = inp.t + 1
+    # keep the GPU busy while the calls are queued, so that each pair of events brackets the
+    # kernel and not the host's launch overhead
+    torch.cuda._sleep(100_000_000)
+    for i in range(steps + m):  # the first cycle is warm-up
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        kvc.kvc_append(pool[i % 8], qb, cnt, ring, t0 + i, inp.theta)
+        b.record(stream)
+        if i >= m:
+            evs.append((a, b))
+            fills.append((i + 1) % m == 0)  # count goes m .. qmax-1, then this call fills and compresses
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    plain = [x for x, f in zip(ms, fills) if not f]
+    comp = [x for x, f in zip(ms, fills) if f]
+    es = 2 if inp.dtype == "bf16" else 4
+    row = inp.D * es
+    b_plain = nq * (3 * row + 8)                      # q_pre read, buffer row and ring row written, count
+    b_comp = b_plain + nq * (inp.qmax - 1 + m) * row  # + the buffer staged and the survivors written back
+    return {"query_heads": nq, "calls": len(ms), "us_plain": 1e3 * statistics.median(plain),
+            "us_compress": 1e3 * statistics.median(comp), "bytes_plain": b_plain, "bytes_compress_max": b_comp,
+            "gbs_plain": b_plain / (statistics.median(plain) / 1e3) / 1e9,
+            "note": "one kvc_append per decode step (ring row by rotation), calls queued behind a GPU sleep; "
+                    "bound: latency (one dependent HBM round trip; FPS on filling calls)"}
+
+
 def gpu_arm(args, rank, world, local_rank):
     import torch
     from decoding_kv_cache_gb300 import build as kbuild
@@ -308,6 +350,8 @@ def gpu_arm(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ee) / n_e2e, world)
 
+    app = append_timing(inp, dev, stream)
+
     pk, pk_kind = peaks()
     hbm = float(pk["hbm_gbs"])
     dom_ms = phase_ms[dom]
@@ -330,6 +374,7 @@ def gpu_arm(args, rank, world, local_rank):
         "phases_ms": phase_ms,
         "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "append": app,
         "gpu_launches": args.steps * kvc.kvc_evict_launch_count(cache, inp.n_r, inp.n_b),
         "clocks": clk,
     }

@@ -85,6 +85,16 @@ namespace {
 std::atomic<int> g_debug_fault{0};  // test-only fault switch, read at each scoring launch
 }
 
+// Rotary angles of step t in fp64 (BeaconKV write-up, "打分时的 RoPE 对齐": beacons are turned
+// to position t): pair (i, i + D/2) turns by t * theta^(-2i/D); cos and sin rounded to fp32.
+void rope_table(float2 (&rope)[64], int D, int64_t t, double theta) {
+  for (int i = 0; i < D / 2; ++i) {
+    const double ang = (double)t * pow(theta, -2.0 * (double)i / (double)D);
+    rope[i] = make_float2((float)cos(ang), (float)sin(ang));
+  }
+  for (int i = D / 2; i < 64; ++i) rope[i] = make_float2(0.f, 0.f);
+}
+
 void fill_score_args(ScoreArgs* a, const CacheGeom& g, int dtype, const LayerPtrs& K, const void* q_recent, int n_r,
                      const void* qbuf, const int32_t* count, int qmax, int n_b, int64_t t, double theta,
                      float* scores, int32_t* beacon_picks, int32_t* status, const Opts& o, float* entropy) {
@@ -112,13 +122,7 @@ void fill_score_args(ScoreArgs* a, const CacheGeom& g, int dtype, const LayerPtr
   a->M = obs_rows_used(g.Hq / g.Hkv, n_r, n_b, o.ext);
   a->M_pad = obs_rows(a->M, dtype);
   a->M_n = (a->M + 15) / 16 * 16;
-  // Rotary angles of the current step in fp64 (BeaconKV write-up, "打分时的 RoPE 对齐":
-  // beacons are turned to position t): pair (i, i + D/2) turns by t * theta^(-2i/D).
-  for (int i = 0; i < g.D / 2; ++i) {
-    const double ang = (double)t * pow(theta, -2.0 * (double)i / (double)g.D);
-    a->rope[i] = make_float2((float)cos(ang), (float)sin(ang));
-  }
-  for (int i = g.D / 2; i < 64; ++i) a->rope[i] = make_float2(0.f, 0.f);
+  rope_table(a->rope, g.D, t, theta);
   a->nchunk = (g.N + kChunk - 1) / kChunk;
 }
 
@@ -185,6 +189,40 @@ int kvc_fps_update(int32_t dtype, int32_t L, int32_t B, int32_t Hq, int32_t D, v
   if (nq > (1LL << 30)) return KVC_ERR_TOO_LARGE;
   if (!aligned16(qbuf)) return KVC_ERR_ALIGNMENT;
   return launch_fps_update(dtype, (int)nq, D, qbuf, qmax, count, picks, status, static_cast<cudaStream_t>(stream));
+}
+
+int kvc_append(int32_t dtype, int32_t L, int32_t B, int32_t Hq, int32_t D, const void* q_pre, const void* q_post,
+               int64_t t, double rope_theta, void* qbuf, int32_t qmax, int32_t* count, void* q_recent, int32_t n_r,
+               int32_t* picks, int32_t* status, void* stream) {
+  int rc = check_dtype_dim(dtype, D);
+  if (rc) return rc;
+  if (L < 1 || B < 1 || Hq < 1 || !q_pre || !qbuf || !count || qmax < 2 || qmax > kMaxQmax || n_r < 0 ||
+      n_r > 64 || t < 0)
+    return KVC_ERR_INVALID_ARG;
+  if (qmax % 2) return KVC_ERR_NOT_DIVISIBLE;
+  if (n_r > 0 && !q_recent) return KVC_ERR_INVALID_ARG;
+  if (n_r > 0 && !q_post && (!(rope_theta > 1.0) || !isfinite(rope_theta))) return KVC_ERR_INVALID_ARG;
+  const long long nq = (long long)L * B * Hq;
+  if (nq > (1LL << 30)) return KVC_ERR_TOO_LARGE;
+  if (!aligned16(q_pre) || !aligned16(qbuf) || (q_post && !aligned16(q_post)) || (q_recent && !aligned16(q_recent)))
+    return KVC_ERR_ALIGNMENT;
+  AppendArgs a;
+  a.q_pre = q_pre;
+  a.q_post = q_post;
+  a.qbuf = qbuf;
+  a.count = count;
+  a.q_recent = n_r > 0 ? q_recent : nullptr;
+  a.picks = picks;
+  a.status = status;
+  a.nheads = (int)nq;
+  a.qmax = qmax;
+  a.n_r = n_r;
+  a.ring_slot = n_r > 0 ? (int)(t % n_r) : 0;
+  if (n_r > 0 && !q_post)
+    rope_table(a.rope, D, t, rope_theta);
+  else
+    for (int i = 0; i < 64; ++i) a.rope[i] = make_float2(0.f, 0.f);
+  return launch_append(a, dtype, D, static_cast<cudaStream_t>(stream));
 }
 
 size_t kvc_score_workspace_size(const kvc_cache* c, int32_t n_r, int32_t n_b) {

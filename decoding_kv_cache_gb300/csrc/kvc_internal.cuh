@@ -88,6 +88,20 @@ struct CacheGeom {
 
 // ---- launchers (host) ---------------------------------------------------------
 // Each returns KVC_OK or KVC_ERR_LAUNCH; arguments are already validated.
+struct AppendArgs {         // kvc_append, flattened over query heads
+  const void* q_pre;        // [nheads][D] pre-RoPE query of this step
+  const void* q_post;       // [nheads][D] post-RoPE query, or null (then q_pre is turned to t)
+  void* qbuf;               // [nheads][qmax][D]
+  int32_t* count;           // [nheads]
+  void* q_recent;           // [nheads][n_r][D] ring
+  int32_t* picks;           // [nheads][qmax/2] or null
+  int32_t* status;
+  int nheads, qmax, n_r;
+  int ring_slot;            // t mod n_r
+  float2 rope[64];          // (cos, sin) of t * theta^(-2i/D), i < D/2, from fp64 (when q_post is null)
+};
+int launch_append(const AppendArgs& a, int dtype, int D, cudaStream_t s);
+
 int launch_fps_update(int dtype, int nheads_q, int D, void* qbuf, int qmax, int32_t* count, int32_t* picks,
                       int32_t* status, cudaStream_t s);
 

@@ -21,8 +21,8 @@ KVC_MAX_LAYERS = 128
 
 EXPORTED = ("kvc_fps_update", "kvc_score_workspace_size", "kvc_score", "kvc_select", "kvc_compact",
             "kvc_evict_workspace_size", "kvc_evict", "kvc_evict_launch_count", "kvc_strerror", "kvc_abi_version",
-            "kvc_score_static", "kvc_debug_fault", "kvc_head_budget")
-KVC_ABI_VERSION = 2
+            "kvc_score_static", "kvc_debug_fault", "kvc_head_budget", "kvc_append")
+KVC_ABI_VERSION = 3
 KVC_AGG_MAX, KVC_AGG_MEAN, KVC_AGG_SUM = 0, 1, 2
 KVC_BUDGET_GIVEN, KVC_BUDGET_ENTROPY = 0, 1
 ROW_AGG = {"max": KVC_AGG_MAX, "mean": KVC_AGG_MEAN}
@@ -65,6 +65,7 @@ def lib():
     po = C.POINTER(kvc_opts)
     sig = {
         "kvc_fps_update": (C.c_int, [i32, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp]),
+        "kvc_append": (C.c_int, [i32, i32, i32, i32, i32, vp, vp, i64, dbl, vp, i32, vp, vp, i32, vp, vp, vp]),
         "kvc_score_workspace_size": (sz, [pc, i32, i32]),
         "kvc_score": (C.c_int, [pc, vp, i32, vp, vp, i32, i32, i64, dbl, vp, vp, po, vp, sz, vp]),
         "kvc_select": (C.c_int, [vp, i32, i32, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp]),
@@ -153,6 +154,24 @@ def kvc_fps_update(qbuf: torch.Tensor, count: torch.Tensor, picks: Optional[torc
     nq = qbuf.numel() // (qmax * D)
     _check(lib().kvc_fps_update(_dtype_code(qbuf), 1, 1, nq, D, _p(qbuf), qmax, _p(count), _p(picks), _p(status),
                                 _stream(stream)))
+
+
+def kvc_append(q_pre: torch.Tensor, qbuf: torch.Tensor, count: torch.Tensor, q_recent: Optional[torch.Tensor],
+               t: int, rope_theta: float = 1e4, q_post: Optional[torch.Tensor] = None,
+               picks: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None, stream=None):
+    """One decode step's queries into the observation state (see kvc.h): ``q_pre`` [..., D] joins
+    each head's [..., qmax, D] buffer (compressed when full), and ``q_post`` (or ``q_pre`` turned to
+    ``t``) joins ring row ``t mod n_r`` of ``q_recent`` [..., n_r, D] (None or n_r = 0: no ring)."""
+    qmax, D = qbuf.shape[-2], qbuf.shape[-1]
+    nq = qbuf.numel() // (qmax * D)
+    if q_pre.numel() != nq * D or (q_post is not None and q_post.numel() != nq * D):
+        raise ValueError("q_pre / q_post need one [D] row per buffer")
+    n_r = 0 if q_recent is None else q_recent.shape[-2]
+    if q_recent is not None and q_recent.numel() != nq * n_r * D:
+        raise ValueError("q_recent needs one [n_r, D] ring per buffer")
+    _check(lib().kvc_append(_dtype_code(qbuf), 1, 1, nq, D, _p(q_pre), _p(q_post), int(t), float(rope_theta),
+                            _p(qbuf), qmax, _p(count), _p(q_recent) if n_r else None, n_r, _p(picks), _p(status),
+                            _stream(stream)))
 
 
 def kvc_score_workspace_size(cache: Cache, n_r: int, n_b: int) -> int:

@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 2
+#define KVC_ABI_VERSION 3
 #define KVC_MAX_LAYERS 128
 
 #if defined(__GNUC__)
@@ -145,6 +145,44 @@ typedef struct {
  */
 KVC_API int kvc_fps_update(int32_t dtype, int32_t L, int32_t B, int32_t Hq, int32_t D, void* qbuf, int32_t qmax,
                    int32_t* count, int32_t* picks, int32_t* status, void* stream);
+
+/*
+ * kvc_append -- one decode step's queries into the observation state.
+ * BeaconKV write-up, "Continual FPS：有界内存的在线最远点采样": each head's buffer of
+ * pre-RoPE queries grows to B_Q^max and is cut back to B_Q^min by farthest-point
+ * sampling; "观察 query 集 = 最近查询 + 信标查询": the recent observation queries are
+ * the latest n_r queries at their own positions.
+ *
+ * For every query head, in this order:
+ *   - ring: row t mod n_r of q_recent receives q_post, or, when q_post is NULL, q_pre
+ *     turned to position t exactly as kvc_score turns beacons (rotate-half pairs,
+ *     angle t * theta^(-2i/D) from fp64, cos/sin rounded to fp32, each product and
+ *     the sum rounded to fp32, the result rounded to the storage type);
+ *   - a buffer found full (count == qmax) is compressed as kvc_fps_update does
+ *     (qmax/2 survivors in time order, count = qmax/2);
+ *   - q_pre is written to buffer row count and count grows by one;
+ *   - a buffer that has just become full is compressed the same way.
+ * Rows at or past the new count are left as those writes leave them. A count < 0
+ * or > qmax sets KVC_STATUS_COUNT_RANGE and leaves that head's buffer and count
+ * (its ring row is still written). A decode loop calls this once per step and
+ * kvc_evict (or kvc_score) with the same qbuf, count and q_recent when the cache
+ * reaches B_max.
+ *
+ *   dtype        kvc_dtype of every query array
+ *   L, B, Hq, D  sizes; query heads are flat in (l, b, hq) order
+ *   q_pre        [L,B,Hq,D] this step's pre-RoPE queries (device, read)
+ *   q_post       [L,B,Hq,D] this step's post-RoPE queries (device, read) or NULL
+ *   t            this step's position (>= 0); rope_theta the rotary base (> 1; read
+ *                only when q_post is NULL and n_r > 0)
+ *   qbuf, count  [L,B,Hq,qmax,D] and [L,B,Hq] int32 (device, in/out); qmax even, 2..64
+ *   q_recent     [L,B,Hq,n_r,D] ring (device, in/out); n_r in 0..64 (0: no ring, may be NULL)
+ *   picks        [L,B,Hq,qmax/2] int32 (device, out) or NULL: the old rows of this
+ *                call's last compression per head, ascending; -1 rows where none ran
+ *   status       device int32 or NULL
+ */
+KVC_API int kvc_append(int32_t dtype, int32_t L, int32_t B, int32_t Hq, int32_t D, const void* q_pre,
+                       const void* q_post, int64_t t, double rope_theta, void* qbuf, int32_t qmax, int32_t* count,
+                       void* q_recent, int32_t n_r, int32_t* picks, int32_t* status, void* stream);
 
 /*
  * kvc_score -- importance of every cached key from the observation queries.

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
     exported = set(re.findall(r"\bT (kvc_\w+)", out))
     assert set(_declared()) <= exported
     assert set(kvc.EXPORTED) == set(_declared())
-    assert lib.kvc_abi_version() == kvc.KVC_ABI_VERSION == 2
+    assert lib.kvc_abi_version() == kvc.KVC_ABI_VERSION == 3
 
 
 def test_header_compiles_as_c():
@@ -144,3 +144,21 @@ def test_select_and_fps_reject_bad_args(lib):
     assert lib.kvc_fps_update(0, 1, 1, 4, 100, 0x1000, 32, 0x1000, None, None, None) == -3
     assert lib.kvc_fps_update(3, 1, 1, 4, 128, 0x1000, 32, 0x1000, None, None, None) == -2
     assert lib.kvc_fps_update(0, 1, 1, 4, 128, 0x1008, 32, 0x1000, None, None, None) == -8
+
+
+def test_append_rejects_bad_args(lib):
+    call = lambda **kw: lib.kvc_append(
+        kw.get("dtype", 0), 1, 1, 4, kw.get("D", 128), kw.get("q_pre", 0x1000), kw.get("q_post", None),
+        kw.get("t", 5), kw.get("theta", 1e6), kw.get("qbuf", 0x1000), kw.get("qmax", 32), kw.get("count", 0x1000),
+        kw.get("ring", 0x1000), kw.get("n_r", 16), None, None, None)
+    assert call(qmax=31) == -5               # odd buffer
+    assert call(qmax=66) == -1               # larger than supported
+    assert call(D=100) == -3
+    assert call(dtype=3) == -2
+    assert call(q_pre=0x1008) == -8          # misaligned
+    assert call(q_post=0x1004) == -8
+    assert call(ring=None) == -1             # a ring is needed when n_r > 0
+    assert call(theta=1.0) == -1             # rotation needs a base > 1 without q_post
+    assert call(t=-1) == -1
+    assert call(count=None) == -1
+    assert call(n_r=65) == -1
