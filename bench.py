@@ -183,11 +183,12 @@ def algorithmic_bytes(inp, kept_idx, kept_len):
     return k_read, moved * 4 * row, moved
 
 
-def append_timing(inp, dev, stream, cycles: int = 3):
+def append_timing(inp, dev, stream, reps: int = 20):
     """Per-decode-step kvc_append over every query head of the workload (the step that feeds the
-    eviction's observation state), on copies of its buffers: `cycles` fill/compress cycles, one call
-    per step, each bracketed by CUDA events. Calls that fill the buffers (and so run FPS) are
-    reported apart from plain appends; their bytes are the rows read and written."""
+    eviction's observation state), on copies of its buffers. One fill/compress cycle is captured as
+    two CUDA graphs: the qmax/2 - 1 calls that only append, and the call that fills the buffers and
+    compresses them; the graphs are replayed alternately with CUDA events around each replay, so
+    the times are the GPU's (kernel plus inter-kernel latency), not the host's launch overhead."""
     import torch
     from decoding_kv_cache_gb300 import kvc
     qb, cnt, ring = inp.qbuf.clone(), inp.count.clone(), inp.q_recent.clone()
@@ -195,34 +196,47 @@ def append_timing(inp, dev, stream, cycles: int = 3):
     g = torch.Generator(device=dev).manual_seed(1234)
     pool = [torch.randn((inp.L, inp.B, inp.Hq, inp.D), generator=g, device=dev).to(inp.K.dtype) for _ in range(8)]
     m = inp.qmax // 2
-    cnt.fill_(m)
-    steps = cycles * m
-    evs, fills = [], []
-    t0 = inp.t + 1
-    # keep the GPU busy while the calls are queued, so that each pair of events brackets the
-    # kernel and not the host's launch overhead
-    torch.cuda._sleep(100_000_000)
-    for i in range(steps + m):  # the first cycle is warm-up
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        kvc.kvc_append(pool[i % 8], qb, cnt, ring, t0 + i, inp.theta)
-        b.record(stream)
-        if i >= m:
-            evs.append((a, b))
-            fills.append((i + 1) % m == 0)  # count goes m .. qmax-1, then this call fills and compresses
-    torch.cuda.synchronize()
-    ms = [a.elapsed_time(b) for a, b in evs]
-    plain = [x for x, f in zip(ms, fills) if not f]
-    comp = [x for x, f in zip(ms, fills) if f]
+    cs = torch.cuda.Stream(device=dev)
+    cs.wait_stream(stream)
+    res = {}
+    for post in (False, True):  # ring row by rotation, then from a given post-RoPE query
+        kw = lambda i: dict(q_post=pool[(i + 3) % 8] if post else None)
+        with torch.cuda.stream(cs):
+            cnt.fill_(m)
+            for i in range(m):  # warm-up: one cycle outside the graphs
+                kvc.kvc_append(pool[i % 8], qb, cnt, ring, inp.t + 1 + i, inp.theta, **kw(i))
+            ga, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(ga, stream=cs):
+                for i in range(m - 1):
+                    kvc.kvc_append(pool[i % 8], qb, cnt, ring, inp.t + 1 + i, inp.theta, **kw(i))
+            with torch.cuda.graph(gb, stream=cs):
+                kvc.kvc_append(pool[(m - 1) % 8], qb, cnt, ring, inp.t + m, inp.theta, **kw(m - 1))
+            ev = []
+            for r in range(reps + 2):
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record(cs)
+                ga.replay()
+                e[1].record(cs)
+                gb.replay()
+                e[2].record(cs)
+                if r >= 2:
+                    ev.append(e)
+        torch.cuda.synchronize()
+        plain = statistics.median(e[0].elapsed_time(e[1]) for e in ev) / (m - 1)
+        comp = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+        res["post_given" if post else "rotated"] = (plain, comp, (plain * (m - 1) + comp) / m)
+        del ga, gb
+    stream.wait_stream(cs)
     es = 2 if inp.dtype == "bf16" else 4
     row = inp.D * es
     b_plain = nq * (3 * row + 8)                      # q_pre read, buffer row and ring row written, count
     b_comp = b_plain + nq * (inp.qmax - 1 + m) * row  # + the buffer staged and the survivors written back
-    return {"query_heads": nq, "calls": len(ms), "us_plain": 1e3 * statistics.median(plain),
-            "us_compress": 1e3 * statistics.median(comp), "bytes_plain": b_plain, "bytes_compress_max": b_comp,
-            "gbs_plain": b_plain / (statistics.median(plain) / 1e3) / 1e9,
-            "note": "one kvc_append per decode step (ring row by rotation), calls queued behind a GPU sleep; "
-                    "bound: latency (one dependent HBM round trip; FPS on filling calls)"}
+    pr, cr, avg = res["rotated"]
+    return {"query_heads": nq, "replays": reps, "us_plain": 1e3 * pr, "us_compress": 1e3 * cr,
+            "us_per_step_avg": 1e3 * avg, "us_plain_post_given": 1e3 * res["post_given"][0],
+            "bytes_plain": b_plain, "bytes_compress_max": b_comp, "gbs_plain": b_plain / (pr / 1e3) / 1e9,
+            "note": "kvc_append per decode step, CUDA-graph replays of one fill/compress cycle; ring row by "
+                    "rotation unless post_given; bound: latency"}
 
 
 def gpu_arm(args, rank, world, local_rank):

@@ -157,10 +157,12 @@ int kvc_head_budget(const float* entropy, int32_t L, int32_t B, int32_t Hkv, int
 }
 
 int kvc_evict_launch_count(const kvc_cache* c, int32_t n_r, int32_t n_b) {
-  (void)n_r;
-  (void)n_b;
-  if (c && c->dtype == KVC_BF16) return 4;  // observation rows, fused scoring, select, compact
-  return 6;                                  // observation rows, pass 1, combine, pass 2, select, compact
+  CacheGeom g;
+  LayerPtrs K, V;
+  if (!c || n_r < 0 || n_b < 0) return 0;
+  kvc_cache probe = *c;
+  if (check_cache(&probe, &g, &K, &V)) return 0;
+  return score_launches(g, c->dtype, n_r, n_b, false) + 2;  // + select, compact
 }
 
 const char* kvc_strerror(int code) {

@@ -56,6 +56,14 @@ __global__ void append_kernel(AppendArgs a) {
       hi.y = __shfl_sync(kFull, vpre.y, from);
       hi.z = __shfl_sync(kFull, vpre.z, from);
       hi.w = __shfl_sync(kFull, vpre.w, from);
+      // this lane's (cos, sin) pairs, read with warp-uniform indices (a per-lane index into the
+      // parameter block would serialise the warp's constant loads)
+      float2 cs[per];
+#pragma unroll
+      for (int i = 0; i < hd; ++i) {
+        const float2 v = a.rope[i];
+        if (lane == i / per) cs[i % per] = v;
+      }
       if (lane < hd / per) {
         const T* lo_e = reinterpret_cast<const T*>(&vpre);
         const T* hi_e = reinterpret_cast<const T*>(&hi);
@@ -63,11 +71,10 @@ __global__ void append_kernel(AppendArgs a) {
         alignas(16) T o2[per];
 #pragma unroll
         for (int u = 0; u < per; ++u) {
-          const float2 cs = a.rope[lane * per + u];
           const float x0 = to_f32(lo_e[u]), x1 = to_f32(hi_e[u]);
           // each product and the sum rounded on its own (no fused multiply-add), as for beacons
-          o1[u] = from_f32<T>(__fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y)));
-          o2[u] = from_f32<T>(__fadd_rn(__fmul_rn(x1, cs.x), __fmul_rn(x0, cs.y)));
+          o1[u] = from_f32<T>(__fsub_rn(__fmul_rn(x0, cs[u].x), __fmul_rn(x1, cs[u].y)));
+          o2[u] = from_f32<T>(__fadd_rn(__fmul_rn(x1, cs[u].x), __fmul_rn(x0, cs[u].y)));
         }
         reinterpret_cast<uint4*>(dst)[lane] = *reinterpret_cast<const uint4*>(o1);
         reinterpret_cast<uint4*>(dst)[lane + vpr / 2] = *reinterpret_cast<const uint4*>(o2);

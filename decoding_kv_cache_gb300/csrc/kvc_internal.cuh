@@ -113,6 +113,7 @@ struct ScoreWs {            // carved out of the caller's workspace
   float* rw;                // [heads][M_pad] row weight of a mean over the query head's rows (0: no row)
   float* escale;            // [heads] 1 / (valid rows * log2 N): entropy in bits -> normalised mean
   float* ent;               // [heads] entropy accumulator when the caller keeps none (kvc_evict)
+  float* lse2p;             // bf16 two-pass streaming kernel: [heads][ranges][M_pad] log2-sum-exp2 per key range
 };
 
 struct ScoreArgs {
@@ -167,6 +168,21 @@ struct FusedPlan {
 bool score_resident_plan(const ScoreArgs& a, FusedPlan* p, size_t* smem);
 long long score_resident_words(const FusedPlan& p, bool entropy);
 int launch_score_resident(const ScoreArgs& a, const ScoreWs& ws, const FusedPlan& p, size_t smem, cudaStream_t s);
+
+// Two-pass streaming kernel (bf16, max/max, 128- or 256-row tiles): every (head, key range) is an
+// independent work item of both passes; a combine kernel between them forms lse2.
+struct SplitPlan {
+  int rk;      // 128-key chunks per range
+  int R;       // ranges per head
+  int items;   // heads * R
+  int grid;    // CTAs (one per SM)
+  int stages;  // K ring depth
+};
+int split_ranges(int nchunk, int M_pad);
+bool score_split_plan(const ScoreArgs& a, SplitPlan* p, size_t* smem);
+int launch_score_split(const ScoreArgs& a, const ScoreWs& ws, const SplitPlan& p, size_t smem, cudaStream_t s);
+// kernels launch_score starts for these arguments (host only; default options when !ext)
+int score_launches(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext);
 
 // entropy non-null: each (layer, sequence)'s budgets are reallocated over its Hkv heads first
 int launch_select(const float* scores, int heads, int N, int P, int R, const int32_t* budget, int budget_all,

@@ -20,6 +20,9 @@
 //     combine    per head: merge the partials into lse2 per row
 //     pass2      per (key chunk, head): max over rows of s*log2(e)/sqrt(D) - lse2, exp2
 // Softmax is kept in base 2 throughout: exp(s/sqrt(D) - lse) = exp2(s*c2 - lse2).
+#include <stdlib.h>
+#include <string.h>
+
 #include "fps_warp.cuh"
 #include "kvc_internal.cuh"
 
@@ -329,6 +332,9 @@ size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext,
   const size_t o_rw = off;    off += ext ? align256(heads * M_pad * sizeof(float)) : 0;
   const size_t o_esc = off;   off += ext ? align256(heads * sizeof(float)) : 0;
   const size_t o_ent = off;   off += ext ? align256(heads * sizeof(float)) : 0;
+  // the two-pass streaming kernel's per-range partials (bf16, default options only)
+  const size_t o_l2p = off;
+  if (dtype == KVC_BF16 && !ext) off += align256(heads * (size_t)split_ranges((int)nchunk, (int)M_pad) * M_pad * sizeof(float));
   if (carve) {
     char* b = static_cast<char*>(base);
     carve->obs = b + o_obs;
@@ -338,6 +344,7 @@ size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext,
     carve->rw = ext ? reinterpret_cast<float*>(b + o_rw) : nullptr;
     carve->escale = ext ? reinterpret_cast<float*>(b + o_esc) : nullptr;
     carve->ent = ext ? reinterpret_cast<float*>(b + o_ent) : nullptr;
+    carve->lse2p = (dtype == KVC_BF16 && !ext) ? reinterpret_cast<float*>(b + o_l2p) : nullptr;
   }
   return off;
 }
@@ -347,24 +354,77 @@ static bool set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess;
 }
 
+// KVC_SCORE_PATH (a test and profiling aid; unset in normal use) forces the bf16 scoring kernel:
+// "resident" (single read; falls through where it does not apply), "split" (two-pass streaming;
+// default options only) or "fused" (two-pass with group exchange). 0 = automatic choice.
+static int score_path_override() {
+  const char* v = getenv("KVC_SCORE_PATH");
+  if (!v || !*v) return 0;
+  if (!strcmp(v, "resident")) return 1;
+  if (!strcmp(v, "split")) return 2;
+  if (!strcmp(v, "fused")) return 3;
+  return 0;
+}
+
+// Which bf16 scoring kernel runs (sets a->tiles); 0 = fp32 passes.
+enum ScorePath { kPathF32 = 0, kPathResident = 1, kPathSplit = 2, kPathFused = 3 };
+static ScorePath choose_score(ScoreArgs* a, FusedPlan* rp, size_t* rsmem, SplitPlan* sp, size_t* ssmem) {
+  a->tiles = 1;
+  if (a->dtype != KVC_BF16) return kPathF32;
+  // A 256-row observation tile goes to the single-read kernel as two 128-row tiles when no query
+  // head's rows cross the tile boundary (or the aggregation is max over everything, where heads do
+  // not matter).
+  if (a->M_pad == 2 * 128) {
+    bool straddle = false;
+    const int per_q = a->n_r + a->n_b, G = a->g.Hq / a->g.Hkv;
+    if (a->row_agg != KVC_AGG_MAX || a->group_agg != KVC_AGG_MAX)
+      for (int g = 0; g < G; ++g) straddle |= (g * a->qstride) / 128 != (g * a->qstride + per_q - 1) / 128;
+    if (!straddle) a->tiles = 2;
+  }
+  bool resident = score_resident_plan(*a, rp, rsmem);
+  // The two-pass streaming kernel takes over where the single-read kernel's per-round meetings
+  // would involve many CTAs (more than 16 per head, i.e. more than 4096 keys) or two row tiles.
+  bool split = score_split_plan(*a, sp, ssmem);
+  const int path = score_path_override();
+  if (split && path == 0) split = !resident || a->M_pad > 128 || rp->group_size > 16;
+  if (split && path != 0) split = path == 2;
+  if (resident && path == 3) resident = false;
+  if (split) resident = false;
+  if (!resident) a->tiles = 1;
+  return resident ? kPathResident : (split ? kPathSplit : kPathFused);
+}
+
+int score_launches(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext) {
+  ScoreArgs a;
+  memset(&a, 0, sizeof(a));
+  a.g = g;
+  a.dtype = dtype;
+  a.n_r = n_r;
+  a.n_b = n_b;
+  a.ext = ext ? 1 : 0;
+  a.qstride = obs_qstride(n_r, n_b, ext);
+  a.M = obs_rows_used(g.Hq / g.Hkv, n_r, n_b, ext);
+  a.M_pad = obs_rows(a.M, dtype);
+  a.nchunk = (g.N + kChunk - 1) / kChunk;
+  FusedPlan rp;
+  SplitPlan sp;
+  size_t r1 = 0, r2 = 0;
+  switch (choose_score(&a, &rp, &r1, &sp, &r2)) {
+    case kPathF32: return 4;    // observation rows, pass 1, combine, pass 2
+    case kPathSplit: return 4;  // observation rows, pass 1, combine, pass 2
+    default: return 2;          // observation rows, one scoring kernel
+  }
+}
+
 int launch_score(const ScoreArgs& a_in, const ScoreWs& ws, cudaStream_t s) {
   ScoreArgs a = a_in;
   const int heads = a.g.L * a.g.B * a.g.Hkv;
   // the single-read kernel's plan is fixed first: the observation kernel zeroes its exchange words.
-  // A 256-row observation tile goes to it as two 128-row tiles when no query head's rows cross the
-  // tile boundary (or the aggregation is max over everything, where heads do not matter).
   FusedPlan rp;
-  size_t rsmem = 0;
-  a.tiles = 1;
-  if (a.dtype == KVC_BF16 && a.M_pad == 2 * 128) {
-    bool straddle = false;
-    const int per_q = a.n_r + a.n_b, G = a.g.Hq / a.g.Hkv;
-    if (a.row_agg != KVC_AGG_MAX || a.group_agg != KVC_AGG_MAX)
-      for (int g = 0; g < G; ++g) straddle |= (g * a.qstride) / 128 != (g * a.qstride + per_q - 1) / 128;
-    if (!straddle) a.tiles = 2;
-  }
-  bool resident = a.dtype == KVC_BF16 && score_resident_plan(a, &rp, &rsmem);
-  if (!resident) a.tiles = 1;
+  SplitPlan sp;
+  size_t rsmem = 0, ssmem = 0;
+  const ScorePath path = choose_score(&a, &rp, &rsmem, &sp, &ssmem);
+  const bool resident = path == kPathResident, split = path == kPathSplit;
   a.xch_zero = resident ? reinterpret_cast<unsigned long long*>(ws.part) : nullptr;
   a.xch_zero_words = resident ? score_resident_words(rp, a.entropy != nullptr) : 0;
   const int D = a.g.D;
@@ -397,6 +457,7 @@ int launch_score(const ScoreArgs& a_in, const ScoreWs& ws, cudaStream_t s) {
   const dim3 grid(a.nchunk, heads);
   if (a.dtype == KVC_BF16) {
     if (resident) return launch_score_resident(a, ws, rp, rsmem, s);
+    if (split) return launch_score_split(a, ws, sp, ssmem, s);
     return launch_score_fused(a, ws, ws.part, s);
   } else {
     const size_t sm1 = sizeof(float) * ((size_t)a.M_pad * (D + 1) + (size_t)kChunk * D);

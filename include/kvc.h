@@ -332,8 +332,9 @@ KVC_API int kvc_head_budget(const float* entropy, int32_t L, int32_t B, int32_t 
                             int32_t recent, const int32_t* budget, int32_t budget_all, int32_t* budget_out,
                             int32_t* status, void* stream);
 
-/* Number of kernels one kvc_evict call with these arguments launches (host only;
- * for accounting, e.g. counting launches inside a timed region). */
+/* Number of kernels one kvc_evict call with these arguments and default options
+ * launches (host only; for accounting, e.g. counting launches inside a timed region;
+ * it queries the current device's SM count and shared memory). 0 for a bad cache. */
 KVC_API int kvc_evict_launch_count(const kvc_cache* c, int32_t n_r, int32_t n_b);
 
 /* Human-readable text for a KVC_ERR_* code (static storage). */

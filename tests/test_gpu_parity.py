@@ -192,3 +192,30 @@ def test_compact_rejects_malformed_lists():
     for h in (0, 1, 2):
         assert torch.equal(K[0, 0, h], inp.K[0, 0, h])
     assert torch.equal(K[0, 0, 3, :200], inp.K[0, 0, 3, 56:256])
+
+
+PATH_CASES = [
+    ("qwen7b-reasonalloc", dict(L=1, B=1, N=5000)),   # 224 rows: two row tiles
+    ("qwen3-14b-long", dict(L=1, B=1, N=2100)),       # 240 rows, ragged last range
+    ("qwen3-4b", dict(L=2, N=1000)),                  # 128 rows
+    ("qwen3-4b", dict(L=1, N=129, D=64)),             # D 64, one key past a chunk
+    ("llama8b-planted", dict(L=1, B=2, N=4500)),      # 128 rows, several ranges
+]
+
+
+@pytest.mark.parametrize("path", ["resident", "split", "fused"])
+@pytest.mark.parametrize("name,over", PATH_CASES, ids=[_ids(c) for c in PATH_CASES])
+def test_each_scoring_kernel_matches_oracle(monkeypatch, path, name, over):
+    """Every bf16 scoring kernel (single-read, two-pass streaming, two-pass with group exchange),
+    forced through KVC_SCORE_PATH, against the oracle on the same inputs."""
+    monkeypatch.setenv("KVC_SCORE_PATH", path)
+    inp = make_inputs(name, **over)
+    gpu = run_evict(inp, DEV)
+    _, gpu_picks = run_score(inp, DEV)
+    ora = O.evict(inp)
+    if check_beacon_picks(inp, gpu_picks, ora["beacon_picks"]):
+        ora = O.evict(inp, forced_picks=gpu_picks)
+    assert gpu["status"] == 0
+    assert_scores_close(gpu["scores"], ora["scores"], f"{name} via {path}")
+    check_kept(inp, gpu, ora, gpu["scores"])
+    check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
