@@ -13,7 +13,10 @@
 // non-decreasing).
 //
 // One warp per (head, K-or-V). Each tile of kept rows is fetched with one bulk copy per run of
-// consecutive sources into a 3-stage shared-memory ring and written back with one bulk store.
+// consecutive sources into a 4-stage shared-memory ring and written back with one bulk store.
+// Three tiles' loads and one tile's store are in flight at a time (the stage reloaded next is the
+// one stored in the previous step), and each tile's source indices are read one step ahead, so
+// no global read of the kept list sits between a tile's arrival and the next loads.
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -28,8 +31,9 @@ struct CompactArgs {
   int validate;
 };
 
-constexpr int kRing = 3;
-constexpr int kTileBytes = 16384;
+constexpr int kRing = 4;
+constexpr int kTileBytes = 12288;  // 48 rows of 256 bytes (96, 24 or 48 for the other row sizes)
+constexpr int kSrcRegs = (kTileBytes / 128 + 31) / 32;  // source indices per lane for one tile
 
 __device__ __forceinline__ uint32_t sm_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -73,7 +77,17 @@ __global__ void __launch_bounds__(32) compact_bulk_kernel(CompactArgs a) {
   }
   __syncwarp();
 
-  auto issue_loads = [&](int i) {
+  // source indices of tile i: row r0 + lane of each 32-row block (-1 past the tile's rows)
+  auto fetch_src = [&](int i, int (&v)[kSrcRegs]) {
+    const int k0 = first + i * T;
+    const int nrows = i < ntiles ? min(T, len - k0) : 0;
+#pragma unroll
+    for (int b = 0; b < kSrcRegs; ++b) {
+      const int r = b * 32 + lane;
+      v[b] = (r < nrows) ? src[k0 + r] : -1;
+    }
+  };
+  auto issue_loads = [&](int i, const int (&v)[kSrcRegs]) {
     const int s = i % kRing;
     const int k0 = first + i * T;
     const int nrows = min(T, len - k0);
@@ -83,12 +97,15 @@ __global__ void __launch_bounds__(32) compact_bulk_kernel(CompactArgs a) {
                    "r"(nrows * rb)
                    : "memory");
     __syncwarp();
-    for (int r0 = 0; r0 < nrows; r0 += 32) {
+#pragma unroll
+    for (int b = 0; b < kSrcRegs; ++b) {
+      const int r0 = b * 32;
+      if (r0 >= nrows) break;
       const int r = r0 + lane;
       const bool live = r < nrows;
-      const int sk = live ? src[k0 + r] : 0;
-      const int prev = (live && r > r0) ? src[k0 + r - 1] : -2;
-      const bool start = live && (r == r0 || prev + 1 != sk);
+      const int sk = v[b];
+      const int prev = __shfl_up_sync(kFull, sk, 1);
+      const bool start = live && (lane == 0 || prev + 1 != sk);
       const unsigned starts = __ballot_sync(kFull, start);
       if (start) {
         const unsigned later = (lane < 31) ? (starts >> (lane + 1)) : 0u;
@@ -104,8 +121,14 @@ __global__ void __launch_bounds__(32) compact_bulk_kernel(CompactArgs a) {
     }
   };
 
-  const int pro = ntiles < kRing ? ntiles : kRing;
-  for (int i = 0; i < pro; ++i) issue_loads(i);
+  // prologue: loads of the first kRing - 1 tiles, and the indices of the next one
+  int nxt[kSrcRegs];
+  const int pro = ntiles < kRing - 1 ? ntiles : kRing - 1;
+  for (int i = 0; i < pro; ++i) {
+    fetch_src(i, nxt);
+    issue_loads(i, nxt);
+  }
+  fetch_src(kRing - 1, nxt);
   bool ok = true;
   for (int i = 0; i < ntiles && ok; ++i) {
     const int s = i % kRing;
@@ -130,12 +153,15 @@ __global__ void __launch_bounds__(32) compact_bulk_kernel(CompactArgs a) {
                      "r"(sm_u32(sm + s * kTileBytes)), "r"(nrows * rb)
                      : "memory");
         asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
-        // the stage is reusable once this store has read it
-        asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+        // the stage reloaded next is the one stored in the previous step: its store must have read it
+        asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
       }
     }
     ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
-    if (ok && i + kRing < ntiles) issue_loads(i + kRing);
+    if (ok && i + kRing - 1 < ntiles) {
+      issue_loads(i + kRing - 1, nxt);
+      fetch_src(i + kRing, nxt);
+    }
   }
   if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
   __syncwarp();
