@@ -47,6 +47,14 @@
  *   append     BeaconKV page, "Continual FPS" and "观察 query 集": one decode step's
  *              pre-RoPE query joins its head's buffer (compressed by FPS as soon as
  *              it is full) and its post-RoPE query joins the recent ring.
+ *   epikv      EPIKV page ("方法论：EPIKV", items 1-3): a token's signal at layer l is the
+ *              L2 norm of the change of the residual stream between consecutive
+ *              tokens, g_l(t) = ||h_l(t) - h_l(t-1)||_2; it is made position-free by a
+ *              causal rolling z-score z_l = (g_l - mu_l) / (sigma_l + eps); the
+ *              eviction score is z_A - z_B for an A-band layer (kept when its signal
+ *              is high) and a B-band layer (kept when low). oracle_epikv_score; the
+ *              window, eps, token 0 and the std's normaliser are this build's
+ *              readings (the page states none).
  *   compact    The kept tokens' K and V rows, in original order, at the head's
  *              front (out-of-place gather here); slots past the kept count keep
  *              their old contents.
@@ -826,6 +834,59 @@ int oracle_append(int32_t dtype, int32_t nheads_q, int32_t D, const void* q_pre,
     free(rot);
   }
   return done;
+}
+
+/* EPIKV page, "方法论：EPIKV": the epiphany signal and its causal rolling z-score, per
+ * sequence b of B, for the hidden states of two layers hA, hB [B][N][dm] (storage
+ * type dtype). Readings (the page gives no window, eps or first-token rule):
+ *   g(0) = 0 (token 0 has no predecessor) and token 0 lies in no window;
+ *   for t >= 1: g(t) = sqrt(sum_i (h(t)_i - h(t-1)_i)^2);
+ *   window(t) = tokens max(1, t - W + 1) .. t (causal, t itself included), n = min(t, W);
+ *   mu(t) = mean of g over window(t); sigma(t) = sqrt(mean of (g - mu)^2) (population);
+ *   z(t) = (g(t) - mu(t)) / (sigma(t) + eps) for t >= 1, z(0) = 0;
+ *   score(t) = zA(t) - zB(t).
+ * Outputs (fp64): g [2][B][N] (may be NULL) and score [B][N]. Returns 0, or -1 on bad sizes. */
+int oracle_epikv_score(int32_t dtype, int32_t B, int32_t N, int32_t dm, const void* hA, const void* hB, int32_t W,
+                       double eps, double* g_out, double* score) {
+  if (B < 0 || N < 0 || dm < 1 || W < 1 || !(eps >= 0.0)) return -1;
+  double* g = (double*)malloc(sizeof(double) * 2 * (size_t)(B > 0 ? B : 1) * (size_t)(N > 0 ? N : 1));
+#pragma omp parallel for schedule(static)
+  for (int64_t bt = 0; bt < (int64_t)B * N; ++bt) {
+    const int64_t b = bt / N, t = bt % N;
+    for (int layer = 0; layer < 2; ++layer) {
+      const void* h = layer == 0 ? hA : hB;
+      double ss = 0.0;
+      if (t >= 1)
+        for (int i = 0; i < dm; ++i) {
+          const double d = load_elem(h, dtype, (b * N + t) * dm + i) - load_elem(h, dtype, (b * N + t - 1) * dm + i);
+          ss += d * d;
+        }
+      g[((int64_t)layer * B + b) * N + t] = sqrt(ss);
+    }
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t bt = 0; bt < (int64_t)B * N; ++bt) {
+    const int64_t b = bt / N, t = bt % N;
+    double z[2] = {0.0, 0.0};
+    if (t >= 1) {
+      const int64_t lo = t - W + 1 > 1 ? t - W + 1 : 1;
+      const double n = (double)(t - lo + 1);
+      for (int layer = 0; layer < 2; ++layer) {
+        const double* gl = g + ((int64_t)layer * B + b) * N;
+        double sum = 0.0;
+        for (int64_t u = lo; u <= t; ++u) sum += gl[u];
+        const double mu = sum / n;
+        double var = 0.0;
+        for (int64_t u = lo; u <= t; ++u) var += (gl[u] - mu) * (gl[u] - mu);
+        const double sigma = sqrt(var / n);
+        z[layer] = (gl[t] - mu) / (sigma + eps);
+      }
+    }
+    score[b * N + t] = z[0] - z[1];
+  }
+  if (g_out) memcpy(g_out, g, sizeof(double) * 2 * (size_t)B * (size_t)N);
+  free(g);
+  return 0;
 }
 
 int oracle_set_threads(int n) {

@@ -82,6 +82,9 @@ def lib():
         L.oracle_append.restype = C.c_int
         L.oracle_append.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_double,
                                     C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]
+        L.oracle_epikv_score.restype = C.c_int
+        L.oracle_epikv_score.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32,
+                                         C.c_double, C.c_void_p, C.c_void_p]
         L.oracle_set_threads.restype = C.c_int
         L.oracle_set_threads.argtypes = [C.c_int]
         _lib = L
@@ -303,3 +306,22 @@ def append(q_pre_bits: np.ndarray, q_post_bits, t: int, theta: float, qbuf_bits:
     if rc < 0:
         raise ValueError("oracle_append: bad sizes")
     return qb, cnt, qr, picks, err
+
+
+def epikv_score(hA_bits: np.ndarray, hB_bits: np.ndarray, window: int, eps: float, dtype: str, threads: int = 0):
+    """EPIKV signal and score (see oracle_epikv_score): hA, hB [B, N, dm] as storage bits (uint16 for
+    bf16, float32 otherwise). Returns (g [2, B, N], score [B, N]) in fp64."""
+    if threads:
+        set_threads(threads)
+    a = np.ascontiguousarray(hA_bits)
+    b = np.ascontiguousarray(hB_bits)
+    if a.shape != b.shape or a.ndim != 3:
+        raise ValueError("hA and hB must be [B, N, dm] of one shape")
+    B, N, dm = a.shape
+    g = np.zeros((2, B, N), np.float64)
+    sc = np.zeros((B, N), np.float64)
+    rc = lib().oracle_epikv_score(0 if dtype == "bf16" else 1, B, N, dm, _ptr(a), _ptr(b), int(window), float(eps),
+                                  _ptr(g), _ptr(sc))
+    if rc < 0:
+        raise ValueError("oracle_epikv_score: bad sizes")
+    return g, sc
