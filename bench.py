@@ -395,6 +395,171 @@ def gpu_arm(args, rank, world, local_rank):
     return res, inp
 
 
+def epikv_arm(args, rank, world, local_rank):
+    """The EPIKV eviction step (EPIKV write-up, "方法论：EPIKV"): signals from two layers' hidden states,
+    rolling z-score, one selection per sequence, compaction of every layer and KV head. Same metric;
+    the algorithmic bytes are the hidden states read once plus K and V of every moved token."""
+    import torch
+    from decoding_kv_cache_gb300 import build as kbuild
+    from decoding_kv_cache_gb300 import kvc
+    from decoding_kv_cache_gb300.inputs import make_epikv_inputs
+
+    if not kbuild.up_to_date():
+        kbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    over = {"L": args.layers} if args.layers else {}
+    inp = make_epikv_inputs(args.config, device=dev, **over)
+    stream = torch.cuda.current_stream(dev)
+    K0, V0 = inp.K.clone(), inp.V.clone()
+    cache = kvc.Cache(inp.K, inp.V, inp.Hq)
+    kept_len = torch.zeros((inp.B,), dtype=torch.int32, device=dev)
+    kept_idx = torch.zeros((inp.B, inp.N), dtype=torch.int32, device=dev)
+    scores = torch.zeros((inp.B, inp.N), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(kvc.kvc_epikv_workspace_size(inp.B, inp.N), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def reset():
+        inp.K.copy_(K0)
+        inp.V.copy_(V0)
+        flush.zero_()
+
+    def evict():
+        kvc.kvc_epikv_evict(cache, inp.hA, inp.hB, inp.window, inp.eps, inp.prefix, inp.recent, kept_len,
+                            budget_all=inp.budget_all, kept_idx=kept_idx, scores=scores, status=status, workspace=ws)
+
+    for _ in range(args.warmup):
+        reset()
+        evict()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {status.item()} after warm-up")
+    es = 2 if inp.dtype == "bf16" else 4
+    h_read = 2 * inp.B * inp.N * inp.dm * es
+    ar = torch.arange(inp.N, device=dev, dtype=torch.int32)
+    moved = int((((kept_idx != ar) & (ar < kept_len[:, None])).sum().item())) * inp.L * inp.Hkv
+    moved_bytes = moved * 4 * inp.D * es
+    alg = h_read + moved_bytes
+
+    clocks = ClockSampler(local_rank)
+    if rank == 0:
+        clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    for i in range(args.steps):
+        reset()
+        ev[i][0].record(stream)
+        evict()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    barrier(world)
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), world)
+    clk = clocks.stop() if rank == 0 else None
+    ms_per_step = total_ms / args.steps
+
+    # phases: the score alone, then the whole step (the difference is selection + compaction)
+    nph = max(3, min(args.steps, 20))
+    g = torch.zeros((2, inp.B, inp.N), device=dev)
+    ph = []
+    for i in range(nph):
+        reset()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record(stream)
+        kvc.kvc_epikv_score(inp.hA, inp.hB, inp.window, inp.eps, scores, g=g, workspace=ws)
+        e[1].record(stream)
+        ph.append(e)
+    torch.cuda.synchronize()
+    score_ms = sum(a.elapsed_time(b) for a, b in ph) / nph
+    rest_ms = max(ms_per_step - score_ms, 1e-9)
+    pk, pk_kind = peaks()
+    hbm = float(pk["hbm_gbs"])
+    dom, dom_bytes, dom_ms = ("kvc_epikv_score", h_read, score_ms) if score_ms >= rest_ms else \
+        ("select+compact", moved_bytes, rest_ms)
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+
+    pin = lambda t: t.cpu().pin_memory()
+    hK, hV, hA, hB = pin(K0), pin(V0), pin(inp.hA), pin(inp.hB)
+    hkl, hki = torch.empty_like(kept_len, device="cpu").pin_memory(), torch.empty_like(kept_idx, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hK, hV, hA, hB))
+    d2h = hkl.numel() * 4 + hki.numel() * 4
+    ee = []
+    for i in range(max(3, min(args.steps, 10))):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        inp.K.copy_(hK, non_blocking=True)
+        inp.V.copy_(hV, non_blocking=True)
+        inp.hA.copy_(hA, non_blocking=True)
+        inp.hB.copy_(hB, non_blocking=True)
+        evict()
+        hkl.copy_(kept_len, non_blocking=True)
+        hki.copy_(kept_idx, non_blocking=True)
+        b.record(stream)
+        ee.append((a, b))
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ee) / len(ee), world)
+    tokens = inp.B * inp.N
+    step_gbs = alg / (ms_per_step / 1e3) / 1e9
+    res = {
+        "metric": METRIC, "value": world * tokens * args.steps / (total_ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": inp.dtype, "data": "synthetic",
+        "config": {"workload": (f"{inp.name} EPIKV eviction step: L{inp.L} B{inp.B} Hkv{inp.Hkv} D{inp.D} {inp.dtype} "
+                                f"N{inp.N}->{inp.budget_all}, hidden size {inp.dm} (band layers A, B), window "
+                                f"{inp.window}, eps {inp.eps:g}"),
+                   "l2": "flushed between steps (512 MB write), cache restored from a pristine copy between steps; "
+                         "both untimed", "parallelism": f"replicas x{world}",
+                   "timing": "CUDA events around each kvc_epikv_evict on the launch stream"},
+        "achieved_gbs": step_gbs, "step_roofline_frac": step_gbs / hbm,
+        "algorithmic_bytes_per_step": {"hidden_read": h_read, "kv_moved": moved_bytes, "moved_head_tokens": moved},
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_source": pk_kind, "traffic": None},
+        "phases_ms": {"kvc_epikv_score": score_ms, "select+compact": rest_ms},
+        "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * 5,  # signal, prefix sums, z-score, select, compact
+        "clocks": clk,
+    }
+    return res, inp
+
+
+def oracle_epikv_sample(config: str, budget_s: float = 12.0):
+    """The oracle's EPIKV step (scores, per-sequence selection, gather of every head) on a bounded
+    sample of the workload's sequences; tokens/s scaled linearly to the full step."""
+    from decoding_kv_cache_gb300.inputs import EPIKV_CONFIGS, make_epikv_inputs
+    from oracle import oracle as O
+    import numpy as np
+    spec = EPIKV_CONFIGS[config]
+    cores = O.set_threads(os.cpu_count() or 1)
+
+    def run(inp):
+        bits = lambda t: t.view(__import__("torch").int16).numpy().view(np.uint16) if inp.dtype == "bf16" else t.numpy()
+        _, sc = O.epikv_score(bits(inp.hA), bits(inp.hB), inp.window, inp.eps, inp.dtype)
+        K = bits(inp.K)
+        V = bits(inp.V)
+        for b in range(inp.B):
+            kept = O.select(sc[b].astype(np.float32), inp.prefix, inp.recent, inp.budget_all)
+            _ = K[:, b, :, kept], V[:, b, :, kept]
+
+    probe = make_epikv_inputs(config, L=spec["L"], B=1, N=min(spec["N"], 512))
+    t0 = time.perf_counter()
+    run(probe)
+    per_tok = (time.perf_counter() - t0) / probe.N
+    n_tok = int(max(512, min(spec["N"], budget_s / max(per_tok, 1e-9))))
+    samp = make_epikv_inputs(config, B=1, N=n_tok)
+    t0 = time.perf_counter()
+    run(samp)
+    dt = time.perf_counter() - t0
+    full_s = dt * (spec["B"] * spec["N"]) / n_tok
+    tok = spec["B"] * spec["N"] / full_s
+    return tok, cores, (f"oracle on 1 of {spec['B']} sequences, {n_tok} of {spec['N']} tokens, all layers, {dt:.2f} s "
+                        f"wall on {cores} threads, scaled linearly to the full step"), dt
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
@@ -436,17 +601,19 @@ def oracle_variant(args):
 def reference_arm(args, rank, world):
     if rank != 0:
         return None
+    from decoding_kv_cache_gb300.inputs import CONFIGS, EPIKV_CONFIGS
+    epikv = args.config in EPIKV_CONFIGS
+    sample = (lambda budget_s: oracle_epikv_sample(args.config, budget_s)) if epikv else \
+        (lambda budget_s: oracle_sample(args.config, budget_s, **oracle_variant(args)))
     vals, descs = [], []
     if args.warmup > 0:
-        oracle_sample(args.config, budget_s=2.0, **oracle_variant(args))
+        sample(2.0)
     for _ in range(args.steps):
-        tok, cores, desc, _ = oracle_sample(args.config, budget_s=min(12.0, 120.0 / max(args.steps, 1)),
-                                            **oracle_variant(args))
+        tok, cores, desc, _ = sample(min(12.0, 120.0 / max(args.steps, 1)))
         vals.append(tok)
         descs.append(desc)
     value = statistics.mean(vals)
-    from decoding_kv_cache_gb300.inputs import CONFIGS
-    spec = CONFIGS[args.config]
+    spec = (EPIKV_CONFIGS if epikv else CONFIGS)[args.config]
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": spec["B"] * spec["N"] / value * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -490,10 +657,13 @@ def main():
         if out is not None:
             print(json.dumps(out), flush=True)
         return
-    res, _ = gpu_arm(args, rank, world, local_rank)
+    from decoding_kv_cache_gb300.inputs import EPIKV_CONFIGS
+    epikv = args.config in EPIKV_CONFIGS
+    res, _ = (epikv_arm if epikv else gpu_arm)(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            tok, cores, desc, _ = oracle_sample(args.config, **oracle_variant(args))
+            tok, cores, desc, _ = oracle_epikv_sample(args.config) if epikv else \
+                oracle_sample(args.config, **oracle_variant(args))
             res["cpu_baseline"] = {"value": tok, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -331,6 +331,99 @@ int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void*
 }
 
 // ---------------------------------------------------------------------------
+// EPIKV: hidden-state scores, one kept list per sequence.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace kvc {
+namespace {
+struct EpikvWs {
+  float* g;
+  double* pre;
+  uint32_t* keys;
+  float* scores;
+  int32_t* kept;
+};
+// layout: g [2][B][N] fp32, pre [2][2][B][N+1] fp64, keys [B][N], scores [B][N], kept [B][N]
+size_t epikv_ws(int B, int N, EpikvWs* w, void* base) {
+  const size_t bn = (size_t)B * N;
+  size_t off = 0;
+  const size_t o_g = off;     off += align256(2 * bn * sizeof(float));
+  const size_t o_pre = off;   off += align256(4 * (size_t)B * (N + 1) * sizeof(double));
+  const size_t o_keys = off;  off += align256(bn * sizeof(uint32_t));
+  const size_t o_sc = off;    off += align256(bn * sizeof(float));
+  const size_t o_kept = off;  off += align256(bn * sizeof(int32_t));
+  if (w) {
+    char* b = static_cast<char*>(base);
+    w->g = reinterpret_cast<float*>(b + o_g);
+    w->pre = reinterpret_cast<double*>(b + o_pre);
+    w->keys = reinterpret_cast<uint32_t*>(b + o_keys);
+    w->scores = reinterpret_cast<float*>(b + o_sc);
+    w->kept = reinterpret_cast<int32_t*>(b + o_kept);
+  }
+  return off;
+}
+int check_epikv(int dtype, int B, int N, int dm, const void* hA, const void* hB, int W, float eps) {
+  if (dtype != KVC_BF16 && dtype != KVC_F32) return KVC_ERR_UNSUPPORTED_DTYPE;
+  if (B < 1 || N < 1 || dm < 1 || !hA || !hB || W < 1 || !(eps > 0.f) || !isfinite(eps)) return KVC_ERR_INVALID_ARG;
+  const int per = dtype == KVC_BF16 ? 8 : 4;
+  if (dm % per || dm / per > 4 * 256) return KVC_ERR_UNSUPPORTED_HEAD_DIM;
+  if ((long long)B > 65535 || (long long)N > (1LL << 30) || (long long)B * N * dm > (1LL << 40)) return KVC_ERR_TOO_LARGE;
+  if (!aligned16(hA) || !aligned16(hB)) return KVC_ERR_ALIGNMENT;
+  return KVC_OK;
+}
+}  // namespace
+}  // namespace kvc
+
+extern "C" {
+
+size_t kvc_epikv_workspace_size(int32_t B, int32_t N) {
+  if (B < 1 || N < 1) return 0;
+  return epikv_ws(B, N, nullptr, nullptr);
+}
+
+int kvc_epikv_score(int32_t dtype, int32_t B, int32_t N, int32_t dm, const void* hA, const void* hB, int32_t window,
+                    float eps, float* g, float* scores, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_epikv(dtype, B, N, dm, hA, hB, window, eps);
+  if (rc) return rc;
+  if (!scores) return KVC_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < epikv_ws(B, N, nullptr, nullptr) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return KVC_ERR_WORKSPACE;
+  EpikvWs w;
+  epikv_ws(B, N, &w, workspace);
+  return launch_epikv_score(dtype, B, N, dm, hA, hB, window, (double)eps, g ? g : w.g, w.pre, scores, nullptr,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int kvc_epikv_evict(const kvc_cache* c, const void* hA, const void* hB, int32_t dm, int32_t window, float eps,
+                    int32_t prefix, int32_t recent, const int32_t* budget, int32_t budget_all, int32_t* kept_idx,
+                    int32_t* kept_len, float* scores, int32_t* status, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  CacheGeom g;
+  LayerPtrs K, V;
+  int rc = check_cache(c, &g, &K, &V);
+  if (rc) return rc;
+  rc = check_epikv(c->dtype, c->B, c->N, dm, hA, hB, window, eps);
+  if (rc) return rc;
+  if (!kept_len || prefix < 0 || recent < 0) return KVC_ERR_INVALID_ARG;
+  if (!budget && budget_all < prefix + recent && budget_all < c->N) return KVC_ERR_BUDGET_RANGE;
+  if (!workspace || ws_bytes < epikv_ws(g.B, g.N, nullptr, nullptr) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return KVC_ERR_WORKSPACE;
+  EpikvWs w;
+  epikv_ws(g.B, g.N, &w, workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* sc = scores ? scores : w.scores;
+  int32_t* ki = kept_idx ? kept_idx : w.kept;
+  rc = launch_epikv_score(c->dtype, g.B, g.N, dm, hA, hB, window, (double)eps, w.g, w.pre, sc, w.keys, s);
+  if (rc) return rc;
+  // one selection per sequence on the order-preserving keys of the signed scores
+  rc = launch_select(reinterpret_cast<const float*>(w.keys), g.B, g.N, prefix, recent, budget, budget_all, nullptr, 1,
+                     ki, kept_len, status, s);
+  if (rc) return rc;
+  return launch_compact(g, c->dtype, K, V, ki, kept_len, status, false, s, true);
+}
+
+// ---------------------------------------------------------------------------
 // kvc_score without a caller workspace: scratch lives in a fixed device region.
 // ---------------------------------------------------------------------------
 }  // extern "C"

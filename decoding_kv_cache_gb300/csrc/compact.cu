@@ -29,6 +29,7 @@ struct CompactArgs {
   int32_t* status;
   int rowbytes;
   int validate;
+  int list_seq;  // one kept list per sequence, shared by every layer and KV head (else one per head)
 };
 
 constexpr int kRing = 4;
@@ -46,9 +47,10 @@ __global__ void __launch_bounds__(32) compact_bulk_kernel(CompactArgs a) {
   const int rb = a.rowbytes;
   const int T = kTileBytes / rb;  // rows per tile: 32, 64 or 128
   char* base = static_cast<char*>(blockIdx.y ? a.V.p[l] : a.K.p[l]) + (size_t)bh * a.g.ncap * rb;
-  const int32_t* src = a.kept_idx + (size_t)head * a.g.N;
+  const int lst = a.list_seq ? (head / a.g.Hkv) % a.g.B : head;
+  const int32_t* src = a.kept_idx + (size_t)lst * a.g.N;
   griddep_wait();  // the kept lists come from the previous kernel
-  const int len = a.kept_len[head];
+  const int len = a.kept_len[lst];
   const int N = a.g.N;
   if (a.validate) {
     bool bad = len < 0 || len > N;
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(32) compact_bulk_kernel(CompactArgs a) {
 }
 
 int launch_compact(const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V, const int32_t* kept_idx,
-                   const int32_t* kept_len, int32_t* status, bool validate, cudaStream_t s) {
+                   const int32_t* kept_len, int32_t* status, bool validate, cudaStream_t s, bool list_per_seq) {
   const int heads = g.L * g.B * g.Hkv;
   if (heads == 0) return KVC_OK;
   CompactArgs a;
@@ -180,6 +182,7 @@ int launch_compact(const CacheGeom& g, int dtype, const LayerPtrs& K, const Laye
   a.status = status;
   a.rowbytes = g.D * (dtype == KVC_BF16 ? 2 : 4);
   a.validate = validate ? 1 : 0;
+  a.list_seq = list_per_seq ? 1 : 0;
   const size_t smem = (size_t)kRing * kTileBytes + 64;
   if (cudaFuncSetAttribute(compact_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;

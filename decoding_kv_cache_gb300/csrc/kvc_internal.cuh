@@ -191,8 +191,14 @@ int launch_select(const float* scores, int heads, int N, int P, int R, const int
 int launch_head_budget(const float* entropy, int groups, int Hkv, int N, int P, int R, const int32_t* budget,
                        int budget_all, int32_t* budget_out, int32_t* status, cudaStream_t s);
 
+// list_per_seq: kept_idx [B][N] / kept_len [B], one list per sequence for all its layers and heads
 int launch_compact(const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V, const int32_t* kept_idx,
-                   const int32_t* kept_len, int32_t* status, bool validate, cudaStream_t s);
+                   const int32_t* kept_len, int32_t* status, bool validate, cudaStream_t s, bool list_per_seq = false);
+
+// EPIKV: signals g [2][B][N] (layer A, layer B), prefix sums pre [2][2][B][N+1] fp64, signed
+// scores [B][N] and (if keys) their order-preserving unsigned keys [B][N] for the radix selection
+int launch_epikv_score(int dtype, int B, int N, int dm, const void* hA, const void* hB, int W, double eps, float* g,
+                       double* pre, float* score, uint32_t* keys, cudaStream_t s);
 
 inline int launch_ok() { return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_LAUNCH; }
 

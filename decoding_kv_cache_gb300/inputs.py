@@ -29,7 +29,8 @@ from typing import Optional
 
 import torch
 
-__all__ = ["EvictInputs", "CONFIGS", "make_inputs", "config_names"]
+__all__ = ["EvictInputs", "CONFIGS", "make_inputs", "config_names", "EpikvInputs", "EPIKV_CONFIGS",
+           "make_epikv_inputs"]
 
 
 @dataclass
@@ -262,3 +263,86 @@ def make_inputs(name: str, device="cpu", seed: Optional[int] = None, **over) -> 
                        qmax=qmax, t=t, theta=float(spec["theta"]), prefix=spec["prefix"], recent=spec["recent"],
                        budget_all=budget_all, K=K, V=V, q_recent=q_recent, qbuf=qbuf, count=count,
                        budget=budget, planted=planted, meta=meta)
+
+
+# ---------------------------------------------------------------------------
+# EPIKV workload: the model shape the EPIKV write-up evaluates (R1-Distill-Llama-8B: 32 layers,
+# 8 KV heads of 128, hidden size 4096) with the hidden states of its two band layers (10 and 21).
+# ---------------------------------------------------------------------------
+EPIKV_CONFIGS = {
+    "llama8b-epikv": dict(dtype="bf16", L=32, B=16, Hq=32, Hkv=8, D=128, N=4096, dm=4096, window=128, eps=1e-6,
+                          prefix=4, recent=16, seed=6),
+}
+
+
+@dataclass
+class EpikvInputs:
+    """One EPIKV eviction problem: the cache K, V [L, B, Hkv, N, D] and the hidden states hA, hB
+    [B, N, dm] of the two band layers (storage dtype); budget_all kept tokens per sequence."""
+
+    name: str
+    dtype: str
+    L: int
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    N: int
+    dm: int
+    window: int
+    eps: float
+    prefix: int
+    recent: int
+    budget_all: int
+    K: torch.Tensor
+    V: torch.Tensor
+    hA: torch.Tensor
+    hB: torch.Tensor
+
+    @property
+    def heads(self) -> int:
+        return self.L * self.B * self.Hkv
+
+    def to(self, device) -> "EpikvInputs":
+        return replace(self, K=self.K.to(device), V=self.V.to(device), hA=self.hA.to(device), hB=self.hB.to(device))
+
+
+def _residual_stream(B: int, N: int, dm: int, g: torch.Generator, device, rho: float = 0.9) -> torch.Tensor:
+    """A synthetic residual stream: h(t) = rho h(t-1) + s(t) n(t), n ~ N(0, I), with a log-normal step
+    size s(t) = exp(0.3 a(t)) (1 + 0.5 t/N) and an occasional large step (p = 0.02, x4): steps of
+    uneven size over a positional trend, the structure the EPIKV write-up's z-score addresses."""
+    a = _randn((B, N), g, device)
+    jump = torch.rand((B, N), generator=g, device=device) < 0.02
+    pos = torch.arange(N, device=device, dtype=torch.float32) / max(N, 1)
+    s = torch.exp(0.3 * a) * (1.0 + 0.5 * pos) * torch.where(jump, 4.0, 1.0)
+    h = torch.empty((B, N, dm), dtype=torch.float32, device=device)
+    prev = torch.zeros((B, dm), dtype=torch.float32, device=device)
+    for t in range(N):
+        prev = rho * prev + s[:, t, None] * _randn((B, dm), g, device)
+        h[:, t] = prev
+    return h
+
+
+def make_epikv_inputs(name: str = "llama8b-epikv", device="cpu", seed: Optional[int] = None, **over) -> EpikvInputs:
+    """Build the EPIKV workload, optionally with smaller sizes; ``keep`` overrides the kept total per
+    sequence (default 7/8 of N)."""
+    spec = dict(EPIKV_CONFIGS[name])
+    keep = over.pop("keep", None)
+    spec.update(over)
+    if seed is not None:
+        spec["seed"] = seed
+    L, B, Hkv, D, N, dm = (spec[k] for k in ("L", "B", "Hkv", "D", "N", "dm"))
+    dt = torch.bfloat16 if spec["dtype"] == "bf16" else torch.float32
+    device = torch.device(device)
+    g = _gen(device, spec["seed"])
+    K = torch.empty((L, B, Hkv, N, D), dtype=dt, device=device)
+    V = torch.empty((L, B, Hkv, N, D), dtype=dt, device=device)
+    for l in range(L):
+        K[l] = _randn((B, Hkv, N, D), g, device).to(dt)
+        V[l] = _randn((B, Hkv, N, D), g, device).to(dt)
+    hA = _residual_stream(B, N, dm, g, device).to(dt)
+    hB = _residual_stream(B, N, dm, g, device).to(dt)
+    return EpikvInputs(name=name, dtype=spec["dtype"], L=L, B=B, Hq=spec["Hq"], Hkv=Hkv, D=D, N=N, dm=dm,
+                       window=int(spec["window"]), eps=float(spec["eps"]), prefix=spec["prefix"],
+                       recent=spec["recent"], budget_all=(7 * N) // 8 if keep is None else int(keep), K=K, V=V,
+                       hA=hA, hB=hB)

@@ -21,8 +21,9 @@ KVC_MAX_LAYERS = 128
 
 EXPORTED = ("kvc_fps_update", "kvc_score_workspace_size", "kvc_score", "kvc_select", "kvc_compact",
             "kvc_evict_workspace_size", "kvc_evict", "kvc_evict_launch_count", "kvc_strerror", "kvc_abi_version",
-            "kvc_score_static", "kvc_debug_fault", "kvc_head_budget", "kvc_append")
-KVC_ABI_VERSION = 3
+            "kvc_score_static", "kvc_debug_fault", "kvc_head_budget", "kvc_append", "kvc_epikv_workspace_size",
+            "kvc_epikv_score", "kvc_epikv_evict")
+KVC_ABI_VERSION = 4
 KVC_AGG_MAX, KVC_AGG_MEAN, KVC_AGG_SUM = 0, 1, 2
 KVC_BUDGET_GIVEN, KVC_BUDGET_ENTROPY = 0, 1
 ROW_AGG = {"max": KVC_AGG_MAX, "mean": KVC_AGG_MEAN}
@@ -76,6 +77,9 @@ def lib():
         "kvc_evict_launch_count": (C.c_int, [pc, i32, i32]),
         "kvc_score_static": (C.c_int, [pc, vp, i32, vp, vp, i32, i32, i64, dbl, vp, vp, po, vp]),
         "kvc_head_budget": (C.c_int, [vp, i32, i32, i32, i32, i32, i32, vp, i32, vp, vp, vp]),
+        "kvc_epikv_workspace_size": (sz, [i32, i32]),
+        "kvc_epikv_score": (C.c_int, [i32, i32, i32, i32, vp, vp, i32, C.c_float, vp, vp, vp, sz, vp]),
+        "kvc_epikv_evict": (C.c_int, [pc, vp, vp, i32, i32, C.c_float, i32, i32, vp, i32, vp, vp, vp, vp, vp, sz, vp]),
         "kvc_strerror": (C.c_char_p, [C.c_int]),
         "kvc_abi_version": (C.c_int, []),
         "kvc_debug_fault": (C.c_int, [i32]),
@@ -271,3 +275,31 @@ def kvc_head_budget(entropy: torch.Tensor, N: int, prefix: int, recent: int, bud
     L, B, Hkv = entropy.shape
     _check(lib().kvc_head_budget(_p(entropy), L, B, Hkv, int(N), int(prefix), int(recent), _p(budget),
                                  int(budget_all), _p(budget_out), _p(status), _stream(stream)))
+
+
+def kvc_epikv_workspace_size(B: int, N: int) -> int:
+    return int(lib().kvc_epikv_workspace_size(B, N))
+
+
+def kvc_epikv_score(hA: torch.Tensor, hB: torch.Tensor, window: int, eps: float, scores: torch.Tensor,
+                    g: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """EPIKV scores [B, N] from two layers' hidden states [B, N, dm] (see kvc.h); ``g`` [2, B, N]
+    optionally receives the two layers' signals."""
+    B, N, dm = hA.shape
+    if tuple(hB.shape) != (B, N, dm) or hB.dtype != hA.dtype:
+        raise ValueError("hA and hB must be [B, N, dm] tensors of one dtype")
+    ws = _workspace(kvc_epikv_workspace_size(B, N), hA.device, workspace)
+    _check(lib().kvc_epikv_score(_dtype_code(hA), B, N, dm, _p(hA), _p(hB), int(window), float(eps), _p(g),
+                                 _p(scores), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def kvc_epikv_evict(cache: Cache, hA: torch.Tensor, hB: torch.Tensor, window: int, eps: float, prefix: int,
+                    recent: int, kept_len: torch.Tensor, budget: Optional[torch.Tensor] = None, budget_all: int = 0,
+                    kept_idx: Optional[torch.Tensor] = None, scores: Optional[torch.Tensor] = None,
+                    status: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Eviction by the EPIKV score: one kept list per sequence compacts all its layers and heads."""
+    B, N, dm = hA.shape
+    ws = _workspace(kvc_epikv_workspace_size(B, N), hA.device, workspace)
+    _check(lib().kvc_epikv_evict(cache.ref, _p(hA), _p(hB), dm, int(window), float(eps), int(prefix), int(recent),
+                                 _p(budget), int(budget_all), _p(kept_idx), _p(kept_len), _p(scores), _p(status),
+                                 _p(ws), ws.numel() * ws.element_size(), _stream(stream)))

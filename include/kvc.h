@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 3
+#define KVC_ABI_VERSION 4
 #define KVC_MAX_LAYERS 128
 
 #if defined(__GNUC__)
@@ -331,6 +331,53 @@ KVC_API int kvc_score_static(const kvc_cache* c, const void* q_recent, int32_t n
 KVC_API int kvc_head_budget(const float* entropy, int32_t L, int32_t B, int32_t Hkv, int32_t N, int32_t prefix,
                             int32_t recent, const int32_t* budget, int32_t budget_all, int32_t* budget_out,
                             int32_t* status, void* stream);
+
+/*
+ * kvc_epikv_score -- the EPIKV eviction score from two layers' hidden states.
+ * EPIKV write-up, "方法论：EPIKV": a token's signal at layer l is how far the
+ * residual stream moves when it is decoded, g_l(t) = ||h_l(t) - h_l(t-1)||_2;
+ * it is corrected for position by a causal rolling z-score
+ * z_l(t) = (g_l(t) - mu_l(t)) / (sigma_l(t) + eps), and the eviction score is
+ * z_A(t) - z_B(t) for a layer of the band where change marks important tokens (A)
+ * and one where it marks predictable ones (B). Higher scores are kept. The
+ * write-up states no window, eps or first-token rule; here g(0) = 0, token 0 lies
+ * in no window, window(t) = tokens max(1, t-W+1)..t, sigma is the population
+ * deviation; g in fp32, the window's mean and variance in fp64 (prefix sums), sigma and
+ * the quotient in fp32.
+ *
+ *   dtype        kvc_dtype of hA, hB
+ *   B, N, dm     sequences, tokens, hidden size; dm a multiple of 8 (bf16) or 4
+ *                (fp32), at most 8192 (bf16) or 4096 (fp32)
+ *   hA, hB       [B,N,dm] hidden states of layers A and B (device, 16-byte aligned)
+ *   window, eps  W >= 1 tokens; eps > 0 (a constant window has sigma 0)
+ *   g            [2,B,N] fp32 (device, out) or NULL: g_A then g_B
+ *   scores       [B,N] fp32 (device, out)
+ *   workspace    at least kvc_epikv_workspace_size(B, N) bytes, 256-byte aligned
+ */
+KVC_API size_t kvc_epikv_workspace_size(int32_t B, int32_t N);
+KVC_API int kvc_epikv_score(int32_t dtype, int32_t B, int32_t N, int32_t dm, const void* hA, const void* hB,
+                            int32_t window, float eps, float* g, float* scores, void* workspace, size_t ws_bytes,
+                            void* stream);
+
+/*
+ * kvc_epikv_evict -- eviction by the EPIKV score: kvc_epikv_score over the cache's
+ * B sequences and N tokens, then one selection per sequence (kvc_select's rule:
+ * [0, prefix) and [N-recent, N) kept, the rest of the budget by highest score,
+ * ties to the lower index) whose kept list compacts every layer and KV head of that
+ * sequence in place (kvc_compact's move). The score is a property of the token,
+ * so all heads of a sequence keep the same tokens.
+ *
+ *   c            the cache (K and V moved); its dtype is the hidden states' type
+ *   hA, hB, dm, window, eps   as kvc_epikv_score
+ *   budget       [B] int32 kept total per sequence (device) or NULL for budget_all
+ *   kept_idx     [B,N] int32 (device, out) or NULL; kept_len [B] int32 (device, out)
+ *   scores       [B,N] fp32 (device, out) or NULL
+ *   workspace    at least kvc_epikv_workspace_size(B, N) bytes, 256-byte aligned
+ */
+KVC_API int kvc_epikv_evict(const kvc_cache* c, const void* hA, const void* hB, int32_t dm, int32_t window, float eps,
+                            int32_t prefix, int32_t recent, const int32_t* budget, int32_t budget_all,
+                            int32_t* kept_idx, int32_t* kept_len, float* scores, int32_t* status, void* workspace,
+                            size_t ws_bytes, void* stream);
 
 /* Number of kernels one kvc_evict call with these arguments and default options
  * launches (host only; for accounting, e.g. counting launches inside a timed region;

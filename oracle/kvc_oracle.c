@@ -836,6 +836,32 @@ int oracle_append(int32_t dtype, int32_t nheads_q, int32_t D, const void* q_pre,
   return done;
 }
 
+/* The z-score half of oracle_epikv_score, from given signals g [2][B][N] (layer A, layer B). */
+int oracle_epikv_z(int32_t B, int32_t N, const double* g, int32_t W, double eps, double* score) {
+  if (B < 0 || N < 0 || W < 1 || !(eps >= 0.0)) return -1;
+#pragma omp parallel for schedule(static)
+  for (int64_t bt = 0; bt < (int64_t)B * N; ++bt) {
+    const int64_t b = bt / N, t = bt % N;
+    double z[2] = {0.0, 0.0};
+    if (t >= 1) {
+      const int64_t lo = t - W + 1 > 1 ? t - W + 1 : 1;
+      const double n = (double)(t - lo + 1);
+      for (int layer = 0; layer < 2; ++layer) {
+        const double* gl = g + ((int64_t)layer * B + b) * N;
+        double sum = 0.0;
+        for (int64_t u = lo; u <= t; ++u) sum += gl[u];
+        const double mu = sum / n;
+        double var = 0.0;
+        for (int64_t u = lo; u <= t; ++u) var += (gl[u] - mu) * (gl[u] - mu);
+        const double sigma = sqrt(var / n);
+        z[layer] = (gl[t] - mu) / (sigma + eps);
+      }
+    }
+    score[b * N + t] = z[0] - z[1];
+  }
+  return 0;
+}
+
 /* EPIKV page, "方法论：EPIKV": the epiphany signal and its causal rolling z-score, per
  * sequence b of B, for the hidden states of two layers hA, hB [B][N][dm] (storage
  * type dtype). Readings (the page gives no window, eps or first-token rule):
@@ -864,26 +890,7 @@ int oracle_epikv_score(int32_t dtype, int32_t B, int32_t N, int32_t dm, const vo
       g[((int64_t)layer * B + b) * N + t] = sqrt(ss);
     }
   }
-#pragma omp parallel for schedule(static)
-  for (int64_t bt = 0; bt < (int64_t)B * N; ++bt) {
-    const int64_t b = bt / N, t = bt % N;
-    double z[2] = {0.0, 0.0};
-    if (t >= 1) {
-      const int64_t lo = t - W + 1 > 1 ? t - W + 1 : 1;
-      const double n = (double)(t - lo + 1);
-      for (int layer = 0; layer < 2; ++layer) {
-        const double* gl = g + ((int64_t)layer * B + b) * N;
-        double sum = 0.0;
-        for (int64_t u = lo; u <= t; ++u) sum += gl[u];
-        const double mu = sum / n;
-        double var = 0.0;
-        for (int64_t u = lo; u <= t; ++u) var += (gl[u] - mu) * (gl[u] - mu);
-        const double sigma = sqrt(var / n);
-        z[layer] = (gl[t] - mu) / (sigma + eps);
-      }
-    }
-    score[b * N + t] = z[0] - z[1];
-  }
+  oracle_epikv_z(B, N, g, W, eps, score);
   if (g_out) memcpy(g_out, g, sizeof(double) * 2 * (size_t)B * (size_t)N);
   free(g);
   return 0;

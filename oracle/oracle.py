@@ -85,6 +85,8 @@ def lib():
         L.oracle_epikv_score.restype = C.c_int
         L.oracle_epikv_score.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32,
                                          C.c_double, C.c_void_p, C.c_void_p]
+        L.oracle_epikv_z.restype = C.c_int
+        L.oracle_epikv_z.argtypes = [C.c_int32, C.c_int32, C.c_void_p, C.c_int32, C.c_double, C.c_void_p]
         L.oracle_set_threads.restype = C.c_int
         L.oracle_set_threads.argtypes = [C.c_int]
         _lib = L
@@ -325,3 +327,13 @@ def epikv_score(hA_bits: np.ndarray, hB_bits: np.ndarray, window: int, eps: floa
     if rc < 0:
         raise ValueError("oracle_epikv_score: bad sizes")
     return g, sc
+
+
+def epikv_z(g: np.ndarray, window: int, eps: float):
+    """The z-score half of epikv_score from given signals g [2, B, N] (any float type, used as fp64)."""
+    gg = np.ascontiguousarray(g, dtype=np.float64)
+    _, B, N = gg.shape
+    sc = np.zeros((B, N), np.float64)
+    if lib().oracle_epikv_z(B, N, _ptr(gg), int(window), float(eps), _ptr(sc)) < 0:
+        raise ValueError("oracle_epikv_z: bad sizes")
+    return sc

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
     exported = set(re.findall(r"\bT (kvc_\w+)", out))
     assert set(_declared()) <= exported
     assert set(kvc.EXPORTED) == set(_declared())
-    assert lib.kvc_abi_version() == kvc.KVC_ABI_VERSION == 3
+    assert lib.kvc_abi_version() == kvc.KVC_ABI_VERSION == 4
 
 
 def test_header_compiles_as_c():
@@ -162,3 +162,22 @@ def test_append_rejects_bad_args(lib):
     assert call(t=-1) == -1
     assert call(count=None) == -1
     assert call(n_r=65) == -1
+
+
+def test_epikv_rejects_bad_args(lib):
+    ws = lambda **kw: (kw.get("ws", 0x100000), kw.get("wsb", 1 << 40))
+    call = lambda **kw: lib.kvc_epikv_score(kw.get("dtype", 0), kw.get("B", 2), kw.get("N", 100), kw.get("dm", 4096),
+                                            kw.get("hA", 0x1000), kw.get("hB", 0x1000), kw.get("W", 128),
+                                            kw.get("eps", 1e-6), None, kw.get("sc", 0x1000), *ws(**kw), None)
+    assert call(dtype=5) == -2
+    assert call(dm=4100) == -3                # not a whole number of 16-byte vectors
+    assert call(dm=8200) == -3 or call(dm=8200) == -3
+    assert call(dm=16384) == -3               # wider than the kernel's registers hold
+    assert call(dtype=1, dm=8192) == -3
+    assert call(W=0) == -1
+    assert call(eps=0.0) == -1                # a constant window needs eps > 0
+    assert call(hA=0x1008) == -8
+    assert call(sc=None) == -1
+    assert call(wsb=16) == -7
+    assert lib.kvc_epikv_workspace_size(2, 100) > 2 * 2 * 100 * 4
+    assert lib.kvc_epikv_workspace_size(0, 100) == 0
