@@ -5,7 +5,7 @@
 // For long caches and 256-row observation tiles the single-read kernel (score_resident.cu) has to
 // spread a head over many CTAs that meet every round (32 per head at 8k keys, 128 at 32k), and
 // those meetings, not the memory system, set its pace. Here the keys of a head are cut into
-// ranges of 1024 or 2048 keys and every (head, range) is an independent work item:
+// ranges of 1024 or 4096 keys and every (head, range) is an independent work item:
 //   pass 1      per item: S = Q K^T on the tensor cores (all observation rows of the head, one or
 //               two 128-row tiles against each 128-key chunk), each row's running (max, sum of
 //               exp2) over the range; the row's log2-sum-exp2 over the range is stored
@@ -383,10 +383,11 @@ __global__ void split_combine_kernel(ScoreArgs a, ScoreWs ws, SplitPlan p) {
 // ---------------------------------------------------------------------------
 static int split_tail_bytes(int NT) { return 1024 + 512 + 2 * NT * kSplitRows * 8 + 2 * 4 * kChunk * 4; }
 
-// Chunks per range: 8 (1024 keys) for one row tile, 16 (2048 keys) for two, so that the item's
-// observation tile(s) are loaded once per 256 or 512 KB of keys.
+// Chunks per range: 8 (1024 keys) for one row tile, 32 (4096 keys) for two (whose single tile
+// buffer is reloaded between items with the tensor pipe idle), so that the item's
+// observation tile(s) are loaded once per 256 KB or 1 MB of keys.
 int split_ranges(int nchunk, int M_pad) {
-  const int rk = M_pad > 128 ? 16 : 8;
+  const int rk = M_pad > 128 ? 32 : 8;
   return (nchunk + rk - 1) / rk;
 }
 
@@ -399,7 +400,7 @@ bool score_split_plan(const ScoreArgs& a, SplitPlan* p, size_t* smem) {
     return false;
   const int NT = a.M_pad / kSplitRows, D = a.g.D;
   const int heads = a.g.L * a.g.B * a.g.Hkv;
-  p->rk = NT == 1 ? 8 : 16;
+  p->rk = NT == 1 ? 8 : 32;
   p->R = split_ranges(a.nchunk, a.M_pad);
   p->items = heads * p->R;
   p->grid = p->items < nsm ? p->items : nsm;

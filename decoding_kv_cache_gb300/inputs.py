@@ -308,18 +308,28 @@ class EpikvInputs:
 
 
 def _residual_stream(B: int, N: int, dm: int, g: torch.Generator, device, rho: float = 0.9) -> torch.Tensor:
-    """A synthetic residual stream: h(t) = rho h(t-1) + s(t) n(t), n ~ N(0, I), with a log-normal step
-    size s(t) = exp(0.3 a(t)) (1 + 0.5 t/N) and an occasional large step (p = 0.02, x4): steps of
-    uneven size over a positional trend, the structure the EPIKV write-up's z-score addresses."""
+    """A synthetic residual stream: h(t) = rho h(t-1) + s(t) n(t), h(-1) = 0, n ~ N(0, I), with a
+    log-normal step size s(t) = exp(0.3 a(t)) (1 + 0.5 t/N) and an occasional large step (p = 0.02,
+    x4): steps of uneven size over a positional trend, the structure the EPIKV write-up's z-score
+    addresses. The recurrence runs over blocks of 64 tokens: inside a block as one product with the
+    lower-triangular matrix of powers of rho, across blocks through the carried last row."""
     a = _randn((B, N), g, device)
     jump = torch.rand((B, N), generator=g, device=device) < 0.02
     pos = torch.arange(N, device=device, dtype=torch.float32) / max(N, 1)
     s = torch.exp(0.3 * a) * (1.0 + 0.5 * pos) * torch.where(jump, 4.0, 1.0)
     h = torch.empty((B, N, dm), dtype=torch.float32, device=device)
-    prev = torch.zeros((B, dm), dtype=torch.float32, device=device)
-    for t in range(N):
-        prev = rho * prev + s[:, t, None] * _randn((B, dm), g, device)
-        h[:, t] = prev
+    T = 64
+    k = torch.arange(T, device=device, dtype=torch.float32)
+    expo = k[:, None] - k[None, :]
+    A = torch.where(expo >= 0, rho ** expo.clamp(min=0), torch.zeros_like(expo))  # A[i, j] = rho^(i-j), j <= i
+    decay = (rho ** (k + 1.0))[None, :, None]                                        # rho^(i+1)
+    prev = torch.zeros((B, 1, dm), dtype=torch.float32, device=device)
+    for t0 in range(0, N, T):
+        n = min(T, N - t0)
+        x = s[:, t0:t0 + n, None] * _randn((B, n, dm), g, device)
+        blk = torch.matmul(A[:n, :n], x) + decay[:, :n] * prev
+        h[:, t0:t0 + n] = blk
+        prev = blk[:, -1:]
     return h
 
 
