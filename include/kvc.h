@@ -294,7 +294,7 @@ KVC_API int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, con
  *
  * - Size limit: the call is rejected with KVC_ERR_WORKSPACE, before any launch, when
  *   kvc_score_workspace_size() for these arguments exceeds KVC_STATIC_SCRATCH_BYTES
- *   (the Qwen3-4B-shaped step, about 10.6 MB, fits; larger caches do not).
+ *   (the Qwen3-4B-shaped step, about 11.9 MB, fits; larger caches do not).
  * - Set-up: the first call on a device looks up the region's device address with that
  *   device current; make that first call before any CUDA stream capture.
  * - Sharing: every call on a device uses the same region and leaves its contents behind
