@@ -64,11 +64,23 @@ __global__ void __launch_bounds__(32) compact_bulk_kernel(CompactArgs a) {
       return;
     }
   }
-  // first index that moves: smallest k with src[k] != k (src[k] - k never decreases)
-  int lo = 0, hi = len;
+  // first index that moves: smallest k with src[k] != k (src[k] - k never decreases, so the
+  // test is monotone). A 32-way search: each step the lanes probe 32 points of [lo, hi) at once
+  // and a ballot narrows it 33-fold, so 2048 entries take 3 dependent loads instead of 11.
+  int lo = 0, hi = len;  // first lies in [lo, hi]
   while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (src[mid] == mid) lo = mid + 1; else hi = mid;
+    const int span = hi - lo;
+    const int pt = lo + (int)(((long long)span * (lane + 1)) / 33);  // < hi, non-decreasing in lane
+    const bool moved = pt < hi && src[pt] != pt;
+    const unsigned m = __ballot_sync(kFull, moved);
+    if (m) {
+      const int l = __ffs(m) - 1;  // first probe that moved: first <= its point
+      const int prev = l ? lo + (int)(((long long)span * l) / 33) : lo - 1;
+      hi = lo + (int)(((long long)span * (l + 1)) / 33);
+      lo = prev + 1;
+    } else {
+      lo = lo + (int)(((long long)span * 32) / 33) + 1;  // every probe kept its place
+    }
   }
   const int first = lo;
   if (first >= len) return;
