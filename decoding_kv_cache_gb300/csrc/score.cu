@@ -186,16 +186,34 @@ __device__ __forceinline__ HeadLoc head_loc(const CacheGeom& g, int head) {
 // ---------------------------------------------------------------------------
 // fp32 passes (CUDA-core FMA; fp32 storage is the small-model path)
 // ---------------------------------------------------------------------------
+// q . k over D floats with four independent accumulators (the loop fully unrolled, so the shared
+// memory loads of later terms are in flight while earlier products accumulate)
+template <int D>
+__device__ __forceinline__ float dot_f32(const float* __restrict__ q, const float* __restrict__ k) {
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int d = 0; d < D; d += 4) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[u] = fmaf(q[d + u], k[d + u], acc[u]);
+  }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
+// fp32 caches are scored in chunks of 32 keys (one row per thread in pass 1, one key per thread
+// in pass 2), so that even a small cache spreads over many CTAs
+constexpr int kF32Chunk = 32;
+
+template <int D>
 __global__ void __launch_bounds__(128) pass1_f32_kernel(ScoreArgs a, ScoreWs ws, float c2) {
   extern __shared__ __align__(16) float smf[];
-  const int D = a.g.D, LQ = D + 1;
+  constexpr int LQ = D + 1;
   float* Qs = smf;                   // [M_pad][D+1]
-  float* Ks = Qs + a.M_pad * LQ;     // [kChunk][D]
+  float* Ks = Qs + a.M_pad * LQ;     // [kF32Chunk][D]
   const int chunk = blockIdx.x, head = blockIdx.y;
   const HeadLoc hl = head_loc(a.g, head);
   const float* Kh = static_cast<const float*>(a.K.p[hl.l]) + (size_t)hl.bh * a.g.ncap * D;
-  const int j0 = chunk * kChunk;
-  const int nvalid = min(kChunk, a.g.N - j0);
+  const int j0 = chunk * kF32Chunk;
+  const int nvalid = min(kF32Chunk, a.g.N - j0);
   const float* obs = static_cast<const float*>(ws.obs) + (size_t)head * a.M_pad * D;
   for (int e = threadIdx.x; e < a.M_pad * D; e += blockDim.x) Qs[(e / D) * LQ + e % D] = obs[e];
   for (int e = threadIdx.x; e < nvalid * D; e += blockDim.x) Ks[e] = Kh[(size_t)j0 * D + e];
@@ -203,9 +221,7 @@ __global__ void __launch_bounds__(128) pass1_f32_kernel(ScoreArgs a, ScoreWs ws,
   for (int r = threadIdx.x; r < a.M_pad; r += blockDim.x) {
     float m = -INFINITY, s = 0.f;
     for (int j = 0; j < nvalid; ++j) {
-      float dot = 0.f;
-      for (int d = 0; d < D; ++d) dot = fmaf(Qs[r * LQ + d], Ks[j * D + d], dot);
-      const float x = dot * c2;
+      const float x = dot_f32<D>(Qs + r * LQ, Ks + j * D) * c2;
       if (x > m) {
         s = s * exp2f(m - x) + 1.f;
         m = x;
@@ -217,18 +233,19 @@ __global__ void __launch_bounds__(128) pass1_f32_kernel(ScoreArgs a, ScoreWs ws,
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(128) pass2_f32_kernel(ScoreArgs a, ScoreWs ws, float c2) {
   extern __shared__ __align__(16) float smf[];
-  const int D = a.g.D, LK = D + 1;
+  constexpr int LK = D + 1;
   float* Qs = smf;                  // [M_pad][D]
-  float* Ks = Qs + a.M_pad * D;     // [kChunk][D+1]
-  float* L2s = Ks + kChunk * LK;    // [M_pad]
+  float* Ks = Qs + a.M_pad * D;     // [kF32Chunk][D+1]
+  float* L2s = Ks + kF32Chunk * LK; // [M_pad]
   float* RWs = L2s + a.M_pad;       // [M_pad] row weights (extended epilogue, mean over rows)
   const int chunk = blockIdx.x, head = blockIdx.y;
   const HeadLoc hl = head_loc(a.g, head);
   const float* Kh = static_cast<const float*>(a.K.p[hl.l]) + (size_t)hl.bh * a.g.ncap * D;
-  const int j0 = chunk * kChunk;
-  const int nvalid = min(kChunk, a.g.N - j0);
+  const int j0 = chunk * kF32Chunk;
+  const int nvalid = min(kF32Chunk, a.g.N - j0);
   const float* obs = static_cast<const float*>(ws.obs) + (size_t)head * a.M_pad * D;
   const bool mean = a.ext && a.row_agg == KVC_AGG_MEAN;
   for (int e = threadIdx.x; e < a.M_pad * D; e += blockDim.x) Qs[e] = obs[e];
@@ -242,11 +259,7 @@ __global__ void __launch_bounds__(128) pass2_f32_kernel(ScoreArgs a, ScoreWs ws,
   if (!a.ext) {
     if (j >= nvalid) return;
     float best = -INFINITY;
-    for (int r = 0; r < a.M_pad; ++r) {
-      float dot = 0.f;
-      for (int d = 0; d < D; ++d) dot = fmaf(Qs[r * D + d], Ks[j * LK + d], dot);
-      best = fmaxf(best, dot * c2 - L2s[r]);
-    }
+    for (int r = 0; r < a.M_pad; ++r) best = fmaxf(best, dot_f32<D>(Qs + r * D, Ks + j * LK) * c2 - L2s[r]);
     a.scores[(size_t)head * a.g.N + j0 + j] = exp2f(best);
     return;
   }
@@ -258,9 +271,7 @@ __global__ void __launch_bounds__(128) pass2_f32_kernel(ScoreArgs a, ScoreWs ws,
   int cur = -1;
   if (j < nvalid) {
     for (int r = 0; r < a.M_pad; ++r) {
-      float dot = 0.f;
-      for (int d = 0; d < D; ++d) dot = fmaf(Qs[r * D + d], Ks[j * LK + d], dot);
-      const float y = dot * c2 - fminf(L2s[r], 1e30f);  // unused rows: p = 0, p * log2 p = 0
+      const float y = dot_f32<D>(Qs + r * D, Ks + j * LK) * c2 - fminf(L2s[r], 1e30f);  // unused rows: p = 0
       const float e = exp2f(y);
       hacc = fmaf(e, y, hacc);
       const int sg = r / a.qstride;
@@ -319,7 +330,7 @@ size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext,
   const int G = g.Hq / g.Hkv;
   const int M = obs_rows_used(G, n_r, n_b, ext);
   const size_t M_pad = (size_t)obs_rows(M, dtype);
-  const size_t nchunk = (size_t)(g.N + kChunk - 1) / kChunk;
+  const size_t nchunk = dtype == KVC_BF16 ? (size_t)(g.N + kChunk - 1) / kChunk : (size_t)(g.N + kF32Chunk - 1) / kF32Chunk;
   size_t off = 0;
   const size_t o_obs = off;   off += align256(heads * M_pad * g.D * es);
   const size_t o_valid = off; off += align256(heads * M_pad);
@@ -460,14 +471,18 @@ int launch_score(const ScoreArgs& a_in, const ScoreWs& ws, cudaStream_t s) {
     if (split) return launch_score_split(a, ws, sp, ssmem, s);
     return launch_score_fused(a, ws, ws.part, s);
   } else {
-    const size_t sm1 = sizeof(float) * ((size_t)a.M_pad * (D + 1) + (size_t)kChunk * D);
-    const size_t sm2 = sizeof(float) * ((size_t)a.M_pad * D + (size_t)kChunk * (D + 1) + 2 * (size_t)a.M_pad);
-    if (!set_smem(pass1_f32_kernel, sm1) || !set_smem(pass2_f32_kernel, sm2)) return KVC_ERR_LAUNCH;
-    pass1_f32_kernel<<<grid, 128, sm1, s>>>(a, ws, c2);
+    a.nchunk = (a.g.N + kF32Chunk - 1) / kF32Chunk;
+    const dim3 fgrid(a.nchunk, heads);
+    const size_t sm1 = sizeof(float) * ((size_t)a.M_pad * (D + 1) + (size_t)kF32Chunk * D);
+    const size_t sm2 = sizeof(float) * ((size_t)a.M_pad * D + (size_t)kF32Chunk * (D + 1) + 2 * (size_t)a.M_pad);
+    auto p1 = D == 128 ? pass1_f32_kernel<128> : pass1_f32_kernel<64>;
+    auto p2 = D == 128 ? pass2_f32_kernel<128> : pass2_f32_kernel<64>;
+    if (!set_smem(p1, sm1) || !set_smem(p2, sm2)) return KVC_ERR_LAUNCH;
+    p1<<<fgrid, 128, sm1, s>>>(a, ws, c2);
     if (launch_ok()) return KVC_ERR_LAUNCH;
     combine_kernel<<<heads, (a.M_pad + 31) / 32 * 32, 0, s>>>(a, ws);
     if (launch_ok()) return KVC_ERR_LAUNCH;
-    pass2_f32_kernel<<<grid, 128, sm2, s>>>(a, ws, c2);
+    p2<<<fgrid, kF32Chunk, sm2, s>>>(a, ws, c2);
   }
   return launch_ok();
 }
