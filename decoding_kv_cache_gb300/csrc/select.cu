@@ -4,11 +4,15 @@
 // are always kept, the rest of the budget is filled by top score; "实验": the cache drops to
 // 7/8 of B_KV^max. ReasonAlloc note, "Core Mechanism": the budget may differ per head.
 //
-// One CTA per head (256 or 1024 threads). Scores are non-negative fp32, so their IEEE bit patterns order like
-// the values; a 4-pass radix select (8-bit digits, shared-memory histograms) finds the
-// bit pattern T of the k-th largest middle score and how many copies of T must be kept.
-// A final ordered sweep keeps every middle score above T and the lowest-index copies of T,
-// which is the same set as sorting by (score descending, index ascending).
+// One CTA per head (256 or 1024 threads, each holding 8 consecutive tokens of a tile; a head of
+// one tile stays in registers). Scores are non-negative fp32, so their IEEE bit patterns order
+// like the values; a radix select finds the bit pattern T of the k-th largest middle score and
+// how many copies of T must be kept. The leading bits shared by every middle score (from their
+// minimum and maximum) are skipped; then 8-bit digits, one shared-memory histogram pass each (two
+// barriers, the next pass's bins cleared during this one), stopping early once the rank's bucket
+// is kept whole (T is then a prefix and ties are compared on the bits resolved so far). A final
+// ordered sweep keeps every middle score above T and the lowest-index copies of T, which is the
+// same set as sorting by (score descending, index ascending).
 //
 // Online head budgets (ReasonAlloc note, "Core Mechanism" and "Key Concepts"): with an
 // entropy array, the budgets of the Hkv heads of one (layer, sequence) are first reallocated
@@ -117,30 +121,51 @@ __global__ void head_budget_kernel(const float* __restrict__ entropy, int Hkv, i
   for (int h = threadIdx.x; h < Hkv; h += 32) budget_out[(size_t)lb * Hkv + h] = sout[h];
 }
 
-// Block-wide exclusive prefix count of a flag, in thread order. Returns this thread's
-// prefix; *total receives the block total. Uses warp ballots and one shared array.
-__device__ __forceinline__ int block_excl_count(bool flag, int* wsum, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned bal = __ballot_sync(kFull, flag);
-  const int in_warp = __popc(bal & ((1u << lane) - 1u));
-  if (lane == 0) wsum[warp] = __popc(bal);
+// Block-wide exclusive prefix sum, in thread order, of two counts packed in one 64-bit word (each
+// half stays below 2^32, so the halves never carry into each other). Returns this thread's prefix;
+// *total receives the block total. wsum holds 33 words; every thread of the block calls it.
+__device__ __forceinline__ unsigned long long block_excl_scan64(unsigned long long v, unsigned long long* wsum,
+                                                                unsigned long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
+  unsigned long long inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long u = __shfl_up_sync(kFull, inc, o);
+    if (lane >= o) inc += u;
+  }
+  if (lane == 31) wsum[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    const int v = lane < (int)(blockDim.x >> 5) ? wsum[lane] : 0;  // entries past the block's warps are unset
-    int inc = v;
+    const unsigned long long w = lane < nw ? wsum[lane] : 0ull;  // entries past the block's warps are unset
+    unsigned long long winc = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(kFull, inc, o);
-      if (lane >= o) inc += u;
+      const unsigned long long u = __shfl_up_sync(kFull, winc, o);
+      if (lane >= o) winc += u;
     }
-    wsum[lane] = inc - v;       // exclusive
-    if (lane == 31) wsum[32] = inc;
+    wsum[lane] = winc - w;  // exclusive over warps
+    if (lane == 31) wsum[32] = winc;
   }
   __syncthreads();
-  const int r = wsum[warp] + in_warp;
+  const unsigned long long r = wsum[warp] + (inc - v);
   *total = wsum[32];
   __syncthreads();  // wsum is reused by the next call
   return r;
+}
+
+constexpr int kSweep = 8;  // consecutive tokens per thread: a tile is kSweep * threads tokens
+
+// This thread's kSweep consecutive tokens from j: two 16-byte loads where the source allows
+// (vec: base 16-byte aligned and j a multiple of kSweep), else element by element; tokens past N
+// read as 0.
+__device__ __forceinline__ void load_group(const uint32_t* p, int j, int N, bool vec, uint32_t (&w)[kSweep]) {
+  if (vec && j + kSweep <= N) {
+    const uint4 x = *reinterpret_cast<const uint4*>(p + j), y = *reinterpret_cast<const uint4*>(p + j + 4);
+    w[0] = x.x, w[1] = x.y, w[2] = x.z, w[3] = x.w, w[4] = y.x, w[5] = y.y, w[6] = y.z, w[7] = y.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < kSweep; ++e) w[e] = j + e < N ? p[j + e] : 0u;
+  }
 }
 
 template <int kThreads>
@@ -150,12 +175,15 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
                                                              int32_t* __restrict__ kept_idx,
                                                              int32_t* __restrict__ kept_len, int32_t* status,
                                                              int use_smem) {
-  extern __shared__ uint32_t sh_bits[];
-  __shared__ unsigned hist[256];
-  __shared__ int wsum[33];
-  __shared__ unsigned s_digit, s_k;
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kTile = kSweep * kThreads;
+  extern __shared__ __align__(16) uint32_t sh_bits[];
+  __shared__ __align__(16) unsigned hist[2][256];
+  __shared__ unsigned long long wsum[33];
+  __shared__ uint32_t s_min[kWarps], s_max[kWarps];
+  __shared__ unsigned s_digit, s_k, s_cnt;
   __shared__ int32_t s_alloc[kMaxBudgetHeads];
-  const int head = blockIdx.x, tid = threadIdx.x;
+  const int head = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   griddep_wait();  // the scores (and entropies) come from the previous kernel
   const float* sc = scores + (size_t)head * N;
   int32_t* out = kept_idx + (size_t)head * N;
@@ -174,34 +202,90 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
     if (tid == 0) kept_len[head] = N;
     return;
   }
+  // Where the tokens come from: one tile is held in registers for the whole kernel; longer heads
+  // are staged in shared memory (or read from global memory when too long) tile by tile.
+  const int ntiles = (N + kTile - 1) / kTile;
   const uint32_t* bits = reinterpret_cast<const uint32_t*>(sc);
-  if (use_smem) {
-    for (int j = tid; j < N; j += blockDim.x) sh_bits[j] = __float_as_uint(sc[j]);
-    __syncthreads();
+  bool vec = (N & 3) == 0 && (reinterpret_cast<uintptr_t>(sc) & 15) == 0;
+  if (ntiles > 1 && use_smem) {
+    if (vec) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(sc);
+      uint4* d4 = reinterpret_cast<uint4*>(sh_bits);
+#pragma unroll 4
+      for (int i = tid; i < N / 4; i += kThreads) d4[i] = s4[i];
+    } else {
+#pragma unroll 4
+      for (int j = tid; j < N; j += kThreads) sh_bits[j] = bits[j];
+    }
     bits = sh_bits;
+    vec = true;
   }
+  uint32_t w[kSweep];
+  if (ntiles == 1) load_group(bits, tid * kSweep, N, vec, w);
+  auto tile_load = [&](int j0) {
+    if (ntiles > 1) load_group(bits, j0 + tid * kSweep, N, vec, w);
+  };
+  for (int i = tid; i < 256; i += kThreads) hist[0][i] = 0;
+
   const int lo = P, hi = N - R, kmid = b - P - R;
-  uint32_t T = 0xffffffffu;  // with kmid == 0 nothing of the middle passes "> T" or "== T, rank < 0"
+  // Threshold on the bits under `mask`: a middle token whose masked bits exceed T is kept, and of
+  // those equal to T the keq of lowest index. With kmid == 0 nothing of the middle is kept.
+  uint32_t T = 0xffffffffu, mask = 0xffffffffu;
   unsigned keq = 0;
   if (kmid > 0) {
-    uint32_t prefix = 0, mask = 0;
+    // the leading bits that every middle token shares (from their minimum and maximum) need no
+    // digit pass: scores in (0, 1] share several, and a digit over them would fill one bin
+    uint32_t mn = 0xffffffffu, mx = 0u;
+    for (int j0 = 0; j0 < N; j0 += kTile) {
+      tile_load(j0);
+#pragma unroll
+      for (int e = 0; e < kSweep; ++e) {
+        const int j = j0 + tid * kSweep + e;
+        if (j >= lo && j < hi) {
+          mn = min(mn, w[e]);
+          mx = max(mx, w[e]);
+        }
+      }
+    }
+    mn = __reduce_min_sync(kFull, mn);
+    mx = __reduce_max_sync(kFull, mx);
+    if (lane == 0) {
+      s_min[warp] = mn;
+      s_max[warp] = mx;
+    }
+    __syncthreads();  // also orders the zeroing of hist[0] before the first pass
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) {
+      mn = min(mn, s_min[i]);
+      mx = max(mx, s_max[i]);
+    }
+    int rem = (mn ^ mx) ? 32 - __clz(mn ^ mx) : 0;  // bits below the shared prefix
+    mask = rem >= 32 ? 0u : ~((1u << rem) - 1u);
+    uint32_t prefix = mn & mask;
     unsigned k = (unsigned)kmid;  // rank (1-based, from the top) still to locate
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-      __syncthreads();
-      for (int j = lo + tid; j < hi; j += blockDim.x) {
-        const uint32_t u = bits[j];
-        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+    int cur = 0;
+    while (rem > 0) {
+      const int width = rem < 8 ? rem : 8;
+      const int shift = rem - width;
+      const uint32_t dmask = (1u << width) - 1u;
+      for (int i = tid; i < 256; i += kThreads) hist[cur ^ 1][i] = 0;  // the next pass's bins
+      for (int j0 = 0; j0 < N; j0 += kTile) {
+        tile_load(j0);
+#pragma unroll
+        for (int e = 0; e < kSweep; ++e) {
+          const int j = j0 + tid * kSweep + e;
+          if (j >= lo && j < hi && (w[e] & mask) == prefix) atomicAdd(&hist[cur][(w[e] >> shift) & dmask], 1u);
+        }
       }
       __syncthreads();
       if (tid < 32) {
         // lane l holds digits 255-8l ... 248-8l, so lane order is descending digit order
-        unsigned c[8], local = 0;
+        const uint4 x = *reinterpret_cast<const uint4*>(&hist[cur][248 - 8 * tid]);
+        const uint4 y = *reinterpret_cast<const uint4*>(&hist[cur][252 - 8 * tid]);
+        const unsigned c[8] = {y.w, y.z, y.y, y.x, x.w, x.z, x.y, x.x};  // digits 255-8l-q
+        unsigned local = 0;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          c[q] = hist[255 - 8 * tid - q];
-          local += c[q];
-        }
+        for (int q = 0; q < 8; ++q) local += c[q];
         unsigned inc = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -216,6 +300,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
             if (cum + c[q] >= k) {
               s_digit = 255u - 8u * tid - q;
               s_k = k - cum;
+              s_cnt = c[q];
               break;
             }
             cum += c[q];
@@ -224,45 +309,63 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
       }
       __syncthreads();
       prefix |= s_digit << shift;
-      mask |= 255u << shift;
+      mask |= dmask << shift;
       k = s_k;
-      __syncthreads();
+      rem = shift;
+      cur ^= 1;
+      if (s_k == s_cnt) break;  // the rank's bucket is kept whole: its lower bits do not matter
     }
     T = prefix;
     keq = k;
   }
-  // ordered sweep: write kept indices ascending
-  int base_out = 0, base_eq = 0;
-  for (int j0 = 0; j0 < N; j0 += blockDim.x) {
-    const int j = j0 + tid;
-    const bool live = j < N;
-    const uint32_t u = live ? bits[j] : 0u;
-    const bool mid = live && j >= lo && j < hi;
-    const bool eq = mid && u == T;
-    int eq_tot;
-    const int eq_rank = base_eq + block_excl_count(eq, wsum, &eq_tot);
-    const bool keep = live && (!mid || u > T || (eq && (unsigned)eq_rank < keq));
-    int keep_tot;
-    const int pos = base_out + block_excl_count(keep, wsum, &keep_tot);
-    if (keep) out[pos] = j;
-    base_eq += eq_tot;
-    base_out += keep_tot;
+  // Ordered sweep: one scan per tile gives every token the number of kept tokens above the
+  // threshold and of tied tokens before it. The kept tied tokens are the first keq, so a kept
+  // token's slot is nk + min(neq, keq).
+  int base_k = 0, base_eq = 0;  // totals of the earlier tiles
+  for (int j0 = 0; j0 < N; j0 += kTile) {
+    tile_load(j0);
+    const int jt = j0 + tid * kSweep;
+    unsigned gt = 0, eqm = 0;
+#pragma unroll
+    for (int e = 0; e < kSweep; ++e) {
+      const int j = jt + e;
+      if (j < N) {
+        const uint32_t v = w[e] & mask;
+        if (j < lo || j >= hi || v > T) gt |= 1u << e;
+        else if (v == T) eqm |= 1u << e;
+      }
+    }
+    unsigned long long tot;
+    const unsigned long long ex =
+        block_excl_scan64(((unsigned long long)__popc(eqm) << 32) | (unsigned)__popc(gt), wsum, &tot);
+    int nk = base_k + (int)(ex & 0xffffffffull), neq = base_eq + (int)(ex >> 32);
+#pragma unroll
+    for (int e = 0; e < kSweep; ++e) {
+      const bool is_gt = (gt >> e) & 1u, is_eq = (eqm >> e) & 1u;
+      if (is_gt || (is_eq && neq < (int)keq)) out[nk + min(neq, (int)keq)] = jt + e;
+      nk += is_gt;
+      neq += is_eq;
+    }
+    base_k += (int)(tot & 0xffffffffull);
+    base_eq += (int)(tot >> 32);
   }
-  if (tid == 0) kept_len[head] = base_out;
+  if (tid == 0) kept_len[head] = base_k + min(base_eq, (int)keq);
 }
 
 int launch_select(const float* scores, int heads, int N, int P, int R, const int32_t* budget, int budget_all,
                   const float* entropy, int Hkv, int32_t* kept_idx, int32_t* kept_len, int32_t* status,
                   cudaStream_t s) {
   if (heads == 0) return KVC_OK;
-  const size_t bytes = (size_t)N * 4;
-  const int use_smem = bytes <= 200u * 1024u ? 1 : 0;
-  const size_t smem = use_smem ? bytes : 0;
   // A head's scores up to 64 KB: 256 threads, so that several heads share an SM and each barrier
   // spans 8 warps (R1-Qwen-7B-shaped heads of 8192 keys: 88 -> 58 us); longer heads fill an SM's
   // shared memory alone and need 1024 threads (Qwen3-14B-shaped, 32768 keys: 0.81 ms vs 2.4 ms).
   auto kern = N <= 16384 ? select_kernel<256> : select_kernel<kSelThreads>;
   const int threads = N <= 16384 ? 256 : kSelThreads;
+  // one tile (kSweep tokens per thread) stays in registers; longer heads are staged in shared
+  // memory when they fit
+  const size_t bytes = (size_t)(N + kSweep - 1) / kSweep * kSweep * 4;
+  const int use_smem = N > kSweep * threads && bytes <= 200u * 1024u ? 1 : 0;
+  const size_t smem = use_smem ? bytes : 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   if (launch_pdl(kern, dim3(heads), dim3(threads), smem, s, false, scores, N, P, R, budget, budget_all,

@@ -173,6 +173,40 @@ def test_select_matches_oracle_on_the_same_scores():
                 assert np.array_equal(ki[l, b, h, :len(ref)], ref)
 
 
+@pytest.mark.parametrize("N,heads", [(3001, 6), (20001, 3), (60001, 2)])
+@pytest.mark.parametrize("dist", ["uniform", "quantised", "split"])
+def test_select_sizes_and_distributions(N, heads, dist):
+    """Every launch shape of the selection (256 threads with the scores in shared memory, 1024
+    threads, and the global-memory path past 51200 tokens), token counts that are not a multiple
+    of 4 or of the sweep's groups, and three score laws: distinct values, heavy exact ties, and a
+    split where the k-th largest score's leading digit holds exactly the kept middle tokens (the
+    digit search then stops after its first digit)."""
+    from decoding_kv_cache_gb300 import kvc
+    g = torch.Generator().manual_seed(N + len(dist))
+    P, R = 4, 16
+    kmid = (N * 7) // 8 - P - R
+    if dist == "uniform":
+        sc = torch.rand((heads, N), generator=g)
+    elif dist == "quantised":
+        sc = torch.randint(0, 40, (heads, N), generator=g).float() / 64.0
+    else:
+        sc = 0.25 + torch.rand((heads, N), generator=g) * 0.2
+        for h in range(heads):
+            mid = torch.randperm(N - P - R, generator=g)[:kmid] + P
+            sc[h, mid] = 0.75 + torch.rand(kmid, generator=g) * 0.2
+    bud = torch.full((heads,), kmid + P + R, dtype=torch.int32)
+    bud[-1] = P + R + 1
+    kept_idx = torch.full((1, 1, heads, N), -7, dtype=torch.int32, device=DEV)
+    kept_len = torch.zeros((1, 1, heads), dtype=torch.int32, device=DEV)
+    kvc.kvc_select(sc.view(1, 1, heads, N).to(DEV), P, R, kept_idx, kept_len, budget=bud.view(1, 1, heads).to(DEV))
+    torch.cuda.synchronize()
+    ki, kl = kept_idx.cpu().numpy()[0, 0], kept_len.cpu().numpy()[0, 0]
+    for h in range(heads):
+        ref = O.select(sc[h].numpy(), P, R, int(bud[h]))
+        assert kl[h] == len(ref), h
+        assert np.array_equal(ki[h, :len(ref)], ref), h
+
+
 def test_compact_rejects_malformed_lists():
     from decoding_kv_cache_gb300 import kvc
     inp = make_inputs("qwen3-4b", L=1, N=256)
