@@ -119,6 +119,22 @@ def test_tiny_cache_shorter_than_windows():
     assert e.value.code == -4
 
 
+@pytest.mark.parametrize("N", [1, 2, 31])
+def test_one_or_few_token_caches(N):
+    """Caches of one, two and 31 tokens: a single ragged key chunk (the key loads zero-fill past
+    the cache), windows as long as or longer than the cache. One key: every softmax weight, so
+    every score, is 1 (the kernel forms s*c2 - lse2 in fp32, so within a few ulps). With 31 tokens
+    a budget of 26 leaves six middle tokens to choose."""
+    inp = make_inputs("qwen3-4b", L=1, N=N, keep=20 if N <= 20 else N - 5)
+    gpu = run_evict(inp, DEV)
+    ora = O.evict(inp)
+    assert_scores_close(gpu["scores"], ora["scores"], f"N={N}")
+    if N == 1:
+        assert np.abs(gpu["scores"].astype(np.float64) - 1.0).max() <= 2.0 ** -20
+    check_kept(inp, gpu, ora, gpu["scores"])
+    check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
+
+
 @pytest.mark.parametrize("dtype,D,qmax", [("f32", 64, 32), ("bf16", 128, 32), ("bf16", 128, 64), ("bf16", 64, 16)])
 def test_fps_update_matches_oracle(dtype, D, qmax):
     from decoding_kv_cache_gb300 import kvc
