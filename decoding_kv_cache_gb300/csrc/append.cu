@@ -28,7 +28,6 @@ __global__ void append_kernel(AppendArgs a) {
   void* scratch = smem_raw + warp * per_warp;
   const int qh = blockIdx.x * wpb + warp;
   if (qh >= a.nheads) return;  // the whole warp leaves together
-  fps_stage_init<T, D>(scratch, npad);
   constexpr int per = 16 / (int)sizeof(T);  // elements per 16-byte vector
   constexpr int vpr = D / per;              // vectors per row (8 .. 32)
   constexpr int hd = D / 2;
@@ -105,16 +104,11 @@ __global__ void append_kernel(AppendArgs a) {
   T* xs = reinterpret_cast<T*>(scratch);
   float* G = reinterpret_cast<float*>(xs + (size_t)npad * LD);
   int* pk = reinterpret_cast<int*>(G + (size_t)npad * (npad + 1));
-  stage_rows_issue<T, D>(x, c0, npad, xs, fps_stage_bar<T, D>(scratch, npad));
+  stage_rows_issue<T, D>(x, c0, npad, xs);
   // the new row's global copy (not among the staged rows: it goes to row c0 < qmax when the
   // buffer is filling, to row qmax/2 after a compression when it was full)
   const int new_row = c0 == a.qmax ? m : c0;
-  if (!stage_rows_wait<T>(fps_stage_bar<T, D>(scratch, npad), 0u)) {
-    if (lane == 0) status_or(a.status, KVC_STATUS_TIMEOUT);  // buffer and count left as they were
-    if (pick_out)
-      for (int k = lane; k < m; k += kWarp) pick_out[k] = -1;
-    return;
-  }
+  stage_rows_wait<T>();
   int c = c0;
   int compressions = 0;
   // one compression of the c == qmax staged rows: FPS picks, survivors to global rows [0, m)

@@ -19,7 +19,6 @@ __global__ void fps_update_kernel(T* __restrict__ qbuf, int nheads, int qmax, in
   void* scratch = smem_raw + warp * per;
   const int qh = blockIdx.x * wpb + warp;
   if (qh >= nheads) return;  // the whole warp leaves together
-  fps_stage_init<T, D>(scratch, npad);
   const int m = qmax / 2;
   const int c = count[qh];
   T* x = qbuf + (size_t)qh * qmax * D;
@@ -30,12 +29,7 @@ __global__ void fps_update_kernel(T* __restrict__ qbuf, int nheads, int qmax, in
     return;
   }
   int* pk;
-  bool ok;
-  const T* xs = fps_buffer<T, D>(x, qmax, m, npad, scratch, 0u, &pk, &ok);
-  if (!ok) {  // the staged copy is not complete: leave the buffer as it is
-    if (lane == 0) status_or(status, KVC_STATUS_TIMEOUT);
-    return;
-  }
+  const T* xs = fps_buffer<T, D>(x, qmax, m, npad, scratch, &pk);
   // Survivors to the front in time order, written back from the staged copy (same bytes).
   constexpr int LD = Staging<T, D>::LD;
   for (int k = 0; k < m; ++k) {

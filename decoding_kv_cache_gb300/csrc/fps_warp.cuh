@@ -27,52 +27,35 @@ struct Staging<float, D> {
 };
 
 // Shared scratch one warp needs for a buffer of up to npad rows (npad a multiple of 16):
-// staged rows, Gram matrix, picks, and the staging mbarrier (offsets stay multiples of 16).
+// staged rows, Gram matrix and picks (offsets stay multiples of 16).
 template <typename T, int D>
 __host__ __device__ constexpr size_t fps_scratch_bytes(int npad) {
   return (size_t)npad * Staging<T, D>::LD * sizeof(T) + (size_t)npad * (npad + 1) * sizeof(float) +
-         (size_t)npad * sizeof(int) + 16;
-}
-template <typename T, int D>
-__device__ __forceinline__ uint64_t* fps_stage_bar(void* scratch, int npad) {
-  return reinterpret_cast<uint64_t*>(static_cast<char*>(scratch) + fps_scratch_bytes<T, D>(npad) - 16);
-}
-// Prepare a warp's staging barrier once per kernel (lane 0 initialises it; the warp syncs).
-template <typename T, int D>
-__device__ __forceinline__ void fps_stage_init(void* scratch, int npad) {
-  if constexpr (sizeof(T) == 2) {
-    if ((threadIdx.x & 31) == 0) {
-      const uint32_t b = (uint32_t)__cvta_generic_to_shared(fps_stage_bar<T, D>(scratch, npad));
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(b) : "memory");
-      asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
-    __syncwarp();
-  }
+         (size_t)npad * sizeof(int);
 }
 
 // Copy rows [0, n) of x (global, 16-byte aligned) into xs[npad][LD]; rows [n, npad) become zero.
-// bf16 rows (LD * 2 a multiple of 16 bytes) go straight to shared memory, one bulk copy per row,
-// completed in bytes on the warp's staging barrier: stage_rows_issue only starts them and
-// stage_rows_wait completes them (phase = how many times the barrier was used before), so other
-// memory work can overlap. fp32 rows (odd LD) pass through registers in batches of eight loads
-// per lane, each batch in flight before its stores; they are complete when issue returns.
+// bf16 rows (LD * 2 a multiple of 16 bytes) go straight to shared memory as 16-byte cp.async copies,
+// eight or sixteen per lane for a 32-row buffer (one bulk copy per row instead issued 32 copies one
+// after another, ~3k cycles): stage_rows_issue only starts them and stage_rows_wait completes
+// them, so other memory work can overlap. fp32 rows (odd LD) pass through registers in batches of
+// eight loads per lane, each batch in flight before its stores; they are complete when issue returns.
 template <typename T, int D>
-__device__ __forceinline__ void stage_rows_issue(const T* __restrict__ x, int n, int npad, T* xs, uint64_t* bar) {
+__device__ __forceinline__ void stage_rows_issue(const T* __restrict__ x, int n, int npad, T* xs) {
   const int lane = threadIdx.x & 31;
   constexpr int LD = Staging<T, D>::LD;
   if constexpr (sizeof(T) == 2) {
-    const uint32_t b = (uint32_t)__cvta_generic_to_shared(bar);
-    if (lane == 0)
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(b), "r"((uint32_t)(n * D * 2))
+    constexpr int vpr = D / 8;  // 16-byte vectors per row
+    for (int e = lane; e < n * vpr; e += kWarp) {
+      const int r = e / vpr, v = e % vpr;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
+                       (uint32_t)__cvta_generic_to_shared(xs + r * LD + v * 8)),
+                   "l"(x + (size_t)r * D + v * 8)
                    : "memory");
-    __syncwarp();
-    for (int r = lane; r < n; r += kWarp)
-      asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-                       (uint32_t)__cvta_generic_to_shared(xs + r * LD)),
-                   "l"(x + (size_t)r * D), "r"(D * 2), "r"(b)
-                   : "memory");
-    for (int e = lane; e < (npad - n) * (D / 8); e += kWarp)  // zero rows past n
-      *reinterpret_cast<uint4*>(xs + (n + e / (D / 8)) * LD + (e % (D / 8)) * 8) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+    for (int e = lane; e < (npad - n) * vpr; e += kWarp)  // zero rows past n
+      *reinterpret_cast<uint4*>(xs + (n + e / vpr) * LD + (e % vpr) * 8) = make_uint4(0u, 0u, 0u, 0u);
   } else {
     constexpr int per = 16 / sizeof(T);
     constexpr int vpr = D / per;
@@ -99,24 +82,13 @@ __device__ __forceinline__ void stage_rows_issue(const T* __restrict__ x, int n,
     }
   }
 }
-// Complete the staging started by stage_rows_issue; false if the copies did not land in time.
+
+// Complete the staging started by stage_rows_issue (this lane's copies, then the warp's: the
+// rows are read by other lanes). The copies depend on nothing else, so the wait always ends.
 template <typename T>
-__device__ __forceinline__ bool stage_rows_wait(uint64_t* bar, uint32_t phase) {
-  bool ok = true;
-  if constexpr (sizeof(T) == 2) {
-    const uint32_t b = (uint32_t)__cvta_generic_to_shared(bar);
-    ok = false;
-    for (uint32_t it = 0; it < (1u << 22) && !ok; ++it) {
-      uint32_t done;
-      asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-                   : "=r"(done)
-                   : "r"(b), "r"(phase & 1u)
-                   : "memory");
-      ok = done != 0;
-    }
-  }
+__device__ __forceinline__ void stage_rows_wait() {
+  if constexpr (sizeof(T) == 2) asm volatile("cp.async.wait_group 0;\n" ::: "memory");
   __syncwarp();
-  return ok;
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
@@ -274,23 +246,22 @@ __device__ __forceinline__ void fps_gram(const float* G, int ldg, int n, int m, 
   __syncwarp();
 }
 
-// FPS over a staged buffer. Scratch layout: staged rows, then G, then picks, then the staging
-// barrier (fps_scratch_bytes; fps_stage_init once per kernel). fps_buffer_issue starts staging
-// rows [0, n) of x; fps_buffer_finish completes it (phase = earlier uses of the barrier), forms the
-// Gram matrix and runs FPS for m picks (all n rows are picked when m >= n). finish returns the
-// staged rows (*picks_out points at the picks) and sets *ok to false if the staging timed out.
+// FPS over a staged buffer. Scratch layout: staged rows, then G, then picks (fps_scratch_bytes).
+// fps_buffer_issue starts staging rows [0, n) of x; fps_buffer_finish completes it, forms the Gram
+// matrix and runs FPS for m picks (all n rows are picked when m >= n). finish returns the staged
+// rows (*picks_out points at the picks).
 template <typename T, int D>
 __device__ __forceinline__ void fps_buffer_issue(const T* __restrict__ x, int n, int npad, void* scratch) {
-  stage_rows_issue<T, D>(x, n, npad, reinterpret_cast<T*>(scratch), fps_stage_bar<T, D>(scratch, npad));
+  stage_rows_issue<T, D>(x, n, npad, reinterpret_cast<T*>(scratch));
 }
+
 template <typename T, int D>
-__device__ __forceinline__ T* fps_buffer_finish(int n, int m, int npad, void* scratch, uint32_t phase, int** picks_out,
-                                                bool* ok) {
+__device__ __forceinline__ T* fps_buffer_finish(int n, int m, int npad, void* scratch, int** picks_out) {
   T* xs = reinterpret_cast<T*>(scratch);
   float* G = reinterpret_cast<float*>(xs + (size_t)npad * Staging<T, D>::LD);
   int* picks = reinterpret_cast<int*>(G + (size_t)npad * (npad + 1));
   *picks_out = picks;
-  *ok = stage_rows_wait<T>(fps_stage_bar<T, D>(scratch, npad), phase);
+  stage_rows_wait<T>();
   if (m < n) {
     gram_rows<D>(xs, npad, G);
     fps_gram(G, npad + 1, n, m, picks);
@@ -300,11 +271,12 @@ __device__ __forceinline__ T* fps_buffer_finish(int n, int m, int npad, void* sc
   }
   return xs;
 }
+
 template <typename T, int D>
-__device__ __forceinline__ T* fps_buffer(const T* __restrict__ x, int n, int m, int npad, void* scratch, uint32_t phase,
-                                         int** picks_out, bool* ok) {
+__device__ __forceinline__ T* fps_buffer(const T* __restrict__ x, int n, int m, int npad, void* scratch,
+                                         int** picks_out) {
   fps_buffer_issue<T, D>(x, n, npad, scratch);
-  return fps_buffer_finish<T, D>(n, m, npad, scratch, phase, picks_out, ok);
+  return fps_buffer_finish<T, D>(n, m, npad, scratch, picks_out);
 }
 
 }  // namespace kvc

@@ -53,8 +53,6 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
   constexpr int rpi = kWarp / lpr;
   const int i0 = (lane % lpr) * per, rsel = lane / lpr;
   float2* rope_s = reinterpret_cast<float2*>(smem_raw + (size_t)nw * ((fps_scratch_bytes<T, D>(npad) + 15) & ~(size_t)15));
-  fps_stage_init<T, D>(scratch, npad);
-  uint32_t stage_phase = 0;
   __shared__ int s_nvalid;  // valid observation rows of this KV head (for the entropy's mean)
   const bool mean_w = a.ext && a.row_agg == KVC_AGG_MEAN;
 
@@ -78,15 +76,16 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
       if (u * kWarp + lane < nv) rv[u] = qr[u * kWarp + lane];
     if (it == 0) {
       // while those are in flight: this CTA's share of the scoring kernel's exchange words (they
-      // start at zero) and the rotation table in shared memory (a per-lane index into the
-      // parameter block would serialise)
+      // start at zero) and the rotation table in shared memory, read from the parameter block at
+      // warp-uniform indices (a per-lane index there serialises; the rotation reads it per lane)
       if (a.xch_zero) {
         const long long share = (a.xch_zero_words + gridDim.x - 1) / gridDim.x;
         const long long lo = (long long)blockIdx.x * share;
         const long long hi = lo + share < a.xch_zero_words ? lo + share : a.xch_zero_words;
         for (long long w = lo + threadIdx.x; w < hi; w += blockDim.x) a.xch_zero[w] = 0ull;
       }
-      for (int i = threadIdx.x; i < hd; i += blockDim.x) rope_s[i] = a.rope[i];
+      for (int i = warp; i < hd; i += nw)  // warp-uniform indices: broadcast parameter reads
+        if (lane == 0) rope_s[i] = a.rope[i];
       // the scoring kernel combines a head's tiles into its scores with atomics: start at zero
       if (a.tiles > 1)
         for (int j = threadIdx.x; j < a.g.N; j += blockDim.x) a.scores[(size_t)head * a.g.N + j] = 0.f;
@@ -113,9 +112,7 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
     for (int r = lane; r < a.n_r; r += kWarp) valid[g * qs + r] = 1;
     // beacons: the buffer itself when it holds at most n_b rows, else FPS down to n_b
     int* pk;
-    bool staged;
-    const T* xs = fps_buffer_finish<T, D>(c, a.n_b, npad, scratch, stage_phase++, &pk, &staged);
-    if (!staged && lane == 0) status_or(a.status, KVC_STATUS_TIMEOUT);
+    const T* xs = fps_buffer_finish<T, D>(c, a.n_b, npad, scratch, &pk);
     const int nb = c < a.n_b ? c : a.n_b;
     if (a.ext) {
       if (lane == 0) atomicAdd(&s_nvalid, a.n_r + nb);
@@ -138,11 +135,28 @@ __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
       alignas(16) T o2[per];
       if (k < nb) {
         const T* src = xs + pk[k] * LD;
+        // the lane's `per` pairs: one 16-byte read per half for bf16 rows (LD * 2 and i0 * 2 are
+        // multiples of 16), element reads for fp32 rows (odd LD); the table in 16-byte reads
+        alignas(16) T xa[per];
+        alignas(16) T xb[per];
+        if constexpr (sizeof(T) == 2) {
+          *reinterpret_cast<uint4*>(xa) = *reinterpret_cast<const uint4*>(src + i0);
+          *reinterpret_cast<uint4*>(xb) = *reinterpret_cast<const uint4*>(src + i0 + hd);
+        } else {
+#pragma unroll
+          for (int u = 0; u < per; ++u) {
+            xa[u] = src[i0 + u];
+            xb[u] = src[i0 + u + hd];
+          }
+        }
+        alignas(16) float2 csv[per];
+#pragma unroll
+        for (int q2 = 0; q2 < per / 2; ++q2)
+          reinterpret_cast<float4*>(csv)[q2] = reinterpret_cast<const float4*>(rope_s + i0)[q2];
 #pragma unroll
         for (int u = 0; u < per; ++u) {
-          const int i = i0 + u;
-          const float2 cs = rope_s[i];
-          const float x0 = to_f32(src[i]), x1 = to_f32(src[i + hd]);
+          const float2 cs = csv[u];
+          const float x0 = to_f32(xa[u]), x1 = to_f32(xb[u]);
           // each product and the sum rounded separately (no fused multiply-add), so the
           // rounding to the storage type below is a reproducible decision
           o1[u] = from_f32<T>(__fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y)));
