@@ -114,6 +114,54 @@ __device__ __forceinline__ void gram_rows(const __nv_bfloat16* xs, int npad, flo
   constexpr int LD = Staging<__nv_bfloat16, D>::LD;
   const int ldg = npad + 1;
   const int nt = npad / 16;
+  if (nt == 2) {
+    // 32 rows: the three upper tiles (0,0), (0,1), (1,1) in one pass over D, six independent
+    // accumulation chains (tile row by tile row, the chains of the second row waited on the first)
+    float acc[3][2][4];
+#pragma unroll
+    for (int t = 0; t < 3; ++t)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[t][h][k] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t af[2][4], bf[2][4];
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        ldsm_x4(af[m], xs + (m * 16 + (lane & 15)) * LD + ks * 16 + (lane >> 4) * 8);
+        ldsm_x4(bf[m], xs + (m * 16 + ((lane >> 4) << 3) + (lane & 7)) * LD + ks * 16 + ((lane >> 3) & 1) * 8);
+      }
+      const int tm[3] = {0, 0, 1}, tn[3] = {0, 1, 1};
+#pragma unroll
+      for (int t = 0; t < 3; ++t) {
+        mma_16816(acc[t][0], af[tm[t]], bf[tn[t]][0], bf[tn[t]][1]);
+        mma_16816(acc[t][1], af[tm[t]], bf[tn[t]][2], bf[tn[t]][3]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 3; ++t) {
+      const int mt = t == 2 ? 1 : 0, ct = t == 0 ? 0 : 1;
+      const int r0 = mt * 16 + (lane >> 2);
+      const int cb = ct * 16 + 2 * (lane & 3);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = cb + 8 * h;
+        G[r0 * ldg + c] = acc[t][h][0];
+        G[r0 * ldg + c + 1] = acc[t][h][1];
+        G[(r0 + 8) * ldg + c] = acc[t][h][2];
+        G[(r0 + 8) * ldg + c + 1] = acc[t][h][3];
+        if (mt != ct) {
+          G[c * ldg + r0] = acc[t][h][0];
+          G[(c + 1) * ldg + r0] = acc[t][h][1];
+          G[c * ldg + r0 + 8] = acc[t][h][2];
+          G[(c + 1) * ldg + r0 + 8] = acc[t][h][3];
+        }
+      }
+    }
+    __syncwarp();
+    return;
+  }
   for (int mt = 0; mt < nt; ++mt) {
     float acc[4][2][4];
 #pragma unroll
