@@ -602,15 +602,15 @@ def oracle_sample(config: str, budget_s: float = 12.0, **variant):
     L = max(1, min(spec["L"], want_heads // (spec["B"] * spec["Hkv"])))
     B = spec["B"] if L > 1 else max(1, min(spec["B"], want_heads // spec["Hkv"]))
     samp = make_inputs(config, L=L, B=B)
-    # a sample that is the whole step and takes less than the budget is run again until the budget
-    # is spent (at most 64 runs), so that the figure rests on seconds of work
+    # a sample that is the whole step is run again while another run fits in the budget (at most
+    # 64 runs), so that the figure rests on seconds of work
     reps = 0
     t0 = time.perf_counter()
     while True:
         O.evict(samp, **variant)
         reps += 1
         dt = time.perf_counter() - t0
-        if samp.heads < heads_full or dt >= budget_s or reps >= 64:
+        if samp.heads < heads_full or dt + dt / reps > budget_s or reps >= 64:
             break
     full_s = dt / reps * heads_full / samp.heads
     tok = spec["B"] * spec["N"] / full_s
