@@ -287,9 +287,8 @@ int kvc_compact(const kvc_cache* c, const int32_t* kept_idx, const int32_t* kept
 size_t kvc_evict_workspace_size(const kvc_cache* c, int32_t n_r, int32_t n_b) {
   const size_t sw = kvc_score_workspace_size(c, n_r, n_b);
   if (!sw) return 0;
-  const size_t heads = (size_t)c->L * c->B * c->Hkv;
-  // scores and kept indices (used when the caller passes NULL), and each head's first moved index
-  return sw + 2 * align256(heads * (size_t)c->N * 4) + align256(heads * 4);
+  const size_t per = (size_t)c->L * c->B * c->Hkv * (size_t)c->N * 4;
+  return sw + 2 * align256(per);  // scores and kept indices, used when the caller passes NULL
 }
 
 int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf, const int32_t* count,
@@ -310,15 +309,13 @@ int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void*
   if (o.head_budget == KVC_BUDGET_ENTROPY && g.Hkv > 64) return KVC_ERR_TOO_LARGE;
   const size_t sw = score_ws_bytes(g, c->dtype, n_r, n_b, o.ext, nullptr, nullptr);
   const size_t per = align256((size_t)g.L * g.B * g.Hkv * (size_t)g.N * 4);
-  const size_t fst = align256((size_t)g.L * g.B * g.Hkv * 4);
-  if (!workspace || ws_bytes < sw + 2 * per + fst || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+  if (!workspace || ws_bytes < sw + 2 * per || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return KVC_ERR_WORKSPACE;
   char* wb = static_cast<char*>(workspace);
   ScoreWs ws;
   score_ws_bytes(g, c->dtype, n_r, n_b, o.ext, &ws, wb);
   float* sc = scores ? scores : reinterpret_cast<float*>(wb + sw);
   int32_t* ki = kept_idx ? kept_idx : reinterpret_cast<int32_t*>(wb + sw + per);
-  int32_t* first = reinterpret_cast<int32_t*>(wb + sw + 2 * per);  // selection -> compaction
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the entropy goes to the caller's array, else (when the budgets need it) to the workspace's
   float* ent = o.entropy ? o.entropy : (o.head_budget == KVC_BUDGET_ENTROPY ? ws.ent : nullptr);
@@ -328,9 +325,9 @@ int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void*
   rc = launch_score(a, ws, s);
   if (rc) return rc;
   rc = launch_select(sc, g.L * g.B * g.Hkv, g.N, prefix, recent, budget, budget_all,
-                     o.head_budget == KVC_BUDGET_ENTROPY ? ent : nullptr, g.Hkv, ki, kept_len, status, s, first);
+                     o.head_budget == KVC_BUDGET_ENTROPY ? ent : nullptr, g.Hkv, ki, kept_len, status, s);
   if (rc) return rc;
-  return launch_compact(g, c->dtype, K, V, ki, kept_len, status, false, s, false, first);
+  return launch_compact(g, c->dtype, K, V, ki, kept_len, status, false, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -346,10 +343,8 @@ struct EpikvWs {
   uint32_t* keys;
   float* scores;
   int32_t* kept;
-  int32_t* first;
 };
-// layout: g [2][B][N] fp32, pre [2][2][B][N+1] fp64, keys [B][N], scores [B][N], kept [B][N],
-// first [B] (each sequence's first moved index, from the selection to the compaction)
+// layout: g [2][B][N] fp32, pre [2][2][B][N+1] fp64, keys [B][N], scores [B][N], kept [B][N]
 size_t epikv_ws(int B, int N, EpikvWs* w, void* base) {
   const size_t bn = (size_t)B * N;
   size_t off = 0;
@@ -358,7 +353,6 @@ size_t epikv_ws(int B, int N, EpikvWs* w, void* base) {
   const size_t o_keys = off;  off += align256(bn * sizeof(uint32_t));
   const size_t o_sc = off;    off += align256(bn * sizeof(float));
   const size_t o_kept = off;  off += align256(bn * sizeof(int32_t));
-  const size_t o_first = off; off += align256((size_t)B * sizeof(int32_t));
   if (w) {
     char* b = static_cast<char*>(base);
     w->g = reinterpret_cast<float*>(b + o_g);
@@ -366,7 +360,6 @@ size_t epikv_ws(int B, int N, EpikvWs* w, void* base) {
     w->keys = reinterpret_cast<uint32_t*>(b + o_keys);
     w->scores = reinterpret_cast<float*>(b + o_sc);
     w->kept = reinterpret_cast<int32_t*>(b + o_kept);
-    w->first = reinterpret_cast<int32_t*>(b + o_first);
   }
   return off;
 }
@@ -425,9 +418,9 @@ int kvc_epikv_evict(const kvc_cache* c, const void* hA, const void* hB, int32_t 
   if (rc) return rc;
   // one selection per sequence on the order-preserving keys of the signed scores
   rc = launch_select(reinterpret_cast<const float*>(w.keys), g.B, g.N, prefix, recent, budget, budget_all, nullptr, 1,
-                     ki, kept_len, status, s, w.first);
+                     ki, kept_len, status, s);
   if (rc) return rc;
-  return launch_compact(g, c->dtype, K, V, ki, kept_len, status, false, s, true, w.first);
+  return launch_compact(g, c->dtype, K, V, ki, kept_len, status, false, s, true);
 }
 
 // ---------------------------------------------------------------------------

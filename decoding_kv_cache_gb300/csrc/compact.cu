@@ -30,7 +30,6 @@ struct CompactArgs {
   int rowbytes;
   int validate;
   int list_seq;  // one kept list per sequence, shared by every layer and KV head (else one per head)
-  const int32_t* first;  // per list: its first index that moves, from the selection; NULL: search
 };
 
 constexpr int kRing = 4;
@@ -52,7 +51,6 @@ __global__ void __launch_bounds__(32) compact_bulk_kernel(CompactArgs a) {
   const int32_t* src = a.kept_idx + (size_t)lst * a.g.N;
   griddep_wait();  // the kept lists come from the previous kernel
   const int len = a.kept_len[lst];
-  const int given = a.first ? a.first[lst] : -1;  // loaded beside len: no search round trips
   const int N = a.g.N;
   if (a.validate) {
     bool bad = len < 0 || len > N;
@@ -66,12 +64,10 @@ __global__ void __launch_bounds__(32) compact_bulk_kernel(CompactArgs a) {
       return;
     }
   }
-  // first index that moves: smallest k with src[k] != k. The selection kernel of an eviction
-  // step records it (clamped here to [0, len]: a smaller value only re-copies rows in place);
-  // otherwise it is searched for (src[k] - k never decreases, so the test is monotone). A 32-way
-  // search: each step the lanes probe 32 points of [lo, hi) at once and a ballot narrows it
-  // 33-fold, so 2048 entries take 3 dependent loads instead of 11.
-  int lo = a.first ? (given < 0 ? 0 : (given > len ? len : given)) : 0, hi = a.first ? lo : len;  // first in [lo, hi]
+  // first index that moves: smallest k with src[k] != k (src[k] - k never decreases, so the
+  // test is monotone). A 32-way search: each step the lanes probe 32 points of [lo, hi) at once
+  // and a ballot narrows it 33-fold, so 2048 entries take 3 dependent loads instead of 11.
+  int lo = 0, hi = len;  // first lies in [lo, hi]
   while (lo < hi) {
     const int span = hi - lo;
     const int pt = lo + (int)(((long long)span * (lane + 1)) / 33);  // < hi, non-decreasing in lane
@@ -186,8 +182,7 @@ __global__ void __launch_bounds__(32) compact_bulk_kernel(CompactArgs a) {
 }
 
 int launch_compact(const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V, const int32_t* kept_idx,
-                   const int32_t* kept_len, int32_t* status, bool validate, cudaStream_t s, bool list_per_seq,
-                   const int32_t* first) {
+                   const int32_t* kept_len, int32_t* status, bool validate, cudaStream_t s, bool list_per_seq) {
   const int heads = g.L * g.B * g.Hkv;
   if (heads == 0) return KVC_OK;
   CompactArgs a;
@@ -200,7 +195,6 @@ int launch_compact(const CacheGeom& g, int dtype, const LayerPtrs& K, const Laye
   a.rowbytes = g.D * (dtype == KVC_BF16 ? 2 : 4);
   a.validate = validate ? 1 : 0;
   a.list_seq = list_per_seq ? 1 : 0;
-  a.first = first;
   const size_t smem = (size_t)kRing * kTileBytes + 64;
   if (cudaFuncSetAttribute(compact_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;

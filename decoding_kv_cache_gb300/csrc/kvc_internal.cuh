@@ -185,18 +185,15 @@ int launch_score_split(const ScoreArgs& a, const ScoreWs& ws, const SplitPlan& p
 int score_launches(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext);
 
 // entropy non-null: each (layer, sequence)'s budgets are reallocated over its Hkv heads first
-// first_moved (or NULL): per head, the first index of its kept list that is not its own token
-// (min(first dropped token, kept length)), for launch_compact
 int launch_select(const float* scores, int heads, int N, int P, int R, const int32_t* budget, int budget_all,
                   const float* entropy, int Hkv, int32_t* kept_idx, int32_t* kept_len, int32_t* status,
-                  cudaStream_t s, int32_t* first_moved = nullptr);
+                  cudaStream_t s);
 int launch_head_budget(const float* entropy, int groups, int Hkv, int N, int P, int R, const int32_t* budget,
                        int budget_all, int32_t* budget_out, int32_t* status, cudaStream_t s);
 
 // list_per_seq: kept_idx [B][N] / kept_len [B], one list per sequence for all its layers and heads
 int launch_compact(const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V, const int32_t* kept_idx,
-                   const int32_t* kept_len, int32_t* status, bool validate, cudaStream_t s, bool list_per_seq = false,
-                   const int32_t* first = nullptr);
+                   const int32_t* kept_len, int32_t* status, bool validate, cudaStream_t s, bool list_per_seq = false);
 
 // EPIKV: signals g [2][B][N] (layer A, layer B), prefix sums pre [2][2][B][N+1] fp64, signed
 // scores [B][N] and (if keys) their order-preserving unsigned keys [B][N] for the radix selection

@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
                                                              const float* __restrict__ entropy, int Hkv,
                                                              int32_t* __restrict__ kept_idx,
                                                              int32_t* __restrict__ kept_len, int32_t* status,
-                                                             int use_smem, int32_t* __restrict__ first_moved) {
+                                                             int use_smem) {
   constexpr int kWarps = kThreads / 32;
   constexpr int kTile = kSweep * kThreads;
   extern __shared__ __align__(16) uint32_t sh_bits[];
@@ -182,7 +182,6 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
   __shared__ unsigned long long wsum[33];
   __shared__ uint32_t s_min[kWarps], s_max[kWarps];
   __shared__ unsigned s_digit, s_k, s_cnt;
-  __shared__ int s_first;
   __shared__ int32_t s_alloc[kMaxBudgetHeads];
   const int head = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   griddep_wait();  // the scores (and entropies) come from the previous kernel
@@ -208,10 +207,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
   if (b >= N || b < P + R) {  // keep everything (out-of-range budgets are flagged)
     if (b < N && tid == 0) status_or(status, KVC_STATUS_BUDGET_RANGE);
     for (int j = tid; j < N; j += blockDim.x) out[j] = j;
-    if (tid == 0) {
-      kept_len[head] = N;
-      if (first_moved) first_moved[head] = N;
-    }
+    if (tid == 0) kept_len[head] = N;
     return;
   }
   if (ntiles > 1 && use_smem) {
@@ -327,8 +323,6 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
   // threshold and of tied tokens before it. The kept tied tokens are the first keq, so a kept
   // token's slot is nk + min(neq, keq).
   int base_k = 0, base_eq = 0;  // totals of the earlier tiles
-  int my_first = N;             // this thread's first dropped token
-  if (tid == 0) s_first = N;    // ordered before the atomics below by the first scan's barriers
   for (int j0 = 0; j0 < N; j0 += kTile) {
     tile_load(j0);
     const int jt = j0 + tid * kSweep;
@@ -349,28 +343,19 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
 #pragma unroll
     for (int e = 0; e < kSweep; ++e) {
       const bool is_gt = (gt >> e) & 1u, is_eq = (eqm >> e) & 1u;
-      const bool kept = is_gt || (is_eq && neq < (int)keq);
-      if (kept) out[nk + min(neq, (int)keq)] = jt + e;
-      else if (jt + e < N && my_first == N) my_first = jt + e;
+      if (is_gt || (is_eq && neq < (int)keq)) out[nk + min(neq, (int)keq)] = jt + e;
       nk += is_gt;
       neq += is_eq;
     }
     base_k += (int)(tot & 0xffffffffull);
     base_eq += (int)(tot >> 32);
   }
-  const int len = base_k + min(base_eq, (int)keq);
-  if (tid == 0) kept_len[head] = len;
-  if (first_moved) {  // the kept list is 0, 1, ... up to the first dropped token
-    my_first = (int)__reduce_min_sync(kFull, (unsigned)my_first);
-    if (lane == 0) atomicMin(&s_first, my_first);
-    __syncthreads();
-    if (tid == 0) first_moved[head] = min(s_first, len);
-  }
+  if (tid == 0) kept_len[head] = base_k + min(base_eq, (int)keq);
 }
 
 int launch_select(const float* scores, int heads, int N, int P, int R, const int32_t* budget, int budget_all,
                   const float* entropy, int Hkv, int32_t* kept_idx, int32_t* kept_len, int32_t* status,
-                  cudaStream_t s, int32_t* first_moved) {
+                  cudaStream_t s) {
   if (heads == 0) return KVC_OK;
   // A head's scores up to 64 KB: 256 threads, so that several heads share an SM and each barrier
   // spans 8 warps (R1-Qwen-7B-shaped heads of 8192 keys: 88 -> 58 us); longer heads fill an SM's
@@ -385,7 +370,7 @@ int launch_select(const float* scores, int heads, int N, int P, int R, const int
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   if (launch_pdl(kern, dim3(heads), dim3(threads), smem, s, false, scores, N, P, R, budget, budget_all,
-                 entropy, Hkv, kept_idx, kept_len, status, use_smem, first_moved) != cudaSuccess)
+                 entropy, Hkv, kept_idx, kept_len, status, use_smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   return KVC_OK;
 }
