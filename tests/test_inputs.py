@@ -5,7 +5,6 @@ channels, planted keys, ReasonAlloc budgets). No GPU; reduced sizes except where
 the full one."""
 import math
 
-import numpy as np
 import pytest
 import torch
 
