@@ -190,13 +190,14 @@ def test_select_matches_oracle_on_the_same_scores():
 
 
 @pytest.mark.parametrize("N,heads", [(3001, 6), (20001, 3), (60001, 2)])
-@pytest.mark.parametrize("dist", ["uniform", "quantised", "split"])
+@pytest.mark.parametrize("dist", ["uniform", "quantised", "split", "constant"])
 def test_select_sizes_and_distributions(N, heads, dist):
     """Every launch shape of the selection (256 threads with the scores in shared memory, 1024
     threads, and the global-memory path past 51200 tokens), token counts that are not a multiple
-    of 4 or of the sweep's groups, and three score laws: distinct values, heavy exact ties, and a
-    split where the k-th largest score's leading digit holds exactly the kept middle tokens (the
-    digit search then stops after its first digit)."""
+    of 4 or of the sweep's groups, and four score laws: distinct values, heavy exact ties, a split
+    where the k-th largest score's leading digit holds exactly the kept middle tokens (the digit
+    search then stops after its first digit), and one value everywhere (no digit pass at all: the
+    lowest-index middle tokens are kept)."""
     from decoding_kv_cache_gb300 import kvc
     g = torch.Generator().manual_seed(N + len(dist))
     P, R = 4, 16
@@ -205,6 +206,8 @@ def test_select_sizes_and_distributions(N, heads, dist):
         sc = torch.rand((heads, N), generator=g)
     elif dist == "quantised":
         sc = torch.randint(0, 40, (heads, N), generator=g).float() / 64.0
+    elif dist == "constant":
+        sc = torch.full((heads, N), 0.375)
     else:
         sc = 0.25 + torch.rand((heads, N), generator=g) * 0.2
         for h in range(heads):
