@@ -31,7 +31,8 @@ if ROOT not in sys.path:
 
 METRIC = "eviction-step cached tokens/sec and achieved HBM GB/s vs GB300 peak (1 GPU)"
 UNIT = "cached tokens/s"
-DEFAULT_CONFIG = "qwen3-4b"
+DEFAULT_CONFIG = "qwen3-14b-long"
+SINGLE_CORE_CONFIGS = ("tiny", "qwen3-4b")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -177,15 +178,52 @@ def variant_of(args) -> str:
     return "" if v == "max,max" else v
 
 
-def workload_desc(inp, variant=""):
-    keep = "per-head budgets" if inp.budget is not None else f"{inp.budget_all}"
-    d = (f"{inp.name} eviction step: L{inp.L} B{inp.B} Hq{inp.Hq} Hkv{inp.Hkv} D{inp.D} {inp.dtype} "
-         f"N{inp.N}->{keep}, obs {inp.n_r} recent + {inp.n_b} beacons (buffer {inp.qmax})")
+def workload_desc(config: str, variant: str = "", layers: int = 0) -> str:
+    """The workload's name and shape from its spec (no tensors), the same string in both arms."""
+    from decoding_kv_cache_gb300.inputs import CONFIGS, EPIKV_CONFIGS
+    if config in EPIKV_CONFIGS:
+        sp = EPIKV_CONFIGS[config]
+        L = layers or sp["L"]
+        return (f"{config} EPIKV eviction step: L{L} B{sp['B']} Hkv{sp['Hkv']} D{sp['D']} {sp['dtype']} "
+                f"N{sp['N']}->{(7 * sp['N']) // 8}, hidden size {sp['dm']} (band layers A, B), window "
+                f"{sp['window']}, eps {sp['eps']:g}")
+    sp = CONFIGS[config]
+    L = layers or sp["L"]
+    keep = "per-head budgets" if sp["cfg"] == 4 else f"{(7 * sp['N']) // 8}"
+    d = (f"{config} eviction step: L{L} B{sp['B']} Hq{sp['Hq']} Hkv{sp['Hkv']} D{sp['D']} {sp['dtype']} "
+         f"N{sp['N']}->{keep}, obs {sp['n_r']} recent + {sp['n_b']} beacons (buffer {sp['qmax']})")
     if variant:
         d += (f"; aggregation {variant.split('+')[0]} (rows, GQA group)" +
               ("; budgets reallocated per layer by attention entropy" if "budgets" in variant else "") +
               ("; entropy output" if variant.endswith("+entropy") else ""))
     return d
+
+
+def pinned_like(t):
+    """A page-locked host copy of a device tensor (one host allocation, filled by a D2H copy)."""
+    import torch
+    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    h.copy_(t)
+    return h
+
+
+def h2d_anchor(hosts, devs, stream, reps: int = 3):
+    """A plain pinned host-to-device copy of the same tensors the e2e step copies (CUDA events on the
+    launch stream, best of ``reps``): the copy engines' rate that bounds the e2e figure."""
+    import torch
+    nbytes = sum(h.numel() * h.element_size() for h in hosts)
+    best = None
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for h, d in zip(hosts, devs):
+            d.copy_(h, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    return {"bytes": nbytes, "ms": best, "gbs": nbytes / (best / 1e3) / 1e9,
+            "note": "plain pinned H2D copies of the e2e inputs, no kernel, best of %d" % reps}
 
 
 def algorithmic_bytes(inp, kept_idx, kept_len):
@@ -358,10 +396,10 @@ def gpu_arm(args, rank, world, local_rank):
     dom = max(phase_ms, key=phase_ms.get)
 
     # ---- end to end: host buffers in, step, result out ------------------------------------
-    pin = lambda t: t.cpu().pin_memory()
-    hK, hV, hqr, hqb, hc = pin(K0), pin(V0), pin(inp.q_recent), pin(inp.qbuf), pin(inp.count)
+    hK, hV, hqr, hqb, hc = (pinned_like(t) for t in (K0, V0, inp.q_recent, inp.qbuf, inp.count))
     hkl, hki = torch.empty_like(kept_len, device="cpu").pin_memory(), torch.empty_like(kept_idx, device="cpu").pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hK, hV, hqr, hqb, hc))
+    anchor = h2d_anchor((hK, hV), (inp.K, inp.V), stream)
     d2h = hkl.numel() * 4 + hki.numel() * 4
     n_e2e = max(3, min(args.steps, 20))
     ee = []
@@ -393,7 +431,7 @@ def gpu_arm(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": inp.dtype, "data": "synthetic",
-        "config": {"workload": workload_desc(inp, variant), "l2": "flushed between steps (512 MB write, then a 512 MB read so no dirty line is left), cache restored "
+        "config": {"workload": workload_desc(args.config, variant, args.layers), "l2": "flushed between steps (512 MB write, then a 512 MB read so no dirty line is left), cache restored "
                    "from a pristine copy between steps; both untimed", "parallelism": f"replicas x{world}",
                    "timing": "CUDA events around each kvc_evict on the launch stream"},
         "head_tokens_per_s": world * inp.heads * inp.N * args.steps / (total_ms / 1e3),
@@ -405,7 +443,7 @@ def gpu_arm(args, rank, world, local_rank):
                                                                                           else ""), dom)},
         "phases_ms": phase_ms,
         "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "h2d_copy_anchor": anchor},
         "append": app,
         "gpu_launches": args.steps * kvc.kvc_evict_launch_count(cache, inp.n_r, inp.n_b),
         "clocks": clk,
@@ -499,10 +537,10 @@ def epikv_arm(args, rank, world, local_rank):
         ("select+compact", moved_bytes, rest_ms)
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
 
-    pin = lambda t: t.cpu().pin_memory()
-    hK, hV, hA, hB = pin(K0), pin(V0), pin(inp.hA), pin(inp.hB)
+    hK, hV, hA, hB = (pinned_like(t) for t in (K0, V0, inp.hA, inp.hB))
     hkl, hki = torch.empty_like(kept_len, device="cpu").pin_memory(), torch.empty_like(kept_idx, device="cpu").pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hK, hV, hA, hB))
+    anchor = h2d_anchor((hK, hV), (inp.K, inp.V), stream)
     d2h = hkl.numel() * 4 + hki.numel() * 4
     ee = []
     for i in range(max(3, min(args.steps, 10))):
@@ -526,9 +564,7 @@ def epikv_arm(args, rank, world, local_rank):
         "metric": METRIC, "value": world * tokens * args.steps / (total_ms / 1e3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": inp.dtype, "data": "synthetic",
-        "config": {"workload": (f"{inp.name} EPIKV eviction step: L{inp.L} B{inp.B} Hkv{inp.Hkv} D{inp.D} {inp.dtype} "
-                                f"N{inp.N}->{inp.budget_all}, hidden size {inp.dm} (band layers A, B), window "
-                                f"{inp.window}, eps {inp.eps:g}"),
+        "config": {"workload": workload_desc(args.config, "", args.layers),
                    "l2": "flushed between steps (512 MB write, then a 512 MB read so no dirty line is left), cache restored from a pristine copy between steps; "
                          "both untimed", "parallelism": f"replicas x{world}",
                    "timing": "CUDA events around each kvc_epikv_evict on the launch stream"},
@@ -538,7 +574,7 @@ def epikv_arm(args, rank, world, local_rank):
                      "frac": achieved / hbm, "peak_source": pk_kind, "traffic": None},
         "phases_ms": {"kvc_epikv_score": score_ms, "select+compact": rest_ms},
         "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "h2d_copy_anchor": anchor},
         "gpu_launches": args.steps * 5,  # signal, prefix sums, z-score, select, compact
         "clocks": clk,
     }
@@ -582,15 +618,15 @@ def oracle_epikv_sample(config: str, budget_s: float = 12.0):
 # CPU oracle (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(config: str, budget_s: float = 12.0, **variant):
+def oracle_sample(config: str, budget_s: float = 12.0, threads: int = 0, **variant):
     """Time the oracle, as it stands, on a bounded sample of the workload's heads (``variant``:
-    the oracle's row_agg / group_agg / head_budget keywords).
+    the oracle's row_agg / group_agg / head_budget keywords; ``threads`` 0 = every core).
     Returns (tokens/s scaled to the full step, cores, sample description, seconds)."""
     from decoding_kv_cache_gb300.inputs import make_inputs
     from oracle import oracle as O
     from decoding_kv_cache_gb300.inputs import CONFIGS
     spec = CONFIGS[config]
-    cores = O.set_threads(os.cpu_count() or 1)
+    cores = O.set_threads(threads or os.cpu_count() or 1)
     heads_full = spec["L"] * spec["B"] * spec["Hkv"]
     # one layer of one sequence first, to size the sample
     probe = make_inputs(config, L=1, B=1)
@@ -644,7 +680,7 @@ def reference_arm(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": spec["B"] * spec["N"] / value * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.config + (f" ({variant_of(args)})" if variant_of(args) else "")},
+            "config": {"workload": workload_desc(args.config, "" if epikv else variant_of(args))},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores,
                                                                  "kind": "oracle", "sample": descs[-1]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -691,6 +727,10 @@ def main():
             tok, cores, desc, _ = oracle_epikv_sample(args.config) if epikv else \
                 oracle_sample(args.config, **oracle_variant(args))
             res["cpu_baseline"] = {"value": tok, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+            if args.config in SINGLE_CORE_CONFIGS:  # the two small workloads also on one core
+                tok1, c1, desc1, _ = oracle_sample(args.config, threads=1, **oracle_variant(args))
+                res["cpu_baseline_1core"] = {"value": tok1, "unit": UNIT, "cores": c1, "kind": "oracle",
+                                             "sample": desc1}
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

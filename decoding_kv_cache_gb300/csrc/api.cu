@@ -47,21 +47,24 @@ int check_cache(const kvc_cache* c, CacheGeom* g, LayerPtrs* K, LayerPtrs* V) {
 struct Opts {
   bool ext;
   int row_agg, group_agg, head_budget;
+  int kernel;      // KVC_KERNEL_* (a test and profiling aid)
   float* entropy;  // the caller's entropy output, or null
 };
 
 int check_opts(const kvc_opts* o, bool evict, Opts* out) {
-  *out = Opts{false, KVC_AGG_MAX, KVC_AGG_MAX, KVC_BUDGET_GIVEN, nullptr};
+  *out = Opts{false, KVC_AGG_MAX, KVC_AGG_MAX, KVC_BUDGET_GIVEN, KVC_KERNEL_AUTO, nullptr};
   if (!o) return KVC_OK;
   if ((o->row_agg != KVC_AGG_MAX && o->row_agg != KVC_AGG_MEAN) ||
       (o->group_agg != KVC_AGG_MAX && o->group_agg != KVC_AGG_SUM) ||
-      (o->head_budget != KVC_BUDGET_GIVEN && o->head_budget != KVC_BUDGET_ENTROPY) || o->reserved != 0)
+      (o->head_budget != KVC_BUDGET_GIVEN && o->head_budget != KVC_BUDGET_ENTROPY) || o->kernel < KVC_KERNEL_AUTO ||
+      o->kernel > KVC_KERNEL_FUSED)
     return KVC_ERR_INVALID_ARG;
   if (!evict && o->head_budget != KVC_BUDGET_GIVEN) return KVC_ERR_INVALID_ARG;
   if (o->entropy && (reinterpret_cast<uintptr_t>(o->entropy) & 3u)) return KVC_ERR_ALIGNMENT;
   out->row_agg = o->row_agg;
   out->group_agg = o->group_agg;
   out->head_budget = o->head_budget;
+  out->kernel = o->kernel;
   out->entropy = o->entropy;
   out->ext = o->row_agg != KVC_AGG_MAX || o->group_agg != KVC_AGG_MAX || o->entropy ||
              o->head_budget == KVC_BUDGET_ENTROPY;
@@ -105,6 +108,7 @@ void fill_score_args(ScoreArgs* a, const CacheGeom& g, int dtype, const LayerPtr
   a->group_agg = o.group_agg;
   a->entropy = entropy;
   a->tiles = 1;  // launch_score may split 256-row tiles
+  a->kernel = o.kernel;
   a->debug_fault = g_debug_fault.load();
   a->dtype = dtype;
   a->K = K;
@@ -418,7 +422,7 @@ int kvc_epikv_evict(const kvc_cache* c, const void* hA, const void* hB, int32_t 
   if (rc) return rc;
   // one selection per sequence on the order-preserving keys of the signed scores
   rc = launch_select(reinterpret_cast<const float*>(w.keys), g.B, g.N, prefix, recent, budget, budget_all, nullptr, 1,
-                     ki, kept_len, status, s);
+                     ki, kept_len, status, s, true);
   if (rc) return rc;
   return launch_compact(g, c->dtype, K, V, ki, kept_len, status, false, s, true);
 }
@@ -428,29 +432,24 @@ int kvc_epikv_evict(const kvc_cache* c, const void* hA, const void* hB, int32_t 
 // ---------------------------------------------------------------------------
 }  // extern "C"
 
-#include <mutex>
-
 namespace kvc {
 namespace {
 // The region every kvc_score_static call on a device uses (see kvc.h for sharing rules).
 static __device__ __align__(256) unsigned char g_score_scratch[KVC_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the region on the current device, looked up once per device with that
-// device current (the symbol's name is only a host-side stand-in). NULL on failure.
+// Device address of the region in the current context (the symbol's name is only a host-side
+// stand-in). Looked up on every call, not cached: a cached address would outlive the context it
+// came from (after cudaDeviceReset, or a primary context released and made again) and point a
+// launch at freed memory. The lookup is a table read once the module is loaded; the first one on
+// a device loads the module, which is why the first call must come before any stream capture.
+// NULL on failure.
 void* static_scratch() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_score_scratch) != cudaSuccess) return nullptr;
-    g_scratch_addr[dev] = p;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_score_scratch) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
   }
-  return g_scratch_addr[dev];
+  return p;
 }
 }  // namespace
 }  // namespace kvc

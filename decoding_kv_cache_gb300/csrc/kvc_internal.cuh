@@ -135,6 +135,7 @@ struct ScoreArgs {
   unsigned long long* xch_zero;  // words the observation kernel zeroes for the scoring kernel, or null
   long long xch_zero_words;
   int debug_fault;               // kvc_debug_fault mode at launch (0 in normal use)
+  int kernel;                    // KVC_KERNEL_*: the bf16 scoring kernel asked for (0 = automatic)
   // Variants: an aggregation other than max/max or an entropy output runs the kernels'
   // extended epilogue (ext = 1). Rows of query head g then start at g * qstride, a multiple
   // of 16, so every 16-row block of the tile belongs to one query head.
@@ -184,10 +185,11 @@ int launch_score_split(const ScoreArgs& a, const ScoreWs& ws, const SplitPlan& p
 // kernels launch_score starts for these arguments (host only; default options when !ext)
 int score_launches(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext);
 
-// entropy non-null: each (layer, sequence)'s budgets are reallocated over its Hkv heads first
+// entropy non-null: each (layer, sequence)'s budgets are reallocated over its Hkv heads first;
+// keyed: `scores` holds order-preserving unsigned keys already (EPIKV), not fp32 scores
 int launch_select(const float* scores, int heads, int N, int P, int R, const int32_t* budget, int budget_all,
                   const float* entropy, int Hkv, int32_t* kept_idx, int32_t* kept_len, int32_t* status,
-                  cudaStream_t s);
+                  cudaStream_t s, bool keyed = false);
 int launch_head_budget(const float* entropy, int groups, int Hkv, int N, int P, int R, const int32_t* budget,
                        int budget_all, int32_t* budget_out, int32_t* status, cudaStream_t s);
 

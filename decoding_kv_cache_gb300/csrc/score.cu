@@ -379,18 +379,6 @@ static bool set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess;
 }
 
-// KVC_SCORE_PATH (a test and profiling aid; unset in normal use) forces the bf16 scoring kernel:
-// "resident" (single read; falls through where it does not apply), "split" (two-pass streaming;
-// default options only) or "fused" (two-pass with group exchange). 0 = automatic choice.
-static int score_path_override() {
-  const char* v = getenv("KVC_SCORE_PATH");
-  if (!v || !*v) return 0;
-  if (!strcmp(v, "resident")) return 1;
-  if (!strcmp(v, "split")) return 2;
-  if (!strcmp(v, "fused")) return 3;
-  return 0;
-}
-
 // Which bf16 scoring kernel runs (sets a->tiles); 0 = fp32 passes.
 enum ScorePath { kPathF32 = 0, kPathResident = 1, kPathSplit = 2, kPathFused = 3 };
 static ScorePath choose_score(ScoreArgs* a, FusedPlan* rp, size_t* rsmem, SplitPlan* sp, size_t* ssmem) {
@@ -410,10 +398,10 @@ static ScorePath choose_score(ScoreArgs* a, FusedPlan* rp, size_t* rsmem, SplitP
   // The two-pass streaming kernel takes over where the single-read kernel's per-round meetings
   // would involve many CTAs (more than 16 per head, i.e. more than 4096 keys) or two row tiles.
   bool split = score_split_plan(*a, sp, ssmem);
-  const int path = score_path_override();
-  if (split && path == 0) split = !resident || a->M_pad > 128 || rp->group_size > 16;
-  if (split && path != 0) split = path == 2;
-  if (resident && path == 3) resident = false;
+  const int path = a->kernel;  // KVC_KERNEL_*: forced by the caller (tests, profiling) or automatic
+  if (split && path == KVC_KERNEL_AUTO) split = !resident || a->M_pad > 128 || rp->group_size > 16;
+  if (split && path != KVC_KERNEL_AUTO) split = path == KVC_KERNEL_SPLIT;
+  if (resident && path == KVC_KERNEL_FUSED) resident = false;
   if (split) resident = false;
   if (!resident) a->tiles = 1;
   return resident ? kPathResident : (split ? kPathSplit : kPathFused);

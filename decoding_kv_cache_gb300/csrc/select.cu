@@ -5,8 +5,11 @@
 // 7/8 of B_KV^max. ReasonAlloc note, "Core Mechanism": the budget may differ per head.
 //
 // One CTA per head (256 or 1024 threads, each holding 8 consecutive tokens of a tile; a head of
-// one tile stays in registers). Scores are non-negative fp32, so their IEEE bit patterns order
-// like the values; a radix select finds the bit pattern T of the k-th largest middle score and
+// one tile stays in registers). Each fp32 score becomes an unsigned key that orders like the
+// value (sign bit set: all bits flipped; else the sign bit set; -0 taken as +0), so any finite
+// score, negative ones included, ranks as its value does (a NaN with the sign bit clear ranks
+// above +inf, one with it set below -inf); EPIKV hands over such keys already made. A radix
+// select finds the key T of the k-th largest middle score and
 // how many copies of T must be kept. The leading bits shared by every middle score (from their
 // minimum and maximum) are skipped; then 8-bit digits, one shared-memory histogram pass each (two
 // barriers, the next pass's bins cleared during this one), stopping early once the rank's bucket
@@ -155,10 +158,17 @@ __device__ __forceinline__ unsigned long long block_excl_scan64(unsigned long lo
 
 constexpr int kSweep = 8;  // consecutive tokens per thread: a tile is kSweep * threads tokens
 
-// This thread's kSweep consecutive tokens from j: two 16-byte loads where the source allows
-// (vec: base 16-byte aligned and j a multiple of kSweep), else element by element; tokens past N
-// read as 0.
-__device__ __forceinline__ void load_group(const uint32_t* p, int j, int N, bool vec, uint32_t (&w)[kSweep]) {
+// Order-preserving key of an fp32 score's bits (-0 as +0).
+__device__ __forceinline__ uint32_t score_key(uint32_t u) {
+  u = u == 0x80000000u ? 0u : u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// This thread's kSweep consecutive tokens from j as keys: two 16-byte loads where the source
+// allows (vec: base 16-byte aligned and j a multiple of kSweep), else element by element; tokens
+// past N read as 0 (they lie outside the middle). keyed: the words are keys already.
+__device__ __forceinline__ void load_group(const uint32_t* p, int j, int N, bool vec, bool keyed,
+                                           uint32_t (&w)[kSweep]) {
   if (vec && j + kSweep <= N) {
     const uint4 x = *reinterpret_cast<const uint4*>(p + j), y = *reinterpret_cast<const uint4*>(p + j + 4);
     w[0] = x.x, w[1] = x.y, w[2] = x.z, w[3] = x.w, w[4] = y.x, w[5] = y.y, w[6] = y.z, w[7] = y.w;
@@ -166,6 +176,9 @@ __device__ __forceinline__ void load_group(const uint32_t* p, int j, int N, bool
 #pragma unroll
     for (int e = 0; e < kSweep; ++e) w[e] = j + e < N ? p[j + e] : 0u;
   }
+  if (!keyed)
+#pragma unroll
+    for (int e = 0; e < kSweep; ++e) w[e] = score_key(w[e]);
 }
 
 template <int kThreads>
@@ -174,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
                                                              const float* __restrict__ entropy, int Hkv,
                                                              int32_t* __restrict__ kept_idx,
                                                              int32_t* __restrict__ kept_len, int32_t* status,
-                                                             int use_smem) {
+                                                             int use_smem, int keyed) {
   constexpr int kWarps = kThreads / 32;
   constexpr int kTile = kSweep * kThreads;
   extern __shared__ __align__(16) uint32_t sh_bits[];
@@ -194,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
   const uint32_t* bits = reinterpret_cast<const uint32_t*>(sc);
   bool vec = (N & 3) == 0 && (reinterpret_cast<uintptr_t>(sc) & 15) == 0;
   uint32_t w[kSweep];
-  if (ntiles == 1) load_group(bits, tid * kSweep, N, vec, w);
+  if (ntiles == 1) load_group(bits, tid * kSweep, N, vec, keyed, w);
   int b = budget ? budget[head] : budget_all;
   if (entropy) {  // this head's share of its (layer, sequence)'s reallocated total (warp 0)
     const int lb = head / Hkv, h = head % Hkv;
@@ -224,7 +237,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
     vec = true;
   }
   auto tile_load = [&](int j0) {
-    if (ntiles > 1) load_group(bits, j0 + tid * kSweep, N, vec, w);
+    if (ntiles > 1) load_group(bits, j0 + tid * kSweep, N, vec, keyed, w);
   };
   for (int i = tid; i < 256; i += kThreads) hist[0][i] = 0;
 
@@ -235,7 +248,8 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
   unsigned keq = 0;
   if (kmid > 0) {
     // the leading bits that every middle token shares (from their minimum and maximum) need no
-    // digit pass: scores in (0, 1] share several, and a digit over them would fill one bin
+    // digit pass: the keys of scores in (0, 1] share several, and a digit over them would fill
+    // one bin
     uint32_t mn = 0xffffffffu, mx = 0u;
     for (int j0 = 0; j0 < N; j0 += kTile) {
       tile_load(j0);
@@ -355,7 +369,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
 
 int launch_select(const float* scores, int heads, int N, int P, int R, const int32_t* budget, int budget_all,
                   const float* entropy, int Hkv, int32_t* kept_idx, int32_t* kept_len, int32_t* status,
-                  cudaStream_t s) {
+                  cudaStream_t s, bool keyed) {
   if (heads == 0) return KVC_OK;
   // A head's scores up to 64 KB: 256 threads, so that several heads share an SM and each barrier
   // spans 8 warps (R1-Qwen-7B-shaped heads of 8192 keys: 88 -> 58 us); longer heads fill an SM's
@@ -370,7 +384,7 @@ int launch_select(const float* scores, int heads, int N, int P, int R, const int
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   if (launch_pdl(kern, dim3(heads), dim3(threads), smem, s, false, scores, N, P, R, budget, budget_all,
-                 entropy, Hkv, kept_idx, kept_len, status, use_smem) != cudaSuccess)
+                 entropy, Hkv, kept_idx, kept_len, status, use_smem, keyed ? 1 : 0) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   return KVC_OK;
 }

@@ -23,12 +23,14 @@ EXPORTED = ("kvc_fps_update", "kvc_score_workspace_size", "kvc_score", "kvc_sele
             "kvc_evict_workspace_size", "kvc_evict", "kvc_evict_launch_count", "kvc_strerror", "kvc_abi_version",
             "kvc_score_static", "kvc_debug_fault", "kvc_head_budget", "kvc_append", "kvc_epikv_workspace_size",
             "kvc_epikv_score", "kvc_epikv_evict")
-KVC_ABI_VERSION = 4
+KVC_ABI_VERSION = 5
 KVC_AGG_MAX, KVC_AGG_MEAN, KVC_AGG_SUM = 0, 1, 2
 KVC_BUDGET_GIVEN, KVC_BUDGET_ENTROPY = 0, 1
 ROW_AGG = {"max": KVC_AGG_MAX, "mean": KVC_AGG_MEAN}
 GROUP_AGG = {"max": KVC_AGG_MAX, "sum": KVC_AGG_SUM}
 HEAD_BUDGET = {"given": KVC_BUDGET_GIVEN, "entropy": KVC_BUDGET_ENTROPY}
+# bf16 scoring kernel (a test and profiling aid; every kernel computes the same scores)
+KERNEL = {"auto": 0, "resident": 1, "split": 2, "fused": 3}
 KVC_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -46,7 +48,7 @@ class kvc_cache(C.Structure):
 
 class kvc_opts(C.Structure):
     _fields_ = [("row_agg", C.c_int32), ("group_agg", C.c_int32), ("head_budget", C.c_int32),
-                ("reserved", C.c_int32), ("entropy", C.c_void_p)]
+                ("kernel", C.c_int32), ("entropy", C.c_void_p)]
 
 
 _lib = None
@@ -196,12 +198,13 @@ def kvc_debug_fault(mode: int) -> None:
 
 
 def make_opts(row_agg: str = "max", group_agg: str = "max", head_budget: str = "given",
-              entropy: Optional[torch.Tensor] = None):
-    """A ``kvc_opts`` (see kvc.h), or None for the defaults (max/max, budgets as given, no entropy)."""
-    if row_agg == "max" and group_agg == "max" and head_budget == "given" and entropy is None:
+              entropy: Optional[torch.Tensor] = None, kernel: str = "auto"):
+    """A ``kvc_opts`` (see kvc.h), or None for the defaults (max/max, budgets as given, no entropy,
+    automatic kernel choice)."""
+    if row_agg == "max" and group_agg == "max" and head_budget == "given" and entropy is None and kernel == "auto":
         return None
     return kvc_opts(row_agg=ROW_AGG[row_agg], group_agg=GROUP_AGG[group_agg], head_budget=HEAD_BUDGET[head_budget],
-                    reserved=0, entropy=_p(entropy))
+                    kernel=KERNEL[kernel], entropy=_p(entropy))
 
 
 def _opts_ref(o):
@@ -217,11 +220,11 @@ def _workspace(nbytes: int, device, workspace):
 def kvc_score(cache: Cache, q_recent: torch.Tensor, qbuf: torch.Tensor, count: torch.Tensor, n_b: int, t: int,
               rope_theta: float, scores: torch.Tensor, beacon_picks: Optional[torch.Tensor] = None,
               workspace: Optional[torch.Tensor] = None, stream=None, row_agg: str = "max", group_agg: str = "max",
-              entropy: Optional[torch.Tensor] = None):
-    """Scores of every cached key; ``row_agg``/``group_agg``/``entropy`` select the variants of kvc_opts."""
+              entropy: Optional[torch.Tensor] = None, kernel: str = "auto"):
+    """Scores of every cached key; ``row_agg``/``group_agg``/``entropy``/``kernel`` set kvc_opts."""
     n_r, qmax = q_recent.shape[-2], qbuf.shape[-2]
     ws = _workspace(kvc_score_workspace_size(cache, n_r, n_b), scores.device, workspace)
-    o = make_opts(row_agg, group_agg, "given", entropy)
+    o = make_opts(row_agg, group_agg, "given", entropy, kernel)
     _check(lib().kvc_score(cache.ref, _p(q_recent), n_r, _p(qbuf), _p(count), qmax, n_b, int(t), float(rope_theta),
                            _p(scores), _p(beacon_picks), _opts_ref(o), _p(ws), ws.numel() * ws.element_size(),
                            _stream(stream)))
@@ -230,11 +233,11 @@ def kvc_score(cache: Cache, q_recent: torch.Tensor, qbuf: torch.Tensor, count: t
 def kvc_score_static(cache: Cache, q_recent: torch.Tensor, qbuf: torch.Tensor, count: torch.Tensor, n_b: int,
                      t: int, rope_theta: float, scores: torch.Tensor, beacon_picks: Optional[torch.Tensor] = None,
                      stream=None, row_agg: str = "max", group_agg: str = "max",
-                     entropy: Optional[torch.Tensor] = None):
+                     entropy: Optional[torch.Tensor] = None, kernel: str = "auto"):
     """kvc_score with the library's fixed scratch region instead of a workspace (allocates nothing;
     see kvc.h for the size limit and the sharing rules)."""
     n_r, qmax = q_recent.shape[-2], qbuf.shape[-2]
-    o = make_opts(row_agg, group_agg, "given", entropy)
+    o = make_opts(row_agg, group_agg, "given", entropy, kernel)
     _check(lib().kvc_score_static(cache.ref, _p(q_recent), n_r, _p(qbuf), _p(count), qmax, n_b, int(t),
                                   float(rope_theta), _p(scores), _p(beacon_picks), _opts_ref(o), _stream(stream)))
 
@@ -257,12 +260,12 @@ def kvc_evict(cache: Cache, q_recent: torch.Tensor, qbuf: torch.Tensor, count: t
               budget: Optional[torch.Tensor] = None, budget_all: int = 0, kept_idx: Optional[torch.Tensor] = None,
               scores: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
               workspace: Optional[torch.Tensor] = None, stream=None, row_agg: str = "max", group_agg: str = "max",
-              head_budget: str = "given", entropy: Optional[torch.Tensor] = None):
+              head_budget: str = "given", entropy: Optional[torch.Tensor] = None, kernel: str = "auto"):
     """The whole eviction step (beacons, scores, selection, in-place compaction) on one stream.
-    ``row_agg``/``group_agg``/``head_budget``/``entropy`` select the variants of kvc_opts."""
+    ``row_agg``/``group_agg``/``head_budget``/``entropy``/``kernel`` set kvc_opts."""
     n_r, qmax = q_recent.shape[-2], qbuf.shape[-2]
     ws = _workspace(kvc_evict_workspace_size(cache, n_r, n_b), kept_len.device, workspace)
-    o = make_opts(row_agg, group_agg, head_budget, entropy)
+    o = make_opts(row_agg, group_agg, head_budget, entropy, kernel)
     _check(lib().kvc_evict(cache.ref, _p(q_recent), n_r, _p(qbuf), _p(count), qmax, n_b, int(t), float(rope_theta),
                            prefix, recent, _p(budget), int(budget_all), _p(kept_idx), _p(kept_len), _p(scores),
                            _p(status), _opts_ref(o), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))

@@ -11,8 +11,11 @@
  * ---------------------------------------
  * - Pointers named in a "device" comment are CUDA device pointers (or
  *   managed memory); everything else is host memory read during the call only.
- *   The caller owns every buffer; the library allocates nothing, keeps no
- *   global state and never synchronises the stream.
+ *   The caller owns every buffer; the library allocates nothing and never
+ *   synchronises the stream. Results depend only on a call's arguments. The
+ *   library holds two pieces of process state, neither of which a normal call
+ *   depends on: kvc_score_static's fixed device region (its scratch, see there)
+ *   and the test-only switch of kvc_debug_fault (off unless a test turns it on).
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream). Every kernel is launched on it, in call order.
  * - Return value: KVC_OK (0) or a negative KVC_ERR_* code. Every argument is
@@ -41,7 +44,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 4
+#define KVC_ABI_VERSION 5
 #define KVC_MAX_LAYERS 128
 
 #if defined(__GNUC__)
@@ -99,11 +102,19 @@ enum {
 #define KVC_AGG_SUM 2  /* group_agg only */
 #define KVC_BUDGET_GIVEN 0
 #define KVC_BUDGET_ENTROPY 1
+/* Scoring kernel for bf16 caches (kernel field; a test and profiling aid: every
+ * kernel computes the same scores). KVC_KERNEL_AUTO picks by shape; a forced
+ * kernel that does not apply to the call falls back to the automatic choice
+ * (RESIDENT: 128-row tiles and short caches; SPLIT: default options only). */
+#define KVC_KERNEL_AUTO 0
+#define KVC_KERNEL_RESIDENT 1 /* single read of K, logits held in tensor memory */
+#define KVC_KERNEL_SPLIT 2    /* two streaming passes, independent work items */
+#define KVC_KERNEL_FUSED 3    /* two passes with a per-group exchange */
 typedef struct {
   int32_t row_agg;     /* KVC_AGG_MAX or KVC_AGG_MEAN */
   int32_t group_agg;   /* KVC_AGG_MAX or KVC_AGG_SUM */
   int32_t head_budget; /* KVC_BUDGET_GIVEN or KVC_BUDGET_ENTROPY (kvc_evict only) */
-  int32_t reserved;    /* must be 0 */
+  int32_t kernel;      /* KVC_KERNEL_* (0 = automatic) */
   float* entropy;      /* [L,B,Hkv] fp32 (device, out) or NULL */
 } kvc_opts;
 
@@ -234,7 +245,9 @@ KVC_API int kvc_score(const kvc_cache* c, const void* q_recent, int32_t n_r, con
  * scores of [prefix, N-recent), equal scores going to the lower index.
  * kept_idx receives the kept token indices in ascending order.
  *
- *   scores       [L,B,Hkv,N] fp32 (device); compared as IEEE bit patterns (>= 0)
+ *   scores       [L,B,Hkv,N] fp32 (device); ranked by value (any finite value, -0 equal
+ *                to +0; a NaN with the sign bit clear ranks above +inf, one with it set
+ *                below -inf)
  *   budget       [L,B,Hkv] int32 (device) or NULL to use budget_all for all heads;
  *                an entry < prefix + recent sets KVC_STATUS_BUDGET_RANGE and
  *                keeps that head whole
@@ -295,8 +308,10 @@ KVC_API int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, con
  * - Size limit: the call is rejected with KVC_ERR_WORKSPACE, before any launch, when
  *   kvc_score_workspace_size() for these arguments exceeds KVC_STATIC_SCRATCH_BYTES
  *   (the Qwen3-4B-shaped step, about 11.9 MB, fits; larger caches do not).
- * - Set-up: the first call on a device looks up the region's device address with that
- *   device current; make that first call before any CUDA stream capture.
+ * - Set-up: every call looks up the region's device address in the calling thread's
+ *   current context (cudaGetSymbolAddress, with the device current), so a context that
+ *   was reset and made again gets its own region. The first call on a device also loads
+ *   the library's device code there: make that first call before any CUDA stream capture.
  * - Sharing: every call on a device uses the same region and leaves its contents behind
  *   (the library clears what must start at zero). Calls whose kernels overlap on the GPU
  *   (two streams, or two threads) race on the region: order them on one stream.

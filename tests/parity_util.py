@@ -27,7 +27,8 @@ def storage_to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().double().numpy()
 
 
-def run_evict(inp, dev, with_scores=True, row_agg="max", group_agg="max", head_budget="given", entropy=False):
+def run_evict(inp, dev, with_scores=True, row_agg="max", group_agg="max", head_budget="given", entropy=False,
+              kernel="auto"):
     """kvc_evict on a device copy of ``inp``; returns numpy results and the compacted cache.
     ``entropy=True`` also returns the per-head normalised entropy output."""
     from decoding_kv_cache_gb300 import kvc
@@ -40,14 +41,14 @@ def run_evict(inp, dev, with_scores=True, row_agg="max", group_agg="max", head_b
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     kvc.kvc_evict(cache, g.q_recent, g.qbuf, g.count, g.n_b, g.t, g.theta, g.prefix, g.recent, kept_len,
                   budget=g.budget, budget_all=g.budget_all, kept_idx=kept_idx, scores=scores, status=status,
-                  row_agg=row_agg, group_agg=group_agg, head_budget=head_budget, entropy=ent)
+                  row_agg=row_agg, group_agg=group_agg, head_budget=head_budget, entropy=ent, kernel=kernel)
     torch.cuda.synchronize()
     return dict(kept_len=kept_len.cpu().numpy(), kept_idx=kept_idx.cpu().numpy(),
                 scores=None if scores is None else scores.cpu().numpy(), status=int(status.item()),
                 K=g.K.cpu(), V=g.V.cpu(), entropy=None if ent is None else ent.cpu().numpy())
 
 
-def run_score(inp, dev, row_agg="max", group_agg="max", entropy=False):
+def run_score(inp, dev, row_agg="max", group_agg="max", entropy=False, kernel="auto"):
     from decoding_kv_cache_gb300 import kvc
     g = inp.to(dev)
     cache = kvc.Cache(g.K, g.V, g.Hq)
@@ -55,7 +56,8 @@ def run_score(inp, dev, row_agg="max", group_agg="max", entropy=False):
     picks = torch.full((g.L, g.B, g.Hq, max(g.n_b, 1)), -7, dtype=torch.int32, device=dev)[..., :g.n_b].contiguous()
     ent = torch.full((g.L, g.B, g.Hkv), -1.0, dtype=torch.float32, device=dev) if entropy else None
     kvc.kvc_score(cache, g.q_recent, g.qbuf, g.count, g.n_b, g.t, g.theta, scores,
-                  beacon_picks=picks if g.n_b else None, row_agg=row_agg, group_agg=group_agg, entropy=ent)
+                  beacon_picks=picks if g.n_b else None, row_agg=row_agg, group_agg=group_agg, entropy=ent,
+                  kernel=kernel)
     torch.cuda.synchronize()
     if entropy:
         return scores.cpu().numpy(), picks.cpu().numpy(), ent.cpu().numpy()

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
     exported = set(re.findall(r"\bT (kvc_\w+)", out))
     assert set(_declared()) <= exported
     assert set(kvc.EXPORTED) == set(_declared())
-    assert lib.kvc_abi_version() == kvc.KVC_ABI_VERSION == 4
+    assert lib.kvc_abi_version() == kvc.KVC_ABI_VERSION == 5
 
 
 def test_header_compiles_as_c():
@@ -109,11 +109,12 @@ def test_evict_rejects_bad_query_and_budget_args(lib):
     assert call(ws=0x100010) == -7             # workspace not 256-byte aligned
     assert call(qr=0x1004) == -8               # misaligned query pointer
     assert call(n_r=64, n_b=32, qmax=64) == -9  # 4 * 96 observation rows > 256
-    o = lambda **kw: C.byref(kvc.kvc_opts(**{**dict(row_agg=0, group_agg=0, head_budget=0, reserved=0), **kw}))
+    o = lambda **kw: C.byref(kvc.kvc_opts(**{**dict(row_agg=0, group_agg=0, head_budget=0, kernel=0), **kw}))
     assert call(opts=o(row_agg=2)) == -1        # sum is not a row aggregation
     assert call(opts=o(group_agg=1)) == -1      # nor mean a group aggregation
     assert call(opts=o(head_budget=2)) == -1
-    assert call(opts=o(reserved=1)) == -1
+    assert call(opts=o(kernel=4)) == -1
+    assert call(opts=o(kernel=-1)) == -1
     assert call(opts=o(entropy=0x1002)) == -8   # entropy output not 4-byte aligned
     assert call(opts=o(head_budget=1, entropy=0x1004), wsb=16) == -7  # options fine: reaches the workspace check
 
@@ -126,7 +127,7 @@ def test_variant_row_layout_limit(lib):
     call = lambda opts: lib.kvc_evict(C.byref(c), 0x1000, 64, 0x1000, 0x1000, 18, 17, 1023, 1e6, 4, 16, None, 896,
                                       None, 0x1000, None, None, opts, 0x100000, 16, None)
     assert call(None) == -7  # accepted up to the (too small) workspace
-    o = kvc.kvc_opts(row_agg=1, group_agg=0, head_budget=0, reserved=0, entropy=None)
+    o = kvc.kvc_opts(row_agg=1, group_agg=0, head_budget=0, kernel=0, entropy=None)
     assert call(C.byref(o)) == -9
     assert lib.kvc_score_workspace_size(C.byref(c), 64, 17) > 0
 

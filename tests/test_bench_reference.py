@@ -28,6 +28,9 @@ def test_reference_arm_prints_one_contract_line():
               "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
         assert k in d, k
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 1
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["config"]["workload"] == bench.workload_desc("tiny")  # the GPU arm's string, character for character
     assert d["value"] > 0 and d["higher_is_better"] is True and d["vs_baseline"] is None
     assert abs(d["ms_per_step"] - 256 / d["value"] * 1e3) < 1e-6 * d["ms_per_step"]  # tiny: B * N = 256 tokens
     cb = d["cpu_baseline"]

@@ -226,6 +226,33 @@ def test_select_sizes_and_distributions(N, heads, dist):
         assert np.array_equal(ki[h, :len(ref)], ref), h
 
 
+@pytest.mark.parametrize("N", [3001, 20001])
+def test_select_ranks_signed_scores_by_value(N):
+    """kvc_select takes any finite fp32 score, not only the non-negative ones the scoring kernels
+    produce: negative values, -0 next to +0 (equal, so the lower index wins), and +-inf rank as
+    their values do, as in the oracle's sort."""
+    from decoding_kv_cache_gb300 import kvc
+    g = torch.Generator().manual_seed(N)
+    P, R, heads = 4, 16, 4
+    sc = torch.randn((heads, N), generator=g) * 10.0
+    sc[1] = torch.randint(-3, 3, (N,), generator=g).float()       # heavy ties around zero
+    zero = torch.rand(N, generator=g) < 0.5
+    sc[1][zero & (sc[1] == 0)] = -0.0                               # -0 and +0 mixed
+    sc[2] = -torch.rand(N, generator=g)                             # all negative
+    sc[3, 100:200] = float("inf")
+    sc[3, 300:400] = float("-inf")
+    bud = torch.tensor([(N * 7) // 8, N // 2, P + R + 5, (N * 7) // 8], dtype=torch.int32)
+    kept_idx = torch.full((1, 1, heads, N), -7, dtype=torch.int32, device=DEV)
+    kept_len = torch.zeros((1, 1, heads), dtype=torch.int32, device=DEV)
+    kvc.kvc_select(sc.view(1, 1, heads, N).to(DEV), P, R, kept_idx, kept_len, budget=bud.view(1, 1, heads).to(DEV))
+    torch.cuda.synchronize()
+    ki, kl = kept_idx.cpu().numpy()[0, 0], kept_len.cpu().numpy()[0, 0]
+    for h in range(heads):
+        ref = O.select(sc[h].numpy(), P, R, int(bud[h]))
+        assert kl[h] == len(ref), h
+        assert np.array_equal(ki[h, :len(ref)], ref), h
+
+
 def test_compact_rejects_malformed_lists():
     from decoding_kv_cache_gb300 import kvc
     inp = make_inputs("qwen3-4b", L=1, N=256)
@@ -258,13 +285,12 @@ PATH_CASES = [
 
 @pytest.mark.parametrize("path", ["resident", "split", "fused"])
 @pytest.mark.parametrize("name,over", PATH_CASES, ids=[_ids(c) for c in PATH_CASES])
-def test_each_scoring_kernel_matches_oracle(monkeypatch, path, name, over):
+def test_each_scoring_kernel_matches_oracle(path, name, over):
     """Every bf16 scoring kernel (single-read, two-pass streaming, two-pass with group exchange),
-    forced through KVC_SCORE_PATH, against the oracle on the same inputs."""
-    monkeypatch.setenv("KVC_SCORE_PATH", path)
+    forced through kvc_opts.kernel, against the oracle on the same inputs."""
     inp = make_inputs(name, **over)
-    gpu = run_evict(inp, DEV)
-    _, gpu_picks = run_score(inp, DEV)
+    gpu = run_evict(inp, DEV, kernel=path)
+    _, gpu_picks = run_score(inp, DEV, kernel=path)
     ora = O.evict(inp)
     if check_beacon_picks(inp, gpu_picks, ora["beacon_picks"]):
         ora = O.evict(inp, forced_picks=gpu_picks)

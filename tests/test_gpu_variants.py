@@ -87,18 +87,40 @@ def test_entropy_budgets_match_oracle(name, over):
     _, picks = run_score(inp, DEV)
     ora = _oracle(inp, picks, head_budget="entropy")
     np.testing.assert_allclose(gpu["entropy"], ora["entropy"], rtol=0, atol=ENTROPY_ATOL)
-    # the integer reallocation is taken from the GPU's own fp32 entropies on both sides
-    ora = _oracle(inp, picks, head_budget="entropy", forced_entropy=gpu["entropy"])
     assert gpu["status"] == 0
-    assert np.array_equal(gpu["kept_len"], np.minimum(ora["budget_used"], inp.N))
+    # The oracle's rule applied to the GPU's own fp32 entropies: exactly the GPU's budgets (the
+    # integer reallocation after the fixed-point weights is exact arithmetic on both sides).
+    forced = _oracle(inp, picks, head_budget="entropy", forced_entropy=gpu["entropy"])
+    assert np.array_equal(gpu["kept_len"], np.minimum(forced["budget_used"], inp.N))
+    # Against the budgets the oracle takes from its OWN entropies: equal, except in a (layer,
+    # sequence) where some head's fixed-point weight floor((1 - entropy) * 2^24) differs between
+    # the two entropy sets (both within ENTROPY_ATOL of each other), which is where a rounding
+    # difference in an entropy can move a slot from one head to another.
+    own = np.minimum(ora["budget_used"], inp.N)
+    moved = 0
+    for l in range(inp.L):
+        for b in range(inp.B):
+            if np.array_equal(gpu["kept_len"][l, b], own[l, b]):
+                continue
+            assert (_weights(gpu["entropy"][l, b]) != _weights(ora["entropy"][l, b])).any(), (
+                f"budgets differ at {(l, b)} with identical fixed-point weights")
+            assert gpu["kept_len"][l, b].sum() == own[l, b].sum()
+            moved += 1
+    assert moved <= (inp.L * inp.B) // 2, f"{moved} of {inp.L * inp.B} (layer, sequence) groups differ"
     given = inp.budgets().cpu().numpy()
     assert np.array_equal(gpu["kept_len"].sum(-1), np.minimum(given, inp.N).sum(-1))  # layer totals kept
     assert_scores_close(gpu["scores"], ora["scores"], name)
-    check_kept(inp, gpu, ora, gpu["scores"], budgets=ora["budget_used"])
+    check_kept(inp, gpu, forced, gpu["scores"], budgets=forced["budget_used"])
     check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
     # the entropy output is optional: without it the workspace holds the entropies
     gpu2 = run_evict(inp, DEV, head_budget="entropy")
     assert np.array_equal(gpu2["kept_len"], gpu["kept_len"])
+
+
+def _weights(ent):
+    """The head-budget rule's fixed-point utilities floor(clip(1 - entropy, 0, 1) * 2^24), in fp64."""
+    u = np.clip(1.0 - np.asarray(ent, dtype=np.float32).astype(np.float64), 0.0, 1.0)
+    return np.floor(u * 16777216.0).astype(np.int64)
 
 
 @pytest.mark.parametrize("seed", range(6))
