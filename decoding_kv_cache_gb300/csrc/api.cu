@@ -57,7 +57,7 @@ int check_opts(const kvc_opts* o, bool evict, Opts* out) {
   if ((o->row_agg != KVC_AGG_MAX && o->row_agg != KVC_AGG_MEAN) ||
       (o->group_agg != KVC_AGG_MAX && o->group_agg != KVC_AGG_SUM) ||
       (o->head_budget != KVC_BUDGET_GIVEN && o->head_budget != KVC_BUDGET_ENTROPY) || o->kernel < KVC_KERNEL_AUTO ||
-      o->kernel > KVC_KERNEL_FUSED)
+      o->kernel > KVC_KERNEL_WIDE)
     return KVC_ERR_INVALID_ARG;
   if (!evict && o->head_budget != KVC_BUDGET_GIVEN) return KVC_ERR_INVALID_ARG;
   if (o->entropy && (reinterpret_cast<uintptr_t>(o->entropy) & 3u)) return KVC_ERR_ALIGNMENT;

@@ -113,7 +113,8 @@ struct ScoreWs {            // carved out of the caller's workspace
   float* rw;                // [heads][M_pad] row weight of a mean over the query head's rows (0: no row)
   float* escale;            // [heads] 1 / (valid rows * log2 N): entropy in bits -> normalised mean
   float* ent;               // [heads] entropy accumulator when the caller keeps none (kvc_evict)
-  float* lse2p;             // bf16 two-pass streaming kernel: [heads][ranges][M_pad] log2-sum-exp2 per key range
+  float* lse2p;             // bf16 two-pass streaming kernels: [heads][ranges][M_pad] log2-sum-exp2 per key range
+  int32_t* fb;              // wide kernel: [0] items listed for the exact fallback, [1..] the items (zeroed by build_obs)
 };
 
 struct ScoreArgs {
@@ -178,10 +179,24 @@ struct SplitPlan {
   int items;   // heads * R
   int grid;    // CTAs (one per SM)
   int stages;  // K ring depth
+  const int32_t* list;  // null: every item; else [0] = count, [1..] = the items (device, written by the
+                        // previous kernel on the stream)
 };
+// Pass 1 of the two-pass streaming kernel over a device list of items (the wide kernel's fallback).
+int launch_score_split_pass1_list(const ScoreArgs& a, const ScoreWs& ws, const int32_t* list, cudaStream_t s);
 int split_ranges(int nchunk, int M_pad);
 bool score_split_plan(const ScoreArgs& a, SplitPlan* p, size_t* smem);
 int launch_score_split(const ScoreArgs& a, const ScoreWs& ws, const SplitPlan& p, size_t smem, cudaStream_t s);
+__global__ void split_combine_kernel(ScoreArgs a, ScoreWs ws, SplitPlan p);
+
+// Two-pass kernel with the keys on the TMEM lanes (bf16, default options, more than 128 rows): the
+// same work items as the two-pass streaming kernel; an exact fallback for items whose logits spread
+// too far for its one-reference sums, then the combine, between the passes.
+struct WidePlan {
+  int rk, R, items, grid, stages;
+};
+bool score_wide_plan(const ScoreArgs& a, WidePlan* p, size_t* smem);
+int launch_score_wide(const ScoreArgs& a, const ScoreWs& ws, const WidePlan& p, size_t smem, cudaStream_t s);
 // kernels launch_score starts for these arguments (host only; default options when !ext)
 int score_launches(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext);
 

@@ -357,9 +357,13 @@ size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext,
   const size_t o_rw = off;    off += ext ? align256(heads * M_pad * sizeof(float)) : 0;
   const size_t o_esc = off;   off += ext ? align256(heads * sizeof(float)) : 0;
   const size_t o_ent = off;   off += ext ? align256(heads * sizeof(float)) : 0;
-  // the two-pass streaming kernel's per-range partials (bf16, default options only)
+  // the two-pass streaming kernels' per-range partials and the wide kernel's fallback list (bf16,
+  // default options only)
+  const size_t ranges = (size_t)split_ranges((int)nchunk, (int)M_pad);
   const size_t o_l2p = off;
-  if (dtype == KVC_BF16 && !ext) off += align256(heads * (size_t)split_ranges((int)nchunk, (int)M_pad) * M_pad * sizeof(float));
+  if (dtype == KVC_BF16 && !ext) off += align256(heads * ranges * M_pad * sizeof(float));
+  const size_t o_fb = off;
+  if (dtype == KVC_BF16 && !ext) off += align256((1 + heads * ranges) * sizeof(int32_t));
   if (carve) {
     char* b = static_cast<char*>(base);
     carve->obs = b + o_obs;
@@ -370,6 +374,7 @@ size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext,
     carve->escale = ext ? reinterpret_cast<float*>(b + o_esc) : nullptr;
     carve->ent = ext ? reinterpret_cast<float*>(b + o_ent) : nullptr;
     carve->lse2p = (dtype == KVC_BF16 && !ext) ? reinterpret_cast<float*>(b + o_l2p) : nullptr;
+    carve->fb = (dtype == KVC_BF16 && !ext) ? reinterpret_cast<int32_t*>(b + o_fb) : nullptr;
   }
   return off;
 }
@@ -380,8 +385,9 @@ static bool set_smem(K kernel, size_t bytes) {
 }
 
 // Which bf16 scoring kernel runs (sets a->tiles); 0 = fp32 passes.
-enum ScorePath { kPathF32 = 0, kPathResident = 1, kPathSplit = 2, kPathFused = 3 };
-static ScorePath choose_score(ScoreArgs* a, FusedPlan* rp, size_t* rsmem, SplitPlan* sp, size_t* ssmem) {
+enum ScorePath { kPathF32 = 0, kPathResident = 1, kPathSplit = 2, kPathFused = 3, kPathWide = 4 };
+static ScorePath choose_score(ScoreArgs* a, FusedPlan* rp, size_t* rsmem, SplitPlan* sp, size_t* ssmem,
+                              WidePlan* wp, size_t* wsmem) {
   a->tiles = 1;
   if (a->dtype != KVC_BF16) return kPathF32;
   // A 256-row observation tile goes to the single-read kernel as two 128-row tiles when no query
@@ -402,6 +408,14 @@ static ScorePath choose_score(ScoreArgs* a, FusedPlan* rp, size_t* rsmem, SplitP
   if (split && path == KVC_KERNEL_AUTO) split = !resident || a->M_pad > 128 || rp->group_size > 16;
   if (split && path != KVC_KERNEL_AUTO) split = path == KVC_KERNEL_SPLIT;
   if (resident && path == KVC_KERNEL_FUSED) resident = false;
+  // Tiles of more than 128 rows with default options go to the wide kernel (keys on the TMEM lanes,
+  // one MMA chain per chunk over every row), unless another kernel is asked for.
+  const bool wide = score_wide_plan(*a, wp, wsmem) &&
+                    (path == KVC_KERNEL_WIDE || (path == KVC_KERNEL_AUTO && split && a->M_pad > 128));
+  if (wide) {
+    a->tiles = 1;
+    return kPathWide;
+  }
   if (split) resident = false;
   if (!resident) a->tiles = 1;
   return resident ? kPathResident : (split ? kPathSplit : kPathFused);
@@ -421,10 +435,12 @@ int score_launches(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext) {
   a.nchunk = (g.N + kChunk - 1) / kChunk;
   FusedPlan rp;
   SplitPlan sp;
-  size_t r1 = 0, r2 = 0;
-  switch (choose_score(&a, &rp, &r1, &sp, &r2)) {
+  WidePlan wp;
+  size_t r1 = 0, r2 = 0, r3 = 0;
+  switch (choose_score(&a, &rp, &r1, &sp, &r2, &wp, &r3)) {
     case kPathF32: return 4;    // observation rows, pass 1, combine, pass 2
     case kPathSplit: return 4;  // observation rows, pass 1, combine, pass 2
+    case kPathWide: return 5;   // observation rows, pass 1, exact fallback, combine, pass 2
     default: return 2;          // observation rows, one scoring kernel
   }
 }
@@ -435,11 +451,15 @@ int launch_score(const ScoreArgs& a_in, const ScoreWs& ws, cudaStream_t s) {
   // the single-read kernel's plan is fixed first: the observation kernel zeroes its exchange words.
   FusedPlan rp;
   SplitPlan sp;
-  size_t rsmem = 0, ssmem = 0;
-  const ScorePath path = choose_score(&a, &rp, &rsmem, &sp, &ssmem);
-  const bool resident = path == kPathResident, split = path == kPathSplit;
-  a.xch_zero = resident ? reinterpret_cast<unsigned long long*>(ws.part) : nullptr;
-  a.xch_zero_words = resident ? score_resident_words(rp, a.entropy != nullptr) : 0;
+  WidePlan wp;
+  size_t rsmem = 0, ssmem = 0, wsmem = 0;
+  const ScorePath path = choose_score(&a, &rp, &rsmem, &sp, &ssmem, &wp, &wsmem);
+  const bool resident = path == kPathResident, split = path == kPathSplit, wide = path == kPathWide;
+  // the observation kernel zeroes the single-read kernel's exchange words, or the wide kernel's
+  // fallback count
+  a.xch_zero = resident ? reinterpret_cast<unsigned long long*>(ws.part)
+                        : (wide ? reinterpret_cast<unsigned long long*>(ws.fb) : nullptr);
+  a.xch_zero_words = resident ? score_resident_words(rp, a.entropy != nullptr) : (wide ? 1 : 0);
   const int D = a.g.D;
   const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
   // observation rows: one warp per query head of the group
@@ -470,6 +490,7 @@ int launch_score(const ScoreArgs& a_in, const ScoreWs& ws, cudaStream_t s) {
   const dim3 grid(a.nchunk, heads);
   if (a.dtype == KVC_BF16) {
     if (resident) return launch_score_resident(a, ws, rp, rsmem, s);
+    if (wide) return launch_score_wide(a, ws, wp, wsmem, s);
     if (split) return launch_score_split(a, ws, sp, ssmem, s);
     return launch_score_fused(a, ws, ws.part, s);
   } else {

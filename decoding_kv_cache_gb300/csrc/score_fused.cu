@@ -522,7 +522,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 fused_encoder() {
   return fn;
 }
 
-bool fused_maps(FusedMaps* m, const ScoreArgs& a, const ScoreWs& ws) {
+bool fused_maps(FusedMaps* m, const ScoreArgs& a, const ScoreWs& ws, int qrows) {
   auto enc = fused_encoder();
   if (!enc) return false;
   const int D = a.g.D;
@@ -539,7 +539,7 @@ bool fused_maps(FusedMaps* m, const ScoreArgs& a, const ScoreWs& ws) {
   const int heads = a.g.L * a.g.B * a.g.Hkv;
   const cuuint64_t qdims[2] = {(cuuint64_t)D, (cuuint64_t)heads * a.M_pad};
   const cuuint64_t qstrides[1] = {(cuuint64_t)D * 2};
-  const cuuint32_t qbox[2] = {64, 128};
+  const cuuint32_t qbox[2] = {64, (cuuint32_t)qrows};
   return enc(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws.obs, qdims, qstrides, qbox, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

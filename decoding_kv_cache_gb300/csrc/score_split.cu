@@ -94,6 +94,14 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *slot;
   const int bhkv = a.g.B * a.g.Hkv;
+  // Work items: all of them, or (pass 1 as the wide kernel's exact fallback) the listed ones, whose
+  // count and ids the previous kernel wrote: then every role waits for it first.
+  int nitems = p.items;
+  if (p.list) {
+    griddep_wait();
+    nitems = *reinterpret_cast<const volatile int32_t*>(p.list);
+  }
+  auto item_at = [&](int idx) { return p.list ? p.list[1 + idx] : idx; };
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -101,11 +109,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       uint32_t kc = 0;
       bool waited = false, stop = false;
       int it = 0;
-      for (int item = blockIdx.x; item < p.items && !stop && !*abort_flag; item += gridDim.x, ++it) {
+      for (int idx = blockIdx.x; idx < nitems && !stop && !*abort_flag; idx += gridDim.x, ++it) {
+        const int item = item_at(idx);
         const int head = item / p.R, ri = item % p.R;
         const int l = head / bhkv, bh = head % bhkv;
         const int cb = ri * p.rk, nc = min(cb + p.rk, a.nchunk) - cb;
-        if (item + (int)gridDim.x < p.items) tc::prefetch_tensormap(&maps.k[(item + gridDim.x) / p.R / bhkv]);
+        if (idx + (int)gridDim.x < nitems) tc::prefetch_tensormap(&maps.k[item_at(idx + gridDim.x) / p.R / bhkv]);
         auto load_k = [&](int j) -> bool {
           const int s = kc % S;
           if (kc >= (uint32_t)S && !wait_or_abort(&kempty[s], ((kc / S) - 1) & 1, abort_flag, a.status)) return false;
@@ -157,7 +166,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       const uint32_t id = tc::idesc_bf16(128, kChunk);
       bool ok = true, issued = false;
       int it = 0;
-      for (int item = blockIdx.x; item < p.items && ok && !*abort_flag; item += gridDim.x, ++it) {
+      for (int idx = blockIdx.x; idx < nitems && ok && !*abort_flag; idx += gridDim.x, ++it) {
+        const int item = item_at(idx);
         const int ri = item % p.R;
         const int cb = ri * p.rk, nc = min(cb + p.rk, a.nchunk) - cb;
         const int qb = it % kQBuf;
@@ -207,7 +217,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     const int gt = e * 32 + lane;  // 0..255
     uint32_t tcount = 0;
     int it = 0;
-    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
+    for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x, ++it) {
+      const int item = item_at(idx);
       const int head = item / p.R, ri = item % p.R;
       const int cb = ri * p.rk, nc = min(cb + p.rk, a.nchunk) - cb;
       if constexpr (kPass == 1) {
@@ -410,6 +421,7 @@ bool score_split_plan(const ScoreArgs& a, SplitPlan* p, size_t* smem) {
   if (stages > 6) stages = 6;
   if (stages < 2) return false;
   p->stages = stages;
+  p->list = nullptr;
   *smem = (size_t)split_tail_bytes(NT) + qbytes + (size_t)stages * stage;
   return true;
 }
@@ -439,6 +451,28 @@ int launch_score_split(const ScoreArgs& a, const ScoreWs& ws, const SplitPlan& p
                                 wss, pp) != cudaSuccess)
       return KVC_ERR_LAUNCH;
   }
+  return KVC_OK;
+}
+
+int launch_score_split_pass1_list(const ScoreArgs& a, const ScoreWs& ws, const int32_t* list, cudaStream_t s) {
+  SplitPlan p;
+  size_t smem = 0;
+  if (!score_split_plan(a, &p, &smem)) return KVC_ERR_LAUNCH;
+  p.list = list;
+  const int D = a.g.D, NT = a.M_pad / kSplitRows;
+  FusedMaps maps;
+  if (!fused_maps(&maps, a, ws)) return KVC_ERR_LAUNCH;
+  using Kern = void (*)(const FusedMaps, ScoreArgs, ScoreWs, SplitPlan, float);
+  static const Kern table[2][2] = {{score_split_kernel<64, 1, 1>, score_split_kernel<64, 2, 1>},
+                                   {score_split_kernel<128, 1, 1>, score_split_kernel<128, 2, 1>}};
+  Kern kern = table[D == 128][NT == 2];
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return KVC_ERR_LAUNCH;
+  const float c2 = (float)(1.4426950408889634074 / sqrt((double)D));
+  ScoreArgs aa = a;
+  ScoreWs wss = ws;
+  if (launch_pdl(kern, dim3(p.grid), dim3(kSplitThreads), smem, s, false, maps, aa, wss, p, c2) != cudaSuccess)
+    return KVC_ERR_LAUNCH;
   return KVC_OK;
 }
 

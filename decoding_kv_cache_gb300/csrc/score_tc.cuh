@@ -99,7 +99,8 @@ __device__ __forceinline__ float2 lse_merge(float2 x, float2 y) {
   return make_float2(m, x.y * exp2f(x.x - m) + y.y * exp2f(y.x - m));
 }
 
-// Tensor maps over the K cache (per layer) and the observation rows; false if encoding fails.
-bool fused_maps(FusedMaps* m, const ScoreArgs& a, const ScoreWs& ws);
+// Tensor maps over the K cache (per layer) and the observation rows (a box of qrows rows); false
+// if encoding fails.
+bool fused_maps(FusedMaps* m, const ScoreArgs& a, const ScoreWs& ws, int qrows = 128);
 
 }  // namespace kvc

@@ -30,7 +30,7 @@ ROW_AGG = {"max": KVC_AGG_MAX, "mean": KVC_AGG_MEAN}
 GROUP_AGG = {"max": KVC_AGG_MAX, "sum": KVC_AGG_SUM}
 HEAD_BUDGET = {"given": KVC_BUDGET_GIVEN, "entropy": KVC_BUDGET_ENTROPY}
 # bf16 scoring kernel (a test and profiling aid; every kernel computes the same scores)
-KERNEL = {"auto": 0, "resident": 1, "split": 2, "fused": 3}
+KERNEL = {"auto": 0, "resident": 1, "split": 2, "fused": 3, "wide": 4}
 KVC_STATIC_SCRATCH_BYTES = 16 << 20
 
 

@@ -105,11 +105,13 @@ enum {
 /* Scoring kernel for bf16 caches (kernel field; a test and profiling aid: every
  * kernel computes the same scores). KVC_KERNEL_AUTO picks by shape; a forced
  * kernel that does not apply to the call falls back to the automatic choice
- * (RESIDENT: 128-row tiles and short caches; SPLIT: default options only). */
+ * (RESIDENT: 128-row tiles and short caches; SPLIT: default options only; WIDE:
+ * default options and more than 128 observation rows). */
 #define KVC_KERNEL_AUTO 0
 #define KVC_KERNEL_RESIDENT 1 /* single read of K, logits held in tensor memory */
 #define KVC_KERNEL_SPLIT 2    /* two streaming passes, independent work items */
 #define KVC_KERNEL_FUSED 3    /* two passes with a per-group exchange */
+#define KVC_KERNEL_WIDE 4     /* two streaming passes, keys on the tensor-memory lanes (> 128 rows) */
 typedef struct {
   int32_t row_agg;     /* KVC_AGG_MAX or KVC_AGG_MEAN */
   int32_t group_agg;   /* KVC_AGG_MAX or KVC_AGG_SUM */

@@ -113,7 +113,7 @@ def test_evict_rejects_bad_query_and_budget_args(lib):
     assert call(opts=o(row_agg=2)) == -1        # sum is not a row aggregation
     assert call(opts=o(group_agg=1)) == -1      # nor mean a group aggregation
     assert call(opts=o(head_budget=2)) == -1
-    assert call(opts=o(kernel=4)) == -1
+    assert call(opts=o(kernel=5)) == -1
     assert call(opts=o(kernel=-1)) == -1
     assert call(opts=o(entropy=0x1002)) == -8   # entropy output not 4-byte aligned
     assert call(opts=o(head_budget=1, entropy=0x1004), wsb=16) == -7  # options fine: reaches the workspace check

@@ -283,11 +283,12 @@ PATH_CASES = [
 ]
 
 
-@pytest.mark.parametrize("path", ["resident", "split", "fused"])
+@pytest.mark.parametrize("path", ["resident", "split", "fused", "wide"])
 @pytest.mark.parametrize("name,over", PATH_CASES, ids=[_ids(c) for c in PATH_CASES])
 def test_each_scoring_kernel_matches_oracle(path, name, over):
-    """Every bf16 scoring kernel (single-read, two-pass streaming, two-pass with group exchange),
-    forced through kvc_opts.kernel, against the oracle on the same inputs."""
+    """Every bf16 scoring kernel (single-read, two-pass streaming, two-pass with group exchange,
+    two-pass with the keys on the TMEM lanes), forced through kvc_opts.kernel, against the oracle on
+    the same inputs (a kernel that does not apply to a shape falls back to the automatic choice)."""
     inp = make_inputs(name, **over)
     gpu = run_evict(inp, DEV, kernel=path)
     _, gpu_picks = run_score(inp, DEV, kernel=path)
@@ -298,3 +299,48 @@ def test_each_scoring_kernel_matches_oracle(path, name, over):
     assert_scores_close(gpu["scores"], ora["scores"], f"{name} via {path}")
     check_kept(inp, gpu, ora, gpu["scores"])
     check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
+
+
+WIDE_CASES = [
+    ("qwen3-14b-long", dict(L=1, B=2, N=4100)),             # 240 rows: 16-column tail granule, ragged range
+    ("qwen7b-reasonalloc", dict(L=1, B=1, N=8192)),         # 224 rows: whole granules only, two ranges
+    ("qwen7b-reasonalloc", dict(L=1, B=1, N=200, D=64)),    # D 64, one ragged chunk pair
+    ("qwen3-14b-long", dict(L=2, B=1, N=129, Hq=24, Hkv=8)),  # 3 query heads: 144 rows, one key past a chunk
+]
+
+
+@pytest.mark.parametrize("name,over", WIDE_CASES, ids=[_ids(c) for c in WIDE_CASES])
+def test_wide_kernel_shapes(name, over):
+    """The wide kernel's column splits (whole and half granules), ragged chunks and ranges, D 64."""
+    inp = make_inputs(name, **over)
+    gpu = run_evict(inp, DEV, kernel="wide")
+    _, gpu_picks = run_score(inp, DEV, kernel="wide")
+    ora = O.evict(inp)
+    if check_beacon_picks(inp, gpu_picks, ora["beacon_picks"]):
+        ora = O.evict(inp, forced_picks=gpu_picks)
+    assert gpu["status"] == 0
+    assert_scores_close(gpu["scores"], ora["scores"], f"{name} wide")
+    check_kept(inp, gpu, ora, gpu["scores"])
+    check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
+
+
+@pytest.mark.parametrize("where", ["late", "first"])
+def test_wide_kernel_exact_fallback_on_extreme_logits(where):
+    """Keys planted along a recent query with a logit ~160 (base 2) above the rest: late in a lane,
+    its sum overflows the lane's reference; as a lane's first key, the references spread far beyond
+    what one common reference holds. Either way pass 1 lists the item and the exact fallback
+    recomputes it; the scores still match the oracle."""
+    inp = make_inputs("qwen3-14b-long", L=1, B=1, N=1500)
+    G = inp.Hq // inp.Hkv
+    pos = 700 if where == "late" else 5
+    for h in range(inp.Hkv):
+        q = inp.q_recent[0, 0, h * G, 0].float()
+        inp.K[0, 0, h, pos] = (10.0 * q).to(inp.K.dtype)
+    gpu = run_evict(inp, DEV, kernel="wide")
+    _, gpu_picks = run_score(inp, DEV, kernel="wide")
+    ora = O.evict(inp)
+    if check_beacon_picks(inp, gpu_picks, ora["beacon_picks"]):
+        ora = O.evict(inp, forced_picks=gpu_picks)
+    assert gpu["status"] == 0
+    assert_scores_close(gpu["scores"], ora["scores"], f"wide fallback ({where})")
+    check_kept(inp, gpu, ora, gpu["scores"])
