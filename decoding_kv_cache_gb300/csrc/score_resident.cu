@@ -216,8 +216,8 @@ __global__ void __launch_bounds__(kResThreads, 1)
         for (int j = 0; j < n; ++j) {
           const int s = kc % S;
           const uint32_t acc = (uint32_t)((r & 1) * kResChunks + j);
-          if (!wait_or_abort(&kfull[s], (kc / S) & 1, abort_flag, a.status) ||
-              (r >= 2 && !wait_or_abort(&tempty[acc], ((r >> 1) - 1) & 1, abort_flag, a.status))) {
+          if (!spin_or_abort(&kfull[s], (kc / S) & 1, abort_flag, a.status) ||
+              (r >= 2 && !spin_or_abort(&tempty[acc], ((r >> 1) - 1) & 1, abort_flag, a.status))) {
             ok = false;
             break;
           }

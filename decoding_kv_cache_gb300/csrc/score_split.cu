@@ -176,8 +176,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         for (int j = 0; j < nc; ++j) {
           const int s = kc % S;
           const uint32_t sl = tcount % NSLOT;
-          if (!wait_or_abort(&kfull[s], (kc / S) & 1, abort_flag, a.status) ||
-              (tcount >= (uint32_t)NSLOT && !wait_or_abort(&tempty[sl], ((tcount / NSLOT) - 1) & 1, abort_flag, a.status))) {
+          if (!spin_or_abort(&kfull[s], (kc / S) & 1, abort_flag, a.status) ||
+              (tcount >= (uint32_t)NSLOT && !spin_or_abort(&tempty[sl], ((tcount / NSLOT) - 1) & 1, abort_flag, a.status))) {
             ok = false;
             break;
           }

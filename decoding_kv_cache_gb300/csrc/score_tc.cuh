@@ -47,6 +47,28 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
+// The same wait by polling without suspension, for the MMA issuer's waits on the critical path
+// (a key stage landing, a TMEM slot coming free): a suspended try_wait resumed too late there and
+// left the tensor pipe idle between chunks. Bounded: gives up (abort flag, KVC_STATUS_TIMEOUT)
+// after 2^26 polls, and as soon as another role has aborted.
+__device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              int32_t* status) {
+  const uint32_t a = tc::smem_u32(bar);
+  for (uint32_t it = 0; it < (1u << 26); ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 1023u) == 1023u && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  status_or(status, KVC_STATUS_TIMEOUT);
+  return false;
+}
+
 // Tree reductions over a 32-value slice: five dependent steps instead of 32.
 __device__ __forceinline__ float tree_max32(const float (&x)[32]) {
   float a[16];

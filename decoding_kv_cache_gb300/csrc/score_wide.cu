@@ -241,8 +241,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         for (int j = 0; j < nc; ++j) {
           const int s = kc % S;
           const uint32_t sl = tcount & 1;
-          if (!wait_or_abort(&kfull[s], (kc / S) & 1, abort_flag, a.status) ||
-              (tcount >= 2 && !wait_or_abort(&tempty[sl], ((tcount >> 1) - 1) & 1, abort_flag, a.status))) {
+          if (!spin_or_abort(&kfull[s], (kc / S) & 1, abort_flag, a.status) ||
+              (tcount >= 2 && !spin_or_abort(&tempty[sl], ((tcount >> 1) - 1) & 1, abort_flag, a.status))) {
             ok = false;
             break;
           }
