@@ -50,7 +50,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 // The same wait by polling without suspension, for the MMA issuer's waits on the critical path
 // (a key stage landing, a TMEM slot coming free): a suspended try_wait resumed too late there and
 // left the tensor pipe idle between chunks. Bounded: gives up (abort flag, KVC_STATUS_TIMEOUT)
-// after 2^26 polls, and as soon as another role has aborted.
+// after 2^26 polls (about 2 s with the 32 ns pauses), and as soon as another role has aborted.
 __device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               int32_t* status) {
   const uint32_t a = tc::smem_u32(bar);
@@ -63,6 +63,7 @@ __device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, vo
         : "memory");
     if (done) return true;
     if ((it & 1023u) == 1023u && *abort_flag) return false;
+    __nanosleep(32);  // a short pause keeps the poll from taking issue slots from the SMSP's other warps
   }
   *abort_flag = 1;
   status_or(status, KVC_STATUS_TIMEOUT);
