@@ -166,7 +166,8 @@ int kvc_evict_launch_count(const kvc_cache* c, int32_t n_r, int32_t n_b) {
   if (!c || n_r < 0 || n_b < 0) return 0;
   kvc_cache probe = *c;
   if (check_cache(&probe, &g, &K, &V)) return 0;
-  return score_launches(g, c->dtype, n_r, n_b, false) + 2;  // + select, compact
+  // + selection and compaction: one launch up to kSelectCompactMaxN tokens per head, else two
+  return score_launches(g, c->dtype, n_r, n_b, false) + (g.N <= kSelectCompactMaxN ? 1 : 2);
 }
 
 const char* kvc_strerror(int code) {
@@ -328,8 +329,12 @@ int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void*
                   ent);
   rc = launch_score(a, ws, s);
   if (rc) return rc;
-  rc = launch_select(sc, g.L * g.B * g.Hkv, g.N, prefix, recent, budget, budget_all,
-                     o.head_budget == KVC_BUDGET_ENTROPY ? ent : nullptr, g.Hkv, ki, kept_len, status, s);
+  const float* sel_ent = o.head_budget == KVC_BUDGET_ENTROPY ? ent : nullptr;
+  if (g.N <= kSelectCompactMaxN)  // one CTA per head selects, then moves the head's K and V
+    return launch_select_compact(sc, g, c->dtype, K, V, prefix, recent, budget, budget_all, sel_ent, ki, kept_len,
+                                 status, s);
+  rc = launch_select(sc, g.L * g.B * g.Hkv, g.N, prefix, recent, budget, budget_all, sel_ent, g.Hkv, ki, kept_len,
+                     status, s);
   if (rc) return rc;
   return launch_compact(g, c->dtype, K, V, ki, kept_len, status, false, s);
 }

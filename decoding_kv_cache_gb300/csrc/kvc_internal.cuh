@@ -208,6 +208,12 @@ int launch_select(const float* scores, int heads, int N, int P, int R, const int
 int launch_head_budget(const float* entropy, int groups, int Hkv, int N, int P, int R, const int32_t* budget,
                        int budget_all, int32_t* budget_out, int32_t* status, cudaStream_t s);
 
+// kvc_evict's selection and compaction in one launch (one CTA per head; N <= kSelectCompactMaxN)
+constexpr int kSelectCompactMaxN = 16384;
+int launch_select_compact(const float* scores, const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V,
+                          int P, int R, const int32_t* budget, int budget_all, const float* entropy, int32_t* kept_idx,
+                          int32_t* kept_len, int32_t* status, cudaStream_t s);
+
 // list_per_seq: kept_idx [B][N] / kept_len [B], one list per sequence for all its layers and heads
 int launch_compact(const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V, const int32_t* kept_idx,
                    const int32_t* kept_len, int32_t* status, bool validate, cudaStream_t s, bool list_per_seq = false);

@@ -20,8 +20,6 @@
 //               2^-80 of the common reference; an item outside that is listed and recomputed with
 //               a running max per row by the two-pass kernel's pass 1 (score_split.cu) over the
 //               list (keys far out in a heavy tail reach it; the tests force it).
-//               A fixed share of the exp2 runs as a polynomial on the FMA pipes (exp2_poly2), so
-//               that the MUFU unit and the FMA pipes share the pass's one exp2 per logit.
 //   fallback    score_split_kernel's pass 1 over the listed items (usually none: it exits at once)
 //   combine     split_combine_kernel: per head and row, the ranges' partials merged into lse2
 //   pass 2      per item: the same MMA; per key the max over its rows of s c2 - lse2 (lse2 from
@@ -46,9 +44,6 @@ namespace kvc {
 constexpr int kWideEpi = 16;
 constexpr int kWideThreads = 64 + 32 * kWideEpi;
 constexpr int kWideSlotCols = 256;  // TMEM columns per chunk slot (two slots)
-// Of each 4 column groups of a pass-1 load, this many take the FMA-pipe exp2 for one of their two keys
-// (so 2 of 8 logit pairs: a quarter of the exp2 work).
-constexpr int kWidePolyGroups = 0;
 // An item whose references spread by more than this (base 2) is recomputed by the fallback.
 constexpr float kWideSpread = 96.f;
 // A valid row whose range sum falls below 2^-80 of the common reference likewise.
@@ -73,37 +68,15 @@ __device__ __forceinline__ void tmem_ld16x256_x2_async(uint32_t taddr, uint32_t 
                : "r"(taddr));
 }
 
-// 2^x for a pair on the FMA pipes: 2^x = 2^n 2^f with n = rint(x) and f in [-1/2, 1/2]; 2^f from a
-// degree-4 polynomial fitted here to relative error 2.7e-6 on that interval (weighted least squares
-// on Chebyshev nodes); 2^n added to the exponent field. x is clamped below at -125 (2^-125 in
-// place of a smaller value); x >= 128 gives inf or NaN, as the overflow it is.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  x = make_float2(fmaxf(x.x, -125.f), fmaxf(x.y, -125.f));
-  const float2 magic = make_float2(12582912.f, 12582912.f);  // 1.5 * 2^23: x + magic holds rint(x) in its low bits
-  const float2 t = __fadd2_rn(x, magic);
-  const float2 n = __fadd2_rn(t, make_float2(-12582912.f, -12582912.f));
-  const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), x);
-  float2 p = __ffma2_rn(make_float2(0.009571806527674198f, 0.009571806527674198f), f,
-                        make_float2(0.05591800436377525f, 0.05591800436377525f));
-  p = __ffma2_rn(p, f, make_float2(0.24024702608585358f, 0.24024702608585358f));
-  p = __ffma2_rn(p, f, make_float2(0.6931217908859253f, 0.6931217908859253f));
-  p = __ffma2_rn(p, f, make_float2(0.9999992847442627f, 0.9999992847442627f));
-  // bits(t) = bits(magic) + n, and bits(magic) << 23 == 0 (mod 2^32): the shift leaves n << 23
-  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
-}
-
 // Pass 1 on the values of one 16x256b load (n column groups of 8): for each group i, the two keys'
-// pairs of columns (8i + 2(t%4), +1): acc[i] += 2^(v * c2 - ref) for both keys. Of each 4 groups, the
-// last kWidePolyGroups take the FMA-pipe exp2 for their first key.
+// pairs of columns (8i + 2(t%4), +1): acc[i] += 2^(v * c2 - ref) for both keys.
 template <int n>
 __device__ __forceinline__ void wide_acc(float2* acc, const uint32_t* r, float2 c2v, float2 nA, float2 nB) {
 #pragma unroll
   for (int i = 0; i < n; ++i) {
     const float2 xa = __ffma2_rn(make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), c2v, nA);
     const float2 xb = __ffma2_rn(make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), c2v, nB);
-    const bool poly = (i & 3) >= 4 - kWidePolyGroups;
-    const float2 ea = poly ? exp2_poly2(xa) : make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
+    const float2 ea = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
     const float2 eb = make_float2(ex2_approx(xb.x), ex2_approx(xb.y));
     acc[i] = __fadd2_rn(acc[i], __fadd2_rn(ea, eb));
   }
@@ -342,8 +315,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                   }
                   ref = m > -INFINITY ? m * c2 : -INFINITY;
                 }
-                // a key past N gets the offset -inf (2^-125 relative to the reference at most, from the
-                // polynomial's clamp: nothing an fp32 sum that holds the reference's own 1 can show)
+                // a key past N gets the offset -inf: its exp2 is exactly 0
                 const float2 nA = okA ? make_float2(-ref, -ref) : make_float2(-INFINITY, -INFINITY);
                 const float2 nB = okB ? make_float2(-ref, -ref) : make_float2(-INFINITY, -INFINITY);
 #pragma unroll

@@ -20,7 +20,7 @@
 // Online head budgets (ReasonAlloc note, "Core Mechanism" and "Key Concepts"): with an
 // entropy array, the budgets of the Hkv heads of one (layer, sequence) are first reallocated
 // by head_budget_alloc below; kvc_head_budget runs the same function on its own.
-#include "kvc_internal.cuh"
+#include "compact.cuh"
 
 namespace kvc {
 
@@ -181,23 +181,22 @@ __device__ __forceinline__ void load_group(const uint32_t* p, int j, int N, bool
     for (int e = 0; e < kSweep; ++e) w[e] = score_key(w[e]);
 }
 
+// The selection of one head by the whole CTA (kThreads threads); sh_bits is the dynamic shared
+// memory used to stage a head of more than one tile (use_smem). Every thread returns.
 template <int kThreads>
-__global__ void __launch_bounds__(kThreads) select_kernel(const float* __restrict__ scores, int N, int P, int R,
-                                                             const int32_t* __restrict__ budget, int budget_all,
-                                                             const float* __restrict__ entropy, int Hkv,
-                                                             int32_t* __restrict__ kept_idx,
-                                                             int32_t* __restrict__ kept_len, int32_t* status,
-                                                             int use_smem, int keyed) {
+__device__ __forceinline__ void select_head(int head, const float* __restrict__ scores, int N, int P, int R,
+                                            const int32_t* __restrict__ budget, int budget_all,
+                                            const float* __restrict__ entropy, int Hkv, int32_t* __restrict__ kept_idx,
+                                            int32_t* __restrict__ kept_len, int32_t* status, int use_smem, int keyed,
+                                            uint32_t* sh_bits) {
   constexpr int kWarps = kThreads / 32;
   constexpr int kTile = kSweep * kThreads;
-  extern __shared__ __align__(16) uint32_t sh_bits[];
   __shared__ __align__(16) unsigned hist[2][256];
   __shared__ unsigned long long wsum[33];
   __shared__ uint32_t s_min[kWarps], s_max[kWarps];
   __shared__ unsigned s_digit, s_k, s_cnt;
   __shared__ int32_t s_alloc[kMaxBudgetHeads];
-  const int head = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  griddep_wait();  // the scores (and entropies) come from the previous kernel
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* sc = scores + (size_t)head * N;
   int32_t* out = kept_idx + (size_t)head * N;
   // Where the tokens come from: one tile is held in registers for the whole kernel, its loads
@@ -365,6 +364,66 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
     base_eq += (int)(tot >> 32);
   }
   if (tid == 0) kept_len[head] = base_k + min(base_eq, (int)keq);
+}
+
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads) select_kernel(const float* __restrict__ scores, int N, int P, int R,
+                                                             const int32_t* __restrict__ budget, int budget_all,
+                                                             const float* __restrict__ entropy, int Hkv,
+                                                             int32_t* __restrict__ kept_idx,
+                                                             int32_t* __restrict__ kept_len, int32_t* status,
+                                                             int use_smem, int keyed) {
+  extern __shared__ __align__(16) uint32_t sh_bits[];
+  griddep_wait();  // the scores (and entropies) come from the previous kernel
+  select_head<kThreads>(blockIdx.x, scores, N, P, R, budget, budget_all, entropy, Hkv, kept_idx, kept_len, status,
+                        use_smem, keyed, sh_bits);
+}
+
+// Selection and compaction of one head per CTA (256 threads, heads of at most 16384 tokens): the
+// CTA selects, then two of its warps move the head's kept K and V rows (compact_warp). One launch
+// instead of two, and each head's selection overlaps the other heads' moves. The dynamic shared
+// memory stages the scores of a head of more than one tile, then serves as the two warps' rings.
+__global__ void __launch_bounds__(256) select_compact_kernel(const float* __restrict__ scores, int N, int P, int R,
+                                                             const int32_t* __restrict__ budget, int budget_all,
+                                                             const float* __restrict__ entropy, int Hkv,
+                                                             int32_t* __restrict__ kept_idx,
+                                                             int32_t* __restrict__ kept_len, int32_t* status,
+                                                             int use_smem, CompactArgs ca) {
+  extern __shared__ __align__(128) uint8_t smc[];
+  griddep_wait();  // the scores (and entropies) come from the previous kernel
+  select_head<256>(blockIdx.x, scores, N, P, R, budget, budget_all, entropy, Hkv, kept_idx, kept_len, status, use_smem,
+                   0, reinterpret_cast<uint32_t*>(smc));
+  // the head's kept list, written by this CTA, is visible to all its threads, and the staging area is free
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  if (warp < 2) compact_warp(ca, blockIdx.x, warp, smc + warp * kCompactWarpSmem);
+}
+
+int launch_select_compact(const float* scores, const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V,
+                          int P, int R, const int32_t* budget, int budget_all, const float* entropy, int32_t* kept_idx,
+                          int32_t* kept_len, int32_t* status, cudaStream_t s) {
+  const int heads = g.L * g.B * g.Hkv, N = g.N;
+  if (heads == 0) return KVC_OK;
+  CompactArgs ca;
+  ca.g = g;
+  ca.K = K;
+  ca.V = V;
+  ca.kept_idx = kept_idx;
+  ca.kept_len = kept_len;
+  ca.status = status;
+  ca.rowbytes = g.D * (dtype == KVC_BF16 ? 2 : 4);
+  ca.validate = 0;
+  ca.list_seq = 0;
+  const size_t stage = (size_t)(N + kSweep - 1) / kSweep * kSweep * 4;
+  const int use_smem = N > kSweep * 256 ? 1 : 0;
+  size_t smem = 2 * (size_t)kCompactWarpSmem;
+  if (use_smem && stage > smem) smem = stage;
+  if (cudaFuncSetAttribute(select_compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return KVC_ERR_LAUNCH;
+  if (launch_pdl(select_compact_kernel, dim3(heads), dim3(256), smem, s, false, scores, N, P, R, budget, budget_all,
+                 entropy, g.Hkv, kept_idx, kept_len, status, use_smem, ca) != cudaSuccess)
+    return KVC_ERR_LAUNCH;
+  return KVC_OK;
 }
 
 int launch_select(const float* scores, int heads, int N, int P, int R, const int32_t* budget, int budget_all,
