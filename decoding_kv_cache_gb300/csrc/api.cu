@@ -101,6 +101,7 @@ void rope_table(float2 (&rope)[64], int D, int64_t t, double theta) {
 void fill_score_args(ScoreArgs* a, const CacheGeom& g, int dtype, const LayerPtrs& K, const void* q_recent, int n_r,
                      const void* qbuf, const int32_t* count, int qmax, int n_b, int64_t t, double theta,
                      float* scores, int32_t* beacon_picks, int32_t* status, const Opts& o, float* entropy) {
+  memset(a, 0, sizeof(*a));  // every field starts defined (no exchange words to zero, one tile)
   a->g = g;
   a->ext = o.ext ? 1 : 0;
   a->qstride = obs_qstride(n_r, n_b, o.ext);
@@ -166,7 +167,9 @@ int kvc_evict_launch_count(const kvc_cache* c, int32_t n_r, int32_t n_b) {
   if (!c || n_r < 0 || n_b < 0) return 0;
   kvc_cache probe = *c;
   if (check_cache(&probe, &g, &K, &V)) return 0;
-  // + selection and compaction: one launch up to kSelectCompactMaxN tokens per head, else two
+  // + selection and compaction: none for the fp32 cluster kernel (they run in it), one launch up to
+  // kSelectCompactMaxN tokens per head, else two
+  if (evict_fused_small(g, c->dtype, n_r, n_b)) return score_launches(g, c->dtype, n_r, n_b, false);
   return score_launches(g, c->dtype, n_r, n_b, false) + (g.N <= kSelectCompactMaxN ? 1 : 2);
 }
 
@@ -327,9 +330,20 @@ int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void*
   ScoreArgs a;
   fill_score_args(&a, g, c->dtype, K, q_recent, n_r, qbuf, count, qmax, n_b, t, rope_theta, sc, nullptr, status, o,
                   ent);
-  rc = launch_score(a, ws, s);
-  if (rc) return rc;
   const float* sel_ent = o.head_budget == KVC_BUDGET_ENTROPY ? ent : nullptr;
+  // fp32 caches of at most 1024 tokens per head: scoring, selection and compaction in one cluster launch
+  SmallEvict ev;
+  memset(&ev, 0, sizeof(ev));
+  ev.V = V;
+  ev.P = prefix;
+  ev.R = recent;
+  ev.budget_all = budget_all;
+  ev.budget = budget;
+  ev.kept_idx = ki;
+  ev.kept_len = kept_len;
+  bool fused = false;
+  rc = launch_score(a, ws, s, sel_ent ? nullptr : &ev, &fused);
+  if (rc || fused) return rc;
   if (g.N <= kSelectCompactMaxN)  // one CTA per head selects, then moves the head's K and V
     return launch_select_compact(sc, g, c->dtype, K, V, prefix, recent, budget, budget_all, sel_ent, ki, kept_len,
                                  status, s);

@@ -114,8 +114,7 @@ __global__ void append_kernel(AppendArgs a) {
   // one compression of the c == qmax staged rows: FPS picks, survivors to global rows [0, m)
   // from the staged copy, and the staged rows compacted the same way when more work follows
   auto compress = [&](bool more) {
-    gram_rows<D>(xs, npad, G);
-    fps_gram(G, npad + 1, a.qmax, m, pk);  // pk[0..m) ascending; pk[0] = 0
+    fps_rows<T, D>(xs, G, a.qmax, npad, m, pk);  // pk[0..m) ascending; pk[0] = 0
     for (int e = lane; e < m * vpr; e += kWarp) {
       const int k = e / vpr, v = e % vpr;
       const int src = pk[k];

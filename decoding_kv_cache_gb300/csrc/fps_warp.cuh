@@ -6,9 +6,10 @@
 // the largest distance to the chosen set, ties to the lower row. Distances are fp32.
 //
 // A query head's buffer (n <= 64 rows) is staged once into shared memory in its storage
-// type, its Gram matrix G = X X^T is formed once (warp-level bf16 MMA with fp32 accumulate,
-// whose products are exact; plain FMAs for fp32 rows), and each greedy step then needs one
-// G entry per candidate: cos(i, j) = G_ij / sqrt(G_ii G_jj).
+// type; each greedy step needs one dot product per candidate, cos(i, j) = G_ij / sqrt(G_ii G_jj).
+// bf16 rows: the Gram matrix G = X X^T is formed once (warp-level bf16 MMA with fp32 accumulate,
+// whose products are exact). fp32 rows: the dot products are formed as the steps need them (plain
+// FMAs), which is fewer than the whole matrix when m < n.
 #pragma once
 
 #include "kvc_internal.cuh"
@@ -23,7 +24,7 @@ struct Staging<__nv_bfloat16, D> {
 };
 template <int D>
 struct Staging<float, D> {
-  static constexpr int LD = D + 1;  // keeps lane-per-row reads conflict-free
+  static constexpr int LD = D + 4;  // 16-byte rows; eight consecutive rows on distinct bank groups
 };
 
 // Shared scratch one warp needs for a buffer of up to npad rows (npad a multiple of 16):
@@ -35,59 +36,33 @@ __host__ __device__ constexpr size_t fps_scratch_bytes(int npad) {
 }
 
 // Copy rows [0, n) of x (global, 16-byte aligned) into xs[npad][LD]; rows [n, npad) become zero.
-// bf16 rows (LD * 2 a multiple of 16 bytes) go straight to shared memory as 16-byte cp.async copies,
-// eight or sixteen per lane for a 32-row buffer (one bulk copy per row instead issued 32 copies one
-// after another, ~3k cycles): stage_rows_issue only starts them and stage_rows_wait completes
-// them, so other memory work can overlap. fp32 rows (odd LD) pass through registers in batches of
-// eight loads per lane, each batch in flight before its stores; they are complete when issue returns.
+// Rows go straight to shared memory as 16-byte cp.async copies (LD times the element size is a
+// multiple of 16 bytes for both storage types), eight or sixteen per lane for a 32-row buffer (one
+// bulk copy per row instead issued 32 copies one after another, ~3k cycles): stage_rows_issue only
+// starts them and stage_rows_wait completes them, so other memory work can overlap.
 template <typename T, int D>
 __device__ __forceinline__ void stage_rows_issue(const T* __restrict__ x, int n, int npad, T* xs) {
   const int lane = threadIdx.x & 31;
   constexpr int LD = Staging<T, D>::LD;
-  if constexpr (sizeof(T) == 2) {
-    constexpr int vpr = D / 8;  // 16-byte vectors per row
-    for (int e = lane; e < n * vpr; e += kWarp) {
-      const int r = e / vpr, v = e % vpr;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
-                       (uint32_t)__cvta_generic_to_shared(xs + r * LD + v * 8)),
-                   "l"(x + (size_t)r * D + v * 8)
-                   : "memory");
-    }
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
-    for (int e = lane; e < (npad - n) * vpr; e += kWarp)  // zero rows past n
-      *reinterpret_cast<uint4*>(xs + (n + e / vpr) * LD + (e % vpr) * 8) = make_uint4(0u, 0u, 0u, 0u);
-  } else {
-    constexpr int per = 16 / sizeof(T);
-    constexpr int vpr = D / per;
-    const uint4* src = reinterpret_cast<const uint4*>(x);
-    const int total = npad * vpr;
-    for (int e0 = 0; e0 < total; e0 += 8 * kWarp) {
-      uint4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int e = e0 + u * kWarp + lane;
-        v[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (e < total && e / vpr < n) v[u] = src[e];
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int e = e0 + u * kWarp + lane;
-        if (e < total) {
-          const int r = e / vpr, c0 = (e % vpr) * per;
-          const T* t = reinterpret_cast<const T*>(&v[u]);
-#pragma unroll
-          for (int k = 0; k < per; ++k) xs[r * LD + c0 + k] = t[k];
-        }
-      }
-    }
+  constexpr int per = 16 / (int)sizeof(T);
+  constexpr int vpr = D / per;  // 16-byte vectors per row
+  for (int e = lane; e < n * vpr; e += kWarp) {
+    const int r = e / vpr, v = e % vpr;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(xs + r * LD + v * per)),
+                 "l"(x + (size_t)r * D + v * per)
+                 : "memory");
   }
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+  for (int e = lane; e < (npad - n) * vpr; e += kWarp)  // zero rows past n
+    *reinterpret_cast<uint4*>(xs + (n + e / vpr) * LD + (e % vpr) * per) = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // Complete the staging started by stage_rows_issue (this lane's copies, then the warp's: the
 // rows are read by other lanes). The copies depend on nothing else, so the wait always ends.
 template <typename T>
 __device__ __forceinline__ void stage_rows_wait() {
-  if constexpr (sizeof(T) == 2) asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
   __syncwarp();
 }
 
@@ -207,24 +182,6 @@ __device__ __forceinline__ void gram_rows(const __nv_bfloat16* xs, int npad, flo
   __syncwarp();
 }
 
-template <int D>
-__device__ __forceinline__ void gram_rows(const float* xs, int npad, float* G) {
-  const int lane = threadIdx.x & 31;
-  constexpr int LD = Staging<float, D>::LD;
-  const int ldg = npad + 1;
-  for (int i = lane; i < npad; i += kWarp)
-    for (int j = 0; j < npad; ++j) {
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-      for (int d = 0; d < D; d += 2) {
-        s0 = fmaf(xs[i * LD + d], xs[j * LD + d], s0);
-        s1 = fmaf(xs[i * LD + d + 1], xs[j * LD + d + 1], s1);
-      }
-      G[i * ldg + j] = s0 + s1;
-    }
-  __syncwarp();
-}
-
 // Unsigned key with the order of the float (NaN excluded); -0 is first made +0 so that equal
 // floats give equal keys.
 __device__ __forceinline__ uint32_t ordered_key(float f) {
@@ -232,16 +189,18 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Greedy FPS from the Gram matrix of n <= 64 rows: m picks, written ascending to picks[0..m)
-// (warp-shared). Lane l owns candidates l and l+32. A zero row (G_ii = 0) has inverse norm 0,
-// which puts it at distance 1 from everything. All 32 lanes must call it.
-__device__ __forceinline__ void fps_gram(const float* G, int ldg, int n, int m, int* picks) {
+// Greedy FPS over n <= 64 rows given their dot products g(i, j) = row_i . row_j (called by the lane
+// that owns candidate i, for i < n): m picks, written ascending to picks[0..m) (warp-shared). Lane
+// l owns candidates l and l+32. A zero row (g(i, i) = 0) has inverse norm 0, which puts it at
+// distance 1 from everything. All 32 lanes must call it.
+template <typename GF>
+__device__ __forceinline__ void fps_greedy(GF g, int n, int m, int* picks) {
   const int lane = threadIdx.x & 31;
   float inv[2];
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     const int i = lane + kWarp * c;
-    const float ss = i < n ? G[i * ldg + i] : 0.f;
+    const float ss = i < n ? g(i, i) : 0.f;
     inv[c] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
   }
   // inverse norm of the row just chosen, fetched from its owning lane
@@ -258,7 +217,7 @@ __device__ __forceinline__ void fps_gram(const float* G, int ldg, int n, int m, 
     const int i = lane + kWarp * c;
     live[c] = i < n;
     chosen[c] = (i == 0);
-    const float d0 = live[c] ? 1.f - G[i * ldg] * inv[c] * inv0 : -INFINITY;
+    const float d0 = live[c] ? 1.f - g(i, 0) * inv[c] * inv0 : -INFINITY;
     md[c] = d0 == d0 ? d0 : -INFINITY;  // a NaN row can still be picked last, never out of range
   }
   for (int k = 1; k < m; ++k) {
@@ -282,7 +241,7 @@ __device__ __forceinline__ void fps_gram(const float* G, int ldg, int n, int m, 
     for (int c = 0; c < 2; ++c) {
       const int i = lane + kWarp * c;
       if (i == bi) chosen[c] = true;
-      if (live[c] && !chosen[c]) md[c] = fminf(md[c], 1.f - G[i * ldg + bi] * inv[c] * invj);
+      if (live[c] && !chosen[c]) md[c] = fminf(md[c], 1.f - g(i, bi) * inv[c] * invj);
     }
   }
   // ascending output: position = number of chosen rows below this one
@@ -292,6 +251,43 @@ __device__ __forceinline__ void fps_gram(const float* G, int ldg, int n, int m, 
   if (live[0] && chosen[0]) picks[__popc(m0 & below)] = lane;
   if (live[1] && chosen[1]) picks[__popc(m0) + __popc(m1 & below)] = lane + kWarp;
   __syncwarp();
+}
+
+// Greedy FPS from a Gram matrix G (leading dimension ldg).
+__device__ __forceinline__ void fps_gram(const float* G, int ldg, int n, int m, int* picks) {
+  fps_greedy([&](int i, int j) { return G[i * ldg + j]; }, n, m, picks);
+}
+
+// row_i . row_j of staged fp32 rows: 16-byte reads (row i differs per lane, row j is one address for
+// the warp), four FMA chains
+template <int D>
+__device__ __forceinline__ float dot_rows_f32(const float* xs, int i, int j) {
+  constexpr int LD = Staging<float, D>::LD;
+  const float4* a = reinterpret_cast<const float4*>(xs + i * LD);
+  const float4* b = reinterpret_cast<const float4*>(xs + j * LD);
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int u = 0; u < D / 4; ++u) {
+    const float4 x = a[u], y = b[u];
+    a0 = fmaf(x.x, y.x, a0);
+    a1 = fmaf(x.y, y.y, a1);
+    a2 = fmaf(x.z, y.z, a2);
+    a3 = fmaf(x.w, y.w, a3);
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
+// FPS picks over n staged rows. bf16 rows: the whole Gram matrix on warp MMAs (exact products)
+// into G first. fp32 rows: only the dot products FPS reads (each candidate's norm and its product
+// with every chosen row), formed when needed: m + 1 per candidate instead of n (G unused).
+template <typename T, int D>
+__device__ __forceinline__ void fps_rows(const T* xs, float* G, int n, int npad, int m, int* picks) {
+  if constexpr (sizeof(T) == 2) {
+    gram_rows<D>(xs, npad, G);
+    fps_gram(G, npad + 1, n, m, picks);
+  } else {
+    fps_greedy([&](int i, int j) { return dot_rows_f32<D>(xs, i, j); }, n, m, picks);
+  }
 }
 
 // FPS over a staged buffer. Scratch layout: staged rows, then G, then picks (fps_scratch_bytes).
@@ -311,8 +307,7 @@ __device__ __forceinline__ T* fps_buffer_finish(int n, int m, int npad, void* sc
   *picks_out = picks;
   stage_rows_wait<T>();
   if (m < n) {
-    gram_rows<D>(xs, npad, G);
-    fps_gram(G, npad + 1, n, m, picks);
+    fps_rows<T, D>(xs, G, n, npad, m, picks);
   } else {
     for (int k = threadIdx.x & 31; k < n; k += kWarp) picks[k] = k;
     __syncwarp();

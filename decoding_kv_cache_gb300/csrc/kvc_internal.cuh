@@ -148,6 +148,16 @@ struct ScoreArgs {
                                  // with 2, build_obs zeroes the scores and the tiles combine atomically
 };
 
+// kvc_evict's selection and compaction arguments, for the fp32 cluster kernel that runs them
+// itself (launch_score_small)
+struct SmallEvict {
+  LayerPtrs V;
+  int P, R, budget_all;
+  const int32_t* budget;  // [heads] or null
+  int32_t* kept_idx;      // [heads][N]
+  int32_t* kept_len;      // [heads]
+};
+
 // Row stride of a query head and row count of the observation tile for a mode.
 inline int obs_qstride(int n_r, int n_b, bool ext) { return ext ? (n_r + n_b + 15) / 16 * 16 : n_r + n_b; }
 inline int obs_rows_used(int G, int n_r, int n_b, bool ext) { return (G - 1) * obs_qstride(n_r, n_b, ext) + n_r + n_b; }
@@ -155,7 +165,10 @@ inline int obs_rows_used(int G, int n_r, int n_b, bool ext) { return (G - 1) * o
 int obs_rows(int M, int dtype);
 
 size_t score_ws_bytes(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext, ScoreWs* carve, void* base);
-int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s);
+// ev: kvc_evict's selection and compaction, taken into the scoring launch where the fp32 cluster
+// kernel runs (then *fused is set; else the caller launches them)
+int launch_score(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s, const SmallEvict* ev = nullptr,
+                 bool* fused = nullptr);
 size_t fused_xch_bytes(int M_pad);
 int launch_score_fused(const ScoreArgs& a, const ScoreWs& ws, void* xch_base, cudaStream_t s);
 // Single-read kernel (bf16, 128 observation rows, at most 256 keys per SM per head): the plan, or
@@ -197,8 +210,16 @@ struct WidePlan {
 };
 bool score_wide_plan(const ScoreArgs& a, WidePlan* p, size_t* smem);
 int launch_score_wide(const ScoreArgs& a, const ScoreWs& ws, const WidePlan& p, size_t smem, cudaStream_t s);
+// fp32 caches of at most eight CTAs of 128 keys per head (default options): the whole scoring
+// (observation rows included) in one launch, a thread-block cluster per head; kvc_evict's
+// selection and compaction can run in the same launch (SmallEvict).
+bool score_small_plan(const ScoreArgs& a, size_t* smem, bool evict);
+int launch_score_small(const ScoreArgs& a, const ScoreWs& ws, cudaStream_t s, const SmallEvict* ev);
 // kernels launch_score starts for these arguments (host only; default options when !ext)
 int score_launches(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext);
+// whether kvc_evict (default options, given budgets, a buffer of 2 n_b rows) selects and compacts
+// inside the scoring launch
+bool evict_fused_small(const CacheGeom& g, int dtype, int n_r, int n_b);
 
 // entropy non-null: each (layer, sequence)'s budgets are reallocated over its Hkv heads first;
 // keyed: `scores` holds order-preserving unsigned keys already (EPIKV), not fp32 scores

@@ -15,7 +15,9 @@
 //                128-row MMA tile and a head spreads over at most one CTA per SM in
 //                256-key pieces (pass-1 logits kept in TMEM, every key read once);
 //                otherwise score_fused (score_fused.cu), which reads the keys twice
-//   fp32 caches: pass1 / combine / pass2 below on CUDA cores:
+//   fp32 caches of at most 1024 keys per head: score_small (score_small.cu), one cluster launch
+//                that also builds the observation rows (no build_obs launch)
+//   other fp32 caches: pass1 / combine / pass2 below on CUDA cores:
 //     pass1      per (key chunk, head): per-row chunk max and sum of exp2
 //     combine    per head: merge the partials into lse2 per row
 //     pass2      per (key chunk, head): max over rows of s*log2(e)/sqrt(D) - lse2, exp2
@@ -23,8 +25,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-#include "fps_warp.cuh"
-#include "kvc_internal.cuh"
+#include "obs_rows.cuh"
 
 namespace kvc {
 
@@ -34,149 +35,16 @@ namespace kvc {
 template <typename T, int D>
 __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int Hkv = a.g.Hkv, B = a.g.B, Hq = a.g.Hq;
+  __shared__ int s_nvalid;  // valid observation rows of this KV head (for the entropy's mean)
   const int head = blockIdx.x;
-  const int l = head / (B * Hkv), b = (head / Hkv) % B, h = head % Hkv;
-  const int G = Hq / Hkv, per_q = a.n_r + a.n_b, hd = D / 2;
-  const int qs = a.qstride;  // rows of query head g start at g * qs
-  constexpr int LD = Staging<T, D>::LD;
+  const int G = a.g.Hq / a.g.Hkv, qs = a.qstride;
   T* obs = static_cast<T*>(ws.obs) + (size_t)head * a.M_pad * D;
   uint8_t* valid = ws.valid + (size_t)head * a.M_pad;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int npad = (a.qmax + 15) & ~15;
-  void* scratch = smem_raw + warp * ((fps_scratch_bytes<T, D>(npad) + 15) & ~(size_t)15);
-  const T* qrec = static_cast<const T*>(a.q_recent);
-  const T* qbuf = static_cast<const T*>(a.qbuf);
-
-  constexpr int per = 16 / (int)sizeof(T);
-  constexpr int lpr = (D / 2) / per;  // rotation: lanes per beacon row, `per` pairs (i, i + D/2) each
-  constexpr int rpi = kWarp / lpr;
-  const int i0 = (lane % lpr) * per, rsel = lane / lpr;
-  float2* rope_s = reinterpret_cast<float2*>(smem_raw + (size_t)nw * ((fps_scratch_bytes<T, D>(npad) + 15) & ~(size_t)15));
-  __shared__ int s_nvalid;  // valid observation rows of this KV head (for the entropy's mean)
+  // the CTA's nw warps (nw <= G, so every warp has a query head and reaches the shared step of the
+  // first one)
+  obs_group_rows<T, D>(a, ws, head, nw, smem_raw, obs, valid, &s_nvalid);
+  obs_padding<T, D>(a, obs, valid);
   const bool mean_w = a.ext && a.row_agg == KVC_AGG_MEAN;
-
-  // every warp has at least one query head (nw <= G), so the CTA-wide step in the first
-  // iteration is reached by all threads
-  for (int g = warp, it = 0; g < G; g += nw, ++it) {
-    const int hq = h * G + g;
-    const size_t qh = ((size_t)l * B + b) * Hq + hq;
-    T* orow = obs + (size_t)g * qs * D;
-    // Issue this query head's global reads first: stage the whole buffer (rows at or past its
-    // count are staged too but never read: FPS and the Gram entries it uses involve live rows
-    // only), the count, and the first batch of recent rows.
-    fps_buffer_issue<T, D>(qbuf + qh * a.qmax * D, a.qmax, npad, scratch);
-    int c = a.qmax > 0 ? a.count[qh] : 0;
-    const uint4* qr = reinterpret_cast<const uint4*>(qrec + qh * a.n_r * D);
-    uint4* od = reinterpret_cast<uint4*>(orow);
-    const int nv = a.n_r * D * (int)sizeof(T) / 16;  // recent rows, 16-byte vectors
-    uint4 rv[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (u * kWarp + lane < nv) rv[u] = qr[u * kWarp + lane];
-    if (it == 0) {
-      // while those are in flight: this CTA's share of the scoring kernel's exchange words (they
-      // start at zero) and the rotation table in shared memory, read from the parameter block at
-      // warp-uniform indices (a per-lane index there serialises; the rotation reads it per lane)
-      if (a.xch_zero) {
-        const long long share = (a.xch_zero_words + gridDim.x - 1) / gridDim.x;
-        const long long lo = (long long)blockIdx.x * share;
-        const long long hi = lo + share < a.xch_zero_words ? lo + share : a.xch_zero_words;
-        for (long long w = lo + threadIdx.x; w < hi; w += blockDim.x) a.xch_zero[w] = 0ull;
-      }
-      for (int i = warp; i < hd; i += nw)  // warp-uniform indices: broadcast parameter reads
-        if (lane == 0) rope_s[i] = a.rope[i];
-      // the scoring kernel combines a head's tiles into its scores with atomics: start at zero
-      if (a.tiles > 1)
-        for (int j = threadIdx.x; j < a.g.N; j += blockDim.x) a.scores[(size_t)head * a.g.N + j] = 0.f;
-      if (threadIdx.x == 0) s_nvalid = 0;
-      __syncthreads();
-    }
-    if (c < 0 || c > a.qmax) {
-      if (lane == 0) status_or(a.status, KVC_STATUS_COUNT_RANGE);
-      c = c < 0 ? 0 : a.qmax;
-    }
-    // recent queries: already rotated to their own positions, copied as stored
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (u * kWarp + lane < nv) od[u * kWarp + lane] = rv[u];
-    for (int e0 = 8 * kWarp; e0 < nv; e0 += 8 * kWarp) {  // more than 8 vectors per lane: further batches
-      uint4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (e0 + u * kWarp + lane < nv) v[u] = qr[e0 + u * kWarp + lane];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (e0 + u * kWarp + lane < nv) od[e0 + u * kWarp + lane] = v[u];
-    }
-    for (int r = lane; r < a.n_r; r += kWarp) valid[g * qs + r] = 1;
-    // beacons: the buffer itself when it holds at most n_b rows, else FPS down to n_b
-    int* pk;
-    const T* xs = fps_buffer_finish<T, D>(c, a.n_b, npad, scratch, &pk);
-    const int nb = c < a.n_b ? c : a.n_b;
-    if (a.ext) {
-      if (lane == 0) atomicAdd(&s_nvalid, a.n_r + nb);
-      // the mean over this query head's rows weighs each valid row 1 / (its valid rows)
-      if (mean_w) {
-        const float w = a.n_r + nb > 0 ? 1.f / (float)(a.n_r + nb) : 0.f;
-        for (int r = lane; r < qs && g * qs + r < a.M_pad; r += kWarp)
-          ws.rw[(size_t)head * a.M_pad + g * qs + r] = r < a.n_r + nb ? w : 0.f;
-      }
-      // rows between this query head's last row and the next head's first
-      if (g + 1 < G)
-        for (int e = lane; e < (qs - per_q) * D; e += kWarp) orow[(size_t)per_q * D + e] = from_f32<T>(0.f);
-      for (int r = per_q + lane; r < qs && g + 1 < G; r += kWarp) valid[g * qs + r] = 0;
-    }
-    for (int k0 = 0; k0 < a.n_b; k0 += rpi) {
-      const int k = k0 + rsel;
-      if (k >= a.n_b) continue;
-      T* dst = orow + (size_t)(a.n_r + k) * D;
-      alignas(16) T o1[per];
-      alignas(16) T o2[per];
-      if (k < nb) {
-        const T* src = xs + pk[k] * LD;
-        // the lane's `per` pairs: one 16-byte read per half for bf16 rows (LD * 2 and i0 * 2 are
-        // multiples of 16), element reads for fp32 rows (odd LD); the table in 16-byte reads
-        alignas(16) T xa[per];
-        alignas(16) T xb[per];
-        if constexpr (sizeof(T) == 2) {
-          *reinterpret_cast<uint4*>(xa) = *reinterpret_cast<const uint4*>(src + i0);
-          *reinterpret_cast<uint4*>(xb) = *reinterpret_cast<const uint4*>(src + i0 + hd);
-        } else {
-#pragma unroll
-          for (int u = 0; u < per; ++u) {
-            xa[u] = src[i0 + u];
-            xb[u] = src[i0 + u + hd];
-          }
-        }
-        alignas(16) float2 csv[per];
-#pragma unroll
-        for (int q2 = 0; q2 < per / 2; ++q2)
-          reinterpret_cast<float4*>(csv)[q2] = reinterpret_cast<const float4*>(rope_s + i0)[q2];
-#pragma unroll
-        for (int u = 0; u < per; ++u) {
-          const float2 cs = csv[u];
-          const float x0 = to_f32(xa[u]), x1 = to_f32(xb[u]);
-          // each product and the sum rounded separately (no fused multiply-add), so the
-          // rounding to the storage type below is a reproducible decision
-          o1[u] = from_f32<T>(__fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y)));
-          o2[u] = from_f32<T>(__fadd_rn(__fmul_rn(x1, cs.x), __fmul_rn(x0, cs.y)));
-        }
-      } else {
-#pragma unroll
-        for (int u = 0; u < per; ++u) o1[u] = o2[u] = from_f32<T>(0.f);
-      }
-      *reinterpret_cast<uint4*>(dst + i0) = *reinterpret_cast<const uint4*>(o1);
-      *reinterpret_cast<uint4*>(dst + i0 + hd) = *reinterpret_cast<const uint4*>(o2);
-      if (i0 == 0) valid[g * qs + a.n_r + k] = k < nb ? 1 : 0;
-    }
-    if (a.beacon_picks)
-      for (int k = lane; k < a.n_b; k += kWarp) a.beacon_picks[qh * a.n_b + k] = k < nb ? pk[k] : -1;
-    __syncwarp();
-  }
-  // padding rows up to the stored row count
-  for (int e = threadIdx.x; e < (a.M_pad - a.M) * D; e += blockDim.x) obs[(size_t)a.M * D + e] = from_f32<T>(0.f);
-  for (int r = a.M + threadIdx.x; r < a.M_pad; r += blockDim.x) valid[r] = 0;
   if (a.ext) {
     if (mean_w)
       for (int r = (G - 1) * qs + qs + threadIdx.x; r < a.M_pad; r += blockDim.x) ws.rw[(size_t)head * a.M_pad + r] = 0.f;
@@ -385,11 +253,13 @@ static bool set_smem(K kernel, size_t bytes) {
 }
 
 // Which bf16 scoring kernel runs (sets a->tiles); 0 = fp32 passes.
-enum ScorePath { kPathF32 = 0, kPathResident = 1, kPathSplit = 2, kPathFused = 3, kPathWide = 4 };
+enum ScorePath { kPathF32 = 0, kPathResident = 1, kPathSplit = 2, kPathFused = 3, kPathWide = 4, kPathSmall = 5 };
 static ScorePath choose_score(ScoreArgs* a, FusedPlan* rp, size_t* rsmem, SplitPlan* sp, size_t* ssmem,
-                              WidePlan* wp, size_t* wsmem) {
+                              WidePlan* wp, size_t* wsmem, bool evict = false) {
   a->tiles = 1;
-  if (a->dtype != KVC_BF16) return kPathF32;
+  // fp32: one cluster launch for short caches (score_small.cu) unless the streaming passes are asked for
+  if (a->dtype != KVC_BF16)
+    return (a->kernel != KVC_KERNEL_SPLIT && score_small_plan(*a, ssmem, evict)) ? kPathSmall : kPathF32;
   // A 256-row observation tile goes to the single-read kernel as two 128-row tiles when no query
   // head's rows cross the tile boundary (or the aggregation is max over everything, where heads do
   // not matter).
@@ -439,21 +309,44 @@ int score_launches(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext) {
   size_t r1 = 0, r2 = 0, r3 = 0;
   switch (choose_score(&a, &rp, &r1, &sp, &r2, &wp, &r3)) {
     case kPathF32: return 4;    // observation rows, pass 1, combine, pass 2
+    case kPathSmall: return 1;  // one cluster kernel (observation rows included)
     case kPathSplit: return 4;  // observation rows, pass 1, combine, pass 2
     case kPathWide: return 5;   // observation rows, pass 1, exact fallback, combine, pass 2
     default: return 2;          // observation rows, one scoring kernel
   }
 }
 
-int launch_score(const ScoreArgs& a_in, const ScoreWs& ws, cudaStream_t s) {
+bool evict_fused_small(const CacheGeom& g, int dtype, int n_r, int n_b) {
+  ScoreArgs a;
+  memset(&a, 0, sizeof(a));
+  a.g = g;
+  a.dtype = dtype;
+  a.n_r = n_r;
+  a.n_b = n_b;
+  a.qstride = obs_qstride(n_r, n_b, false);
+  a.M = obs_rows_used(g.Hq / g.Hkv, n_r, n_b, false);
+  a.M_pad = obs_rows(a.M, dtype);
+  a.qmax = 2 * n_b;  // the continual-FPS buffer of twice the beacons
+  size_t smem = 0;
+  return dtype == KVC_F32 && score_small_plan(a, &smem, true);
+}
+
+int launch_score(const ScoreArgs& a_in, const ScoreWs& ws, cudaStream_t s, const SmallEvict* ev, bool* fused) {
   ScoreArgs a = a_in;
+  if (fused) *fused = false;
   const int heads = a.g.L * a.g.B * a.g.Hkv;
   // the single-read kernel's plan is fixed first: the observation kernel zeroes its exchange words.
   FusedPlan rp;
   SplitPlan sp;
   WidePlan wp;
   size_t rsmem = 0, ssmem = 0, wsmem = 0;
-  const ScorePath path = choose_score(&a, &rp, &rsmem, &sp, &ssmem, &wp, &wsmem);
+  const ScorePath path = choose_score(&a, &rp, &rsmem, &sp, &ssmem, &wp, &wsmem, ev != nullptr);
+  if (path == kPathSmall) {  // the cluster kernel builds the observation rows itself
+    a.xch_zero = nullptr;
+    a.xch_zero_words = 0;
+    if (ev && fused) *fused = true;
+    return launch_score_small(a, ws, s, ev && fused ? ev : nullptr);
+  }
   const bool resident = path == kPathResident, split = path == kPathSplit, wide = path == kPathWide;
   // the observation kernel zeroes the single-read kernel's exchange words, or the wide kernel's
   // fallback count

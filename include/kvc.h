@@ -106,7 +106,10 @@ enum {
  * kernel computes the same scores). KVC_KERNEL_AUTO picks by shape; a forced
  * kernel that does not apply to the call falls back to the automatic choice
  * (RESIDENT: 128-row tiles and short caches; SPLIT: default options only; WIDE:
- * default options and more than 128 observation rows). */
+ * default options and more than 128 observation rows). fp32 caches: SPLIT forces
+ * the streaming passes; any other value lets a cache of at most 1024 keys per head
+ * with default options take one thread-block-cluster launch after the observation
+ * rows. */
 #define KVC_KERNEL_AUTO 0
 #define KVC_KERNEL_RESIDENT 1 /* single read of K, logits held in tensor memory */
 #define KVC_KERNEL_SPLIT 2    /* two streaming passes, independent work items */

@@ -301,6 +301,36 @@ def test_each_scoring_kernel_matches_oracle(path, name, over):
     check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
 
 
+F32_CASES = [
+    ("tiny", {}),                                     # 8 CTAs of 32 keys per head
+    ("tiny", dict(N=1000, D=128)),                    # 8 CTAs of 125 keys, ragged last CTA
+    ("tiny", dict(N=33)),                             # 2 CTAs of 17 and 16 keys
+    ("tiny", dict(N=1, keep=1)),                      # one key: every score is 1
+    ("tiny", dict(L=2, B=3, N=300, Hq=16, Hkv=2)),    # 256 rows, 12 heads
+    ("tiny", dict(N=1500)),                           # 188 keys per CTA: the streaming passes
+]
+
+
+@pytest.mark.parametrize("path", ["auto", "split"])
+@pytest.mark.parametrize("name,over", F32_CASES, ids=[_ids(c) for c in F32_CASES])
+def test_f32_scoring_paths(path, name, over):
+    """fp32 caches: the one-launch cluster kernel (short caches, chosen automatically) and the
+    streaming passes (forced with kvc_opts.kernel = split, and the automatic choice past 1024 keys)
+    against the oracle."""
+    inp = make_inputs(name, **over)
+    gpu = run_evict(inp, DEV, kernel=path)
+    _, gpu_picks = run_score(inp, DEV, kernel=path)
+    ora = O.evict(inp)
+    if check_beacon_picks(inp, gpu_picks, ora["beacon_picks"]):
+        ora = O.evict(inp, forced_picks=gpu_picks)
+    assert gpu["status"] == 0
+    assert_scores_close(gpu["scores"], ora["scores"], f"{name} via {path}")
+    if inp.N == 1:
+        assert np.abs(gpu["scores"].astype(np.float64) - 1.0).max() <= 2.0 ** -20
+    check_kept(inp, gpu, ora, gpu["scores"])
+    check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
+
+
 WIDE_CASES = [
     ("qwen3-14b-long", dict(L=1, B=2, N=4100)),             # 240 rows: 16-column tail granule, ragged range
     ("qwen7b-reasonalloc", dict(L=1, B=1, N=8192)),         # 224 rows: whole granules only, two ranges
