@@ -230,7 +230,7 @@ int launch_head_budget(const float* entropy, int groups, int Hkv, int N, int P, 
                        int budget_all, int32_t* budget_out, int32_t* status, cudaStream_t s);
 
 // kvc_evict's selection and compaction in one launch (one CTA per head; N <= kSelectCompactMaxN)
-constexpr int kSelectCompactMaxN = 16384;
+constexpr int kSelectCompactMaxN = 65536;
 int launch_select_compact(const float* scores, const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V,
                           int P, int R, const int32_t* budget, int budget_all, const float* entropy, int32_t* kept_idx,
                           int32_t* kept_len, int32_t* status, cudaStream_t s);

@@ -55,10 +55,11 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
                         use_smem, keyed, sh_bits);
 }
 
-// Selection and compaction of one head per CTA (256 threads, heads of at most 16384 tokens): the
-// CTA selects, then two of its warps move the head's kept K and V rows (compact_warp). One launch
-// instead of two, and each head's selection overlaps the other heads' moves. The dynamic shared
-// memory stages the scores of a head of more than one tile, then serves as the two warps' rings.
+// Selection and compaction of one head per CTA (256 threads, heads of at most kSelectCompactMaxN
+// tokens): the CTA selects, then two of its warps move the head's kept K and V rows (compact_warp).
+// One launch instead of two, and each head's selection overlaps the other heads' moves (two CTAs
+// fit on an SM). The dynamic shared memory stages the scores of a head of more than one tile (when
+// they fit), then serves as the two warps' rings.
 __global__ void __launch_bounds__(256) select_compact_kernel(const float* __restrict__ scores, int N, int P, int R,
                                                              const int32_t* __restrict__ budget, int budget_all,
                                                              const float* __restrict__ entropy, int Hkv,
@@ -90,10 +91,12 @@ int launch_select_compact(const float* scores, const CacheGeom& g, int dtype, co
   ca.rowbytes = g.D * (dtype == KVC_BF16 ? 2 : 4);
   ca.validate = 0;
   ca.list_seq = 0;
+  // a head of more than one tile is staged in shared memory when it fits in the two warps' rings
+  // (the CTA's footprint stays at two per SM, so one CTA's selection runs beside another's moves);
+  // a longer head is read from global memory (L2) on every pass
   const size_t stage = (size_t)(N + kSweep - 1) / kSweep * kSweep * 4;
-  const int use_smem = N > kSweep * 256 ? 1 : 0;
-  size_t smem = 2 * (size_t)kCompactWarpSmem;
-  if (use_smem && stage > smem) smem = stage;
+  const size_t smem = 2 * (size_t)kCompactWarpSmem;
+  const int use_smem = (N > kSweep * 256 && stage <= smem) ? 1 : 0;
   if (cudaFuncSetAttribute(select_compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   if (launch_pdl(select_compact_kernel, dim3(heads), dim3(256), smem, s, false, scores, N, P, R, budget, budget_all,
