@@ -302,6 +302,8 @@ int score_launches(const CacheGeom& g, int dtype, int n_r, int n_b, bool ext) {
   a.qstride = obs_qstride(n_r, n_b, ext);
   a.M = obs_rows_used(g.Hq / g.Hkv, n_r, n_b, ext);
   a.M_pad = obs_rows(a.M, dtype);
+  a.M_n = (a.M + 15) / 16 * 16;  // the wide kernel's plan reads it
+  a.qmax = 2 * n_b;
   a.nchunk = (g.N + kChunk - 1) / kChunk;
   FusedPlan rp;
   SplitPlan sp;

@@ -374,3 +374,17 @@ def test_wide_kernel_exact_fallback_on_extreme_logits(where):
     assert gpu["status"] == 0
     assert_scores_close(gpu["scores"], ora["scores"], f"wide fallback ({where})")
     check_kept(inp, gpu, ora, gpu["scores"])
+
+
+@pytest.mark.parametrize("name,over,launches", [
+    ("tiny", {}, 1),                                        # the fp32 cluster kernel
+    ("qwen3-4b", dict(L=1, N=1000), 3),                     # observation rows, single-read scoring, select+compact
+    ("qwen3-14b-long", dict(L=1, B=1, N=2100), 6),          # + wide pass 1, exact fallback, combine, pass 2
+    ("qwen3-4b", dict(L=1, Hq=4, Hkv=1, N=70000), 6),       # two-pass streaming kernel, separate select and compact
+])
+def test_evict_launch_count(name, over, launches):
+    """kvc_evict_launch_count (the benchmark's gpu_launches) names the kernels kvc_evict launches."""
+    from decoding_kv_cache_gb300 import kvc
+    inp = make_inputs(name, device=DEV, **over)
+    cache = kvc.Cache(inp.K, inp.V, inp.Hq)
+    assert kvc.kvc_evict_launch_count(cache, inp.n_r, inp.n_b) == launches
