@@ -71,6 +71,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   float* pbest = reinterpret_cast<float*>(merge + 2 * NT * kSplitRows);  // pass 2: [2][4][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // As the wide kernel's exact fallback the items are listed by the previous kernel, usually none: a
+  // CTA without a listed item leaves before it takes tensor memory or sets anything up.
+  if (p.list) {
+    griddep_wait();
+    if ((int)blockIdx.x >= *reinterpret_cast<const volatile int32_t*>(p.list)) return;
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       tc::mbar_init(&kfull[i], 1);
