@@ -195,8 +195,10 @@ struct SplitPlan {
   const int32_t* list;  // null: every item; else [0] = count, [1..] = the items (device, written by the
                         // previous kernel on the stream)
 };
-// Pass 1 of the two-pass streaming kernel over a device list of items (the wide kernel's fallback).
-int launch_score_split_pass1_list(const ScoreArgs& a, const ScoreWs& ws, const int32_t* list, cudaStream_t s);
+// Pass 1 of the two-pass streaming kernel over a device list of items (the wide kernel's fallback),
+// with the listing kernel's ranges: item = head * R + range, rk key chunks per range.
+int launch_score_split_pass1_list(const ScoreArgs& a, const ScoreWs& ws, const int32_t* list, int rk, int R,
+                                  cudaStream_t s);
 int split_ranges(int nchunk, int M_pad);
 bool score_split_plan(const ScoreArgs& a, SplitPlan* p, size_t* smem);
 int launch_score_split(const ScoreArgs& a, const ScoreWs& ws, const SplitPlan& p, size_t smem, cudaStream_t s);

@@ -460,11 +460,15 @@ int launch_score_split(const ScoreArgs& a, const ScoreWs& ws, const SplitPlan& p
   return KVC_OK;
 }
 
-int launch_score_split_pass1_list(const ScoreArgs& a, const ScoreWs& ws, const int32_t* list, cudaStream_t s) {
+int launch_score_split_pass1_list(const ScoreArgs& a, const ScoreWs& ws, const int32_t* list, int rk, int R,
+                                  cudaStream_t s) {
   SplitPlan p;
   size_t smem = 0;
   if (!score_split_plan(a, &p, &smem)) return KVC_ERR_LAUNCH;
   p.list = list;
+  p.rk = rk;  // the listing kernel's ranges
+  p.R = R;
+  p.items = a.g.L * a.g.B * a.g.Hkv * R;
   const int D = a.g.D, NT = a.M_pad / kSplitRows;
   FusedMaps maps;
   if (!fused_maps(&maps, a, ws)) return KVC_ERR_LAUNCH;

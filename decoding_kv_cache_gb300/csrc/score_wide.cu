@@ -525,8 +525,11 @@ bool score_wide_plan(const ScoreArgs& a, WidePlan* p, size_t* smem) {
     return false;
   const int D = a.g.D;
   const int heads = a.g.L * a.g.B * a.g.Hkv;
-  p->rk = 32;  // the same ranges as the two-pass kernel for 256-row tiles (split_ranges)
-  p->R = split_ranges(a.nchunk, a.M_pad);
+  // ranges of 32 key chunks (the two-pass kernel's for 256-row tiles, split_ranges), or of 64 for heads
+  // of 16384 keys and more: half the items' ends (a few us each, when the epilogue's reductions and
+  // barriers leave the tensor pipe idle) while every SM still gets tens of items
+  p->rk = a.nchunk >= 128 ? 64 : 32;
+  p->R = (a.nchunk + p->rk - 1) / p->rk;
   p->items = heads * p->R;
   p->grid = p->items < nsm ? p->items : nsm;
   const int qbytes = a.M_n * D * 2;
@@ -559,7 +562,7 @@ int launch_score_wide(const ScoreArgs& a, const ScoreWs& ws, const WidePlan& p, 
       return KVC_ERR_LAUNCH;
     if (pass == 1) {
       // the listed items again, with a running max per row (the two-pass kernel's pass 1)
-      if (launch_score_split_pass1_list(a, ws, ws.fb, s) != KVC_OK) return KVC_ERR_LAUNCH;
+      if (launch_score_split_pass1_list(a, ws, ws.fb, p.rk, p.R, s) != KVC_OK) return KVC_ERR_LAUNCH;
       const SplitPlan sp{p.rk, p.R, p.items, p.grid, p.stages};
       if (launch_pdl(split_combine_kernel, dim3(a.g.L * a.g.B * a.g.Hkv), dim3(a.M_pad), 0, s, false, aa, wss, sp) !=
           cudaSuccess)

@@ -354,15 +354,16 @@ def test_wide_kernel_shapes(name, over):
     check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
 
 
-@pytest.mark.parametrize("where", ["late", "first"])
+@pytest.mark.parametrize("where", ["late", "first", "long-late"])
 def test_wide_kernel_exact_fallback_on_extreme_logits(where):
     """Keys planted along a recent query with a logit ~160 (base 2) above the rest: late in a lane,
     its sum overflows the lane's reference; as a lane's first key, the references spread far beyond
     what one common reference holds. Either way pass 1 lists the item and the exact fallback
-    recomputes it; the scores still match the oracle."""
-    inp = make_inputs("qwen3-14b-long", L=1, B=1, N=1500)
+    recomputes it; the scores still match the oracle. long-late: a head of 16500 keys, whose items
+    are ranges of 64 chunks (the last one ragged), with the planted key in the second range."""
+    inp = make_inputs("qwen3-14b-long", L=1, B=1, N=16500 if where == "long-late" else 1500)
     G = inp.Hq // inp.Hkv
-    pos = 700 if where == "late" else 5
+    pos = {"late": 700, "first": 5, "long-late": 9000}[where]
     for h in range(inp.Hkv):
         q = inp.q_recent[0, 0, h * G, 0].float()
         inp.K[0, 0, h, pos] = (10.0 * q).to(inp.K.dtype)
