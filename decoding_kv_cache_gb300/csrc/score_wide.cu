@@ -27,7 +27,8 @@
 //
 // Roles (persistent, one CTA per SM; items b, b + grid, ... for CTA b):
 //   warp 0      TMA producer: the item's observation tile (one buffer) and its key chunks (a ring of
-//               up to five 32 KB stages: a stage stays held until its MMA completes)
+//               three 32 KB stages: a stage stays held until its MMA completes; a deeper ring
+//               measured slower, and this footprint leaves shared memory for the L1 cache)
 //   warp 1      tcgen05.mma issuer (one thread): per chunk one chain into one of two TMEM slots of
 //               256 columns
 //   warps 2-17  epilogue, two groups of eight: group g takes the chunks in TMEM slot g, so that one
