@@ -469,6 +469,13 @@ int launch_score_split_pass1_list(const ScoreArgs& a, const ScoreWs& ws, const i
   p.rk = rk;  // the listing kernel's ranges
   p.R = R;
   p.items = a.g.L * a.g.B * a.g.Hkv * R;
+  // the wide kernel's footprint (three key stages), so that the SMs keep their shared-memory split
+  // between the launches around this one
+  const size_t per_stage = (size_t)kChunk * a.g.D * 2;
+  if (p.stages > 3) {
+    smem -= (size_t)(p.stages - 3) * per_stage;
+    p.stages = 3;
+  }
   const int D = a.g.D, NT = a.M_pad / kSplitRows;
   FusedMaps maps;
   if (!fused_maps(&maps, a, ws)) return KVC_ERR_LAUNCH;
