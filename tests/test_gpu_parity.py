@@ -389,3 +389,22 @@ def test_evict_launch_count(name, over, launches):
     inp = make_inputs(name, device=DEV, **over)
     cache = kvc.Cache(inp.K, inp.V, inp.Hq)
     assert kvc.kvc_evict_launch_count(cache, inp.n_r, inp.n_b) == launches
+
+
+def test_f32_per_head_budget_out_of_range_is_flagged_and_left_whole():
+    """The fp32 cluster kernel's own selection: a head whose budget is below prefix + recent is kept
+    whole and flagged, one whose budget equals N is kept whole without a flag, the rest follow the
+    oracle."""
+    inp = make_inputs("tiny", L=2, B=2, N=300)
+    b = torch.full((inp.L, inp.B, inp.Hkv), 250, dtype=torch.int32)
+    b[0, 1, 0] = 5     # < prefix + recent
+    b[1, 0, 1] = 300   # == N
+    b[1, 1, 0] = 20    # == prefix + recent: no middle key kept
+    inp.budget = b
+    gpu = run_evict(inp, DEV)
+    ora = O.evict(inp)
+    assert gpu["status"] & 0x1
+    assert gpu["kept_len"][0, 1, 0] == 300 and gpu["kept_len"][1, 0, 1] == 300 and gpu["kept_len"][1, 1, 0] == 20
+    assert_scores_close(gpu["scores"], ora["scores"], "tiny per-head budgets")
+    check_kept(inp, gpu, ora, gpu["scores"])
+    check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
