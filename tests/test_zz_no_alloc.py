@@ -59,6 +59,7 @@ SEQUENCE = [
     ("qwen3-14b-long", dict(L=1, B=1, N=700, seed=12), {}),
     ("qwen3-4b", dict(L=2, N=1000, seed=13), dict(entropy=True)),
     ("tiny", {}, dict(row_agg="mean")),
+    ("tiny", dict(N=500, seed=15), {}),  # the fp32 cluster kernel (no observation tiles in the region)
     ("qwen3-4b", dict(L=1, N=1500, seed=14), {}),
 ]
 
