@@ -266,13 +266,19 @@ __device__ __forceinline__ float dot_rows_f32(const float* xs, int i, int j) {
   const float4* a = reinterpret_cast<const float4*>(xs + i * LD);
   const float4* b = reinterpret_cast<const float4*>(xs + j * LD);
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-  for (int u = 0; u < D / 4; ++u) {
+  auto step = [&](int u) {
     const float4 x = a[u], y = b[u];
     a0 = fmaf(x.x, y.x, a0);
     a1 = fmaf(x.y, y.y, a1);
     a2 = fmaf(x.z, y.z, a2);
     a3 = fmaf(x.w, y.w, a3);
+  };
+  if constexpr (D <= 64) {  // every read in flight at once (the greedy steps wait on this product)
+#pragma unroll
+    for (int u = 0; u < D / 4; ++u) step(u);
+  } else {  // D = 128: in batches of eight, so that the cluster kernel stays within its registers
+#pragma unroll 8
+    for (int u = 0; u < D / 4; ++u) step(u);
   }
   return (a0 + a1) + (a2 + a3);
 }

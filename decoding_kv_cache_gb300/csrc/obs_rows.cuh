@@ -111,6 +111,11 @@ __device__ __forceinline__ void obs_group_rows(const ScoreArgs& a, const ScoreWs
         for (int e = lane; e < (qs - per_q) * D; e += kWarp) orow[(size_t)per_q * D + e] = from_f32<T>(0.f);
       for (int r = per_q + lane; r < qs && g + 1 < G; r += kWarp) valid[g * qs + r] = 0;
     }
+    // the lane's `per` pairs of the rotation table (the same for every beacon row), in 16-byte reads
+    alignas(16) float2 csv[per];
+#pragma unroll
+    for (int q2 = 0; q2 < per / 2; ++q2)
+      reinterpret_cast<float4*>(csv)[q2] = reinterpret_cast<const float4*>(rope_s + i0)[q2];
     for (int k0 = 0; k0 < a.n_b; k0 += rpi) {
       const int k = k0 + rsel;
       if (k >= a.n_b) continue;
@@ -118,25 +123,13 @@ __device__ __forceinline__ void obs_group_rows(const ScoreArgs& a, const ScoreWs
       alignas(16) T o1[per];
       alignas(16) T o2[per];
       if (k < nb) {
+        // the lane's `per` pairs: one 16-byte read per half (the staged rows' stride LD and i0 are
+        // multiples of 16 bytes for both storage types)
         const T* src = xs + pk[k] * LD;
-        // the lane's `per` pairs: one 16-byte read per half for bf16 rows (LD * 2 and i0 * 2 are
-        // multiples of 16), element reads for fp32 rows (odd LD); the table in 16-byte reads
         alignas(16) T xa[per];
         alignas(16) T xb[per];
-        if constexpr (sizeof(T) == 2) {
-          *reinterpret_cast<uint4*>(xa) = *reinterpret_cast<const uint4*>(src + i0);
-          *reinterpret_cast<uint4*>(xb) = *reinterpret_cast<const uint4*>(src + i0 + hd);
-        } else {
-#pragma unroll
-          for (int u = 0; u < per; ++u) {
-            xa[u] = src[i0 + u];
-            xb[u] = src[i0 + u + hd];
-          }
-        }
-        alignas(16) float2 csv[per];
-#pragma unroll
-        for (int q2 = 0; q2 < per / 2; ++q2)
-          reinterpret_cast<float4*>(csv)[q2] = reinterpret_cast<const float4*>(rope_s + i0)[q2];
+        *reinterpret_cast<uint4*>(xa) = *reinterpret_cast<const uint4*>(src + i0);
+        *reinterpret_cast<uint4*>(xb) = *reinterpret_cast<const uint4*>(src + i0 + hd);
 #pragma unroll
         for (int u = 0; u < per; ++u) {
           const float2 cs = csv[u];
