@@ -527,9 +527,9 @@ bool score_wide_plan(const ScoreArgs& a, WidePlan* p, size_t* smem) {
   const int D = a.g.D;
   const int heads = a.g.L * a.g.B * a.g.Hkv;
   // ranges of 32 key chunks (the two-pass kernel's for 256-row tiles, split_ranges), or of 64 for heads
-  // of 16384 keys and more: half the items' ends (a few us each, when the epilogue's reductions and
-  // barriers leave the tensor pipe idle) while every SM still gets tens of items
-  p->rk = a.nchunk >= 128 ? 64 : 32;
+  // of 8192 keys and more: half the items' ends (a few us each, when the epilogue's reductions and
+  // barriers leave the tensor pipe idle) while every SM still gets several items
+  p->rk = a.nchunk >= 64 ? 64 : 32;
   p->R = (a.nchunk + p->rk - 1) / p->rk;
   p->items = heads * p->R;
   p->grid = p->items < nsm ? p->items : nsm;
