@@ -239,6 +239,29 @@ def algorithmic_bytes(inp, kept_idx, kept_len):
     return k_read, moved * 4 * row, moved
 
 
+def score_flop(inp):
+    """Tensor work of the scoring passes as the BeaconKV write-up's score defines it ("打分时的 RoPE
+    对齐": every observation row against every cached key, softmax over the keys before the max):
+    QK^T over the M = G (n_r + n_b) observation rows of each KV head, once to find each row's
+    log-sum-exp and once more to take the max, i.e. 4 M D FLOP per cached key. Zero for fp32
+    caches, which are not scored on the tensor cores."""
+    if inp.dtype != "bf16":
+        return 0
+    M = (inp.Hq // inp.Hkv) * (inp.n_r + inp.n_b)
+    return 4 * M * inp.D * inp.heads * inp.N
+
+
+def bounds(nbytes, flop, ms, pk):
+    """The HBM and tensor-pipe times of a piece of work and the one that governs it (the larger), with
+    the fraction of it that ``ms`` achieves. The tensor peak is the measured burst figure: every
+    timed region here is a single step or phase of a few ms at most."""
+    hbm_ms = nbytes / (float(pk["hbm_gbs"]) * 1e9) * 1e3
+    tensor_ms = flop / (float(pk["bf16_tflops"]) * 1e12) * 1e3
+    gov = "tensor" if tensor_ms > hbm_ms else "hbm"
+    return {"hbm_ms": hbm_ms, "tensor_ms": tensor_ms, "governing": gov,
+            "frac": max(hbm_ms, tensor_ms) / ms if ms > 0 else 0.0}
+
+
 def append_timing(inp, dev, stream, reps: int = 20):
     """Per-decode-step kvc_append over every query head of the workload (the step that feeds the
     eviction's observation state), on copies of its buffers. One fill/compress cycle is captured as
@@ -427,6 +450,22 @@ def gpu_arm(args, rank, world, local_rank):
     dom_ms = phase_ms[dom]
     achieved = phase_bytes[dom] / (dom_ms / 1e3) / 1e9 if phase_bytes[dom] else 0.0
     step_gbs = alg / (ms_per_step / 1e3) / 1e9
+    flop = score_flop(inp)
+    phase_flop = {"kvc_score": flop, "kvc_select": 0, "kvc_compact": 0}
+    hbm_view = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_source": pk_kind,
+                "traffic": None if args.layers else recorded_traffic(args.config + (f"/{variant}" if variant else ""),
+                                                                     dom)}
+    dom_bounds = bounds(phase_bytes[dom], phase_flop[dom], dom_ms, pk)
+    if dom_bounds["governing"] == "tensor":
+        # the dominant phase does more tensor work than HBM time: its roofline is the tensor pipe's
+        tf = float(pk["bf16_tflops"])
+        ach_t = phase_flop[dom] / (dom_ms / 1e3) / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": ach_t, "peak": tf, "unit": "TFLOP/s",
+                    "frac": ach_t / tf, "peak_source": pk_kind + " (bf16 burst)", "traffic": hbm_view["traffic"],
+                    "flop_per_launch": phase_flop[dom], "hbm_view": hbm_view}
+    else:
+        roofline = hbm_view
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -437,10 +476,9 @@ def gpu_arm(args, rank, world, local_rank):
         "head_tokens_per_s": world * inp.heads * inp.N * args.steps / (total_ms / 1e3),
         "achieved_gbs": step_gbs, "step_roofline_frac": step_gbs / hbm,
         "algorithmic_bytes_per_step": {"k_read": k_read, "kv_moved": moved_bytes, "moved_tokens": moved},
-        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "peak_source": pk_kind,
-                     "traffic": None if args.layers else recorded_traffic(args.config + (f"/{variant}" if variant
-                                                                                          else ""), dom)},
+        "score_flop_per_step": flop,
+        "step_bounds": bounds(alg, flop, ms_per_step, pk),
+        "roofline": roofline,
         "phases_ms": phase_ms,
         "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "h2d_copy_anchor": anchor},

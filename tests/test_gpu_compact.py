@@ -4,7 +4,8 @@ Every list is valid (strictly increasing, prefix and recent windows kept); they 
 sweep's hazards: a single dropped token right after the prefix (every later row moves by one), a
 single dropped token just before the recent window (one row moves), alternating drops (runs of one
 row), one long dropped block (the recent window moves far, across many tiles), only the windows
-kept, nothing dropped, and random lists. Heads of one launch get different lists. Bit-exact.
+kept, nothing dropped, sparse lists (one kept token in 4 or 9, as with a 1/8 budget: runs of one
+row, one bulk copy each), and random lists. Heads of one launch get different lists. Bit-exact.
 """
 import numpy as np
 import pytest
@@ -24,6 +25,8 @@ def _lists(N, P, R, rng):
         np.concatenate([np.arange(P), mid[:5], mid[-3:], np.arange(N - R, N)]),  # one long dropped block
         np.concatenate([np.arange(P), np.arange(N - R, N)]),  # only the windows
         full,                                    # nothing dropped
+        np.concatenate([np.arange(P), mid[1::4], np.arange(N - R, N)]),  # sparse: every 4th middle token
+        np.concatenate([np.arange(P), mid[3::9], np.arange(N - R, N)]),  # sparse: every 9th (a 1/8 budget)
     ]
     for _ in range(4):
         k = int(rng.integers(0, len(mid) + 1))
