@@ -295,8 +295,11 @@ int kvc_compact(const kvc_cache* c, const int32_t* kept_idx, const int32_t* kept
 size_t kvc_evict_workspace_size(const kvc_cache* c, int32_t n_r, int32_t n_b) {
   const size_t sw = kvc_score_workspace_size(c, n_r, n_b);
   if (!sw) return 0;
-  const size_t per = (size_t)c->L * c->B * c->Hkv * (size_t)c->N * 4;
-  return sw + 2 * align256(per);  // scores and kept indices, used when the caller passes NULL
+  const size_t heads = (size_t)c->L * c->B * c->Hkv;
+  const size_t per = heads * (size_t)c->N * 4;
+  // scores and kept indices (used when the caller passes NULL), and the heads' order for the
+  // selection and compaction
+  return sw + 2 * align256(per) + align256(heads * 4);
 }
 
 int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void* qbuf, const int32_t* count,
@@ -317,7 +320,8 @@ int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void*
   if (o.head_budget == KVC_BUDGET_ENTROPY && g.Hkv > 64) return KVC_ERR_TOO_LARGE;
   const size_t sw = score_ws_bytes(g, c->dtype, n_r, n_b, o.ext, nullptr, nullptr);
   const size_t per = align256((size_t)g.L * g.B * g.Hkv * (size_t)g.N * 4);
-  if (!workspace || ws_bytes < sw + 2 * per || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+  const size_t ord = align256((size_t)g.L * g.B * g.Hkv * 4);
+  if (!workspace || ws_bytes < sw + 2 * per + ord || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return KVC_ERR_WORKSPACE;
   char* wb = static_cast<char*>(workspace);
   ScoreWs ws;
@@ -331,6 +335,14 @@ int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void*
   fill_score_args(&a, g, c->dtype, K, q_recent, n_r, qbuf, count, qmax, n_b, t, rope_theta, sc, nullptr, status, o,
                   ent);
   const float* sel_ent = o.head_budget == KVC_BUDGET_ENTROPY ? ent : nullptr;
+  // per-head budgets as given: the selection-and-compaction CTAs take the heads largest budget first
+  // (the order is written by the observation kernel, which every path to that kernel runs first)
+  int32_t* order = nullptr;
+  if (budget && !sel_ent && g.N <= kSelectCompactMaxN) {
+    order = reinterpret_cast<int32_t*>(wb + sw + 2 * per);
+    a.order_budget = budget;
+    a.order = order;
+  }
   // fp32 caches of at most 1024 tokens per head: scoring, selection and compaction in one cluster launch
   SmallEvict ev;
   memset(&ev, 0, sizeof(ev));
@@ -345,7 +357,7 @@ int kvc_evict(const kvc_cache* c, const void* q_recent, int32_t n_r, const void*
   rc = launch_score(a, ws, s, sel_ent ? nullptr : &ev, &fused);
   if (rc || fused) return rc;
   if (g.N <= kSelectCompactMaxN)  // one CTA per head selects, then moves the head's K and V
-    return launch_select_compact(sc, g, c->dtype, K, V, prefix, recent, budget, budget_all, sel_ent, ki, kept_len,
+    return launch_select_compact(order, sc, g, c->dtype, K, V, prefix, recent, budget, budget_all, sel_ent, ki, kept_len,
                                  status, s);
   rc = launch_select(sc, g.L * g.B * g.Hkv, g.N, prefix, recent, budget, budget_all, sel_ent, g.Hkv, ki, kept_len,
                      status, s);

@@ -135,6 +135,10 @@ struct ScoreArgs {
   float2 rope[64];            // (cos, sin) of t * theta^(-2i/D), i < D/2, from fp64
   unsigned long long* xch_zero;  // words the observation kernel zeroes for the scoring kernel, or null
   long long xch_zero_words;
+  // kvc_evict with per-head budgets: the observation kernel's first CTA also writes the order in
+  // which the selection-and-compaction CTAs take the heads (head_order_cta), or null
+  const int32_t* order_budget;
+  int32_t* order;
   int debug_fault;               // kvc_debug_fault mode at launch (0 in normal use)
   int kernel;                    // KVC_KERNEL_*: the bf16 scoring kernel asked for (0 = automatic)
   // Variants: an aggregation other than max/max or an entropy output runs the kernels'
@@ -233,8 +237,9 @@ int launch_head_budget(const float* entropy, int groups, int Hkv, int N, int P, 
 
 // kvc_evict's selection and compaction in one launch (one CTA per head; N <= kSelectCompactMaxN)
 constexpr int kSelectCompactMaxN = 65536;
-int launch_select_compact(const float* scores, const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V,
-                          int P, int R, const int32_t* budget, int budget_all, const float* entropy, int32_t* kept_idx,
+// order: the head each CTA takes (a permutation of the heads, written by head_order_cta), or null
+int launch_select_compact(const int32_t* order, const float* scores, const CacheGeom& g, int dtype, const LayerPtrs& K,
+                          const LayerPtrs& V, int P, int R, const int32_t* budget, int budget_all, const float* entropy, int32_t* kept_idx,
                           int32_t* kept_len, int32_t* status, cudaStream_t s);
 
 // list_per_seq: kept_idx [B][N] / kept_len [B], one list per sequence for all its layers and heads

@@ -32,11 +32,44 @@ namespace kvc {
 // ---------------------------------------------------------------------------
 // rotary table and observation rows
 // ---------------------------------------------------------------------------
+// The order in which kvc_evict's selection-and-compaction CTAs take the heads when each head has its
+// own budget: largest budget first, so that the longest moves start in the launch's first wave
+// instead of trailing it (one warp moves a head's K, another its V; a head of many scattered kept
+// rows is the slowest). Heads go into 128 buckets, four per octave of the budget clamped to [1, N],
+// largest first; heads within a bucket in any order. Run by one whole CTA.
+__device__ void head_order_cta(const int32_t* budget, int heads, int N, int32_t* order) {
+  __shared__ int cnt[128];
+  auto bucket = [&](int h) {
+    int b = budget[h];
+    b = b < 1 ? 1 : (b > N ? N : b);
+    const int e = 31 - __clz(b);                                   // floor(log2 b)
+    const int f = e >= 2 ? (b >> (e - 2)) & 3 : (b << (2 - e)) & 3;  // the next two bits
+    const int k = 4 * e + f;
+    return 127 - (k < 127 ? k : 127);
+  };
+  for (int i = threadIdx.x; i < 128; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  for (int h = threadIdx.x; h < heads; h += blockDim.x) atomicAdd(&cnt[bucket(h)], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {  // bucket counts -> first positions
+    int sum = 0;
+    for (int i = 0; i < 128; ++i) {
+      const int c = cnt[i];
+      cnt[i] = sum;
+      sum += c;
+    }
+  }
+  __syncthreads();
+  for (int h = threadIdx.x; h < heads; h += blockDim.x) order[atomicAdd(&cnt[bucket(h)], 1)] = h;
+  __syncthreads();
+}
+
 template <typename T, int D>
 __global__ void build_obs_kernel(ScoreArgs a, ScoreWs ws, int nw) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_nvalid;  // valid observation rows of this KV head (for the entropy's mean)
   const int head = blockIdx.x;
+  if (a.order && head == 0) head_order_cta(a.order_budget, a.g.L * a.g.B * a.g.Hkv, a.g.N, a.order);
   const int G = a.g.Hq / a.g.Hkv, qs = a.qstride;
   T* obs = static_cast<T*>(ws.obs) + (size_t)head * a.M_pad * D;
   uint8_t* valid = ws.valid + (size_t)head * a.M_pad;

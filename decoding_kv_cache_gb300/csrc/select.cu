@@ -58,9 +58,11 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
 // Selection and compaction of one head per CTA (256 threads, heads of at most kSelectCompactMaxN
 // tokens): the CTA selects, then two of its warps move the head's kept K and V rows (compact_warp).
 // One launch instead of two, and each head's selection overlaps the other heads' moves (two CTAs
-// fit on an SM). The dynamic shared memory stages the scores of a head of more than one tile (when
+// fit on an SM). CTA b takes head order[b] (largest budget first, when the heads' budgets differ)
+// or head b. The dynamic shared memory stages the scores of a head of more than one tile (when
 // they fit), then serves as the two warps' rings.
-__global__ void __launch_bounds__(256) select_compact_kernel(const float* __restrict__ scores, int N, int P, int R,
+__global__ void __launch_bounds__(256) select_compact_kernel(const int32_t* __restrict__ order,
+                                                             const float* __restrict__ scores, int N, int P, int R,
                                                              const int32_t* __restrict__ budget, int budget_all,
                                                              const float* __restrict__ entropy, int Hkv,
                                                              int32_t* __restrict__ kept_idx,
@@ -68,16 +70,17 @@ __global__ void __launch_bounds__(256) select_compact_kernel(const float* __rest
                                                              int use_smem, CompactArgs ca) {
   extern __shared__ __align__(128) uint8_t smc[];
   griddep_wait();  // the scores (and entropies) come from the previous kernel
-  select_head<256>(blockIdx.x, scores, N, P, R, budget, budget_all, entropy, Hkv, kept_idx, kept_len, status, use_smem,
+  const int head = order ? order[blockIdx.x] : (int)blockIdx.x;
+  select_head<256>(head, scores, N, P, R, budget, budget_all, entropy, Hkv, kept_idx, kept_len, status, use_smem,
                    0, reinterpret_cast<uint32_t*>(smc));
   // the head's kept list, written by this CTA, is visible to all its threads, and the staging area is free
   __syncthreads();
   const int warp = threadIdx.x >> 5;
-  if (warp < 2) compact_warp(ca, blockIdx.x, warp, smc + warp * kCompactWarpSmem);
+  if (warp < 2) compact_warp(ca, head, warp, smc + warp * kCompactWarpSmem);
 }
 
-int launch_select_compact(const float* scores, const CacheGeom& g, int dtype, const LayerPtrs& K, const LayerPtrs& V,
-                          int P, int R, const int32_t* budget, int budget_all, const float* entropy, int32_t* kept_idx,
+int launch_select_compact(const int32_t* order, const float* scores, const CacheGeom& g, int dtype, const LayerPtrs& K,
+                          const LayerPtrs& V, int P, int R, const int32_t* budget, int budget_all, const float* entropy, int32_t* kept_idx,
                           int32_t* kept_len, int32_t* status, cudaStream_t s) {
   const int heads = g.L * g.B * g.Hkv, N = g.N;
   if (heads == 0) return KVC_OK;
@@ -99,7 +102,7 @@ int launch_select_compact(const float* scores, const CacheGeom& g, int dtype, co
   const int use_smem = (N > kSweep * 256 && stage <= smem) ? 1 : 0;
   if (cudaFuncSetAttribute(select_compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVC_ERR_LAUNCH;
-  if (launch_pdl(select_compact_kernel, dim3(heads), dim3(256), smem, s, false, scores, N, P, R, budget, budget_all,
+  if (launch_pdl(select_compact_kernel, dim3(heads), dim3(256), smem, s, false, order, scores, N, P, R, budget, budget_all,
                  entropy, g.Hkv, kept_idx, kept_len, status, use_smem, ca) != cudaSuccess)
     return KVC_ERR_LAUNCH;
   return KVC_OK;

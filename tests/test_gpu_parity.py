@@ -30,6 +30,9 @@ CASES = [
     ("qwen3-4b", dict(L=1, Hq=4, Hkv=1, N=50000)),
     # 224 rows as two 128-row tiles over 20 CTAs per head (the wide exchange batch)
     ("qwen7b-reasonalloc", dict(L=1, B=1, N=5000)),
+    # per-head budgets over 384 heads (more than one wave of selection-and-compaction CTAs, which
+    # take the heads largest budget first)
+    ("qwen7b-reasonalloc", dict(L=12, B=8, N=1000)),
 ]
 
 
