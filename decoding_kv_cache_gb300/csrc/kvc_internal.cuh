@@ -199,10 +199,19 @@ struct SplitPlan {
   const int32_t* list;  // null: every item; else [0] = count, [1..] = the items (device, written by the
                         // previous kernel on the stream)
 };
+// The wide kernel's exact fallback recomputes each of its n listed items as this many sub-ranges on
+// separate CTAs (grid CTAs in all, at most one key chunk each), so that a few listed items of many
+// chunks do not run one chunk after another on one CTA: sub-range 0 writes the item's partial, the
+// others theirs into the workspace's exchange area, and the combine kernel merges them.
+__host__ __device__ inline int fallback_sub(int n, int grid, int rk) {
+  if (n <= 0) return 1;
+  const int s = grid / n;
+  return s < 1 ? 1 : (s > rk ? rk : s);
+}
 // Pass 1 of the two-pass streaming kernel over a device list of items (the wide kernel's fallback),
-// with the listing kernel's ranges: item = head * R + range, rk key chunks per range.
+// with the listing kernel's ranges: item = head * R + range, rk key chunks per range; grid CTAs.
 int launch_score_split_pass1_list(const ScoreArgs& a, const ScoreWs& ws, const int32_t* list, int rk, int R,
-                                  cudaStream_t s);
+                                  int grid, cudaStream_t s);
 int split_ranges(int nchunk, int M_pad);
 bool score_split_plan(const ScoreArgs& a, SplitPlan* p, size_t* smem);
 int launch_score_split(const ScoreArgs& a, const ScoreWs& ws, const SplitPlan& p, size_t smem, cudaStream_t s);

@@ -75,7 +75,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   // CTA without a listed item leaves before it takes tensor memory or sets anything up.
   if (p.list) {
     griddep_wait();
-    if ((int)blockIdx.x >= *reinterpret_cast<const volatile int32_t*>(p.list)) return;
+    const int n = *reinterpret_cast<const volatile int32_t*>(p.list);
+    if ((int)blockIdx.x >= n * fallback_sub(n, (int)gridDim.x, p.rk)) return;
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -100,14 +101,23 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *slot;
   const int bhkv = a.g.B * a.g.Hkv;
-  // Work items: all of them, or (pass 1 as the wide kernel's exact fallback) the listed ones, whose
-  // count and ids the previous kernel wrote: then every role waits for it first.
-  int nitems = p.items;
+  // Work items: all of them, or (pass 1 as the wide kernel's exact fallback) sub-ranges of the listed
+  // ones, whose count and ids the previous kernel wrote: then every role waits for it first.
+  int nitems = p.items, sub = 1;
   if (p.list) {
     griddep_wait();
-    nitems = *reinterpret_cast<const volatile int32_t*>(p.list);
+    const int n = *reinterpret_cast<const volatile int32_t*>(p.list);
+    sub = fallback_sub(n, (int)gridDim.x, p.rk);
+    nitems = n * sub;
   }
-  auto item_at = [&](int idx) { return p.list ? p.list[1 + idx] : idx; };
+  auto item_at = [&](int v) { return p.list ? p.list[1 + v / sub] : v; };
+  // work unit v: its item and key chunks [cb, cb + nc) (the whole range unless the item is split)
+  auto range_of = [&](int v, int item, int& cb, int& nc) {
+    const int c0 = (item % p.R) * p.rk, c1 = min(c0 + p.rk, a.nchunk);
+    const int cs = (p.rk + sub - 1) / sub;
+    cb = min(c0 + (v % sub) * cs, c1);
+    nc = min(cb + cs, c1) - cb;
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -117,9 +127,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       int it = 0;
       for (int idx = blockIdx.x; idx < nitems && !stop && !*abort_flag; idx += gridDim.x, ++it) {
         const int item = item_at(idx);
-        const int head = item / p.R, ri = item % p.R;
+        const int head = item / p.R;
         const int l = head / bhkv, bh = head % bhkv;
-        const int cb = ri * p.rk, nc = min(cb + p.rk, a.nchunk) - cb;
+        int cb, nc;
+        range_of(idx, item, cb, nc);
         if (idx + (int)gridDim.x < nitems) tc::prefetch_tensormap(&maps.k[item_at(idx + gridDim.x) / p.R / bhkv]);
         auto load_k = [&](int j) -> bool {
           const int s = kc % S;
@@ -174,8 +185,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       int it = 0;
       for (int idx = blockIdx.x; idx < nitems && ok && !*abort_flag; idx += gridDim.x, ++it) {
         const int item = item_at(idx);
-        const int ri = item % p.R;
-        const int cb = ri * p.rk, nc = min(cb + p.rk, a.nchunk) - cb;
+        int cb, nc;
+        range_of(idx, item, cb, nc);
         const int qb = it % kQBuf;
         if (!wait_or_abort(&qfull[qb], (it / kQBuf) & 1, abort_flag, a.status)) break;
         tc::fence_after_sync();
@@ -225,8 +236,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     int it = 0;
     for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x, ++it) {
       const int item = item_at(idx);
-      const int head = item / p.R, ri = item % p.R;
-      const int cb = ri * p.rk, nc = min(cb + p.rk, a.nchunk) - cb;
+      const int head = item / p.R;
+      int cb, nc;
+      range_of(idx, item, cb, nc);
       if constexpr (kPass == 1) {
         float2 st[NT];
 #pragma unroll
@@ -284,11 +296,14 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 #pragma unroll
           for (int t = 0; t < NT; ++t) mg[t * kSplitRows + row] = st[t];
         asm volatile("bar.sync %0, 64;\n" ::"r"(2 + q) : "memory");
+        // the item's partial, or a later sub-range's in the exchange area (merged by the combine kernel)
+        float* dst = (idx % sub == 0) ? ws.lse2p + (size_t)item * a.M_pad
+                                      : reinterpret_cast<float*>(ws.part) + (size_t)idx * a.M_pad;
         if (hf == 0 && !*abort_flag)
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
             const float2 m = lse_merge(st[t], mg[t * kSplitRows + row]);
-            ws.lse2p[(size_t)item * a.M_pad + t * kSplitRows + row] = m.y > 0.f ? m.x + log2f(m.y) : -INFINITY;
+            dst[t * kSplitRows + row] = m.y > 0.f ? m.x + log2f(m.y) : -INFINITY;
           }
       } else {
         // lse2 of this thread's rows (q*32 + lane/4 + 8k of each tile) from the combine kernel;
@@ -381,15 +396,25 @@ __global__ void split_combine_kernel(ScoreArgs a, ScoreWs ws, SplitPlan p) {
   if (r >= a.M_pad) return;
   const float* src = ws.lse2p + (size_t)head * p.R * a.M_pad + r;
   float m = -INFINITY, s = 0.f;
-  for (int ri = 0; ri < p.R; ++ri) {
-    const float v = src[(size_t)ri * a.M_pad];
-    if (v == -INFINITY) continue;
+  auto add = [&](float v) {
+    if (v == -INFINITY) return;
     if (v > m) {
       s = s * exp2f(m - v) + 1.f;
       m = v;
     } else {
       s += exp2f(v - m);
     }
+  };
+  for (int ri = 0; ri < p.R; ++ri) add(src[(size_t)ri * a.M_pad]);
+  // the wide kernel's fallback: the later sub-ranges of this head's listed items
+  if (p.list) {
+    const int n = p.list[0];
+    const int sub = fallback_sub(n, p.grid, p.rk);
+    if (sub > 1)
+      for (int i = 0; i < n; ++i)
+        if (p.list[1 + i] / p.R == head)
+          for (int si = 1; si < sub; ++si)
+            add(reinterpret_cast<const float*>(ws.part)[((size_t)i * sub + si) * a.M_pad + r]);
   }
   const bool ok = ws.valid[(size_t)head * a.M_pad + r] != 0 && s > 0.f;
   ws.lse2[(size_t)head * a.M_pad + r] = ok ? m + log2f(s) : INFINITY;
@@ -461,7 +486,7 @@ int launch_score_split(const ScoreArgs& a, const ScoreWs& ws, const SplitPlan& p
 }
 
 int launch_score_split_pass1_list(const ScoreArgs& a, const ScoreWs& ws, const int32_t* list, int rk, int R,
-                                  cudaStream_t s) {
+                                  int grid, cudaStream_t s) {
   SplitPlan p;
   size_t smem = 0;
   if (!score_split_plan(a, &p, &smem)) return KVC_ERR_LAUNCH;
@@ -469,6 +494,7 @@ int launch_score_split_pass1_list(const ScoreArgs& a, const ScoreWs& ws, const i
   p.rk = rk;  // the listing kernel's ranges
   p.R = R;
   p.items = a.g.L * a.g.B * a.g.Hkv * R;
+  p.grid = grid;  // the combine kernel splits the listed items by the same count
   // the wide kernel's footprint (three key stages), so that the SMs keep their shared-memory split
   // between the launches around this one
   const size_t per_stage = (size_t)kChunk * a.g.D * 2;

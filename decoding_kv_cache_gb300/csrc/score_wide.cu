@@ -20,8 +20,10 @@
 //               2^-80 of the common reference; an item outside that is listed and recomputed with
 //               a running max per row by the two-pass kernel's pass 1 (score_split.cu) over the
 //               list (keys far out in a heavy tail reach it; the tests force it).
-//   fallback    score_split_kernel's pass 1 over the listed items (usually none: it exits at once)
-//   combine     split_combine_kernel: per head and row, the ranges' partials merged into lse2
+//   fallback    score_split_kernel's pass 1 over the listed items, each split into sub-ranges over
+//               the launch's CTAs (usually none or a few: with none it exits at once)
+//   combine     split_combine_kernel: per head and row, the ranges' partials (and the listed items'
+//               sub-ranges) merged into lse2
 //   pass 2      per item: the same MMA; per key the max over its rows of s c2 - lse2 (lse2 from
 //               shared memory), the two column halves merged in shared memory, exp2 per key.
 //
@@ -563,8 +565,8 @@ int launch_score_wide(const ScoreArgs& a, const ScoreWs& ws, const WidePlan& p, 
       return KVC_ERR_LAUNCH;
     if (pass == 1) {
       // the listed items again, with a running max per row (the two-pass kernel's pass 1)
-      if (launch_score_split_pass1_list(a, ws, ws.fb, p.rk, p.R, s) != KVC_OK) return KVC_ERR_LAUNCH;
-      const SplitPlan sp{p.rk, p.R, p.items, p.grid, p.stages};
+      if (launch_score_split_pass1_list(a, ws, ws.fb, p.rk, p.R, p.grid, s) != KVC_OK) return KVC_ERR_LAUNCH;
+      const SplitPlan sp{p.rk, p.R, p.items, p.grid, p.stages, ws.fb};
       if (launch_pdl(split_combine_kernel, dim3(a.g.L * a.g.B * a.g.Hkv), dim3(a.M_pad), 0, s, false, aa, wss, sp) !=
           cudaSuccess)
         return KVC_ERR_LAUNCH;
