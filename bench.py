@@ -456,6 +456,11 @@ def gpu_arm(args, rank, world, local_rank):
                 "frac": achieved / hbm, "peak_source": pk_kind,
                 "traffic": None if args.layers else recorded_traffic(args.config + (f"/{variant}" if variant else ""),
                                                                      dom)}
+    if hbm_view["traffic"]:
+        # the same launch's rate on the DRAM bytes ncu counted (writes still in L2 at the end and re-reads
+        # make it differ from the algorithmic rate)
+        hbm_view["achieved_dram"] = hbm_view["traffic"] / (dom_ms / 1e3) / 1e9
+        hbm_view["frac_dram"] = hbm_view["achieved_dram"] / hbm
     dom_bounds = bounds(phase_bytes[dom], phase_flop[dom], dom_ms, pk)
     if dom_bounds["governing"] == "tensor":
         # the dominant phase does more tensor work than HBM time: its roofline is the tensor pipe's
