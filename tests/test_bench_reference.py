@@ -43,3 +43,24 @@ def test_reference_arm_prints_one_contract_line():
 def test_reference_arm_other_ranks_exit_without_work():
     assert _run("--impl", "reference", "--config", "tiny", "--steps", "2", RANK="1", WORLD_SIZE="2",
                 LOCAL_RANK="1") == []
+
+
+def test_roofline_bounds_arithmetic():
+    """The line's two bounds: the scoring's tensor work is QK^T over the M = G (n_r + n_b) observation
+    rows, twice (one pass for the log-sum-exp, one for the max), 4 M D FLOP per cached key, none for
+    fp32 caches; the governing bound is the larger of the bytes at the copy peak and the FLOP at the
+    bf16 peak. Checked against the R1-Qwen-7B shape's numbers worked by hand (G = 7, 32 rows each)."""
+    import types
+    sys.path.insert(0, ROOT)
+    import bench
+    inp = types.SimpleNamespace(dtype="bf16", Hq=28, Hkv=4, n_r=16, n_b=16, D=128, heads=28 * 8 * 4, N=8192)
+    flop = bench.score_flop(inp)
+    assert flop == 4 * 224 * 128 * 896 * 8192 == 841_813_590_016
+    assert bench.score_flop(types.SimpleNamespace(**{**vars(inp), "dtype": "f32"})) == 0
+    pk = {"hbm_gbs": 6782.8, "bf16_tflops": 1934.3}
+    b = bench.bounds(2.81e9, flop, 1.0, pk)
+    assert abs(b["hbm_ms"] - 2.81e9 / 6782.8e9 * 1e3) < 1e-12
+    assert abs(b["tensor_ms"] - flop / 1934.3e12 * 1e3) < 1e-12
+    assert b["governing"] == "tensor" and abs(b["frac"] - b["tensor_ms"]) < 1e-12  # 1 ms step
+    b = bench.bounds(96.6e9, 10 * flop, 20.0, pk)  # bytes dominate: the Qwen3-14B-shaped step's order
+    assert b["governing"] == "hbm" and abs(b["frac"] - b["hbm_ms"] / 20.0) < 1e-12
