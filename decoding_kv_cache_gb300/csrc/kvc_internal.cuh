@@ -200,13 +200,17 @@ struct SplitPlan {
                         // previous kernel on the stream)
 };
 // The wide kernel's exact fallback recomputes each of its n listed items as this many sub-ranges on
-// separate CTAs (grid CTAs in all, at most one key chunk each), so that a few listed items of many
-// chunks do not run one chunk after another on one CTA: sub-range 0 writes the item's partial, the
-// others theirs into the workspace's exchange area, and the combine kernel merges them.
+// separate CTAs (at most grid CTAs in all, kFallbackSub sub-ranges an item, at least one key chunk
+// each), so that a few listed items of many chunks do not run one chunk after another on one CTA:
+// sub-range 0 writes the item's partial, the others theirs into the workspace's exchange area, and
+// the combine kernel merges them (one batch of reads per listed item).
+constexpr int kFallbackSub = 16;
 __host__ __device__ inline int fallback_sub(int n, int grid, int rk) {
-  if (n <= 0) return 1;
-  const int s = grid / n;
-  return s < 1 ? 1 : (s > rk ? rk : s);
+  if (n <= 0 || n > kMaxSMs / 2) return 1;
+  int s = grid / n;
+  if (s > kFallbackSub) s = kFallbackSub;
+  if (s > rk) s = rk;
+  return s < 1 ? 1 : s;
 }
 // Pass 1 of the two-pass streaming kernel over a device list of items (the wide kernel's fallback),
 // with the listing kernel's ranges: item = head * R + range, rk key chunks per range; grid CTAs.

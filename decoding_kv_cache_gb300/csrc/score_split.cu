@@ -406,15 +406,27 @@ __global__ void split_combine_kernel(ScoreArgs a, ScoreWs ws, SplitPlan p) {
     }
   };
   for (int ri = 0; ri < p.R; ++ri) add(src[(size_t)ri * a.M_pad]);
-  // the wide kernel's fallback: the later sub-ranges of this head's listed items
+  // the wide kernel's fallback: the later sub-ranges of this head's listed items (split only when
+  // there are at most grid / 2 of them: their ids go to shared memory first, one read each)
+  __shared__ int s_items[kMaxSMs / 2];
   if (p.list) {
     const int n = p.list[0];
     const int sub = fallback_sub(n, p.grid, p.rk);
+    if (sub > 1) {
+      if (r < n) s_items[r] = p.list[1 + r];
+      __syncthreads();
+    }
     if (sub > 1)
       for (int i = 0; i < n; ++i)
-        if (p.list[1 + i] / p.R == head)
-          for (int si = 1; si < sub; ++si)
-            add(reinterpret_cast<const float*>(ws.part)[((size_t)i * sub + si) * a.M_pad + r]);
+        if (s_items[i] / p.R == head) {
+          // every sub-range's partial in flight at once, then merged
+          const float* sp = reinterpret_cast<const float*>(ws.part) + (size_t)i * sub * a.M_pad + r;
+          float v[kFallbackSub];
+#pragma unroll
+          for (int u = 1; u < kFallbackSub; ++u) v[u] = u < sub ? sp[(size_t)u * a.M_pad] : -INFINITY;
+#pragma unroll
+          for (int u = 1; u < kFallbackSub; ++u) add(v[u]);
+        }
   }
   const bool ok = ws.valid[(size_t)head * a.M_pad + r] != 0 && s > 0.f;
   ws.lse2[(size_t)head * a.M_pad + r] = ok ? m + log2f(s) : INFINITY;
