@@ -411,3 +411,23 @@ def test_f32_per_head_budget_out_of_range_is_flagged_and_left_whole():
     assert_scores_close(gpu["scores"], ora["scores"], "tiny per-head budgets")
     check_kept(inp, gpu, ora, gpu["scores"])
     check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
+
+
+def test_f32_streaming_per_head_budgets():
+    """fp32 heads past the cluster kernel's 1024 keys (the streaming passes, then the selection-and-
+    compaction CTAs in largest-budget-first order) with budgets that differ per head: below prefix +
+    recent (kept whole, flagged), exactly prefix + recent, N, and values in between."""
+    inp = make_inputs("tiny", L=2, B=3, N=1500)
+    g = torch.Generator().manual_seed(7)
+    b = torch.randint(21, 1500, (inp.L, inp.B, inp.Hkv), generator=g, dtype=torch.int32)
+    b[0, 0, 0] = 7      # < prefix + recent
+    b[0, 2, 1] = 20     # == prefix + recent
+    b[1, 1, 0] = 1500   # == N
+    inp.budget = b
+    gpu = run_evict(inp, DEV)
+    ora = O.evict(inp)
+    assert gpu["status"] & 0x1
+    assert gpu["kept_len"][0, 0, 0] == 1500 and gpu["kept_len"][0, 2, 1] == 20 and gpu["kept_len"][1, 1, 0] == 1500
+    assert_scores_close(gpu["scores"], ora["scores"], "tiny streaming per-head budgets")
+    check_kept(inp, gpu, ora, gpu["scores"])
+    check_compaction(inp, gpu["K"], gpu["V"], gpu["kept_idx"], gpu["kept_len"])
